@@ -1,0 +1,373 @@
+#!/usr/bin/env python3
+"""Benchmark of single-token MLA decode on GB300 through libmla_decode.
+
+One step = one full decode call (stage-1 split kernel + stage-2 merge) over
+one batch of synthetic input that is already resident in HBM.  The default
+workload is the HBM-bound headline shape: bs=256 requests x 8192 tokens,
+fp8-e4m3 KV and fp8 q (per-tensor scales), page size 8 with a permuted page
+table (1.21 GB of KV, larger than L2, so no L2 flush is needed).
+
+Prints ONE JSON line (rank 0).  Multi-GPU (torchrun): every rank decodes its
+own batch of the same shape (batch-sharded replicas, no collective on the
+data path); timing is the max over ranks.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--config NAME] [--no-e2e] [--no-cpu-baseline]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MLA decode µs/call and achieved HBM GB/s (% of 8 TB/s) per (bs, kv_len, KV dtype)"
+DEFAULT_CONFIG = "bs256_kv8192_fp8_page8"
+L2_BYTES = 129 * 2**20
+NOMINAL_HBM_GBS = 8000.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def config_meta(name, w):
+    from mla_decode_stage1_gb300 import synth
+    c = synth.CONFIGS[name]
+    return {"workload": name, "bs": w.bs,
+            "kv_len": c["kv_len"] if c["kv_len"] is not None else "U[512,8192]",
+            "q_dtype": w.q_dtype, "kv_dtype": w.kv_dtype, "page_size": w.page_size,
+            "page_table": "permuted" if w.kv_indices is not None else "identity",
+            "heads": 16, "qk_dim": 576, "v_dim": 512,
+            "parallelism": "batch-sharded replicas (one batch per GPU)"}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def stage1_traffic(workload):
+    """DRAM bytes per stage-1 launch from the committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "stage1_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    src = os.path.join(ROOT, "mla_decode_stage1_gb300", "csrc", "stage1.cu")
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    entry = d.get(workload)
+    if not entry or entry.get("stage1_sha") != h:
+        return None
+    return float(entry["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.path is None or not os.path.exists(self.path):
+            return None
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = sorted(r[0] for r in rows)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[2]) if v.lower() == "active"})
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": rows[0][1], "reasons": reasons,
+                "samples": len(rows)}
+
+
+def cpu_baseline(w, target_s=8.0):
+    """The fp64 oracle, as it stands, on the host cores over a bounded sample
+    of the workload's requests.  Returns (GB/s, cores, sample description)."""
+    import oracle
+    from mla_decode_stage1_gb300 import synth
+    cores = os.cpu_count() or 1
+    n = max(1, min(w.bs, cores))
+    args = synth.oracle_args(w)
+    elapsed = 0.0
+    done = 0
+    nbytes = 0
+    per_req_qo = 16 * 576 * (2 if w.q_dtype == "bf16" else 1) + 16 * 512 * 2
+    start = 0
+    while elapsed < target_s and done < w.bs:
+        sel = list(range(start, min(start + n, w.bs)))
+        t0 = time.perf_counter()
+        oracle.mla_decode(**dict(args, select=sel), nthreads=cores)
+        elapsed += time.perf_counter() - t0
+        done += len(sel)
+        nbytes += sum(w.lengths[i] for i in sel) * w.kv_bytes_per_token() + len(sel) * per_req_qo
+        start += len(sel)
+        if elapsed > 0 and (target_s - elapsed) < elapsed / max(1, done) * n:
+            break
+    return nbytes / elapsed / 1e9, cores, f"{done} of {w.bs} requests ({nbytes/1e6:.1f} MB algorithmic), {elapsed:.1f} s"
+
+
+def run_reference(args, world, rank):
+    """Reference arm: the fp64 CPU oracle on the host cores, each step a
+    bounded sample of the same workload (rank 0 only)."""
+    if rank != 0:
+        return
+    from mla_decode_stage1_gb300 import synth
+    w = synth.make_config(args.config, device="cpu")
+    import oracle
+    oargs = synth.oracle_args(w)
+    cores = os.cpu_count() or 1
+    sample = list(range(min(w.bs, max(1, cores // 2))))
+    per_req_qo = 16 * 576 * (2 if w.q_dtype == "bf16" else 1) + 16 * 512 * 2
+    nbytes = sum(w.lengths[i] for i in sample) * w.kv_bytes_per_token() + len(sample) * per_req_qo
+    for _ in range(args.warmup):
+        oracle.mla_decode(**dict(oargs, select=sample[:1]), nthreads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.mla_decode(**dict(oargs, select=sample), nthreads=cores)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = nbytes / dt / 1e9
+    desc = f"{len(sample)} of {w.bs} requests per step"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_meta(args.config, w),
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    import torch
+    import mla_decode_stage1_gb300 as mla
+    from mla_decode_stage1_gb300 import synth
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    # every rank owns one batch of the configured shape (weak scaling)
+    c = synth.CONFIGS[args.config]
+    w = synth.make_workload(bs=c["bs"], lengths=synth.config_lengths(args.config),
+                            page_size=c["page_size"], q_dtype=c["q_dtype"], kv_dtype=c["kv_dtype"],
+                            permute_pages=c["permute_pages"], seed=c["seed"] + 1000 * rank,
+                            device=dev, name=args.config)
+    d = w.to(dev)
+    plan = mla.mla_decode_plan(w.kv_indptr, w.kv_last_page_len, page_size=w.page_size,
+                               q_dtype=w.q_dtype, kv_dtype=w.kv_dtype)
+    info = plan.info()
+    ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=dev)
+    out = torch.empty(w.bs, 16, 512, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(w.bs, 16, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    kw = dict(workspace=ws, q_scale=d.q_scale, kv_scale=d.kv_scale, kv_e8m0=d.kv_e8m0,
+              kv_indices=d.kv_indices, lse=lse)
+    alg_bytes = w.algorithmic_bytes()
+    kv_bytes = w.total_tokens() * w.kv_bytes_per_token()
+    flush = kv_bytes < 2 * L2_BYTES
+    scratch = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if flush else None
+
+    def step():
+        mla.mla_decode_run(plan, d.q, d.kv, out, **kw)
+
+    for _ in range(max(3, args.warmup)):
+        if flush:
+            scratch.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    mla.mla_decode_check(plan, ws)
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    ev_s1 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(K)]
+    with ClockSampler(local) as clk:
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter()
+        for i in range(K):
+            if flush:
+                scratch.fill_(1)
+            plan.set_stage1_events(*ev_s1[i])
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+        if dist is not None:
+            dist.barrier()
+    plan.set_stage1_events(None, None)
+    mla.mla_decode_check(plan, ws)
+    step_ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    s1_ms = sum(a.elapsed_time(b) for a, b in ev_s1) / K
+    if dist is not None:
+        t = torch.tensor([step_ms, s1_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms, s1_ms = float(t[0]), float(t[1])
+    clocks = clk.summary()
+
+    # end to end through the public API: pinned host inputs -> device, decode,
+    # output + lse -> pinned host, every step
+    e2e = None
+    if not args.no_e2e:
+        host = {k: (None if v is None else v.cpu().pin_memory())
+                for k, v in (("q", d.q), ("kv", d.kv), ("q_scale", d.q_scale),
+                             ("kv_scale", d.kv_scale), ("kv_e8m0", d.kv_e8m0),
+                             ("kv_indices", d.kv_indices))}
+        dev_in = {k: (None if v is None else torch.empty_like(v, device=dev)) for k, v in host.items()}
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+        d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+        E = max(1, args.e2e_steps)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+        def e2e_step():
+            for k, v in host.items():
+                if v is not None:
+                    dev_in[k].copy_(v, non_blocking=True)
+            mla.mla_decode_run(plan, dev_in["q"], dev_in["kv"], out, workspace=ws,
+                               q_scale=dev_in["q_scale"], kv_scale=dev_in["kv_scale"],
+                               kv_e8m0=dev_in["kv_e8m0"], kv_indices=dev_in["kv_indices"], lse=lse)
+            out_h.copy_(out, non_blocking=True)
+            lse_h.copy_(lse, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        e0.record(stream)
+        for _ in range(E):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / E
+        if dist is not None:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t[0])
+        e2e = {"value": world * alg_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+               "steps": E}
+        del dev_in, host
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    peak, peak_kind = load_peaks()
+    achieved = alg_bytes / (s1_ms * 1e-3) / 1e9
+    traffic = stage1_traffic(args.config)
+    gbs = world * alg_bytes / (step_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": max(3, args.warmup), "ms_per_step": step_ms, "us_per_call": step_ms * 1e3,
+        "pct_of_8TBps": 100.0 * (alg_bytes / (step_ms * 1e-3) / 1e9) / NOMINAL_HBM_GBS,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.kv_dtype if w.q_dtype == w.kv_dtype else f"{w.q_dtype}q/{w.kv_dtype}kv",
+        "data": "synthetic: seeded N(0,1) q and KV, per-tensor e4m3 quantisation (amax/448)",
+        "config": dict(config_meta(args.config, w),
+                       l2="flushed between steps (2x L2 write)" if flush else
+                       f"inputs larger than L2 ({kv_bytes/1e9:.2f} GB KV)",
+                       algorithmic_bytes=alg_bytes, num_ctas=info.num_ctas,
+                       num_partials=info.num_partials),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind, "traffic": traffic,
+                     "kernel": "mla_stage1_kernel", "stage1_us": s1_ms * 1e3},
+        "gpu_launches": K * (1 + (1 if info.num_merge_jobs > 0 else 0)),
+        "clocks": clocks,
+        "wall_s_timed": t_wall,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if not args.no_cpu_baseline:
+        try:
+            v, cores, sample = cpu_baseline(w.to("cpu"))
+            line["cpu_baseline"] = {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                    "sample": sample}
+        except Exception as e:  # the oracle is optional for the GPU number itself
+            line["cpu_baseline"] = {"value": None, "unit": "GB/s", "cores": os.cpu_count(),
+                                    "kind": "oracle", "sample": f"failed: {e}"}
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,183 @@
+/*
+ * mla_decode.h -- C ABI of libmla_decode: single-token decode attention for
+ * multi-head latent attention (MLA) on one GB300 (sm_103a).
+ *
+ * The operation (kernelindex.com, amd-mixed-mla submissions 668813 "v0092a",
+ * 695854 and 600081): every request b has 16 query heads q[b,h,0:576] that
+ * share one latent KV head.  Over the request's tokens t (reached through
+ * kv_indptr and a page table) the scores are
+ *     s[h,t] = (1/sqrt(576)) * sum_{d<576} q[b,h,d] * k_t[d]
+ * and the output is the softmax-weighted sum of the first 512 dims of k_t:
+ *     out[b,h,:] = sum_t softmax_t(s[h,:]) * k_t[0:512],
+ *     lse[b,h]   = ln sum_t exp(s[h,t]).
+ * The KV row is stored bf16, fp8-e4m3 times one per-tensor fp32 kv_scale, or
+ * MXFP4 (e2m1 nibbles, element 2i in the low nibble of byte i, one e8m0 scale
+ * byte per 32 elements).  The work is cut into split-KV pieces whose partial
+ * results are merged by their log-sum-exp weights (the stage-1 / stage-2
+ * scheme of submission 668813's MXFP4 route and of aiter's
+ * mla_decode_fwd / mla_reduce_v1 calls on all three pages).
+ *
+ * Conventions for every call:
+ *   - Nothing throws and nothing falls back to the CPU: each call returns an
+ *     mla_status.  A call that returns an error has launched nothing.
+ *   - mla_decode_run never synchronises the stream and never reads device
+ *     memory on the host.
+ *   - Pointers named *_host are host memory; every other data pointer is
+ *     device memory owned by the caller.  The plan object is owned by the
+ *     library and released with mla_plan_destroy.
+ */
+#ifndef MLA_DECODE_H_
+#define MLA_DECODE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* mla_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer, bad indptr */
+  MLA_ERR_UNSUPPORTED = 2,   /* valid but not implemented combination (dtype / page size) */
+  MLA_ERR_WORKSPACE = 3,     /* workspace smaller than mla_plan_workspace_size() */
+  MLA_ERR_CUDA = 4,          /* a CUDA runtime / driver call failed */
+  MLA_ERR_DEVICE_TIMEOUT = 5 /* a device-side pipeline wait gave up (see mla_decode_check) */
+} mla_status;
+
+typedef enum {
+  MLA_DTYPE_BF16 = 0,
+  MLA_DTYPE_FP8_E4M3 = 1,   /* OCP e4m3fn, used with a per-tensor fp32 scale */
+  MLA_DTYPE_MXFP4 = 2       /* KV only: 288 packed bytes + e8m0 scales per token */
+} mla_dtype;
+
+typedef struct mla_plan mla_plan;
+
+typedef struct {
+  int32_t batch_size;
+  int32_t page_size;
+  int32_t num_ctas;          /* stage-1 grid size */
+  int32_t num_items;         /* work items (request, token range) */
+  int32_t num_partials;      /* split partial results written to the workspace */
+  int32_t num_merge_jobs;    /* requests merged (or zero-filled) by stage 2 */
+  int64_t total_tokens;
+  int64_t total_tiles;       /* 128-token tiles over all requests */
+  size_t workspace_bytes;
+} mla_plan_info;
+
+/*
+ * mla_decode_plan -- build the work partition for one batch shape.
+ *
+ * Plays the role of aiter's get_mla_metadata_v1 on the pages (submission
+ * 668813 cache builders; submission 600081 "v9" persistent path): it reads
+ * only host arrays, so it causes no device synchronisation.
+ *
+ *   kv_indptr_host        [batch_size+1] int32, non-decreasing, in PAGES:
+ *                         request b owns page-table entries
+ *                         kv_indptr[b] .. kv_indptr[b+1]-1.  With
+ *                         page_size == 1 this is a token offset.
+ *   kv_last_page_len_host [batch_size] int32 tokens used in each request's
+ *                         last page (1..page_size), or NULL for full pages.
+ *   batch_size            >= 1.
+ *   page_size             tokens per page: 1, or a power of two >= 8.
+ *                         page_size 1 requires the identity page table
+ *                         (kv_indices == NULL at run time).
+ *   q_dtype               MLA_DTYPE_BF16 or MLA_DTYPE_FP8_E4M3.
+ *   kv_dtype              MLA_DTYPE_BF16, MLA_DTYPE_FP8_E4M3 or MLA_DTYPE_MXFP4.
+ *   num_splits            0: the planner balances 128-token tiles over the
+ *                         CTAs (a request may be cut anywhere on a tile
+ *                         boundary); S > 0: every request is cut into S
+ *                         contiguous ranges of ceil(tiles/S) tiles, one CTA
+ *                         each, as the pages' fixed-split kernels do.
+ *   num_sms               CTAs of the balanced plan; 0 = the SM count of the
+ *                         current CUDA device.
+ *   plan_out              receives the new plan (library-owned).
+ * Errors: MLA_ERR_INVALID_ARG (null/negative/non-monotone input, bad
+ * last-page length), MLA_ERR_UNSUPPORTED (dtype or page size combination not
+ * implemented), MLA_ERR_CUDA (device query failed when num_sms == 0).
+ */
+mla_status mla_decode_plan(const int32_t* kv_indptr_host, const int32_t* kv_last_page_len_host,
+                           int32_t batch_size, int32_t page_size, mla_dtype q_dtype,
+                           mla_dtype kv_dtype, int32_t num_splits, int32_t num_sms,
+                           mla_plan** plan_out);
+
+/* Bytes of device workspace mla_decode_run needs for this plan (work table,
+ * split partials, error word).  Errors: MLA_ERR_INVALID_ARG on NULL. */
+mla_status mla_plan_workspace_size(const mla_plan* plan, size_t* bytes);
+
+/* Summary numbers of a plan.  Errors: MLA_ERR_INVALID_ARG on NULL. */
+mla_status mla_plan_get_info(const mla_plan* plan, mla_plan_info* info);
+
+/*
+ * Copies the host work table out for inspection: cta_indptr [num_ctas+1]
+ * int32 (items of CTA i are cta_indptr[i] .. cta_indptr[i+1]-1) and items
+ * [num_items][4] int32 = {request, first token, end token, partial slot or -1
+ * for a request written directly}.  Either pointer may be NULL.
+ */
+mla_status mla_plan_get_work(const mla_plan* plan, int32_t* cta_indptr, int32_t* items);
+
+void mla_plan_destroy(mla_plan* plan);
+
+/*
+ * mla_decode_run -- one decode call (stage-1 split kernel + stage-2 merge),
+ * enqueued on `stream`.  The role of aiter's mla_decode_fwd on the pages.
+ *
+ *   q          [batch,16,576] contiguous, bf16 or e4m3 bytes (plan's q_dtype);
+ *              16-byte aligned.
+ *   q_scale    device fp32 [1]; required when q is e4m3, ignored otherwise.
+ *   kv         KV pool, kv_pool_rows rows of 576 bf16 / 576 e4m3 bytes /
+ *              288 packed MXFP4 bytes, contiguous; row r of page p is
+ *              p*page_size + r.  16-byte aligned.
+ *   kv_scale   device fp32 [1]; required for e4m3 KV, ignored otherwise.
+ *   kv_e8m0, kv_e8m0_row_stride
+ *              MXFP4 only: e8m0 scale rows (>= 18 bytes each, row stride in
+ *              bytes); NULL / ignored for other KV types.
+ *   kv_pool_rows  number of rows in the KV pool (bounds every access).
+ *   kv_indices device int32 page table, indexed from kv_indptr; NULL = the
+ *              identity table (request b's pages are kv_indptr[b]..).
+ *              Every entry must be a page inside the pool.
+ *   workspace, workspace_bytes
+ *              device scratch of at least mla_plan_workspace_size() bytes,
+ *              256-byte aligned.  The work table is copied into it on the
+ *              first run with a given workspace pointer (one host-to-device
+ *              copy on `stream`); afterwards runs only launch kernels.  A
+ *              workspace belongs to one plan.
+ *   out        [batch,16,512] bf16, 16-byte aligned.
+ *   lse        [batch,16] fp32 natural-log LSE of the scaled scores, or NULL.
+ *              Empty requests give out = 0 and lse = -inf.
+ * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_WORKSPACE, MLA_ERR_UNSUPPORTED,
+ * MLA_ERR_CUDA (launch failure; the stream state is then the caller's).
+ */
+mla_status mla_decode_run(mla_plan* plan, const void* q, const float* q_scale, const void* kv,
+                          const float* kv_scale, const uint8_t* kv_e8m0,
+                          int64_t kv_e8m0_row_stride, int64_t kv_pool_rows,
+                          const int32_t* kv_indices, void* workspace, size_t workspace_bytes,
+                          void* out, float* lse, mla_stream_t stream);
+
+/*
+ * Synchronises `stream`, reads the workspace's device error word and clears
+ * it.  Returns MLA_OK, MLA_ERR_DEVICE_TIMEOUT if a kernel's bounded
+ * pipeline wait gave up since the last check, or MLA_ERR_CUDA.
+ */
+mla_status mla_decode_check(const mla_plan* plan, void* workspace, mla_stream_t stream);
+
+/*
+ * Optional instrumentation (the pages time their decode stages with CUDA
+ * events, submission 695854, stage timings): when `before` / `after` are
+ * non-NULL cudaEvent_t handles, every following mla_decode_run records
+ * `before` on its stream just before the stage-1 launch and `after` just
+ * after it.  Pass NULL, NULL to stop.  The events stay owned by the caller.
+ * Errors: MLA_ERR_INVALID_ARG on a NULL plan.
+ */
+mla_status mla_plan_set_stage1_events(mla_plan* plan, void* before, void* after);
+
+/* Static, human-readable name of a status code. */
+const char* mla_status_string(mla_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_DECODE_H_ */

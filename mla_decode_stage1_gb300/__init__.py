@@ -1,0 +1,200 @@
+"""Python binding of libmla_decode (single-token MLA decode for GB300, sm_103a).
+
+Argument marshalling only: every step of the decode runs in the library's
+CUDA kernels.  The names mirror the C ABI in include/mla_decode.h:
+``mla_decode_plan``, ``mla_decode_run``, ``mla_decode_check``,
+``mla_status_string``.  PyTorch tensors are accepted for device memory and
+``torch.cuda`` streams; there is no CPU fallback -- importing this package
+fails loudly when the shared library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libmla_decode.so")
+
+HEADS, QK_DIM, V_DIM, TILE = 16, 576, 512, 128
+DTYPES = {"bf16": 0, "fp8": 1, "mxfp4": 2}
+STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED", 3: "MLA_ERR_WORKSPACE",
+          4: "MLA_ERR_CUDA", 5: "MLA_ERR_DEVICE_TIMEOUT"}
+EXPORTS = ("mla_decode_plan", "mla_plan_workspace_size", "mla_plan_get_info", "mla_plan_get_work",
+           "mla_plan_destroy", "mla_decode_run", "mla_decode_check", "mla_status_string",
+           "mla_plan_set_stage1_events")
+
+
+class MlaError(RuntimeError):
+    def __init__(self, call: str, status: int):
+        super().__init__(f"{call} failed: {STATUS.get(status, status)}")
+        self.status = status
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("batch_size", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("num_ctas", ctypes.c_int32), ("num_items", ctypes.c_int32),
+                ("num_partials", ctypes.c_int32), ("num_merge_jobs", ctypes.c_int32),
+                ("total_tokens", ctypes.c_int64), ("total_tiles", ctypes.c_int64),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with "
+                          "`python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    lib.mla_decode_plan.argtypes = [P, P, i32, i32, ctypes.c_int, ctypes.c_int, i32, i32,
+                                    ctypes.POINTER(P)]
+    lib.mla_plan_workspace_size.argtypes = [P, ctypes.POINTER(sz)]
+    lib.mla_plan_get_info.argtypes = [P, ctypes.POINTER(PlanInfo)]
+    lib.mla_plan_get_work.argtypes = [P, P, P]
+    lib.mla_plan_destroy.argtypes = [P]
+    lib.mla_plan_destroy.restype = None
+    lib.mla_decode_run.argtypes = [P, P, P, P, P, P, i64, i64, P, P, sz, P, P, P]
+    lib.mla_decode_check.argtypes = [P, P, P]
+    lib.mla_plan_set_stage1_events.argtypes = [P, P, P]
+    lib.mla_status_string.argtypes = [ctypes.c_int]
+    lib.mla_status_string.restype = ctypes.c_char_p
+    for name in ("mla_decode_plan", "mla_plan_workspace_size", "mla_plan_get_info",
+                 "mla_plan_get_work", "mla_decode_run", "mla_decode_check",
+                 "mla_plan_set_stage1_events"):
+        getattr(lib, name).restype = ctypes.c_int
+    return lib
+
+
+_lib = _load()
+
+
+def mla_status_string(status: int) -> str:
+    return _lib.mla_status_string(int(status)).decode()
+
+
+def _check(call, status):
+    if status != 0:
+        raise MlaError(call, status)
+
+
+def _i32_array(x):
+    import numpy as np
+    if x is None:
+        return None, None
+    if hasattr(x, "detach"):
+        x = x.detach().cpu().numpy()
+    a = np.ascontiguousarray(x, dtype=np.int32)
+    return a, a.ctypes.data_as(ctypes.c_void_p)
+
+
+class Plan:
+    """Owns an mla_plan* (host object)."""
+
+    def __init__(self, handle, q_dtype, kv_dtype, page_size):
+        self._h = handle
+        self.q_dtype, self.kv_dtype, self.page_size = q_dtype, kv_dtype, page_size
+
+    @property
+    def handle(self):
+        return self._h
+
+    def info(self) -> PlanInfo:
+        info = PlanInfo()
+        _check("mla_plan_get_info", _lib.mla_plan_get_info(self._h, ctypes.byref(info)))
+        return info
+
+    @property
+    def workspace_bytes(self) -> int:
+        n = ctypes.c_size_t()
+        _check("mla_plan_workspace_size", _lib.mla_plan_workspace_size(self._h, ctypes.byref(n)))
+        return n.value
+
+    def work(self):
+        """(cta_indptr [num_ctas+1], items [num_items,4]) as numpy int32."""
+        import numpy as np
+        inf = self.info()
+        ind = np.zeros(inf.num_ctas + 1, np.int32)
+        items = np.zeros((inf.num_items, 4), np.int32)
+        _check("mla_plan_get_work", _lib.mla_plan_get_work(
+            self._h, ind.ctypes.data_as(ctypes.c_void_p), items.ctypes.data_as(ctypes.c_void_p)))
+        return ind, items
+
+    def set_stage1_events(self, before=None, after=None):
+        """torch.cuda.Event objects (or None) recorded around each stage-1 launch."""
+        b = None if before is None else ctypes.c_void_p(before.cuda_event)
+        a = None if after is None else ctypes.c_void_p(after.cuda_event)
+        _check("mla_plan_set_stage1_events", _lib.mla_plan_set_stage1_events(self._h, b, a))
+
+    def __del__(self):
+        if getattr(self, "_h", None):
+            _lib.mla_plan_destroy(self._h)
+            self._h = None
+
+
+def mla_decode_plan(kv_indptr, kv_last_page_len=None, *, page_size: int, q_dtype: str,
+                    kv_dtype: str, num_splits: int = 0, num_sms: int = 0,
+                    batch_size: int | None = None) -> Plan:
+    """Plan a batch from the HOST kv_indptr (in pages) and optional last-page
+    lengths.  num_sms=0 queries the current CUDA device."""
+    ind, ind_p = _i32_array(kv_indptr)
+    last, last_p = _i32_array(kv_last_page_len)
+    bs = len(ind) - 1 if batch_size is None else int(batch_size)
+    h = ctypes.c_void_p()
+    _check("mla_decode_plan", _lib.mla_decode_plan(ind_p, last_p, bs, int(page_size),
+                                                   DTYPES[q_dtype], DTYPES[kv_dtype],
+                                                   int(num_splits), int(num_sms), ctypes.byref(h)))
+    plan = Plan(h, q_dtype, kv_dtype, int(page_size))
+    plan._keep = (ind, last)
+    return plan
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def mla_decode_run(plan: Plan, q, kv, out, *, workspace, q_scale=None, kv_scale=None,
+                   kv_e8m0=None, kv_indices=None, lse=None, kv_pool_rows: int | None = None,
+                   stream=None) -> None:
+    """Enqueue one decode on `stream` (default: torch's current stream).
+
+    q [bs,16,576] bf16 or uint8 (e4m3 bytes); kv [rows,576] bf16 / uint8 e4m3
+    bytes, or [rows,288] uint8 packed MXFP4; out [bs,16,512] bf16; lse
+    [bs,16] fp32 or None; workspace a uint8 CUDA tensor of at least
+    plan.workspace_bytes; scales are fp32 CUDA tensors of one element.
+    """
+    for name, t in (("q", q), ("kv", kv), ("out", out), ("workspace", workspace)):
+        if t is None or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    rows = int(kv.shape[0]) if kv_pool_rows is None else int(kv_pool_rows)
+    stride = 0 if kv_e8m0 is None else int(kv_e8m0.stride(0))
+    status = _lib.mla_decode_run(plan.handle, _ptr(q), _ptr(q_scale), _ptr(kv), _ptr(kv_scale),
+                                 _ptr(kv_e8m0), stride, rows, _ptr(kv_indices), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _ptr(out),
+                                 _ptr(lse), _stream_ptr(stream))
+    _check("mla_decode_run", status)
+
+
+def mla_decode_check(plan: Plan, workspace, stream=None) -> None:
+    """Synchronise and raise MlaError if a device-side wait gave up."""
+    _check("mla_decode_check", _lib.mla_decode_check(plan.handle, _ptr(workspace),
+                                                     _stream_ptr(stream)))
+
+
+class MlaDecoder:
+    """Convenience owner of a plan and its workspace for one batch shape."""
+
+    def __init__(self, kv_indptr, kv_last_page_len=None, *, page_size, q_dtype, kv_dtype,
+                 num_splits=0, device="cuda"):
+        import torch
+        self.plan = mla_decode_plan(kv_indptr, kv_last_page_len, page_size=page_size,
+                                    q_dtype=q_dtype, kv_dtype=kv_dtype, num_splits=num_splits)
+        self.workspace = torch.empty(max(self.plan.workspace_bytes, 256), dtype=torch.uint8,
+                                     device=device)
+
+    def __call__(self, q, kv, out, **kw):
+        mla_decode_run(self.plan, q, kv, out, workspace=self.workspace, **kw)
+        return out

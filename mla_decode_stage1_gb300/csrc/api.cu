@@ -1,0 +1,401 @@
+// api.cu -- host side of libmla_decode: argument validation, the work
+// planner, workspace layout, TMA descriptor set-up and the kernel launches.
+// The C declarations and their contracts are in include/mla_decode.h.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/mla_decode.h"
+#include "kernels.h"
+
+using mla::MergeJob;
+using mla::WorkItem;
+
+struct mla_plan {
+  int32_t bs = 0, page_size = 0, num_splits = 0;
+  int q_dtype = 0, kv_dtype = 0, qmode = 0;
+  int32_t num_ctas = 0, num_partials = 0;
+  int64_t total_tokens = 0, total_tiles = 0;
+  std::vector<int32_t> cta_indptr;
+  std::vector<WorkItem> items;
+  std::vector<MergeJob> jobs;
+  // workspace layout (byte offsets)
+  size_t off_err = 0, off_indptr = 0, off_items = 0, off_jobs = 0, off_part_o = 0,
+         off_part_lse = 0, ws_bytes = 0;
+  std::vector<uint8_t> table;  // image of [0, off_part_o) uploaded once per workspace
+  // per-run caches
+  void* uploaded_ws = nullptr;
+  CUtensorMap tmap;
+  const void* tmap_ptr = nullptr;
+  int64_t tmap_rows = -1;
+  int32_t tmap_box_rows = -1;
+  cudaEvent_t ev_before = nullptr, ev_after = nullptr;
+};
+
+namespace {
+
+constexpr size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
+
+int qmode_of(int q_dtype, int kv_dtype) {
+  if (q_dtype == MLA_DTYPE_BF16 && kv_dtype == MLA_DTYPE_BF16) return mla::kQBf16KvBf16;
+  if (q_dtype == MLA_DTYPE_FP8_E4M3 && kv_dtype == MLA_DTYPE_FP8_E4M3) return mla::kQFp8KvFp8;
+  if (q_dtype == MLA_DTYPE_BF16 && kv_dtype == MLA_DTYPE_FP8_E4M3) return mla::kQBf16KvFp8;
+  if (q_dtype == MLA_DTYPE_FP8_E4M3 && kv_dtype == MLA_DTYPE_BF16) return mla::kQFp8KvBf16;
+  return -1;
+}
+
+// Items of the balanced plan: the T tiles of all requests, in request order,
+// cut into G nearly equal contiguous ranges (one per CTA).
+void plan_balanced(mla_plan* P, const std::vector<int64_t>& tiles, const std::vector<int32_t>& len,
+                   const std::vector<int32_t>& page_base, const std::vector<int32_t>& npages,
+                   int32_t G) {
+  const int64_t T = P->total_tiles;
+  P->num_ctas = G;
+  P->cta_indptr.assign(1, 0);
+  int32_t b = 0;
+  int64_t in_req = 0;  // tiles of request b already assigned
+  for (int32_t i = 0; i < G; ++i) {
+    int64_t need = (T * (i + 1)) / G - (T * i) / G;
+    while (need > 0) {
+      while (tiles[b] - in_req == 0) { ++b; in_req = 0; }
+      const int64_t take = std::min(need, tiles[b] - in_req);
+      WorkItem w{};
+      w.b = b;
+      w.tok_begin = static_cast<int32_t>(in_req * mla::kTile);
+      w.tok_end = static_cast<int32_t>(std::min<int64_t>((in_req + take) * mla::kTile, len[b]));
+      w.slot = 0;
+      w.page_base = page_base[b];
+      w.npages = npages[b];
+      P->items.push_back(w);
+      in_req += take;
+      need -= take;
+    }
+    P->cta_indptr.push_back(static_cast<int32_t>(P->items.size()));
+  }
+}
+
+// Items of the fixed-split plan: request b cut into S ranges of
+// ceil(tiles_b / S) tiles; one CTA per non-empty range.
+void plan_fixed(mla_plan* P, const std::vector<int64_t>& tiles, const std::vector<int32_t>& len,
+                const std::vector<int32_t>& page_base, const std::vector<int32_t>& npages,
+                int32_t S) {
+  P->cta_indptr.assign(1, 0);
+  for (int32_t b = 0; b < P->bs; ++b) {
+    const int64_t per = (tiles[b] + S - 1) / S;
+    for (int32_t s = 0; s < S && per > 0; ++s) {
+      const int64_t t0 = per * s, t1 = std::min<int64_t>(per * (s + 1), tiles[b]);
+      if (t1 <= t0) continue;
+      WorkItem w{};
+      w.b = b;
+      w.tok_begin = static_cast<int32_t>(t0 * mla::kTile);
+      w.tok_end = static_cast<int32_t>(std::min<int64_t>(t1 * mla::kTile, len[b]));
+      w.page_base = page_base[b];
+      w.npages = npages[b];
+      P->items.push_back(w);
+      P->cta_indptr.push_back(static_cast<int32_t>(P->items.size()));
+    }
+  }
+  P->num_ctas = static_cast<int32_t>(P->items.size());
+}
+
+// Partial slots (consecutive per split request), direct writes and merge jobs.
+void assign_slots(mla_plan* P, const std::vector<int32_t>& len) {
+  std::vector<int32_t> nitems(P->bs, 0);
+  for (const WorkItem& w : P->items) nitems[w.b]++;
+  std::vector<int32_t> first(P->bs, -1);
+  int32_t next = 0;
+  for (int32_t b = 0; b < P->bs; ++b) {
+    if (nitems[b] >= 2) {
+      first[b] = next;
+      P->jobs.push_back(MergeJob{b, next, nitems[b], 0});
+      next += nitems[b];
+    } else if (len[b] == 0) {
+      P->jobs.push_back(MergeJob{b, 0, 0, 0});
+    }
+  }
+  std::vector<int32_t> used(P->bs, 0);
+  for (WorkItem& w : P->items) w.slot = (nitems[w.b] >= 2) ? first[w.b] + used[w.b]++ : -1;
+  P->num_partials = next;
+}
+
+void layout_workspace(mla_plan* P) {
+  size_t off = 0;
+  P->off_err = off;
+  off = align256(off + 16);
+  P->off_indptr = off;
+  off = align256(off + sizeof(int32_t) * P->cta_indptr.size());
+  P->off_items = off;
+  off = align256(off + sizeof(WorkItem) * P->items.size());
+  P->off_jobs = off;
+  off = align256(off + sizeof(MergeJob) * P->jobs.size());
+  P->off_part_o = off;
+  off = align256(off + sizeof(float) * static_cast<size_t>(P->num_partials) * mla::kHeads * mla::kVDim);
+  P->off_part_lse = off;
+  off = align256(off + sizeof(float) * static_cast<size_t>(P->num_partials) * mla::kHeads);
+  P->ws_bytes = std::max<size_t>(off, 256);
+  P->table.assign(P->off_part_o, 0);
+  std::memcpy(P->table.data() + P->off_indptr, P->cta_indptr.data(),
+              sizeof(int32_t) * P->cta_indptr.size());
+  if (!P->items.empty())
+    std::memcpy(P->table.data() + P->off_items, P->items.data(), sizeof(WorkItem) * P->items.size());
+  if (!P->jobs.empty())
+    std::memcpy(P->table.data() + P->off_jobs, P->jobs.data(), sizeof(MergeJob) * P->jobs.size());
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// KV pool as a 2-D tensor [pool_rows, 576 elements]; boxes of 128 bytes x
+// box_rows rows with the 128-byte swizzle; out-of-bounds reads fill zeros.
+bool make_kv_map(CUtensorMap* map, const void* kv, int kv_dtype, int64_t rows, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const bool b16 = kv_dtype == MLA_DTYPE_BF16;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(mla::kQkDim), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(mla::kQkDim * (b16 ? 2 : 1))};
+  const cuuint32_t box[2] = {b16 ? 64u : 128u, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, b16 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+             const_cast<void*>(kv), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+mla_status mla_decode_plan(const int32_t* kv_indptr_host, const int32_t* kv_last_page_len_host,
+                           int32_t batch_size, int32_t page_size, mla_dtype q_dtype,
+                           mla_dtype kv_dtype, int32_t num_splits, int32_t num_sms,
+                           mla_plan** plan_out) {
+  if (plan_out == nullptr) return MLA_ERR_INVALID_ARG;
+  *plan_out = nullptr;
+  if (kv_indptr_host == nullptr || batch_size < 1 || page_size < 1 || num_splits < 0 ||
+      num_sms < 0)
+    return MLA_ERR_INVALID_ARG;
+  if (q_dtype < MLA_DTYPE_BF16 || q_dtype > MLA_DTYPE_MXFP4 || kv_dtype < MLA_DTYPE_BF16 ||
+      kv_dtype > MLA_DTYPE_MXFP4)
+    return MLA_ERR_INVALID_ARG;
+  const int qmode = qmode_of(q_dtype, kv_dtype);
+  if (qmode < 0) return MLA_ERR_UNSUPPORTED;
+  if (kv_indptr_host[0] < 0) return MLA_ERR_INVALID_ARG;
+  std::vector<int32_t> len(batch_size), page_base(batch_size), npages(batch_size);
+  std::vector<int64_t> tiles(batch_size);
+  int64_t total_tok = 0, total_tiles = 0;
+  for (int32_t b = 0; b < batch_size; ++b) {
+    const int64_t np = static_cast<int64_t>(kv_indptr_host[b + 1]) - kv_indptr_host[b];
+    if (np < 0) return MLA_ERR_INVALID_ARG;
+    int64_t n = np * page_size;
+    if (np > 0 && kv_last_page_len_host != nullptr) {
+      const int32_t last = kv_last_page_len_host[b];
+      if (last < 1 || last > page_size) return MLA_ERR_INVALID_ARG;
+      n -= page_size - last;
+    }
+    if (n > INT32_MAX - mla::kTile) return MLA_ERR_INVALID_ARG;
+    len[b] = static_cast<int32_t>(n);
+    page_base[b] = kv_indptr_host[b];
+    npages[b] = static_cast<int32_t>(np);
+    tiles[b] = (n + mla::kTile - 1) / mla::kTile;
+    total_tok += n;
+    total_tiles += tiles[b];
+  }
+  if (num_sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return MLA_ERR_CUDA;
+  }
+  mla_plan* P = new (std::nothrow) mla_plan();
+  if (P == nullptr) return MLA_ERR_INVALID_ARG;
+  P->bs = batch_size;
+  P->page_size = page_size;
+  P->num_splits = num_splits;
+  P->q_dtype = q_dtype;
+  P->kv_dtype = kv_dtype;
+  P->qmode = qmode;
+  P->total_tokens = total_tok;
+  P->total_tiles = total_tiles;
+  if (num_splits == 0) {
+    const int32_t G = static_cast<int32_t>(std::min<int64_t>(num_sms, total_tiles));
+    if (G > 0) plan_balanced(P, tiles, len, page_base, npages, G);
+    else P->cta_indptr.assign(1, 0);
+  } else {
+    plan_fixed(P, tiles, len, page_base, npages, num_splits);
+  }
+  assign_slots(P, len);
+  layout_workspace(P);
+  *plan_out = P;
+  return MLA_OK;
+}
+
+mla_status mla_plan_workspace_size(const mla_plan* plan, size_t* bytes) {
+  if (plan == nullptr || bytes == nullptr) return MLA_ERR_INVALID_ARG;
+  *bytes = plan->ws_bytes;
+  return MLA_OK;
+}
+
+mla_status mla_plan_get_info(const mla_plan* plan, mla_plan_info* info) {
+  if (plan == nullptr || info == nullptr) return MLA_ERR_INVALID_ARG;
+  info->batch_size = plan->bs;
+  info->page_size = plan->page_size;
+  info->num_ctas = plan->num_ctas;
+  info->num_items = static_cast<int32_t>(plan->items.size());
+  info->num_partials = plan->num_partials;
+  info->num_merge_jobs = static_cast<int32_t>(plan->jobs.size());
+  info->total_tokens = plan->total_tokens;
+  info->total_tiles = plan->total_tiles;
+  info->workspace_bytes = plan->ws_bytes;
+  return MLA_OK;
+}
+
+mla_status mla_plan_get_work(const mla_plan* plan, int32_t* cta_indptr, int32_t* items) {
+  if (plan == nullptr) return MLA_ERR_INVALID_ARG;
+  if (cta_indptr != nullptr)
+    std::memcpy(cta_indptr, plan->cta_indptr.data(), sizeof(int32_t) * plan->cta_indptr.size());
+  if (items != nullptr)
+    for (size_t i = 0; i < plan->items.size(); ++i) {
+      items[4 * i + 0] = plan->items[i].b;
+      items[4 * i + 1] = plan->items[i].tok_begin;
+      items[4 * i + 2] = plan->items[i].tok_end;
+      items[4 * i + 3] = plan->items[i].slot;
+    }
+  return MLA_OK;
+}
+
+void mla_plan_destroy(mla_plan* plan) { delete plan; }
+
+mla_status mla_decode_run(mla_plan* plan, const void* q, const float* q_scale, const void* kv,
+                          const float* kv_scale, const uint8_t* kv_e8m0,
+                          int64_t kv_e8m0_row_stride, int64_t kv_pool_rows,
+                          const int32_t* kv_indices, void* workspace, size_t workspace_bytes,
+                          void* out, float* lse, mla_stream_t stream_) {
+  (void)kv_e8m0;
+  (void)kv_e8m0_row_stride;
+  if (plan == nullptr || q == nullptr || kv == nullptr || out == nullptr || workspace == nullptr)
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(out, 16) || !aligned(workspace, 256))
+    return MLA_ERR_INVALID_ARG;
+  if (kv_pool_rows < 1 || kv_pool_rows > INT32_MAX) return MLA_ERR_INVALID_ARG;
+  if (plan->q_dtype == MLA_DTYPE_FP8_E4M3 && q_scale == nullptr) return MLA_ERR_INVALID_ARG;
+  if (plan->kv_dtype == MLA_DTYPE_FP8_E4M3 && kv_scale == nullptr) return MLA_ERR_INVALID_ARG;
+  if (workspace_bytes < plan->ws_bytes) return MLA_ERR_WORKSPACE;
+  int box_rows = mla::kTile;
+  if (kv_indices != nullptr) {
+    // A page table needs whole 1024-byte swizzle atoms per page.
+    if (!is_pow2(plan->page_size) || plan->page_size < 8) return MLA_ERR_UNSUPPORTED;
+    box_rows = std::min(plan->page_size, mla::kTile);
+    if (kv_pool_rows % plan->page_size != 0) return MLA_ERR_INVALID_ARG;
+  }
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (plan->tmap_ptr != kv || plan->tmap_rows != kv_pool_rows || plan->tmap_box_rows != box_rows) {
+    if (!make_kv_map(&plan->tmap, kv, plan->kv_dtype, kv_pool_rows, box_rows)) return MLA_ERR_CUDA;
+    plan->tmap_ptr = kv;
+    plan->tmap_rows = kv_pool_rows;
+    plan->tmap_box_rows = box_rows;
+  }
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (plan->uploaded_ws != workspace) {
+    if (cudaMemcpyAsync(ws, plan->table.data(), plan->table.size(), cudaMemcpyHostToDevice,
+                        stream) != cudaSuccess)
+      return MLA_ERR_CUDA;
+    plan->uploaded_ws = workspace;
+  }
+  float* part_o = reinterpret_cast<float*>(ws + plan->off_part_o);
+  float* part_lse = reinterpret_cast<float*>(ws + plan->off_part_lse);
+  int32_t* err = reinterpret_cast<int32_t*>(ws + plan->off_err);
+  if (plan->num_ctas > 0) {
+    mla::Stage1Params p{};
+    p.tmap_kv = plan->tmap;
+    p.q = q;
+    p.q_scale = q_scale;
+    p.kv_scale = kv_scale;
+    p.kv_indices = kv_indices;
+    p.items = reinterpret_cast<const WorkItem*>(ws + plan->off_items);
+    p.cta_indptr = reinterpret_cast<const int32_t*>(ws + plan->off_indptr);
+    p.part_o = part_o;
+    p.part_lse = part_lse;
+    p.out = static_cast<uint16_t*>(out);
+    p.lse = lse;
+    p.err = err;
+    p.page_size = plan->page_size;
+    p.box_rows = box_rows;
+    p.pool_rows = kv_pool_rows;
+    if (plan->ev_before != nullptr && cudaEventRecord(plan->ev_before, stream) != cudaSuccess)
+      return MLA_ERR_CUDA;
+    if (mla::launch_stage1(plan->qmode, p, plan->num_ctas, stream) != cudaSuccess)
+      return MLA_ERR_CUDA;
+    if (plan->ev_after != nullptr && cudaEventRecord(plan->ev_after, stream) != cudaSuccess)
+      return MLA_ERR_CUDA;
+  }
+  if (!plan->jobs.empty()) {
+    mla::Stage2Params s{};
+    s.jobs = reinterpret_cast<const MergeJob*>(ws + plan->off_jobs);
+    s.part_o = part_o;
+    s.part_lse = part_lse;
+    s.out = static_cast<uint16_t*>(out);
+    s.lse = lse;
+    s.num_jobs = static_cast<int32_t>(plan->jobs.size());
+    if (mla::launch_stage2(s, stream) != cudaSuccess) return MLA_ERR_CUDA;
+  }
+  return MLA_OK;
+}
+
+mla_status mla_decode_check(const mla_plan* plan, void* workspace, mla_stream_t stream_) {
+  if (plan == nullptr || workspace == nullptr) return MLA_ERR_INVALID_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  int32_t word = 0;
+  int32_t* dev = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + plan->off_err);
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MLA_ERR_CUDA;
+  if (cudaMemcpy(&word, dev, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  if (word == 0) return MLA_OK;
+  if (cudaMemset(dev, 0, sizeof(word)) != cudaSuccess) return MLA_ERR_CUDA;
+  return (word & ~mla::kErrBadPage) ? MLA_ERR_DEVICE_TIMEOUT : MLA_ERR_INVALID_ARG;
+}
+
+mla_status mla_plan_set_stage1_events(mla_plan* plan, void* before, void* after) {
+  if (plan == nullptr) return MLA_ERR_INVALID_ARG;
+  plan->ev_before = static_cast<cudaEvent_t>(before);
+  plan->ev_after = static_cast<cudaEvent_t>(after);
+  return MLA_OK;
+}
+
+const char* mla_status_string(mla_status status) {
+  switch (status) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED";
+    case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
+    case MLA_ERR_DEVICE_TIMEOUT: return "MLA_ERR_DEVICE_TIMEOUT";
+  }
+  return "MLA_ERR_UNKNOWN";
+}
+
+}  // extern "C"

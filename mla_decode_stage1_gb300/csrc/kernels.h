@@ -1,0 +1,88 @@
+// kernels.h -- internal interface between the host API (api.cu) and the two
+// CUDA kernels (stage1.cu, stage2.cu).  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace mla {
+
+constexpr int kHeads = 16;     // query heads per request, one latent KV head
+constexpr int kQkDim = 576;    // 512 latent + 64 rope dims take part in QK^T
+constexpr int kVDim = 512;     // V = the first 512 dims of the latent row
+constexpr int kTile = 128;     // tokens per stage-1 tile (UMMA M)
+
+// Scores are kept in the log2 domain: s2 = s * log2(e).  p = 2^(s2 - m + kPOff)
+// with m the running max, allowed to lag the true max by at most kTau.
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kPOff = 4.0f;
+constexpr float kTau = 4.0f;
+constexpr float kPLoScale = 16.0f;    // the low part of p is stored x2^4
+// (p <= 2^(kPOff+kTau) = 256, so |p - e4m3(p)| * 16 <= 256 <= 448)
+
+// Device error word bits (one per pipeline role that gave up a wait).
+enum : int32_t {
+  kErrProducer = 1, kErrMma = 2, kErrSoftmax = 4, kErrQPrep = 8, kErrDrain = 16,
+  kErrBadPage = 32
+};
+
+// One work item: a contiguous token range of one request.
+struct WorkItem {
+  int32_t b;          // request
+  int32_t tok_begin;  // first token (multiple of kTile)
+  int32_t tok_end;    // one past the last token
+  int32_t slot;       // partial slot, or -1: write out/lse directly
+  int32_t page_base;  // kv_indptr[b]: first page-table entry of the request
+  int32_t npages;     // page-table entries of the request
+  int32_t pad0, pad1;
+};
+static_assert(sizeof(WorkItem) == 32, "work item is two int4");
+
+// One stage-2 job: merge `count` consecutive partials of request b (count 0:
+// the request is empty, write zeros and -inf).
+struct MergeJob {
+  int32_t b, first, count, pad;
+};
+
+enum QMode : int {
+  kQBf16KvBf16 = 0,   // kind::f16, B = q (16 rows)
+  kQFp8KvFp8 = 1,     // kind::f8f6f4, B = q bytes (16 rows)
+  kQBf16KvFp8 = 2,    // kind::f8f6f4, B = [q_hi ; q_lo] e4m3 (32 rows)
+  kQFp8KvBf16 = 3     // kind::f16, q decoded to bf16 (exact), B = 16 rows
+};
+
+struct Stage1Params {
+  CUtensorMap tmap_kv;          // [pool_rows, 576] elements, 128-byte boxes, 128B swizzle
+  const void* q;                // [bs,16,576]
+  const float* q_scale;         // device [1] (fp8 q) or null
+  const float* kv_scale;        // device [1] (fp8 kv) or null
+  const int32_t* kv_indices;    // page table or null (identity)
+  const WorkItem* items;
+  const int32_t* cta_indptr;
+  float* part_o;                // [num_partials,16,512] fp32, normalised
+  float* part_lse;              // [num_partials,16] log2 domain
+  uint16_t* out;                // [bs,16,512] bf16 bits
+  float* lse;                   // [bs,16] natural log, nullable
+  int32_t* err;                 // device error word
+  int32_t page_size;
+  int32_t box_rows;             // rows per TMA box: 128 (identity) or page_size
+  int64_t pool_rows;
+};
+
+struct Stage2Params {
+  const MergeJob* jobs;
+  const float* part_o;
+  const float* part_lse;
+  uint16_t* out;
+  float* lse;
+  int32_t num_jobs;
+};
+
+// Host launchers; return the cudaError_t of the launch.
+cudaError_t launch_stage1(int qmode, const Stage1Params& p, int num_ctas, cudaStream_t stream);
+cudaError_t launch_stage2(const Stage2Params& p, cudaStream_t stream);
+int stage1_smem_bytes(int qmode);
+
+}  // namespace mla

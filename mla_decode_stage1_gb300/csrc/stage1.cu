@@ -1,0 +1,729 @@
+// stage1.cu -- split-KV stage-1 kernel of MLA decode for sm_103a.
+//
+// What it computes (kernelindex.com, amd-mixed-mla submission 668813, MXFP4
+// qh16 stage-1 kernel; submission 695854, fp8 split stage-1 kernel): for one
+// token range of one request and all 16 heads at once, the scores
+// s = q . k^T * (1/sqrt(576)) over 576 dims, an exp2-domain online softmax,
+// and the partial output O = softmax(s) . V with V the first 512 dims of the
+// same rows, plus the log-sum-exp of the range.
+//
+// How (GB300-first, not the pages' Triton design):
+//  * one persistent CTA per SM walks a planner-built list of work items; the
+//    KV rows stream HBM -> shared memory through 2-D TMA boxes (128-byte
+//    swizzle) into a ring of 128-token x 128-dim slots guarded by mbarriers;
+//  * QK^T runs on the 5th-generation tensor cores with the tokens as M:
+//    S^T[128 tok x 16 heads] = K[128 x 576] . Q^T, accumulated in TMEM;
+//  * PV reuses the very same shared-memory bytes as an MN-major operand:
+//    O^T[512 x 16] += V^T[512 x 128 tok] . P^T, four M=128 blocks in TMEM;
+//  * warp roles: warp 0 TMA producer, warp 1 UMMA issuer (+ TMEM owner),
+//    warps 2-3 prepare q for the next item, warps 4-7 do the softmax and the
+//    epilogue (one thread per token / per output dim, TMEM lane = thread);
+//  * every mbarrier wait is bounded (see mbar_wait) and reports into the
+//    device error word instead of hanging.
+//
+// Precision: fp8 KV is consumed as raw e4m3 bytes by kind::f8f6f4 UMMAs with
+// the per-tensor scales folded into one score factor and into l.  A bf16 q
+// meeting fp8 KV is split into q_hi + q_lo (two e4m3 terms with a per-request
+// scale, ~bf16 precision) that share one UMMA with N = 32.  p is likewise
+// split into p_hi + 2^-4 p_lo e4m3 terms accumulated in two TMEM regions.
+// bf16 KV runs kind::f16 with bf16 q and bf16 p.
+
+#include <cstddef>
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace mla {
+
+template <int QM>
+struct Layout {
+  static constexpr bool kKv8 = (QM == kQFp8KvFp8 || QM == kQBf16KvFp8);
+  static constexpr int kNq = (QM == kQBf16KvFp8) ? 32 : 16;        // UMMA N of QK^T
+  static constexpr int kSlotBytes = kKv8 ? 16384 : 32768;           // 128 tokens x 128 dims
+  static constexpr int kSlotsPerTile = 5;                           // 4 V slots + rope slot
+  static constexpr int kQAtoms = kKv8 ? 5 : 9;                      // 128-byte K atoms of q
+  static constexpr int kQAtomBytes = kNq * 128;
+  static constexpr int kQBytes = kQAtoms * kQAtomBytes;
+  static constexpr int kPBytes = 4096;
+  static constexpr int kMiscBytes = 2048;
+  static constexpr int kMaxSmem = 232448;
+  static constexpr int kNumSlots =
+      (kMaxSmem - 1024 - 2 * kQBytes - 2 * kPBytes - kMiscBytes) / kSlotBytes;
+  // QK^T of tile g+1 is issued before PV of tile g only if the ring holds the
+  // slots of both tiles at once (slots are taken round-robin).
+  static constexpr bool kLookahead = kNumSlots >= 2 * kSlotsPerTile;
+  static constexpr int kQOff = kNumSlots * kSlotBytes;
+  static constexpr int kPOff = kQOff + 2 * kQBytes;
+  static constexpr int kMiscOff = kPOff + 2 * kPBytes;
+  static constexpr int kSmemBytes = kMiscOff + kMiscBytes + 1024;
+  static_assert(kNumSlots >= kSlotsPerTile, "ring too small");
+  static_assert(kSmemBytes <= kMaxSmem, "shared memory over budget");
+  static_assert(kNumSlots <= 16, "barrier table sized for 16 slots");
+};
+
+// Misc region: barriers, reduction scratch, q scales, TMEM address.
+struct Misc {
+  uint64_t full[16], empty[16];
+  uint64_t s_full[2], s_empty[2], p_full[2], pv_done[2], q_full[2], q_empty[2], drain;
+  alignas(16) float red[2][4][16];   // read back as float4
+  float qscale[2][2];
+  float qred[2];
+  uint32_t tmem_base;
+  int32_t abort_sm, abort_qp;   // set by a thread whose bounded wait gave up
+};
+static_assert(sizeof(Misc) <= 2048, "misc region");
+static_assert(offsetof(Misc, red) % 16 == 0, "reduction scratch is read as float4");
+
+// TMEM columns: S^T double buffer [0,64), O_hi^T [64,128), O_lo^T [128,192).
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColS = 0, kColOhi = 64, kColOlo = 128;
+
+// Byte offset of (row, byte x) inside a 128-byte-wide K-major operand with
+// the 128-byte swizzle (8-row / 1024-byte atoms, 16-byte chunks XOR row%8).
+__device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t x) {
+  return (row >> 3) * 1024u + (row & 7u) * 128u + ((((x >> 4) ^ row) & 7u) << 4) + (x & 15u);
+}
+
+// ---------------------------------------------------------------- producer
+template <int QM>
+__device__ void run_producer(const Stage1Params& p, Misc* ms, uint32_t ring, int it0, int it1,
+                             int lane) {
+  using L = Layout<QM>;
+  const uint64_t pol = l2_policy_evict_first();
+  uint32_t q = 0;
+  bool ok = true;
+  const int box_rows = p.box_rows;
+  const uint32_t box_bytes = static_cast<uint32_t>(box_rows) * 128u;
+  for (int it = it0; it < it1 && ok; ++it) {
+    const WorkItem w = p.items[it];
+    for (int t0 = w.tok_begin; t0 < w.tok_end && ok; t0 += kTile) {
+      const int nvalid = min(kTile, w.tok_end - t0);
+      const int nbox = (nvalid + box_rows - 1) / box_rows;   // boxes holding valid tokens
+      int row = 0;
+      if (lane < nbox) {
+        const int pos = t0 + lane * box_rows;
+        if (p.kv_indices != nullptr) {
+          int page = p.kv_indices[w.page_base + pos / p.page_size];
+          if (page < 0 || static_cast<int64_t>(page + 1) * p.page_size > p.pool_rows) {
+            atomicOr(p.err, kErrBadPage);
+            page = 0;
+          }
+          row = page * p.page_size + pos % p.page_size;
+        } else {
+          row = w.page_base * p.page_size + pos;
+        }
+      }
+      for (int c = 0; c < L::kSlotsPerTile; ++c, ++q) {
+        const uint32_t s = q % L::kNumSlots, ph = (q / L::kNumSlots) & 1u;
+        if (lane == 0) ok = mbar_wait(smem_u32(&ms->empty[s]), ph ^ 1u, p.err, kErrProducer);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        const int ncol = L::kKv8 ? 1 : (c < 4 ? 2 : 1);
+        const uint32_t full = smem_u32(&ms->full[s]);
+        if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(nbox * ncol) * box_bytes);
+        __syncwarp();
+        if (lane < nbox) {
+          for (int cb = 0; cb < ncol; ++cb) {
+            const int x = L::kKv8 ? c * 128 : c * 128 + cb * 64;
+            const uint32_t dst = ring + s * L::kSlotBytes + cb * 16384u + lane * box_bytes;
+            tma_load_2d(dst, &p.tmap_kv, full, x, row, pol);
+          }
+        }
+      }
+    }
+  }
+  // Drain: wait (bounded) until the last copies issued into each slot landed.
+  if (lane == 0) {
+    const uint32_t n = q < static_cast<uint32_t>(L::kNumSlots) ? q : L::kNumSlots;
+    for (uint32_t i = 0; i < n; ++i) {
+      const uint32_t qq = q - 1 - i;
+      if (!mbar_wait(smem_u32(&ms->full[qq % L::kNumSlots]), (qq / L::kNumSlots) & 1u, p.err,
+                     kErrDrain))
+        break;
+    }
+  }
+}
+
+// ------------------------------------------------------------- UMMA issuer
+template <int QM>
+__device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint32_t slot_addr, uint32_t qaddr,
+                                         int c) {
+  using L = Layout<QM>;
+  if constexpr (L::kKv8) {
+    constexpr uint32_t idesc = make_idesc(0, 0, false, false, 128, L::kNq);
+    const int ks = (c == 4) ? 2 : 4;                 // rope slot: 64 dims = 2 K-steps
+    const uint32_t qa = qaddr + c * L::kQAtomBytes;
+    for (int kk = 0; kk < ks; ++kk) {
+      const uint64_t a = smem_desc(slot_addr + kk * 32, 16, 1024);
+      const uint64_t b = smem_desc(qa + kk * 32, 16, 1024);
+      umma_f8f6f4(tmem_s, a, b, idesc, (c | kk) != 0);
+    }
+  } else {
+    constexpr uint32_t idesc = make_idesc(1, 1, false, false, 128, 16);
+    const int ks = (c == 4) ? 4 : 8;                 // 16 dims per K-step
+    for (int kk = 0; kk < ks; ++kk) {
+      const uint32_t atom = kk >> 2, koff = (kk & 3) * 32;
+      const uint64_t a = smem_desc(slot_addr + atom * 16384 + koff, 16, 1024);
+      const uint64_t b = smem_desc(qaddr + (2 * c + atom) * L::kQAtomBytes + koff, 16, 1024);
+      umma_f16(tmem_s, a, b, idesc, (c | kk) != 0);
+    }
+  }
+}
+
+template <int QM>
+__device__ __forceinline__ bool issue_pv(const Stage1Params& p, Misc* ms, uint32_t ring,
+                                         uint32_t pbase, uint32_t tmem, uint32_t q0, uint32_t t,
+                                         bool first) {
+  using L = Layout<QM>;
+  const uint32_t pb = t & 1u;
+  if (!mbar_wait(smem_u32(&ms->p_full[pb]), (t >> 1) & 1u, p.err, kErrMma)) return false;
+  tc_fence_after();
+  const uint32_t pa = pbase + pb * L::kPBytes;
+  for (int c = 0; c < 4; ++c) {
+    const uint32_t slot = ring + ((q0 + c) % L::kNumSlots) * L::kSlotBytes;
+    if constexpr (L::kKv8) {
+      constexpr uint32_t idesc = make_idesc(0, 0, true, false, 128, 16);
+      for (int kk = 0; kk < 4; ++kk) {              // 32 tokens per K-step
+        const uint64_t a = smem_desc(slot + kk * 4096, 1024, 1024);
+        const uint64_t bh = smem_desc(pa + kk * 32, 16, 1024);
+        const uint64_t bl = smem_desc(pa + 2048 + kk * 32, 16, 1024);
+        const uint32_t acc = (first && kk == 0) ? 0u : 1u;
+        umma_f8f6f4(tmem + kColOhi + 16 * c, a, bh, idesc, acc);
+        umma_f8f6f4(tmem + kColOlo + 16 * c, a, bl, idesc, acc);
+      }
+    } else {
+      constexpr uint32_t idesc = make_idesc(1, 1, true, false, 128, 16);
+      for (int kk = 0; kk < 8; ++kk) {              // 16 tokens per K-step
+        const uint64_t a = smem_desc(slot + kk * 2048, 16384, 1024);
+        const uint64_t b = smem_desc(pa + (kk >> 2) * 2048 + (kk & 3) * 32, 16, 1024);
+        umma_f16(tmem + kColOhi + 16 * c, a, b, idesc, (first && kk == 0) ? 0u : 1u);
+      }
+    }
+  }
+  tc_commit(smem_u32(&ms->pv_done[pb]));
+  for (int c = 0; c < 4; ++c) tc_commit(smem_u32(&ms->empty[(q0 + c) % L::kNumSlots]));
+  return true;
+}
+
+template <int QM>
+__device__ void run_mma(const Stage1Params& p, Misc* ms, uint32_t ring, uint32_t qbase,
+                        uint32_t pbase, uint32_t tmem, int it0, int it1) {
+  using L = Layout<QM>;
+  uint32_t q = 0, g = 0;
+  bool ok = true;
+  bool pend = false, pend_first = false;
+  uint32_t pend_q = 0, pend_g = 0;
+  int k = 0;
+  for (int it = it0; it < it1 && ok; ++it, ++k) {
+    const WorkItem w = p.items[it];
+    const uint32_t qb = k & 1;
+    if (!mbar_wait(smem_u32(&ms->q_full[qb]), (k >> 1) & 1, p.err, kErrMma)) { ok = false; break; }
+    tc_fence_after();
+    const uint32_t qaddr = qbase + qb * L::kQBytes;
+    const int ntile = (w.tok_end - w.tok_begin + kTile - 1) / kTile;
+    for (int j = 0; j < ntile; ++j) {
+      const uint32_t sb = g & 1u;
+      if (!mbar_wait(smem_u32(&ms->s_empty[sb]), ((g >> 1) & 1u) ^ 1u, p.err, kErrMma)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      for (int c = 0; c < L::kSlotsPerTile; ++c) {
+        const uint32_t qq = q + c, s = qq % L::kNumSlots;
+        if (!mbar_wait(smem_u32(&ms->full[s]), (qq / L::kNumSlots) & 1u, p.err, kErrMma)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_qk<QM>(tmem + kColS + 32 * sb, ring + s * L::kSlotBytes, qaddr, c);
+        if (c == 4) tc_commit(smem_u32(&ms->empty[s]));
+      }
+      if (!ok) break;
+      tc_commit(smem_u32(&ms->s_full[sb]));
+      if (j == ntile - 1) tc_commit(smem_u32(&ms->q_empty[qb]));
+      if constexpr (L::kLookahead) {
+        if (pend && !issue_pv<QM>(p, ms, ring, pbase, tmem, pend_q, pend_g, pend_first)) {
+          ok = false;
+          break;
+        }
+        pend = true;
+        pend_q = q;
+        pend_g = g;
+        pend_first = (j == 0);
+      } else {
+        if (!issue_pv<QM>(p, ms, ring, pbase, tmem, q, g, j == 0)) { ok = false; break; }
+      }
+      q += L::kSlotsPerTile;
+      ++g;
+    }
+  }
+  if (L::kLookahead && ok && pend) issue_pv<QM>(p, ms, ring, pbase, tmem, pend_q, pend_g, pend_first);
+  // Drain: every UMMA issued by this thread has completed before TMEM is freed.
+  tc_commit(smem_u32(&ms->drain));
+  mbar_wait(smem_u32(&ms->drain), 0, p.err, kErrDrain);
+}
+
+// Softmax / q-prep threads share named barriers, so a thread must never leave
+// alone: a wait that gives up raises the group's abort flag and the thread
+// carries on to the next named barrier, after which the whole group leaves.
+__device__ __forceinline__ void wait_or_flag(uint32_t bar, uint32_t parity, int32_t* err,
+                                             int32_t code, volatile int32_t* flag) {
+  if (!mbar_wait(bar, parity, err, code)) *flag = 1;
+}
+
+// -------------------------------------------------------------- q prepare
+// 64 threads write q of the next item into a free q buffer in the UMMA
+// operand layout and publish the score factors.
+template <int QM>
+__device__ void run_qprep(const Stage1Params& p, Misc* ms, uint8_t* qgen, int it0, int it1,
+                          int tq) {
+  using L = Layout<QM>;
+  constexpr float kSmScale = 1.0f / 24.0f;          // 1/sqrt(576)
+  volatile int32_t* abort = &ms->abort_qp;
+  int k = 0;
+  for (int it = it0; it < it1; ++it, ++k) {
+    const uint32_t qb = k & 1;
+    wait_or_flag(smem_u32(&ms->q_empty[qb]), ((k >> 1) & 1) ^ 1, p.err, kErrQPrep, abort);
+    named_bar_sync(2, 64);
+    if (*abort) return;
+    const int b = p.items[it].b;
+    uint8_t* dst = qgen + qb * L::kQBytes;
+    float c_hi = 0.f, c_lo = 0.f;
+    if constexpr (QM == kQBf16KvFp8) {
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
+                                                        static_cast<int64_t>(b) * kHeads * kQkDim);
+      uint4 v[18];
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < 18; ++i) {
+        v[i] = __ldg(src + tq + 64 * i);
+        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v[i]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __bfloat1622float2(h2[e]);
+          amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      if ((tq & 31) == 0) ms->qred[tq >> 5] = amax;
+      named_bar_sync(2, 64);
+      amax = fmaxf(fmaxf(ms->qred[0], ms->qred[1]), 1e-30f);
+      const float s_hi = amax / 448.0f, inv_hi = 448.0f / amax;
+#pragma unroll
+      for (int i = 0; i < 18; ++i) {
+        const int vid = tq + 64 * i;
+        const int h = vid / 72, d0 = (vid % 72) * 8;
+        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v[i]);
+        uint32_t hw[2], lw[2];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __bfloat1622float2(h2[e]);
+          const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+              make_float2(f.x * inv_hi, f.y * inv_hi), __NV_SATFINITE, __NV_E4M3);
+          const float2 hf = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(hi, __NV_E4M3)));
+          const float rx = (f.x - hf.x * s_hi) * inv_hi * 16.0f;
+          const float ry = (f.y - hf.y * s_hi) * inv_hi * 16.0f;
+          const __nv_fp8x2_storage_t lo =
+              __nv_cvt_float2_to_fp8x2(make_float2(rx, ry), __NV_SATFINITE, __NV_E4M3);
+          const int w = e >> 1, sh = (e & 1) * 16;
+          if ((e & 1) == 0) { hw[w] = 0; lw[w] = 0; }
+          hw[w] |= static_cast<uint32_t>(hi) << sh;
+          lw[w] |= static_cast<uint32_t>(lo) << sh;
+        }
+        const int atom = d0 >> 7, x = d0 & 127;
+        uint8_t* base = dst + atom * L::kQAtomBytes;
+        *reinterpret_cast<uint2*>(base + sw128(h, x)) = make_uint2(hw[0], hw[1]);
+        *reinterpret_cast<uint2*>(base + sw128(16 + h, x)) = make_uint2(lw[0], lw[1]);
+      }
+      const float kvs = __ldg(p.kv_scale);
+      c_hi = s_hi * kvs * kSmScale * kLog2e;
+      c_lo = s_hi * (1.0f / 16.0f) * kvs * kSmScale * kLog2e;
+    } else if constexpr (QM == kQFp8KvFp8) {
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.q) +
+                                                        static_cast<int64_t>(b) * kHeads * kQkDim);
+#pragma unroll
+      for (int i = 0; i < 9; ++i) {
+        const int vid = tq + 64 * i;
+        const int h = vid / 36, d0 = (vid % 36) * 16;
+        const uint4 v = __ldg(src + vid);
+        *reinterpret_cast<uint4*>(dst + (d0 >> 7) * L::kQAtomBytes + sw128(h, d0 & 127)) = v;
+      }
+      c_hi = __ldg(p.q_scale) * __ldg(p.kv_scale) * kSmScale * kLog2e;
+    } else {
+      // bf16 operand for kind::f16; fp8 q is decoded exactly to bf16 first.
+#pragma unroll 2
+      for (int i = 0; i < 18; ++i) {
+        const int vid = tq + 64 * i;
+        const int h = vid / 72, d0 = (vid % 72) * 8;
+        uint4 v;
+        if constexpr (QM == kQBf16KvBf16) {
+          v = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
+                                                   static_cast<int64_t>(b) * kHeads * kQkDim) +
+                    vid);
+        } else {
+          const uint2 raw = __ldg(reinterpret_cast<const uint2*>(
+                                      static_cast<const uint8_t*>(p.q) +
+                                      static_cast<int64_t>(b) * kHeads * kQkDim) +
+                                  vid);
+          uint32_t wv[4];
+          const uint32_t rr[2] = {raw.x, raw.y};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const __nv_fp8x2_storage_t pr =
+                static_cast<__nv_fp8x2_storage_t>((rr[e >> 1] >> ((e & 1) * 16)) & 0xFFFFu);
+            const float2 f = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3)));
+            const __nv_bfloat162 bb = __float22bfloat162_rn(f);
+            wv[e] = *reinterpret_cast<const uint32_t*>(&bb);
+          }
+          v = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+        }
+        const int atom = d0 >> 6, x = (d0 & 63) * 2;
+        *reinterpret_cast<uint4*>(dst + atom * L::kQAtomBytes + sw128(h, x)) = v;
+      }
+      c_hi = (QM == kQFp8KvBf16 ? __ldg(p.q_scale) : 1.0f) * kSmScale * kLog2e;
+    }
+    fence_proxy_async_smem();
+    named_bar_sync(2, 64);
+    if (tq == 0) {
+      ms->qscale[qb][0] = c_hi;
+      ms->qscale[qb][1] = c_lo;
+      mbar_arrive(smem_u32(&ms->q_full[qb]));
+    }
+  }
+}
+
+// ------------------------------------------------------ softmax / epilogue
+// Reduce 16 per-thread values over the 128 softmax threads (op = max or
+// sum).  A 16-shuffle transpose-reduce leaves head h(lane) in lanes 2j, 2j+1;
+// four warp results meet in shared memory.
+template <bool kMax>
+__device__ __forceinline__ void reduce16(float (&v)[16], float (&out)[16], float (*red)[16],
+                                         int qw, int lane) {
+  auto op = [](float a, float b) { return kMax ? fmaxf(a, b) : a + b; };
+  float r8[8], r4[4], r2[2], r1;
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float send = b4 ? v[i] : v[i + 8], keep = b4 ? v[i + 8] : v[i];
+    r8[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float send = b3 ? r8[i] : r8[i + 4], keep = b3 ? r8[i + 4] : r8[i];
+    r4[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float send = b2 ? r4[i] : r4[i + 2], keep = b2 ? r4[i + 2] : r4[i];
+    r2[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 4));
+  }
+  {
+    const float send = b1 ? r2[0] : r2[1], keep = b1 ? r2[1] : r2[0];
+    r1 = op(keep, __shfl_xor_sync(0xffffffffu, send, 2));
+  }
+  r1 = op(r1, __shfl_xor_sync(0xffffffffu, r1, 1));
+  const int h = (b4 ? 8 : 0) + (b3 ? 4 : 0) + (b2 ? 2 : 0) + (b1 ? 1 : 0);
+  if ((lane & 1) == 0) red[qw][h] = r1;
+  named_bar_sync(1, 128);
+#pragma unroll
+  for (int i = 0; i < 16; i += 4) {
+    float4 a = *reinterpret_cast<const float4*>(&red[0][i]);
+    float4 bq = *reinterpret_cast<const float4*>(&red[1][i]);
+    float4 cq = *reinterpret_cast<const float4*>(&red[2][i]);
+    float4 dq = *reinterpret_cast<const float4*>(&red[3][i]);
+    out[i + 0] = op(op(a.x, bq.x), op(cq.x, dq.x));
+    out[i + 1] = op(op(a.y, bq.y), op(cq.y, dq.y));
+    out[i + 2] = op(op(a.z, bq.z), op(cq.z, dq.z));
+    out[i + 3] = op(op(a.w, bq.w), op(cq.w, dq.w));
+  }
+}
+
+template <int QM>
+__device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, uint8_t* pgen,
+                            uint32_t tmem, int it0, int it1, int tid) {
+  using L = Layout<QM>;
+  volatile int32_t* abort = &ms->abort_sm;
+  const int qw = tid >> 5, lane = tid & 31;
+  const uint32_t tl = tmem + (static_cast<uint32_t>(qw * 32) << 16);   // this warp's lanes
+  uint32_t g = 0, q = 0;
+  int k = 0;
+  float m[16], l[16];
+  for (int it = it0; it < it1; ++it, ++k) {
+    const WorkItem w = p.items[it];
+    const uint32_t qb = k & 1;
+    wait_or_flag(smem_u32(&ms->q_full[qb]), (k >> 1) & 1, p.err, kErrSoftmax, abort);
+    const float c_hi = ms->qscale[qb][0], c_lo = ms->qscale[qb][1];
+    named_bar_sync(1, 128);
+    if (*abort) return;
+    if (tid == 0) mbar_arrive(smem_u32(&ms->q_empty[qb]));
+    const int ntile = (w.tok_end - w.tok_begin + kTile - 1) / kTile;
+    for (int j = 0; j < ntile; ++j, ++g, q += L::kSlotsPerTile) {
+      const uint32_t sb = g & 1u;
+      wait_or_flag(smem_u32(&ms->s_full[sb]), (g >> 1) & 1u, p.err, kErrSoftmax, abort);
+      tc_fence_after();
+      float s[16];
+      {
+        float a[16];
+        tmem_ld16(tl + kColS + 32 * sb, a);
+        if constexpr (L::kNq == 32) {
+          float bl[16];
+          tmem_ld16(tl + kColS + 32 * sb + 16, bl);
+          tmem_wait_ld();
+#pragma unroll
+          for (int h = 0; h < 16; ++h) s[h] = a[h] * c_hi + bl[h] * c_lo;
+        } else {
+          tmem_wait_ld();
+#pragma unroll
+          for (int h = 0; h < 16; ++h) s[h] = a[h] * c_hi;
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&ms->s_empty[sb]));
+      const int nvalid = min(kTile, w.tok_end - (w.tok_begin + j * kTile));
+      const bool valid = tid < nvalid;
+#pragma unroll
+      for (int h = 0; h < 16; ++h) s[h] = valid ? s[h] : -INFINITY;
+      float mt[16];
+      reduce16<true>(s, mt, ms->red[g & 1u], qw, lane);
+      if (*abort) return;
+      bool resc = false;
+      float alpha[16];
+#pragma unroll
+      for (int h = 0; h < 16; ++h) {
+        alpha[h] = 1.0f;
+        if (j == 0) {
+          m[h] = mt[h];
+          l[h] = 0.0f;
+        } else if (mt[h] > m[h] + kTau) {
+          alpha[h] = ex2(m[h] - mt[h]);
+          m[h] = mt[h];
+          resc = true;
+        }
+      }
+      if (resc) {
+        // The running max moved by more than kTau: scale O (both parts) once
+        // the previous tile's PV has landed in TMEM.
+        const uint32_t gp = g - 1;
+        wait_or_flag(smem_u32(&ms->pv_done[gp & 1u]), (gp >> 1) & 1u, p.err, kErrSoftmax, abort);
+        tc_fence_after();
+        const int nparts = L::kKv8 ? 2 : 1;
+        for (int part = 0; part < nparts; ++part) {
+          for (int c = 0; c < 4; ++c) {
+            const uint32_t col = (part ? kColOlo : kColOhi) + 16 * c;
+            float o[16];
+            tmem_ld16(tl + col, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int h = 0; h < 16; ++h) o[h] *= alpha[h];
+            tmem_st16(tl + col, o);
+          }
+        }
+        tmem_wait_st();
+#pragma unroll
+        for (int h = 0; h < 16; ++h) l[h] *= alpha[h];
+      }
+      float pv[16];
+#pragma unroll
+      for (int h = 0; h < 16; ++h) {
+        pv[h] = valid ? ex2(s[h] - m[h] + kPOff) : 0.0f;
+        l[h] += pv[h];
+      }
+      // P buffer (g & 1) is free once PV of tile g-2 completed.
+      if (g >= 2)
+        wait_or_flag(smem_u32(&ms->pv_done[sb]), ((g >> 1) - 1) & 1u, p.err, kErrSoftmax, abort);
+      uint8_t* pbuf = pgen + sb * L::kPBytes;
+      if constexpr (L::kKv8) {
+#pragma unroll
+        for (int h = 0; h < 16; h += 2) {
+          const __nv_fp8x2_storage_t hi =
+              __nv_cvt_float2_to_fp8x2(make_float2(pv[h], pv[h + 1]), __NV_SATFINITE, __NV_E4M3);
+          const float2 hf = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(hi, __NV_E4M3)));
+          const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+              make_float2((pv[h] - hf.x) * kPLoScale, (pv[h + 1] - hf.y) * kPLoScale),
+              __NV_SATFINITE, __NV_E4M3);
+          pbuf[sw128(h, tid)] = static_cast<uint8_t>(hi & 0xFF);
+          pbuf[sw128(h + 1, tid)] = static_cast<uint8_t>(hi >> 8);
+          pbuf[2048 + sw128(h, tid)] = static_cast<uint8_t>(lo & 0xFF);
+          pbuf[2048 + sw128(h + 1, tid)] = static_cast<uint8_t>(lo >> 8);
+        }
+      } else {
+        const uint32_t atom = tid >> 6, x = (tid & 63) * 2;
+#pragma unroll
+        for (int h = 0; h < 16; ++h) {
+          const __nv_bfloat16 v = __float2bfloat16_rn(pv[h]);
+          *reinterpret_cast<__nv_bfloat16*>(pbuf + atom * 2048 + sw128(h, x)) = v;
+        }
+      }
+      if (nvalid < kTile) {
+        // Tail tile: rows past the range may hold anything (stale slots,
+        // unused page slots); zero their V bytes so that 0 * V stays 0.
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t qq = q + c, s2 = qq % L::kNumSlots;
+          wait_or_flag(smem_u32(&ms->full[s2]), (qq / L::kNumSlots) & 1u, p.err, kErrSoftmax,
+                       abort);
+          if (!valid) {
+            uint8_t* row = ring_gen + s2 * L::kSlotBytes + tid * 128;
+            const int nbox = L::kKv8 ? 1 : 2;
+            for (int cb = 0; cb < nbox; ++cb)
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                reinterpret_cast<uint4*>(row + cb * 16384)[i] = make_uint4(0, 0, 0, 0);
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&ms->p_full[sb]));
+    }
+    // ------------------------------------------------------------ epilogue
+    const uint32_t gl = g - 1;
+    wait_or_flag(smem_u32(&ms->pv_done[gl & 1u]), (gl >> 1) & 1u, p.err, kErrSoftmax, abort);
+    tc_fence_after();
+    float lt[16];
+    reduce16<false>(l, lt, ms->red[g & 1u], qw, lane);
+    if (*abort) return;
+    // fp8 V entered the UMMAs as raw e4m3: its per-tensor scale is applied here.
+    const float vscale = L::kKv8 ? __ldg(p.kv_scale) : 1.0f;
+    float inv[16];
+#pragma unroll
+    for (int h = 0; h < 16; ++h) inv[h] = vscale / lt[h];
+    const int slot = w.slot;
+    for (int c = 0; c < 4; ++c) {
+      float oh[16];
+      tmem_ld16(tl + kColOhi + 16 * c, oh);
+      if constexpr (L::kKv8) {
+        float ol[16];
+        tmem_ld16(tl + kColOlo + 16 * c, ol);
+        tmem_wait_ld();
+#pragma unroll
+        for (int h = 0; h < 16; ++h) oh[h] = (oh[h] + ol[h] * (1.0f / kPLoScale)) * inv[h];
+      } else {
+        tmem_wait_ld();
+#pragma unroll
+        for (int h = 0; h < 16; ++h) oh[h] *= inv[h];
+      }
+      const int d = c * 128 + tid;
+      if (slot >= 0) {
+        float* po = p.part_o + static_cast<int64_t>(slot) * kHeads * kVDim + d;
+#pragma unroll
+        for (int h = 0; h < 16; ++h) po[h * kVDim] = oh[h];
+      } else {
+        uint16_t* po = p.out + static_cast<int64_t>(w.b) * kHeads * kVDim + d;
+#pragma unroll
+        for (int h = 0; h < 16; ++h) {
+          const __nv_bfloat16 v = __float2bfloat16_rn(oh[h]);
+          po[h * kVDim] = *reinterpret_cast<const uint16_t*>(&v);
+        }
+      }
+    }
+    tc_fence_before();
+    if (tid < 16) {
+      float mh = 0.f, lh = 1.f;
+#pragma unroll
+      for (int h = 0; h < 16; ++h)
+        if (h == tid) { mh = m[h]; lh = lt[h]; }
+      const float lse2 = mh + __log2f(lh) - kPOff;
+      if (slot >= 0)
+        p.part_lse[static_cast<int64_t>(slot) * kHeads + tid] = lse2;
+      else if (p.lse != nullptr)
+        p.lse[static_cast<int64_t>(w.b) * kHeads + tid] = lse2 * kLn2;
+    }
+  }
+}
+
+// -------------------------------------------------------------------- kernel
+template <int QM>
+__global__ void __launch_bounds__(256, 1) mla_stage1_kernel(const __grid_constant__ Stage1Params p) {
+  using L = Layout<QM>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t ring = smem_u32(smem);
+  Misc* ms = reinterpret_cast<Misc*>(smem + L::kMiscOff);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int it0 = p.cta_indptr[blockIdx.x], it1 = p.cta_indptr[blockIdx.x + 1];
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < L::kNumSlots; ++i) {
+      mbar_init(smem_u32(&ms->full[i]), 1);
+      mbar_init(smem_u32(&ms->empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&ms->s_full[i]), 1);
+      mbar_init(smem_u32(&ms->s_empty[i]), 128);
+      mbar_init(smem_u32(&ms->p_full[i]), 128);
+      mbar_init(smem_u32(&ms->pv_done[i]), 1);
+      mbar_init(smem_u32(&ms->q_full[i]), 1);
+      mbar_init(smem_u32(&ms->q_empty[i]), 2);
+    }
+    mbar_init(smem_u32(&ms->drain), 1);
+    ms->abort_sm = 0;
+    ms->abort_qp = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) prefetch_tensormap(&p.tmap_kv);
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&ms->tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ms->tmem_base;
+
+  if (warp == 0) {
+    run_producer<QM>(p, ms, ring, it0, it1, lane);
+  } else if (warp == 1) {
+    if (lane == 0)
+      run_mma<QM>(p, ms, ring, ring + L::kQOff, ring + L::kPOff, tmem, it0, it1);
+    __syncwarp();
+  } else if (warp < 4) {
+    run_qprep<QM>(p, ms, smem + L::kQOff, it0, it1, threadIdx.x - 64);
+  } else {
+    run_softmax<QM>(p, ms, smem, smem + L::kPOff, tmem, it0, it1, threadIdx.x - 128);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+int stage1_smem_bytes(int qmode) {
+  switch (qmode) {
+    case kQBf16KvBf16: return Layout<kQBf16KvBf16>::kSmemBytes;
+    case kQFp8KvFp8: return Layout<kQFp8KvFp8>::kSmemBytes;
+    case kQBf16KvFp8: return Layout<kQBf16KvFp8>::kSmemBytes;
+    case kQFp8KvBf16: return Layout<kQFp8KvBf16>::kSmemBytes;
+  }
+  return -1;
+}
+
+template <int QM>
+static cudaError_t launch_t(const Stage1Params& p, int num_ctas, cudaStream_t stream) {
+  const int smem = Layout<QM>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(mla_stage1_kernel<QM>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  mla_stage1_kernel<QM><<<num_ctas, 256, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_stage1(int qmode, const Stage1Params& p, int num_ctas, cudaStream_t stream) {
+  switch (qmode) {
+    case kQBf16KvBf16: return launch_t<kQBf16KvBf16>(p, num_ctas, stream);
+    case kQFp8KvFp8: return launch_t<kQFp8KvFp8>(p, num_ctas, stream);
+    case kQBf16KvFp8: return launch_t<kQBf16KvFp8>(p, num_ctas, stream);
+    case kQFp8KvBf16: return launch_t<kQFp8KvBf16>(p, num_ctas, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace mla

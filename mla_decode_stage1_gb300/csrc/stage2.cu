@@ -1,0 +1,75 @@
+// stage2.cu -- log-sum-exp merge of split partials (stage 2).
+//
+// The merge algebra of the log2-domain stage-2 kernel of kernelindex.com,
+// amd-mixed-mla submission 668813 (and the natural-log reduce kernels of
+// submissions 695854 and 600081): for one (request, head) with partials
+// (o_s, lse_s), M = max_s lse_s, w_s = 2^(lse_s - M),
+// out = sum_s w_s o_s / sum_s w_s (cast to bf16), lse = (M + log2 sum w) ln 2.
+// Partials with lse = -inf carry no weight; a request with no partials is
+// empty and gets out = 0, lse = -inf.
+//
+// One warp per (request, head); a lane owns 16 of the 512 dims as four
+// float4 columns, so every partial row is read as coalesced 512-byte lines.
+
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace mla {
+
+__global__ void __launch_bounds__(256) mla_stage2_kernel(const Stage2Params p) {
+  const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int job = gw >> 4, h = gw & 15;
+  if (job >= p.num_jobs) return;
+  const MergeJob J = p.jobs[job];
+  uint16_t* out = p.out + (static_cast<int64_t>(J.b) * kHeads + h) * kVDim;
+  float acc[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+  float M = -INFINITY, wsum = 0.0f;
+  for (int s = lane; s < J.count; s += 32)
+    M = fmaxf(M, p.part_lse[static_cast<int64_t>(J.first + s) * kHeads + h]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if (M != -INFINITY) {
+    for (int s = 0; s < J.count; ++s) {
+      const int64_t row = static_cast<int64_t>(J.first + s) * kHeads + h;
+      const float w = ex2(p.part_lse[row] - M);
+      if (w == 0.0f) continue;
+      wsum += w;
+      const float4* src = reinterpret_cast<const float4*>(p.part_o + row * kVDim);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4 v = src[lane + 32 * i];
+        acc[4 * i + 0] += w * v.x;
+        acc[4 * i + 1] += w * v.y;
+        acc[4 * i + 2] += w * v.z;
+        acc[4 * i + 3] += w * v.w;
+      }
+    }
+  }
+  const float inv = wsum > 0.0f ? 1.0f / wsum : 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(acc[4 * i + 0] * inv, acc[4 * i + 1] * inv);
+    const __nv_bfloat162 b = __floats2bfloat162_rn(acc[4 * i + 2] * inv, acc[4 * i + 3] * inv);
+    uint2 v;
+    v.x = *reinterpret_cast<const uint32_t*>(&a);
+    v.y = *reinterpret_cast<const uint32_t*>(&b);
+    reinterpret_cast<uint2*>(out)[lane + 32 * i] = v;
+  }
+  if (lane == 0 && p.lse != nullptr)
+    p.lse[static_cast<int64_t>(J.b) * kHeads + h] =
+        wsum > 0.0f ? (M + __log2f(wsum)) * kLn2 : -INFINITY;
+}
+
+cudaError_t launch_stage2(const Stage2Params& p, cudaStream_t stream) {
+  if (p.num_jobs <= 0) return cudaSuccess;
+  const int warps = p.num_jobs * kHeads;
+  mla_stage2_kernel<<<(warps + 7) / 8, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -1,0 +1,195 @@
+"""CPU tests of the C ABI: the library loads, exports every declared symbol,
+validates its arguments, and the planner's work table is a correct and
+balanced partition.  No kernel is launched."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mla_decode.h")
+
+
+@pytest.fixture(scope="module")
+def mla():
+    import __graft_entry__
+    __graft_entry__._builder().build()
+    import mla_decode_stage1_gb300 as m
+    return m
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(mla):
+    names = declared_functions()
+    assert len(names) >= 8
+    lib = ctypes.CDLL(mla.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in mla_decode.h but not exported"
+    assert set(names) == set(mla.EXPORTS)
+
+
+def test_status_strings(mla):
+    for code, name in mla.STATUS.items():
+        assert mla.mla_status_string(code) == name
+    assert mla.mla_status_string(99) == "MLA_ERR_UNKNOWN"
+
+
+def plan(mla, indptr, last=None, ps=1, qd="bf16", kd="fp8", S=0, sms=148):
+    return mla.mla_decode_plan(np.asarray(indptr, np.int32), last, page_size=ps, q_dtype=qd,
+                               kv_dtype=kd, num_splits=S, num_sms=sms)
+
+
+@pytest.mark.parametrize("indptr,last,ps,err", [
+    ([0, 5, 3], None, 1, 1),          # decreasing
+    ([-1, 5], None, 1, 1),            # negative start
+    ([0, 2], [0], 8, 1),              # last page length 0
+    ([0, 2], [9], 8, 1),              # last page length > page size
+])
+def test_plan_rejects_bad_input(mla, indptr, last, ps, err):
+    with pytest.raises(mla.MlaError) as e:
+        plan(mla, indptr, None if last is None else np.asarray(last, np.int32), ps=ps)
+    assert e.value.status == err
+
+
+def test_plan_rejects_bad_scalars(mla):
+    lib = mla._lib
+    h = ctypes.c_void_p()
+    ind = np.array([0, 4], np.int32)
+    p = ind.ctypes.data_as(ctypes.c_void_p)
+    assert lib.mla_decode_plan(None, None, 1, 1, 0, 0, 0, 1, ctypes.byref(h)) == 1
+    assert lib.mla_decode_plan(p, None, 0, 1, 0, 0, 0, 1, ctypes.byref(h)) == 1
+    assert lib.mla_decode_plan(p, None, 1, 0, 0, 0, 0, 1, ctypes.byref(h)) == 1
+    assert lib.mla_decode_plan(p, None, 1, 1, 0, 0, -1, 1, ctypes.byref(h)) == 1
+    assert lib.mla_decode_plan(p, None, 1, 1, 7, 0, 0, 1, ctypes.byref(h)) == 1
+    assert lib.mla_decode_plan(p, None, 1, 1, 0, 0, 0, 1, None) == 1
+    assert lib.mla_plan_get_info(None, None) == 1
+    assert lib.mla_plan_workspace_size(None, None) == 1
+
+
+def test_run_rejects_bad_arguments_without_launching(mla):
+    pl = plan(mla, [0, 16], ps=1)
+    lib = mla._lib
+    buf = ctypes.create_string_buffer(1 << 16)
+    a = ctypes.addressof(buf)
+    a256 = ctypes.c_void_p((a + 255) & ~255)
+    # null q / kv / out / workspace
+    assert lib.mla_decode_run(pl.handle, None, None, a256, a256, None, 0, 16, None, a256,
+                              1 << 12, a256, None, None) == 1
+    # misaligned kv
+    assert lib.mla_decode_run(pl.handle, a256, None, ctypes.c_void_p(a256.value + 8), a256, None,
+                              0, 16, None, a256, 1 << 12, a256, None, None) == 1
+    # fp8 KV without a scale pointer
+    assert lib.mla_decode_run(pl.handle, a256, None, a256, None, None, 0, 16, None, a256,
+                              1 << 12, a256, None, None) == 1
+    # workspace too small
+    assert lib.mla_decode_run(pl.handle, a256, None, a256, a256, None, 0, 16, None, a256,
+                              0, a256, None, None) == 3
+    # a page table needs a power-of-two page size >= 8
+    pl4 = plan(mla, [0, 4], ps=4)
+    assert lib.mla_decode_run(pl4.handle, a256, None, a256, a256, None, 0, 16, a256, a256,
+                              1 << 14, a256, None, None) == 2
+
+
+def test_unsupported_combinations(mla):
+    with pytest.raises(mla.MlaError) as e:
+        plan(mla, [0, 4], qd="mxfp4", kd="fp8")
+    assert e.value.status == 2
+
+
+def lengths_of(indptr, last, ps):
+    n = np.diff(np.asarray(indptr)).astype(np.int64) * ps
+    if last is not None:
+        n -= np.where(n > 0, ps - np.asarray(last), 0)
+    return n
+
+
+def check_partition(pl, lengths):
+    ind, items = pl.work()
+    info = pl.info()
+    assert ind[0] == 0 and ind[-1] == info.num_items and np.all(np.diff(ind) >= 1)
+    covered = {b: [] for b in range(len(lengths))}
+    for b, t0, t1, slot in items:
+        assert 0 <= t0 < t1 <= lengths[b] and t0 % 128 == 0
+        covered[b].append((t0, t1, slot))
+    nslots = set()
+    for b, rngs in covered.items():
+        rngs.sort()
+        if lengths[b] == 0:
+            assert rngs == []
+            continue
+        assert rngs[0][0] == 0 and rngs[-1][1] == lengths[b]
+        for (a0, a1, _), (b0, b1, _) in zip(rngs, rngs[1:]):
+            assert a1 == b0, "gap or overlap"
+        slots = [s for _, _, s in rngs]
+        if len(rngs) == 1:
+            assert slots == [-1]
+        else:
+            assert slots == list(range(slots[0], slots[0] + len(slots)))
+            nslots.update(slots)
+    assert len(nslots) == info.num_partials
+    n_split = sum(1 for r in covered.values() if len(r) >= 2)
+    n_empty = sum(1 for n in lengths if n == 0)
+    assert info.num_merge_jobs == n_split + n_empty
+    assert info.total_tokens == sum(lengths)
+    return ind, items
+
+
+@pytest.mark.parametrize("bs,kv,ps,sms", [(256, 8192, 8, 148), (256, 8192, 8, 152), (64, 8192, 8, 152),
+                                          (32, 1024, 1, 152), (4, 1024, 1, 152), (3, 100, 1, 152)])
+def test_balanced_plan_regular(mla, bs, kv, ps, sms):
+    indptr = np.arange(bs + 1) * (kv // ps)
+    pl = plan(mla, indptr, ps=ps, sms=sms)
+    ind, items = check_partition(pl, [kv] * bs)
+    info = pl.info()
+    tiles = bs * ((kv + 127) // 128)
+    assert info.num_ctas == min(sms, tiles)
+    # tiles per CTA differ by at most one
+    per = []
+    for i in range(info.num_ctas):
+        per.append(sum((t1 - t0 + 127) // 128 for _, t0, t1, _ in items[ind[i]:ind[i + 1]]))
+    assert max(per) - min(per) <= 1 and sum(per) == tiles
+
+
+def test_balanced_plan_ragged_with_last_pages(mla):
+    rng = np.random.default_rng(0)
+    ps = 16
+    lens = rng.integers(0, 5000, 97)
+    lens[::13] = 0
+    npages = (lens + ps - 1) // ps
+    indptr = np.concatenate([[0], np.cumsum(npages)])
+    last = np.where(npages > 0, lens - (npages - 1) * ps, ps).astype(np.int32)
+    pl = plan(mla, indptr, last, ps=ps, sms=152)
+    check_partition(pl, lens_of := lengths_of(indptr, last, ps))
+    assert np.array_equal(lens_of, lens)
+
+
+@pytest.mark.parametrize("S", [1, 2, 3, 7, 32])
+def test_fixed_split_plan(mla, S):
+    lens = [1, 130, 900, 4096, 0, 128]
+    indptr = np.concatenate([[0], np.cumsum(lens)])
+    pl = plan(mla, indptr, ps=1, S=S)
+    ind, items = check_partition(pl, lens)
+    assert np.all(np.diff(ind) == 1)     # one item per CTA
+    for b, n in enumerate(lens):
+        tiles = (n + 127) // 128
+        per = (tiles + S - 1) // S if tiles else 0
+        got = [(t0, t1) for bb, t0, t1, _ in items if bb == b]
+        exp = [(s * per * 128, min((s + 1) * per * 128, n)) for s in range(S)
+               if per and s * per < tiles]
+        assert got == exp
+
+
+def test_workspace_size_covers_partials(mla):
+    lens = [4096] * 8
+    indptr = np.concatenate([[0], np.cumsum(lens)])
+    pl = plan(mla, indptr, ps=1, S=4)
+    info = pl.info()
+    assert info.num_partials == 32
+    assert pl.workspace_bytes >= 32 * 16 * 512 * 4 + 32 * 16 * 4
