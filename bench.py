@@ -37,13 +37,15 @@ NOMINAL_HBM_GBS = 8000.0
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--bs", type=int, default=0,
+                    help="override the batch size of the configuration (profiling runs)")
     return ap.parse_args()
 
 
@@ -221,11 +223,15 @@ def main():
 
     # every rank owns one batch of the configured shape (weak scaling)
     c = synth.CONFIGS[args.config]
-    w = synth.make_workload(bs=c["bs"], lengths=synth.config_lengths(args.config),
+    lengths = synth.config_lengths(args.config)
+    if args.bs:
+        lengths = (lengths * ((args.bs + len(lengths) - 1) // len(lengths)))[: args.bs]
+    w = synth.make_workload(bs=len(lengths), lengths=lengths,
                             page_size=c["page_size"], q_dtype=c["q_dtype"], kv_dtype=c["kv_dtype"],
                             permute_pages=c["permute_pages"], seed=c["seed"] + 1000 * rank,
                             device=dev, name=args.config)
     d = w.to(dev)
+    torch.cuda.empty_cache()
     plan = mla.mla_decode_plan(w.kv_indptr, w.kv_last_page_len, page_size=w.page_size,
                                q_dtype=w.q_dtype, kv_dtype=w.kv_dtype)
     info = plan.info()
@@ -255,6 +261,9 @@ def main():
           for _ in range(K)]
     ev_s1 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
              for _ in range(K)]
+    for a, b in ev_s1:   # torch creates the CUDA event on first record
+        a.record(stream)
+        b.record(stream)
     with ClockSampler(local) as clk:
         if dist is not None:
             dist.barrier()

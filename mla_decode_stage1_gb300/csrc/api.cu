@@ -11,7 +11,7 @@
 #include <new>
 #include <vector>
 
-#include "../../include/mla_decode.h"
+#include "mla_decode.h"
 #include "kernels.h"
 
 using mla::MergeJob;
@@ -168,19 +168,21 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// KV pool as a 2-D tensor [pool_rows, 576 elements]; boxes of 128 bytes x
-// box_rows rows with the 128-byte swizzle; out-of-bounds reads fill zeros.
+// KV pool as a 3-D tensor {64-byte chunk, row, chunk index}: a box of
+// box_rows rows x all chunks lands in shared memory as [chunk][row][64 B]
+// with the 64-byte swizzle.  Out-of-bounds rows are filled with zeros.
 bool make_kv_map(CUtensorMap* map, const void* kv, int kv_dtype, int64_t rows, int box_rows) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return false;
   const bool b16 = kv_dtype == MLA_DTYPE_BF16;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(mla::kQkDim), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(mla::kQkDim * (b16 ? 2 : 1))};
-  const cuuint32_t box[2] = {b16 ? 64u : 128u, static_cast<cuuint32_t>(box_rows)};
-  const cuuint32_t estr[2] = {1, 1};
-  return enc(map, b16 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+  const uint32_t esz = b16 ? 2 : 1, row_bytes = mla::kQkDim * esz;
+  const cuuint64_t dims[3] = {64 / esz, static_cast<cuuint64_t>(rows), row_bytes / 64};
+  const cuuint64_t strides[2] = {row_bytes, 64};
+  const cuuint32_t box[3] = {64 / esz, static_cast<cuuint32_t>(box_rows), row_bytes / 64};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, b16 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
              const_cast<void*>(kv), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -305,13 +307,15 @@ mla_status mla_decode_run(mla_plan* plan, const void* q, const float* q_scale, c
   if (plan->q_dtype == MLA_DTYPE_FP8_E4M3 && q_scale == nullptr) return MLA_ERR_INVALID_ARG;
   if (plan->kv_dtype == MLA_DTYPE_FP8_E4M3 && kv_scale == nullptr) return MLA_ERR_INVALID_ARG;
   if (workspace_bytes < plan->ws_bytes) return MLA_ERR_WORKSPACE;
+  // Identity table: one TMA box of 128 rows per tile.  Page table: one box
+  // per 8-row group (a group never straddles a page).
   int box_rows = mla::kTile;
   if (kv_indices != nullptr) {
-    // A page table needs whole 1024-byte swizzle atoms per page.
     if (!is_pow2(plan->page_size) || plan->page_size < 8) return MLA_ERR_UNSUPPORTED;
-    box_rows = std::min(plan->page_size, mla::kTile);
+    box_rows = 8;
     if (kv_pool_rows % plan->page_size != 0) return MLA_ERR_INVALID_ARG;
   }
+  const uint32_t row_bytes = mla::kQkDim * (plan->kv_dtype == MLA_DTYPE_BF16 ? 2 : 1);
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   if (plan->tmap_ptr != kv || plan->tmap_rows != kv_pool_rows || plan->tmap_box_rows != box_rows) {
     if (!make_kv_map(&plan->tmap, kv, plan->kv_dtype, kv_pool_rows, box_rows)) return MLA_ERR_CUDA;
@@ -345,6 +349,8 @@ mla_status mla_decode_run(mla_plan* plan, const void* q, const float* q_scale, c
     p.err = err;
     p.page_size = plan->page_size;
     p.box_rows = box_rows;
+    p.chunk_stride = static_cast<uint32_t>(box_rows) * 64u;    // [group][chunk][rows][64 B]
+    p.group_stride = box_rows == 8 ? row_bytes * 8u : 512u;
     p.pool_rows = kv_pool_rows;
     if (plan->ev_before != nullptr && cudaEventRecord(plan->ev_before, stream) != cudaSuccess)
       return MLA_ERR_CUDA;

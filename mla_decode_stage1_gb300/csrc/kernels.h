@@ -54,7 +54,7 @@ enum QMode : int {
 };
 
 struct Stage1Params {
-  CUtensorMap tmap_kv;          // [pool_rows, 576] elements, 128-byte boxes, 128B swizzle
+  CUtensorMap tmap_kv;          // KV pool as [chunk 64 B][row][64 B], 64-byte swizzle
   const void* q;                // [bs,16,576]
   const float* q_scale;         // device [1] (fp8 q) or null
   const float* kv_scale;        // device [1] (fp8 kv) or null
@@ -67,7 +67,9 @@ struct Stage1Params {
   float* lse;                   // [bs,16] natural log, nullable
   int32_t* err;                 // device error word
   int32_t page_size;
-  int32_t box_rows;             // rows per TMA box: 128 (identity) or page_size
+  int32_t box_rows;             // rows per TMA box: 128 (identity table) or 8 (page table)
+  uint32_t chunk_stride;        // smem bytes between 64-byte column chunks of a tile
+  uint32_t group_stride;        // smem bytes between 8-row groups of a tile
   int64_t pool_rows;
 };
 

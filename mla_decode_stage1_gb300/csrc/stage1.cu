@@ -8,15 +8,19 @@
 // same rows, plus the log-sum-exp of the range.
 //
 // How (GB300-first, not the pages' Triton design):
-//  * one persistent CTA per SM walks a planner-built list of work items; the
-//    KV rows stream HBM -> shared memory through 2-D TMA boxes (128-byte
-//    swizzle) into a ring of 128-token x 128-dim slots guarded by mbarriers;
+//  * one persistent CTA per SM walks a planner-built list of work items; KV
+//    rows stream HBM -> shared memory as whole 128-token tiles.  One 3-D TMA
+//    box moves 8 rows x all 576 dims (a page group of 4.5 KB in fp8) into a
+//    [64-byte column chunk][8 rows][64 B] image with the 64-byte swizzle, so
+//    a page-8 table costs 16 TMA operations per tile and an identity table 1;
 //  * QK^T runs on the 5th-generation tensor cores with the tokens as M:
 //    S^T[128 tok x 16 heads] = K[128 x 576] . Q^T, accumulated in TMEM;
 //  * PV reuses the very same shared-memory bytes as an MN-major operand:
 //    O^T[512 x 16] += V^T[512 x 128 tok] . P^T, four M=128 blocks in TMEM;
-//  * warp roles: warp 0 TMA producer, warp 1 UMMA issuer (+ TMEM owner),
-//    warps 2-3 prepare q for the next item, warps 4-7 do the softmax and the
+//  * a tcgen05.mma costs the issuing thread about the same time whatever
+//    its N, so QK^T and PV are issued by two different warps that run side
+//    by side (warp 1 and warp 2); warp 0 is the TMA producer, warp 3
+//    prepares q for the next item, warps 4-7 do the softmax and the
 //    epilogue (one thread per token / per output dim, TMEM lane = thread);
 //  * every mbarrier wait is bounded (see mbar_wait) and reports into the
 //    device error word instead of hanging.
@@ -25,7 +29,8 @@
 // the per-tensor scales folded into one score factor and into l.  A bf16 q
 // meeting fp8 KV is split into q_hi + q_lo (two e4m3 terms with a per-request
 // scale, ~bf16 precision) that share one UMMA with N = 32.  p is likewise
-// split into p_hi + 2^-4 p_lo e4m3 terms accumulated in two TMEM regions.
+// split into p_hi + 2^-4 p_lo e4m3 terms, stacked as the 32 rows of one PV
+// operand so that one UMMA accumulates both parts (TMEM columns 0-15, 16-31).
 // bf16 KV runs kind::f16 with bf16 q and bf16 p.
 
 #include <cstddef>
@@ -43,44 +48,46 @@ template <int QM>
 struct Layout {
   static constexpr bool kKv8 = (QM == kQFp8KvFp8 || QM == kQBf16KvFp8);
   static constexpr int kNq = (QM == kQBf16KvFp8) ? 32 : 16;        // UMMA N of QK^T
-  static constexpr int kSlotBytes = kKv8 ? 16384 : 32768;           // 128 tokens x 128 dims
-  static constexpr int kSlotsPerTile = 5;                           // 4 V slots + rope slot
+  static constexpr int kElem = kKv8 ? 1 : 2;
+  static constexpr int kRowBytes = kQkDim * kElem;                  // 576 | 1152
+  static constexpr int kChunks = kRowBytes / 64;                    // 64-byte column chunks
+  static constexpr int kVChunks = kVDim * kElem / 64;               // chunks holding V
+  static constexpr int kTileBytes = kTile * kRowBytes;              // 72 KB | 144 KB
+  static constexpr int kKSteps = kRowBytes / 32;                    // QK^T steps of 32 bytes
   static constexpr int kQAtoms = kKv8 ? 5 : 9;                      // 128-byte K atoms of q
   static constexpr int kQAtomBytes = kNq * 128;
   static constexpr int kQBytes = kQAtoms * kQAtomBytes;
   static constexpr int kPBytes = 4096;
+  static constexpr uint32_t kOCols = kKv8 ? 32 : 16;               // TMEM columns per O block
   static constexpr int kMiscBytes = 2048;
   static constexpr int kMaxSmem = 232448;
-  static constexpr int kNumSlots =
-      (kMaxSmem - 1024 - 2 * kQBytes - 2 * kPBytes - kMiscBytes) / kSlotBytes;
-  // QK^T of tile g+1 is issued before PV of tile g only if the ring holds the
-  // slots of both tiles at once (slots are taken round-robin).
-  static constexpr bool kLookahead = kNumSlots >= 2 * kSlotsPerTile;
-  static constexpr int kQOff = kNumSlots * kSlotBytes;
+  static constexpr int kNumTiles =
+      (kMaxSmem - 1024 - 2 * kQBytes - 2 * kPBytes - kMiscBytes) / kTileBytes;
+  static constexpr int kQOff = kNumTiles * kTileBytes;
   static constexpr int kPOff = kQOff + 2 * kQBytes;
   static constexpr int kMiscOff = kPOff + 2 * kPBytes;
   static constexpr int kSmemBytes = kMiscOff + kMiscBytes + 1024;
-  static_assert(kNumSlots >= kSlotsPerTile, "ring too small");
+  static_assert(kNumTiles >= 1 && kNumTiles <= 4, "tile ring");
   static_assert(kSmemBytes <= kMaxSmem, "shared memory over budget");
-  static_assert(kNumSlots <= 16, "barrier table sized for 16 slots");
+  static_assert(kTileBytes % 1024 == 0 && kQBytes % 1024 == 0, "operand alignment");
 };
 
 // Misc region: barriers, reduction scratch, q scales, TMEM address.
 struct Misc {
-  uint64_t full[16], empty[16];
-  uint64_t s_full[2], s_empty[2], p_full[2], pv_done[2], q_full[2], q_empty[2], drain;
+  uint64_t full[4], empty[4];
+  uint64_t s_full[2], s_empty[2], p_full[2], pv_done[2], q_full[2], q_empty[2], drain[2];
   alignas(16) float red[2][4][16];   // read back as float4
   float qscale[2][2];
-  float qred[2];
   uint32_t tmem_base;
-  int32_t abort_sm, abort_qp;   // set by a thread whose bounded wait gave up
+  int32_t abort_sm;                  // set by a softmax thread whose bounded wait gave up
 };
 static_assert(sizeof(Misc) <= 2048, "misc region");
 static_assert(offsetof(Misc, red) % 16 == 0, "reduction scratch is read as float4");
 
-// TMEM columns: S^T double buffer [0,64), O_hi^T [64,128), O_lo^T [128,192).
+// TMEM columns: S^T double buffer [0,64), then O^T: four 128-dim blocks of
+// kOCols columns (fp8 KV: 16 heads of p_hi, then 16 heads of p_lo).
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColS = 0, kColOhi = 64, kColOlo = 128;
+constexpr uint32_t kColS = 0, kColO = 64;
 
 // Byte offset of (row, byte x) inside a 128-byte-wide K-major operand with
 // the 128-byte swizzle (8-row / 1024-byte atoms, 16-byte chunks XOR row%8).
@@ -88,220 +95,227 @@ __device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t x) {
   return (row >> 3) * 1024u + (row & 7u) * 128u + ((((x >> 4) ^ row) & 7u) << 4) + (x & 15u);
 }
 
+// Walks the tiles of this CTA's items in order (items hold whole 128-token
+// tiles except for a ragged last one).
+struct TileCursor {
+  const WorkItem* items;
+  int it, it1, k;        // item index, end, item ordinal within the CTA
+  int j, ntile;          // tile within the item
+  uint32_t t;            // tile ordinal within the CTA
+  WorkItem w;
+  __device__ __forceinline__ void init(const WorkItem* items_, int it0, int it1_) {
+    items = items_;
+    it = it0;
+    it1 = it1_;
+    k = 0;
+    j = 0;
+    t = 0;
+    load();
+  }
+  __device__ __forceinline__ void load() {
+    if (it < it1) {
+      w = items[it];
+      ntile = (w.tok_end - w.tok_begin + kTile - 1) / kTile;
+    } else {
+      ntile = 0;
+    }
+  }
+  __device__ __forceinline__ bool done() const { return it >= it1; }
+  __device__ __forceinline__ void advance() {
+    ++t;
+    if (++j == ntile) {
+      ++it;
+      ++k;
+      j = 0;
+      load();
+    }
+  }
+  __device__ __forceinline__ int t0() const { return w.tok_begin + j * kTile; }
+  __device__ __forceinline__ int nvalid() const { return min(kTile, w.tok_end - t0()); }
+};
+
+// First KV row of TMA box `lane` of the cursor's tile (through the page
+// table), or 0 when the lane has no box.
+__device__ __forceinline__ int box_row(const Stage1Params& p, const TileCursor& c, int lane,
+                                       int nbox) {
+  if (c.done() || lane >= nbox) return 0;
+  const int pos = c.t0() + lane * p.box_rows;
+  if (p.kv_indices == nullptr) return c.w.page_base * p.page_size + pos;
+  int page = __ldg(p.kv_indices + c.w.page_base + pos / p.page_size);
+  if (page < 0 || static_cast<int64_t>(page + 1) * p.page_size > p.pool_rows) {
+    atomicOr(p.err, kErrBadPage);
+    page = 0;
+  }
+  return page * p.page_size + pos % p.page_size;
+}
+
 // ---------------------------------------------------------------- producer
+// One warp: lane i owns TMA box i of every tile.  The page-table entries of
+// the next tile are fetched while the current tile is being issued.
 template <int QM>
 __device__ void run_producer(const Stage1Params& p, Misc* ms, uint32_t ring, int it0, int it1,
                              int lane) {
   using L = Layout<QM>;
   const uint64_t pol = l2_policy_evict_first();
-  uint32_t q = 0;
-  bool ok = true;
   const int box_rows = p.box_rows;
-  const uint32_t box_bytes = static_cast<uint32_t>(box_rows) * 128u;
-  for (int it = it0; it < it1 && ok; ++it) {
-    const WorkItem w = p.items[it];
-    for (int t0 = w.tok_begin; t0 < w.tok_end && ok; t0 += kTile) {
-      const int nvalid = min(kTile, w.tok_end - t0);
-      const int nbox = (nvalid + box_rows - 1) / box_rows;   // boxes holding valid tokens
-      int row = 0;
-      if (lane < nbox) {
-        const int pos = t0 + lane * box_rows;
-        if (p.kv_indices != nullptr) {
-          int page = p.kv_indices[w.page_base + pos / p.page_size];
-          if (page < 0 || static_cast<int64_t>(page + 1) * p.page_size > p.pool_rows) {
-            atomicOr(p.err, kErrBadPage);
-            page = 0;
-          }
-          row = page * p.page_size + pos % p.page_size;
-        } else {
-          row = w.page_base * p.page_size + pos;
-        }
-      }
-      for (int c = 0; c < L::kSlotsPerTile; ++c, ++q) {
-        const uint32_t s = q % L::kNumSlots, ph = (q / L::kNumSlots) & 1u;
-        if (lane == 0) ok = mbar_wait(smem_u32(&ms->empty[s]), ph ^ 1u, p.err, kErrProducer);
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok) break;
-        const int ncol = L::kKv8 ? 1 : (c < 4 ? 2 : 1);
-        const uint32_t full = smem_u32(&ms->full[s]);
-        if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(nbox * ncol) * box_bytes);
-        __syncwarp();
-        if (lane < nbox) {
-          for (int cb = 0; cb < ncol; ++cb) {
-            const int x = L::kKv8 ? c * 128 : c * 128 + cb * 64;
-            const uint32_t dst = ring + s * L::kSlotBytes + cb * 16384u + lane * box_bytes;
-            tma_load_2d(dst, &p.tmap_kv, full, x, row, pol);
-          }
-        }
-      }
-    }
+  const uint32_t box_bytes = static_cast<uint32_t>(box_rows) * L::kRowBytes;
+  TileCursor cur;
+  cur.init(p.items, it0, it1);
+  int nbox_next = cur.done() ? 0 : (cur.nvalid() + box_rows - 1) / box_rows;
+  int row_next = box_row(p, cur, lane, nbox_next);
+  bool ok = true;
+  uint32_t t = 0;
+  while (!cur.done() && ok) {
+    const int nbox = nbox_next, row = row_next;
+    TileCursor nxt = cur;
+    nxt.advance();
+    nbox_next = nxt.done() ? 0 : (nxt.nvalid() + box_rows - 1) / box_rows;
+    row_next = box_row(p, nxt, lane, nbox_next);
+    const uint32_t s = t % L::kNumTiles, ph = (t / L::kNumTiles) & 1u;
+    if (lane == 0) ok = mbar_wait(smem_u32(&ms->empty[s]), ph ^ 1u, p.err, kErrProducer);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    if (!ok) break;
+    const uint32_t full = smem_u32(&ms->full[s]);
+    if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(nbox) * box_bytes);
+    __syncwarp();
+    if (lane < nbox) tma_load_3d(ring + s * L::kTileBytes + lane * box_bytes, &p.tmap_kv, full, 0, row, 0, pol);
+    cur = nxt;
+    ++t;
   }
-  // Drain: wait (bounded) until the last copies issued into each slot landed.
+  // Drain: wait (bounded) until the last copies issued into each tile landed.
   if (lane == 0) {
-    const uint32_t n = q < static_cast<uint32_t>(L::kNumSlots) ? q : L::kNumSlots;
+    const uint32_t n = t < static_cast<uint32_t>(L::kNumTiles) ? t : L::kNumTiles;
     for (uint32_t i = 0; i < n; ++i) {
-      const uint32_t qq = q - 1 - i;
-      if (!mbar_wait(smem_u32(&ms->full[qq % L::kNumSlots]), (qq / L::kNumSlots) & 1u, p.err,
+      const uint32_t tt = t - 1 - i;
+      if (!mbar_wait(smem_u32(&ms->full[tt % L::kNumTiles]), (tt / L::kNumTiles) & 1u, p.err,
                      kErrDrain))
         break;
     }
   }
 }
 
-// ------------------------------------------------------------- UMMA issuer
+// ---------------------------------------------------------- UMMA issuers
+// QK^T issuer: S^T[sb] = K_tile . Q^T over kKSteps steps of 32 bytes.  The K
+// tile is K-major with the 64-byte swizzle: column chunk j at j*cs, 8-row
+// groups at gs.
 template <int QM>
-__device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint32_t slot_addr, uint32_t qaddr,
-                                         int c) {
+__device__ void run_qk(const Stage1Params& p, Misc* ms, uint32_t ring, uint32_t qbase,
+                       uint32_t tmem, int it0, int it1) {
   using L = Layout<QM>;
-  if constexpr (L::kKv8) {
-    constexpr uint32_t idesc = make_idesc(0, 0, false, false, 128, L::kNq);
-    const int ks = (c == 4) ? 2 : 4;                 // rope slot: 64 dims = 2 K-steps
-    const uint32_t qa = qaddr + c * L::kQAtomBytes;
-    for (int kk = 0; kk < ks; ++kk) {
-      const uint64_t a = smem_desc(slot_addr + kk * 32, 16, 1024);
-      const uint64_t b = smem_desc(qa + kk * 32, 16, 1024);
-      umma_f8f6f4(tmem_s, a, b, idesc, (c | kk) != 0);
+  constexpr uint32_t idesc = L::kKv8 ? make_idesc(0, 0, false, false, 128, L::kNq)
+                                     : make_idesc(1, 1, false, false, 128, 16);
+  const uint32_t cs = p.chunk_stride, gs = p.group_stride;
+  TileCursor qc;
+  qc.init(p.items, it0, it1);
+  int q_ready = -1;
+  while (!qc.done()) {
+    const uint32_t t = qc.t, sb = t & 1u, s = t % L::kNumTiles;
+    if (q_ready != qc.k) {
+      if (!mbar_wait(smem_u32(&ms->q_full[qc.k & 1]), (qc.k >> 1) & 1, p.err, kErrMma)) break;
+      q_ready = qc.k;
     }
-  } else {
-    constexpr uint32_t idesc = make_idesc(1, 1, false, false, 128, 16);
-    const int ks = (c == 4) ? 4 : 8;                 // 16 dims per K-step
-    for (int kk = 0; kk < ks; ++kk) {
-      const uint32_t atom = kk >> 2, koff = (kk & 3) * 32;
-      const uint64_t a = smem_desc(slot_addr + atom * 16384 + koff, 16, 1024);
-      const uint64_t b = smem_desc(qaddr + (2 * c + atom) * L::kQAtomBytes + koff, 16, 1024);
-      umma_f16(tmem_s, a, b, idesc, (c | kk) != 0);
-    }
-  }
-}
-
-template <int QM>
-__device__ __forceinline__ bool issue_pv(const Stage1Params& p, Misc* ms, uint32_t ring,
-                                         uint32_t pbase, uint32_t tmem, uint32_t q0, uint32_t t,
-                                         bool first) {
-  using L = Layout<QM>;
-  const uint32_t pb = t & 1u;
-  if (!mbar_wait(smem_u32(&ms->p_full[pb]), (t >> 1) & 1u, p.err, kErrMma)) return false;
-  tc_fence_after();
-  const uint32_t pa = pbase + pb * L::kPBytes;
-  for (int c = 0; c < 4; ++c) {
-    const uint32_t slot = ring + ((q0 + c) % L::kNumSlots) * L::kSlotBytes;
-    if constexpr (L::kKv8) {
-      constexpr uint32_t idesc = make_idesc(0, 0, true, false, 128, 16);
-      for (int kk = 0; kk < 4; ++kk) {              // 32 tokens per K-step
-        const uint64_t a = smem_desc(slot + kk * 4096, 1024, 1024);
-        const uint64_t bh = smem_desc(pa + kk * 32, 16, 1024);
-        const uint64_t bl = smem_desc(pa + 2048 + kk * 32, 16, 1024);
-        const uint32_t acc = (first && kk == 0) ? 0u : 1u;
-        umma_f8f6f4(tmem + kColOhi + 16 * c, a, bh, idesc, acc);
-        umma_f8f6f4(tmem + kColOlo + 16 * c, a, bl, idesc, acc);
-      }
-    } else {
-      constexpr uint32_t idesc = make_idesc(1, 1, true, false, 128, 16);
-      for (int kk = 0; kk < 8; ++kk) {              // 16 tokens per K-step
-        const uint64_t a = smem_desc(slot + kk * 2048, 16384, 1024);
-        const uint64_t b = smem_desc(pa + (kk >> 2) * 2048 + (kk & 3) * 32, 16, 1024);
-        umma_f16(tmem + kColOhi + 16 * c, a, b, idesc, (first && kk == 0) ? 0u : 1u);
-      }
-    }
-  }
-  tc_commit(smem_u32(&ms->pv_done[pb]));
-  for (int c = 0; c < 4; ++c) tc_commit(smem_u32(&ms->empty[(q0 + c) % L::kNumSlots]));
-  return true;
-}
-
-template <int QM>
-__device__ void run_mma(const Stage1Params& p, Misc* ms, uint32_t ring, uint32_t qbase,
-                        uint32_t pbase, uint32_t tmem, int it0, int it1) {
-  using L = Layout<QM>;
-  uint32_t q = 0, g = 0;
-  bool ok = true;
-  bool pend = false, pend_first = false;
-  uint32_t pend_q = 0, pend_g = 0;
-  int k = 0;
-  for (int it = it0; it < it1 && ok; ++it, ++k) {
-    const WorkItem w = p.items[it];
-    const uint32_t qb = k & 1;
-    if (!mbar_wait(smem_u32(&ms->q_full[qb]), (k >> 1) & 1, p.err, kErrMma)) { ok = false; break; }
+    if (!mbar_wait(smem_u32(&ms->s_empty[sb]), ((t >> 1) & 1u) ^ 1u, p.err, kErrMma)) break;
+    if (!mbar_wait(smem_u32(&ms->full[s]), (t / L::kNumTiles) & 1u, p.err, kErrMma)) break;
     tc_fence_after();
-    const uint32_t qaddr = qbase + qb * L::kQBytes;
-    const int ntile = (w.tok_end - w.tok_begin + kTile - 1) / kTile;
-    for (int j = 0; j < ntile; ++j) {
-      const uint32_t sb = g & 1u;
-      if (!mbar_wait(smem_u32(&ms->s_empty[sb]), ((g >> 1) & 1u) ^ 1u, p.err, kErrMma)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      for (int c = 0; c < L::kSlotsPerTile; ++c) {
-        const uint32_t qq = q + c, s = qq % L::kNumSlots;
-        if (!mbar_wait(smem_u32(&ms->full[s]), (qq / L::kNumSlots) & 1u, p.err, kErrMma)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        issue_qk<QM>(tmem + kColS + 32 * sb, ring + s * L::kSlotBytes, qaddr, c);
-        if (c == 4) tc_commit(smem_u32(&ms->empty[s]));
-      }
-      if (!ok) break;
-      tc_commit(smem_u32(&ms->s_full[sb]));
-      if (j == ntile - 1) tc_commit(smem_u32(&ms->q_empty[qb]));
-      if constexpr (L::kLookahead) {
-        if (pend && !issue_pv<QM>(p, ms, ring, pbase, tmem, pend_q, pend_g, pend_first)) {
-          ok = false;
-          break;
-        }
-        pend = true;
-        pend_q = q;
-        pend_g = g;
-        pend_first = (j == 0);
-      } else {
-        if (!issue_pv<QM>(p, ms, ring, pbase, tmem, q, g, j == 0)) { ok = false; break; }
-      }
-      q += L::kSlotsPerTile;
-      ++g;
+    const uint32_t tile = ring + s * L::kTileBytes;
+    const uint32_t qaddr = qbase + (qc.k & 1) * L::kQBytes;
+    const uint32_t d = tmem + kColS + 32 * sb;
+#pragma unroll 2
+    for (int kk = 0; kk < L::kKSteps; ++kk) {
+      const uint64_t a = smem_desc(tile + (kk >> 1) * cs + (kk & 1) * 32, 16, gs, kSwizzle64B);
+      const uint64_t b =
+          smem_desc(qaddr + (kk >> 2) * L::kQAtomBytes + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+      if constexpr (L::kKv8)
+        umma_f8f6f4(d, a, b, idesc, kk != 0);
+      else
+        umma_f16(d, a, b, idesc, kk != 0);
     }
+    tc_commit(smem_u32(&ms->s_full[sb]));
+    if (qc.j == qc.ntile - 1) tc_commit(smem_u32(&ms->q_empty[qc.k & 1]));
+    qc.advance();
   }
-  if (L::kLookahead && ok && pend) issue_pv<QM>(p, ms, ring, pbase, tmem, pend_q, pend_g, pend_first);
-  // Drain: every UMMA issued by this thread has completed before TMEM is freed.
-  tc_commit(smem_u32(&ms->drain));
-  mbar_wait(smem_u32(&ms->drain), 0, p.err, kErrDrain);
+  tc_commit(smem_u32(&ms->drain[0]));
+  mbar_wait(smem_u32(&ms->drain[0]), 0, p.err, kErrDrain);
 }
 
-// Softmax / q-prep threads share named barriers, so a thread must never leave
-// alone: a wait that gives up raises the group's abort flag and the thread
-// carries on to the next named barrier, after which the whole group leaves.
+// PV issuer: O^T[128 dims of block c] (+)= V^T . P^T.  V^T is the tile read
+// MN-major: 64-dim atoms at cs (LBO), 8-token groups at gs (SBO).
+template <int QM>
+__device__ void run_pv(const Stage1Params& p, Misc* ms, uint32_t ring, uint32_t pbase,
+                       uint32_t tmem, int it0, int it1) {
+  using L = Layout<QM>;
+  const uint32_t cs = p.chunk_stride, gs = p.group_stride;
+  TileCursor pc;
+  pc.init(p.items, it0, it1);
+  while (!pc.done()) {
+    const uint32_t t = pc.t, pb = t & 1u, s = t % L::kNumTiles;
+    if (!mbar_wait(smem_u32(&ms->p_full[pb]), (t >> 1) & 1u, p.err, kErrMma)) break;
+    tc_fence_after();
+    const uint32_t tile = ring + s * L::kTileBytes;
+    const uint32_t pa = pbase + pb * L::kPBytes;
+    const bool first = pc.j == 0;
+    for (int c = 0; c < 4; ++c) {
+      const uint32_t d = tmem + kColO + L::kOCols * c;
+      if constexpr (L::kKv8) {
+        constexpr uint32_t idesc = make_idesc(0, 0, true, false, 128, 32);
+        const uint32_t blk = tile + (2 * c) * cs;                 // 128 dims = 2 chunks
+        for (int kk = 0; kk < 4; ++kk) {                          // 32 tokens = 4 groups
+          const uint64_t a = smem_desc(blk + kk * 4 * gs, cs, gs, kSwizzle64B);
+          const uint64_t b = smem_desc(pa + kk * 32, 16, 1024, kSwizzle128B);  // p_hi ; p_lo
+          umma_f8f6f4(d, a, b, idesc, (first && kk == 0) ? 0u : 1u);
+        }
+      } else {
+        constexpr uint32_t idesc = make_idesc(1, 1, true, false, 128, 16);
+        const uint32_t blk = tile + (4 * c) * cs;                 // 128 dims = 4 chunks
+        for (int kk = 0; kk < 8; ++kk) {                          // 16 tokens = 2 groups
+          const uint64_t a = smem_desc(blk + kk * 2 * gs, cs, gs, kSwizzle64B);
+          const uint64_t b =
+              smem_desc(pa + (kk >> 2) * 2048 + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+          umma_f16(d, a, b, idesc, (first && kk == 0) ? 0u : 1u);
+        }
+      }
+    }
+    tc_commit(smem_u32(&ms->pv_done[pb]));
+    tc_commit(smem_u32(&ms->empty[s]));      // QK^T of this tile completed before P existed
+    pc.advance();
+  }
+  tc_commit(smem_u32(&ms->drain[1]));
+  mbar_wait(smem_u32(&ms->drain[1]), 0, p.err, kErrDrain);
+}
+
+// Softmax threads share named barriers, so a thread must never leave alone:
+// a wait that gives up raises the group's abort flag and the thread carries
+// on to the next named barrier, after which the whole group leaves.
 __device__ __forceinline__ void wait_or_flag(uint32_t bar, uint32_t parity, int32_t* err,
                                              int32_t code, volatile int32_t* flag) {
   if (!mbar_wait(bar, parity, err, code)) *flag = 1;
 }
 
 // -------------------------------------------------------------- q prepare
-// 64 threads write q of the next item into a free q buffer in the UMMA
-// operand layout and publish the score factors.
+// One warp writes q of the next item into a free q buffer in the UMMA operand
+// layout (K-major, 128-byte swizzle) and publishes the score factors.
 template <int QM>
 __device__ void run_qprep(const Stage1Params& p, Misc* ms, uint8_t* qgen, int it0, int it1,
-                          int tq) {
+                          int lane) {
   using L = Layout<QM>;
   constexpr float kSmScale = 1.0f / 24.0f;          // 1/sqrt(576)
-  volatile int32_t* abort = &ms->abort_qp;
   int k = 0;
   for (int it = it0; it < it1; ++it, ++k) {
     const uint32_t qb = k & 1;
-    wait_or_flag(smem_u32(&ms->q_empty[qb]), ((k >> 1) & 1) ^ 1, p.err, kErrQPrep, abort);
-    named_bar_sync(2, 64);
-    if (*abort) return;
+    bool ok = true;
+    if (lane == 0) ok = mbar_wait(smem_u32(&ms->q_empty[qb]), ((k >> 1) & 1) ^ 1, p.err, kErrQPrep);
+    if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) return;
     const int b = p.items[it].b;
     uint8_t* dst = qgen + qb * L::kQBytes;
     float c_hi = 0.f, c_lo = 0.f;
     if constexpr (QM == kQBf16KvFp8) {
       const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
                                                         static_cast<int64_t>(b) * kHeads * kQkDim);
-      uint4 v[18];
       float amax = 0.f;
-#pragma unroll
-      for (int i = 0; i < 18; ++i) {
-        v[i] = __ldg(src + tq + 64 * i);
-        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v[i]);
+#pragma unroll 4
+      for (int i = 0; i < 36; ++i) {
+        const uint4 v = __ldg(src + lane + 32 * i);
+        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float2 f = __bfloat1622float2(h2[e]);
@@ -310,15 +324,14 @@ __device__ void run_qprep(const Stage1Params& p, Misc* ms, uint8_t* qgen, int it
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      if ((tq & 31) == 0) ms->qred[tq >> 5] = amax;
-      named_bar_sync(2, 64);
-      amax = fmaxf(fmaxf(ms->qred[0], ms->qred[1]), 1e-30f);
+      amax = fmaxf(amax, 1e-30f);
       const float s_hi = amax / 448.0f, inv_hi = 448.0f / amax;
-#pragma unroll
-      for (int i = 0; i < 18; ++i) {
-        const int vid = tq + 64 * i;
+#pragma unroll 4
+      for (int i = 0; i < 36; ++i) {
+        const int vid = lane + 32 * i;
         const int h = vid / 72, d0 = (vid % 72) * 8;
-        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v[i]);
+        const uint4 v = __ldg(src + vid);
+        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v);
         uint32_t hw[2], lw[2];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -330,10 +343,10 @@ __device__ void run_qprep(const Stage1Params& p, Misc* ms, uint8_t* qgen, int it
           const float ry = (f.y - hf.y * s_hi) * inv_hi * 16.0f;
           const __nv_fp8x2_storage_t lo =
               __nv_cvt_float2_to_fp8x2(make_float2(rx, ry), __NV_SATFINITE, __NV_E4M3);
-          const int w = e >> 1, sh = (e & 1) * 16;
-          if ((e & 1) == 0) { hw[w] = 0; lw[w] = 0; }
-          hw[w] |= static_cast<uint32_t>(hi) << sh;
-          lw[w] |= static_cast<uint32_t>(lo) << sh;
+          const int wd = e >> 1, sh = (e & 1) * 16;
+          if ((e & 1) == 0) { hw[wd] = 0; lw[wd] = 0; }
+          hw[wd] |= static_cast<uint32_t>(hi) << sh;
+          lw[wd] |= static_cast<uint32_t>(lo) << sh;
         }
         const int atom = d0 >> 7, x = d0 & 127;
         uint8_t* base = dst + atom * L::kQAtomBytes;
@@ -346,9 +359,9 @@ __device__ void run_qprep(const Stage1Params& p, Misc* ms, uint8_t* qgen, int it
     } else if constexpr (QM == kQFp8KvFp8) {
       const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.q) +
                                                         static_cast<int64_t>(b) * kHeads * kQkDim);
-#pragma unroll
-      for (int i = 0; i < 9; ++i) {
-        const int vid = tq + 64 * i;
+#pragma unroll 6
+      for (int i = 0; i < 18; ++i) {
+        const int vid = lane + 32 * i;
         const int h = vid / 36, d0 = (vid % 36) * 16;
         const uint4 v = __ldg(src + vid);
         *reinterpret_cast<uint4*>(dst + (d0 >> 7) * L::kQAtomBytes + sw128(h, d0 & 127)) = v;
@@ -356,9 +369,9 @@ __device__ void run_qprep(const Stage1Params& p, Misc* ms, uint8_t* qgen, int it
       c_hi = __ldg(p.q_scale) * __ldg(p.kv_scale) * kSmScale * kLog2e;
     } else {
       // bf16 operand for kind::f16; fp8 q is decoded exactly to bf16 first.
-#pragma unroll 2
-      for (int i = 0; i < 18; ++i) {
-        const int vid = tq + 64 * i;
+#pragma unroll 4
+      for (int i = 0; i < 36; ++i) {
+        const int vid = lane + 32 * i;
         const int h = vid / 72, d0 = (vid % 72) * 8;
         uint4 v;
         if constexpr (QM == kQBf16KvBf16) {
@@ -388,8 +401,8 @@ __device__ void run_qprep(const Stage1Params& p, Misc* ms, uint8_t* qgen, int it
       c_hi = (QM == kQFp8KvBf16 ? __ldg(p.q_scale) : 1.0f) * kSmScale * kLog2e;
     }
     fence_proxy_async_smem();
-    named_bar_sync(2, 64);
-    if (tq == 0) {
+    __syncwarp();
+    if (lane == 0) {
       ms->qscale[qb][0] = c_hi;
       ms->qscale[qb][1] = c_lo;
       mbar_arrive(smem_u32(&ms->q_full[qb]));
@@ -450,7 +463,8 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
   volatile int32_t* abort = &ms->abort_sm;
   const int qw = tid >> 5, lane = tid & 31;
   const uint32_t tl = tmem + (static_cast<uint32_t>(qw * 32) << 16);   // this warp's lanes
-  uint32_t g = 0, q = 0;
+  uint32_t g = 0;
+  const uint32_t cs = p.chunk_stride, gs = p.group_stride;
   int k = 0;
   float m[16], l[16];
   for (int it = it0; it < it1; ++it, ++k) {
@@ -462,7 +476,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
     if (*abort) return;
     if (tid == 0) mbar_arrive(smem_u32(&ms->q_empty[qb]));
     const int ntile = (w.tok_end - w.tok_begin + kTile - 1) / kTile;
-    for (int j = 0; j < ntile; ++j, ++g, q += L::kSlotsPerTile) {
+    for (int j = 0; j < ntile; ++j, ++g) {
       const uint32_t sb = g & 1u;
       wait_or_flag(smem_u32(&ms->s_full[sb]), (g >> 1) & 1u, p.err, kErrSoftmax, abort);
       tc_fence_after();
@@ -514,7 +528,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
         const int nparts = L::kKv8 ? 2 : 1;
         for (int part = 0; part < nparts; ++part) {
           for (int c = 0; c < 4; ++c) {
-            const uint32_t col = (part ? kColOlo : kColOhi) + 16 * c;
+            const uint32_t col = kColO + L::kOCols * c + 16 * part;
             float o[16];
             tmem_ld16(tl + col, o);
             tmem_wait_ld();
@@ -560,20 +574,16 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
         }
       }
       if (nvalid < kTile) {
-        // Tail tile: rows past the range may hold anything (stale slots,
+        // Tail tile: rows past the range may hold anything (stale tiles,
         // unused page slots); zero their V bytes so that 0 * V stays 0.
-        for (int c = 0; c < 4; ++c) {
-          const uint32_t qq = q + c, s2 = qq % L::kNumSlots;
-          wait_or_flag(smem_u32(&ms->full[s2]), (qq / L::kNumSlots) & 1u, p.err, kErrSoftmax,
-                       abort);
-          if (!valid) {
-            uint8_t* row = ring_gen + s2 * L::kSlotBytes + tid * 128;
-            const int nbox = L::kKv8 ? 1 : 2;
-            for (int cb = 0; cb < nbox; ++cb)
+        const uint32_t s2 = g % L::kNumTiles;
+        wait_or_flag(smem_u32(&ms->full[s2]), (g / L::kNumTiles) & 1u, p.err, kErrSoftmax, abort);
+        if (!valid) {
+          uint8_t* row = ring_gen + s2 * L::kTileBytes + (tid >> 3) * gs + (tid & 7) * 64;
+          for (int c = 0; c < L::kVChunks; ++c)
 #pragma unroll
-              for (int i = 0; i < 8; ++i)
-                reinterpret_cast<uint4*>(row + cb * 16384)[i] = make_uint4(0, 0, 0, 0);
-          }
+            for (int i = 0; i < 4; ++i)
+              reinterpret_cast<uint4*>(row + c * cs)[i] = make_uint4(0, 0, 0, 0);
         }
       }
       fence_proxy_async_smem();
@@ -595,10 +605,10 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
     const int slot = w.slot;
     for (int c = 0; c < 4; ++c) {
       float oh[16];
-      tmem_ld16(tl + kColOhi + 16 * c, oh);
+      tmem_ld16(tl + kColO + L::kOCols * c, oh);
       if constexpr (L::kKv8) {
         float ol[16];
-        tmem_ld16(tl + kColOlo + 16 * c, ol);
+        tmem_ld16(tl + kColO + L::kOCols * c + 16, ol);
         tmem_wait_ld();
 #pragma unroll
         for (int h = 0; h < 16; ++h) oh[h] = (oh[h] + ol[h] * (1.0f / kPLoScale)) * inv[h];
@@ -649,7 +659,7 @@ __global__ void __launch_bounds__(256, 1) mla_stage1_kernel(const __grid_constan
   const int it0 = p.cta_indptr[blockIdx.x], it1 = p.cta_indptr[blockIdx.x + 1];
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < L::kNumSlots; ++i) {
+    for (int i = 0; i < L::kNumTiles; ++i) {
       mbar_init(smem_u32(&ms->full[i]), 1);
       mbar_init(smem_u32(&ms->empty[i]), 1);
     }
@@ -660,10 +670,9 @@ __global__ void __launch_bounds__(256, 1) mla_stage1_kernel(const __grid_constan
       mbar_init(smem_u32(&ms->pv_done[i]), 1);
       mbar_init(smem_u32(&ms->q_full[i]), 1);
       mbar_init(smem_u32(&ms->q_empty[i]), 2);
+      mbar_init(smem_u32(&ms->drain[i]), 1);
     }
-    mbar_init(smem_u32(&ms->drain), 1);
     ms->abort_sm = 0;
-    ms->abort_qp = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) prefetch_tensormap(&p.tmap_kv);
@@ -679,11 +688,13 @@ __global__ void __launch_bounds__(256, 1) mla_stage1_kernel(const __grid_constan
   if (warp == 0) {
     run_producer<QM>(p, ms, ring, it0, it1, lane);
   } else if (warp == 1) {
-    if (lane == 0)
-      run_mma<QM>(p, ms, ring, ring + L::kQOff, ring + L::kPOff, tmem, it0, it1);
+    if (lane == 0) run_qk<QM>(p, ms, ring, ring + L::kQOff, tmem, it0, it1);
     __syncwarp();
-  } else if (warp < 4) {
-    run_qprep<QM>(p, ms, smem + L::kQOff, it0, it1, threadIdx.x - 64);
+  } else if (warp == 2) {
+    if (lane == 0) run_pv<QM>(p, ms, ring, ring + L::kPOff, tmem, it0, it1);
+    __syncwarp();
+  } else if (warp == 3) {
+    run_qprep<QM>(p, ms, smem + L::kQOff, it0, it1, lane);
   } else {
     run_softmax<QM>(p, ms, smem, smem + L::kPOff, tmem, it0, it1, threadIdx.x - 128);
   }
