@@ -164,6 +164,34 @@ mla_status mla_decode_run(mla_plan* plan, const void* q, const float* q_scale, c
 mla_status mla_decode_check(const mla_plan* plan, void* workspace, mla_stream_t stream);
 
 /*
+ * mla_decode_run_noalloc -- mla_decode_run without a caller-provided workspace.
+ *
+ * The pages have no counterpart of this call.  It is for callers that cannot
+ * allocate device memory (a plug-in or C client inside a process whose
+ * framework owns the device allocator, or code that must not allocate once
+ * it runs): the library keeps a fixed 16 MiB workspace array in device global
+ * memory, which every GPU that loads the library holds until the process
+ * exits.  Inputs, outputs and their rules are those of mla_decode_run.
+ *   - Plans needing more than 16 MiB (mla_plan_workspace_size) are rejected
+ *     with MLA_ERR_WORKSPACE before anything is enqueued.
+ *   - The first call on a device looks the array's address up
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
+ *   - Every call copies its plan's work table into the array (one
+ *     host-to-device copy on `stream`), which also clears the error word.
+ *   - All calls share the one array: calls that overlap on the GPU (other
+ *     streams, other threads) race and corrupt each other; order them.
+ * Errors: as mla_decode_run, plus MLA_ERR_WORKSPACE for an oversized plan
+ * and MLA_ERR_CUDA if the array's address cannot be obtained.
+ */
+mla_status mla_decode_run_noalloc(mla_plan* plan, const void* q, const float* q_scale,
+                                  const void* kv, const float* kv_scale, const uint8_t* kv_e8m0,
+                                  int64_t kv_e8m0_row_stride, int64_t kv_pool_rows,
+                                  const int32_t* kv_indices, void* out, float* lse,
+                                  mla_stream_t stream);
+
+/*
  * Optional instrumentation (the pages time their decode stages with CUDA
  * events, submission 695854, stage timings): when `before` / `after` are
  * non-NULL cudaEvent_t handles, every following mla_decode_run records

@@ -21,7 +21,7 @@ STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED", 3: "M
           4: "MLA_ERR_CUDA", 5: "MLA_ERR_DEVICE_TIMEOUT"}
 EXPORTS = ("mla_decode_plan", "mla_plan_workspace_size", "mla_plan_get_info", "mla_plan_get_work",
            "mla_plan_destroy", "mla_decode_run", "mla_decode_check", "mla_status_string",
-           "mla_plan_set_stage1_events")
+           "mla_plan_set_stage1_events", "mla_decode_run_noalloc")
 
 
 class MlaError(RuntimeError):
@@ -54,11 +54,12 @@ def _load():
     lib.mla_decode_run.argtypes = [P, P, P, P, P, P, i64, i64, P, P, sz, P, P, P]
     lib.mla_decode_check.argtypes = [P, P, P]
     lib.mla_plan_set_stage1_events.argtypes = [P, P, P]
+    lib.mla_decode_run_noalloc.argtypes = [P, P, P, P, P, P, i64, i64, P, P, P, P]
     lib.mla_status_string.argtypes = [ctypes.c_int]
     lib.mla_status_string.restype = ctypes.c_char_p
     for name in ("mla_decode_plan", "mla_plan_workspace_size", "mla_plan_get_info",
                  "mla_plan_get_work", "mla_decode_run", "mla_decode_check",
-                 "mla_plan_set_stage1_events"):
+                 "mla_plan_set_stage1_events", "mla_decode_run_noalloc"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
 
@@ -176,6 +177,24 @@ def mla_decode_run(plan: Plan, q, kv, out, *, workspace, q_scale=None, kv_scale=
                                  workspace.numel() * workspace.element_size(), _ptr(out),
                                  _ptr(lse), _stream_ptr(stream))
     _check("mla_decode_run", status)
+
+
+def mla_decode_run_noalloc(plan: Plan, q, kv, out, *, q_scale=None, kv_scale=None,
+                           kv_e8m0=None, kv_indices=None, lse=None,
+                           kv_pool_rows: int | None = None, stream=None) -> None:
+    """mla_decode_run for callers that cannot allocate a workspace: the
+    library's own fixed device array (16 MiB) is used instead.  Calls share
+    that array, so they must not overlap on the GPU."""
+    for name, t in (("q", q), ("kv", kv), ("out", out)):
+        if t is None or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    rows = int(kv.shape[0]) if kv_pool_rows is None else int(kv_pool_rows)
+    stride = 0 if kv_e8m0 is None else int(kv_e8m0.stride(0))
+    status = _lib.mla_decode_run_noalloc(plan.handle, _ptr(q), _ptr(q_scale), _ptr(kv),
+                                         _ptr(kv_scale), _ptr(kv_e8m0), stride, rows,
+                                         _ptr(kv_indices), _ptr(out), _ptr(lse),
+                                         _stream_ptr(stream))
+    _check("mla_decode_run_noalloc", status)
 
 
 def mla_decode_check(plan: Plan, workspace, stream=None) -> None:

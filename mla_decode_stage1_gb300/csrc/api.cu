@@ -13,30 +13,11 @@
 
 #include "mla_decode.h"
 #include "kernels.h"
+#include "plan.h"
 
 using mla::MergeJob;
 using mla::WorkItem;
 
-struct mla_plan {
-  int32_t bs = 0, page_size = 0, num_splits = 0;
-  int q_dtype = 0, kv_dtype = 0, qmode = 0;
-  int32_t num_ctas = 0, num_partials = 0;
-  int64_t total_tokens = 0, total_tiles = 0;
-  std::vector<int32_t> cta_indptr;
-  std::vector<WorkItem> items;
-  std::vector<MergeJob> jobs;
-  // workspace layout (byte offsets)
-  size_t off_err = 0, off_indptr = 0, off_items = 0, off_jobs = 0, off_part_o = 0,
-         off_part_lse = 0, ws_bytes = 0;
-  std::vector<uint8_t> table;  // image of [0, off_part_o) uploaded once per workspace
-  // per-run caches
-  void* uploaded_ws = nullptr;
-  CUtensorMap tmap;
-  const void* tmap_ptr = nullptr;
-  int64_t tmap_rows = -1;
-  int32_t tmap_box_rows = -1;
-  cudaEvent_t ev_before = nullptr, ev_after = nullptr;
-};
 
 namespace {
 
