@@ -77,6 +77,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t
   return true;
 }
 
+// Global load issued exactly where it is written (an asm volatile cannot be
+// re-materialised at its use, which would put the full memory latency back
+// on the consumer's path).
+__device__ __forceinline__ int32_t ld_nc_early(const int32_t* ptr) {
+  int32_t v;
+  asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(ptr));
+  return v;
+}
+
 // ------------------------------------------------------------------- proxies
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -19,7 +19,9 @@
 //    O^T[512 x 16] += V^T[512 x 128 tok] . P^T, four M=128 blocks in TMEM;
 //  * a tcgen05.mma costs the issuing thread about the same time whatever
 //    its N, so QK^T and PV are issued by two different warps that run side
-//    by side (warp 1 and warp 2); warp 0 is the TMA producer, warp 3
+//    by side: warps 1 and 3 each issue half of the QK^T K-steps into their
+//    own S accumulator, warps 2 and 9 issue PV for O blocks 0-1 and 2-3;
+//    warp 0 is the TMA producer, warp 8
 //    prepares q for the next item, warps 4-7 do the softmax and the
 //    epilogue (one thread per token / per output dim, TMEM lane = thread);
 //  * every mbarrier wait is bounded (see mbar_wait) and reports into the
@@ -75,7 +77,7 @@ struct Layout {
 // Misc region: barriers, reduction scratch, q scales, TMEM address.
 struct Misc {
   uint64_t full[4], empty[4];
-  uint64_t s_full[2], s_empty[2], p_full[2], pv_done[2], q_full[2], q_empty[2], drain[2];
+  uint64_t s_full[2], s_empty[2], p_full[2], pv_done[2], q_full[2], q_empty[2], drain[4];
   alignas(16) float red[2][4][16];   // read back as float4
   float qscale[2][2];
   uint32_t tmem_base;
@@ -84,10 +86,12 @@ struct Misc {
 static_assert(sizeof(Misc) <= 2048, "misc region");
 static_assert(offsetof(Misc, red) % 16 == 0, "reduction scratch is read as float4");
 
-// TMEM columns: S^T double buffer [0,64), then O^T: four 128-dim blocks of
-// kOCols columns (fp8 KV: 16 heads of p_hi, then 16 heads of p_lo).
+// TMEM columns: S^T as 2 buffers x 2 K-halves x 32 columns [0,128) (the two
+// QK^T issuers each accumulate half of the 576 dims), then O^T: four 128-dim
+// blocks of kOCols columns (fp8 KV: 16 heads of p_hi, then 16 of p_lo).
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColS = 0, kColO = 64;
+constexpr uint32_t kColS = 0, kColO = 128;
+constexpr int kThreads = 320;     // 10 warps
 
 // Byte offset of (row, byte x) inside a 128-byte-wide K-major operand with
 // the 128-byte swizzle (8-row / 1024-byte atoms, 16-byte chunks XOR row%8).
@@ -134,52 +138,77 @@ struct TileCursor {
   __device__ __forceinline__ int nvalid() const { return min(kTile, w.tok_end - t0()); }
 };
 
-// First KV row of TMA box `lane` of the cursor's tile (through the page
-// table), or 0 when the lane has no box.
-__device__ __forceinline__ int box_row(const Stage1Params& p, const TileCursor& c, int lane,
-                                       int nbox) {
-  if (c.done() || lane >= nbox) return 0;
+// What lane `lane` needs to issue its TMA box of one tile.  The page-table
+// entry is loaded when the tile is looked ahead at and only checked (and
+// turned into a row) when the box is issued, so the load overlaps the wait.
+struct BoxFetch {
+  int nbox;    // boxes of the tile (lanes [0, nbox) issue one each)
+  int raw;     // page id as loaded (page table), or the row (identity table)
+  int off;     // row offset inside the page
+};
+
+__device__ __forceinline__ BoxFetch box_fetch(const Stage1Params& p, const TileCursor& c,
+                                              int lane) {
+  BoxFetch f{0, 0, 0};
+  if (c.done()) return f;
+  f.nbox = (c.nvalid() + p.box_rows - 1) / p.box_rows;
+  if (lane >= f.nbox) return f;
   const int pos = c.t0() + lane * p.box_rows;
-  if (p.kv_indices == nullptr) return c.w.page_base * p.page_size + pos;
-  int page = __ldg(p.kv_indices + c.w.page_base + pos / p.page_size);
+  if (p.kv_indices == nullptr) {
+    f.raw = c.w.page_base * p.page_size + pos;
+  } else {
+    f.raw = ld_nc_early(p.kv_indices + c.w.page_base + pos / p.page_size);
+    f.off = pos % p.page_size;
+  }
+  return f;
+}
+
+__device__ __forceinline__ int box_row(const Stage1Params& p, const BoxFetch& f, int lane) {
+  if (lane >= f.nbox) return 0;
+  if (p.kv_indices == nullptr) return f.raw;
+  int page = f.raw;
   if (page < 0 || static_cast<int64_t>(page + 1) * p.page_size > p.pool_rows) {
     atomicOr(p.err, kErrBadPage);
     page = 0;
   }
-  return page * p.page_size + pos % p.page_size;
+  return page * p.page_size + f.off;
 }
 
 // ---------------------------------------------------------------- producer
-// One warp: lane i owns TMA box i of every tile.  The page-table entries of
-// the next tile are fetched while the current tile is being issued.
+// One warp: lane i owns TMA box i of every tile.  Page-table entries are
+// fetched two tiles ahead of the tile being issued.
 template <int QM>
 __device__ void run_producer(const Stage1Params& p, Misc* ms, uint32_t ring, int it0, int it1,
                              int lane) {
   using L = Layout<QM>;
   const uint64_t pol = l2_policy_evict_first();
-  const int box_rows = p.box_rows;
-  const uint32_t box_bytes = static_cast<uint32_t>(box_rows) * L::kRowBytes;
-  TileCursor cur;
+  const uint32_t box_bytes = static_cast<uint32_t>(p.box_rows) * L::kRowBytes;
+  TileCursor cur, ahead;
   cur.init(p.items, it0, it1);
-  int nbox_next = cur.done() ? 0 : (cur.nvalid() + box_rows - 1) / box_rows;
-  int row_next = box_row(p, cur, lane, nbox_next);
+  ahead = cur;
+  BoxFetch f0 = box_fetch(p, ahead, lane);
+  ahead.advance();
+  BoxFetch f1 = box_fetch(p, ahead, lane);
+  ahead.advance();
   bool ok = true;
   uint32_t t = 0;
   while (!cur.done() && ok) {
-    const int nbox = nbox_next, row = row_next;
-    TileCursor nxt = cur;
-    nxt.advance();
-    nbox_next = nxt.done() ? 0 : (nxt.nvalid() + box_rows - 1) / box_rows;
-    row_next = box_row(p, nxt, lane, nbox_next);
+    const BoxFetch f = f0;
+    f0 = f1;
+    f1 = box_fetch(p, ahead, lane);
+    ahead.advance();
     const uint32_t s = t % L::kNumTiles, ph = (t / L::kNumTiles) & 1u;
-    if (lane == 0) ok = mbar_wait(smem_u32(&ms->empty[s]), ph ^ 1u, p.err, kErrProducer);
-    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    // every lane waits: a lone lane-0 wait followed by a broadcast cost
+    // about 1500 cycles of reconvergence per tile on GB300
+    ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ms->empty[s]), ph ^ 1u, p.err, kErrProducer));
     if (!ok) break;
+    const int row = box_row(p, f, lane);
     const uint32_t full = smem_u32(&ms->full[s]);
-    if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(nbox) * box_bytes);
+    if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(f.nbox) * box_bytes);
     __syncwarp();
-    if (lane < nbox) tma_load_3d(ring + s * L::kTileBytes + lane * box_bytes, &p.tmap_kv, full, 0, row, 0, pol);
-    cur = nxt;
+    if (lane < f.nbox)
+      tma_load_3d(ring + s * L::kTileBytes + lane * box_bytes, &p.tmap_kv, full, 0, row, 0, pol);
+    cur.advance();
     ++t;
   }
   // Drain: wait (bounded) until the last copies issued into each tile landed.
@@ -200,7 +229,7 @@ __device__ void run_producer(const Stage1Params& p, Misc* ms, uint32_t ring, int
 // groups at gs.
 template <int QM>
 __device__ void run_qk(const Stage1Params& p, Misc* ms, uint32_t ring, uint32_t qbase,
-                       uint32_t tmem, int it0, int it1) {
+                       uint32_t tmem, int it0, int it1, int half, int lane) {
   using L = Layout<QM>;
   constexpr uint32_t idesc = L::kKv8 ? make_idesc(0, 0, false, false, 128, L::kNq)
                                      : make_idesc(1, 1, false, false, 128, 16);
@@ -210,51 +239,65 @@ __device__ void run_qk(const Stage1Params& p, Misc* ms, uint32_t ring, uint32_t 
   int q_ready = -1;
   while (!qc.done()) {
     const uint32_t t = qc.t, sb = t & 1u, s = t % L::kNumTiles;
+    // the whole warp waits (converged); lane 0 issues
     if (q_ready != qc.k) {
-      if (!mbar_wait(smem_u32(&ms->q_full[qc.k & 1]), (qc.k >> 1) & 1, p.err, kErrMma)) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ms->q_full[qc.k & 1]), (qc.k >> 1) & 1,
+                                             p.err, kErrMma)))
+        break;
       q_ready = qc.k;
     }
-    if (!mbar_wait(smem_u32(&ms->s_empty[sb]), ((t >> 1) & 1u) ^ 1u, p.err, kErrMma)) break;
-    if (!mbar_wait(smem_u32(&ms->full[s]), (t / L::kNumTiles) & 1u, p.err, kErrMma)) break;
+    if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ms->s_empty[sb]), ((t >> 1) & 1u) ^ 1u,
+                                           p.err, kErrMma)))
+      break;
+    if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ms->full[s]), (t / L::kNumTiles) & 1u,
+                                           p.err, kErrMma)))
+      break;
     tc_fence_after();
     const uint32_t tile = ring + s * L::kTileBytes;
     const uint32_t qaddr = qbase + (qc.k & 1) * L::kQBytes;
-    const uint32_t d = tmem + kColS + 32 * sb;
-#pragma unroll 2
-    for (int kk = 0; kk < L::kKSteps; ++kk) {
+    const uint32_t d = tmem + kColS + 64 * sb + 32 * half;
+    const int k0 = half * (L::kKSteps / 2), k1 = k0 + L::kKSteps / 2;
+    if (lane == 0) {
+#pragma unroll 3
+    for (int kk = k0; kk < k1; ++kk) {
       const uint64_t a = smem_desc(tile + (kk >> 1) * cs + (kk & 1) * 32, 16, gs, kSwizzle64B);
       const uint64_t b =
           smem_desc(qaddr + (kk >> 2) * L::kQAtomBytes + (kk & 3) * 32, 16, 1024, kSwizzle128B);
       if constexpr (L::kKv8)
-        umma_f8f6f4(d, a, b, idesc, kk != 0);
+        umma_f8f6f4(d, a, b, idesc, kk != k0);
       else
-        umma_f16(d, a, b, idesc, kk != 0);
+        umma_f16(d, a, b, idesc, kk != k0);
     }
     tc_commit(smem_u32(&ms->s_full[sb]));
     if (qc.j == qc.ntile - 1) tc_commit(smem_u32(&ms->q_empty[qc.k & 1]));
+    }
+    __syncwarp();
     qc.advance();
   }
-  tc_commit(smem_u32(&ms->drain[0]));
-  mbar_wait(smem_u32(&ms->drain[0]), 0, p.err, kErrDrain);
+  if (lane == 0) tc_commit(smem_u32(&ms->drain[half]));
+  mbar_wait(smem_u32(&ms->drain[half]), 0, p.err, kErrDrain);
 }
 
 // PV issuer: O^T[128 dims of block c] (+)= V^T . P^T.  V^T is the tile read
 // MN-major: 64-dim atoms at cs (LBO), 8-token groups at gs (SBO).
 template <int QM>
 __device__ void run_pv(const Stage1Params& p, Misc* ms, uint32_t ring, uint32_t pbase,
-                       uint32_t tmem, int it0, int it1) {
+                       uint32_t tmem, int it0, int it1, int half, int lane) {
   using L = Layout<QM>;
   const uint32_t cs = p.chunk_stride, gs = p.group_stride;
   TileCursor pc;
   pc.init(p.items, it0, it1);
   while (!pc.done()) {
     const uint32_t t = pc.t, pb = t & 1u, s = t % L::kNumTiles;
-    if (!mbar_wait(smem_u32(&ms->p_full[pb]), (t >> 1) & 1u, p.err, kErrMma)) break;
+    if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ms->p_full[pb]), (t >> 1) & 1u, p.err,
+                                           kErrMma)))
+      break;
     tc_fence_after();
     const uint32_t tile = ring + s * L::kTileBytes;
     const uint32_t pa = pbase + pb * L::kPBytes;
     const bool first = pc.j == 0;
-    for (int c = 0; c < 4; ++c) {
+    if (lane == 0) {
+    for (int c = 2 * half; c < 2 * half + 2; ++c) {
       const uint32_t d = tmem + kColO + L::kOCols * c;
       if constexpr (L::kKv8) {
         constexpr uint32_t idesc = make_idesc(0, 0, true, false, 128, 32);
@@ -277,10 +320,12 @@ __device__ void run_pv(const Stage1Params& p, Misc* ms, uint32_t ring, uint32_t 
     }
     tc_commit(smem_u32(&ms->pv_done[pb]));
     tc_commit(smem_u32(&ms->empty[s]));      // QK^T of this tile completed before P existed
+    }
+    __syncwarp();
     pc.advance();
   }
-  tc_commit(smem_u32(&ms->drain[1]));
-  mbar_wait(smem_u32(&ms->drain[1]), 0, p.err, kErrDrain);
+  if (lane == 0) tc_commit(smem_u32(&ms->drain[2 + half]));
+  mbar_wait(smem_u32(&ms->drain[2 + half]), 0, p.err, kErrDrain);
 }
 
 // Softmax threads share named barriers, so a thread must never leave alone:
@@ -302,9 +347,9 @@ __device__ void run_qprep(const Stage1Params& p, Misc* ms, uint8_t* qgen, int it
   int k = 0;
   for (int it = it0; it < it1; ++it, ++k) {
     const uint32_t qb = k & 1;
-    bool ok = true;
-    if (lane == 0) ok = mbar_wait(smem_u32(&ms->q_empty[qb]), ((k >> 1) & 1) ^ 1, p.err, kErrQPrep);
-    if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) return;
+    if (!__all_sync(0xffffffffu,
+                    mbar_wait(smem_u32(&ms->q_empty[qb]), ((k >> 1) & 1) ^ 1, p.err, kErrQPrep)))
+      return;
     const int b = p.items[it].b;
     uint8_t* dst = qgen + qb * L::kQBytes;
     float c_hi = 0.f, c_lo = 0.f;
@@ -482,18 +527,21 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
       tc_fence_after();
       float s[16];
       {
-        float a[16];
-        tmem_ld16(tl + kColS + 32 * sb, a);
+        const uint32_t sc = tl + kColS + 64 * sb;
+        float a0[16], a1[16];
+        tmem_ld16(sc, a0);
+        tmem_ld16(sc + 32, a1);
         if constexpr (L::kNq == 32) {
-          float bl[16];
-          tmem_ld16(tl + kColS + 32 * sb + 16, bl);
+          float b0[16], b1[16];
+          tmem_ld16(sc + 16, b0);
+          tmem_ld16(sc + 48, b1);
           tmem_wait_ld();
 #pragma unroll
-          for (int h = 0; h < 16; ++h) s[h] = a[h] * c_hi + bl[h] * c_lo;
+          for (int h = 0; h < 16; ++h) s[h] = (a0[h] + a1[h]) * c_hi + (b0[h] + b1[h]) * c_lo;
         } else {
           tmem_wait_ld();
 #pragma unroll
-          for (int h = 0; h < 16; ++h) s[h] = a[h] * c_hi;
+          for (int h = 0; h < 16; ++h) s[h] = (a0[h] + a1[h]) * c_hi;
         }
       }
       tc_fence_before();
@@ -648,7 +696,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
 
 // -------------------------------------------------------------------- kernel
 template <int QM>
-__global__ void __launch_bounds__(256, 1) mla_stage1_kernel(const __grid_constant__ Stage1Params p) {
+__global__ void __launch_bounds__(kThreads, 1) mla_stage1_kernel(const __grid_constant__ Stage1Params p) {
   using L = Layout<QM>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -661,17 +709,17 @@ __global__ void __launch_bounds__(256, 1) mla_stage1_kernel(const __grid_constan
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::kNumTiles; ++i) {
       mbar_init(smem_u32(&ms->full[i]), 1);
-      mbar_init(smem_u32(&ms->empty[i]), 1);
+      mbar_init(smem_u32(&ms->empty[i]), 2);         // both PV issuers
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&ms->s_full[i]), 1);
+      mbar_init(smem_u32(&ms->s_full[i]), 2);        // both QK^T issuers
       mbar_init(smem_u32(&ms->s_empty[i]), 128);
       mbar_init(smem_u32(&ms->p_full[i]), 128);
-      mbar_init(smem_u32(&ms->pv_done[i]), 1);
+      mbar_init(smem_u32(&ms->pv_done[i]), 2);       // both PV issuers
       mbar_init(smem_u32(&ms->q_full[i]), 1);
-      mbar_init(smem_u32(&ms->q_empty[i]), 2);
-      mbar_init(smem_u32(&ms->drain[i]), 1);
+      mbar_init(smem_u32(&ms->q_empty[i]), 3);       // both QK^T issuers + softmax
     }
+    for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&ms->drain[i]), 1);
     ms->abort_sm = 0;
     fence_mbar_init();
   }
@@ -687,13 +735,11 @@ __global__ void __launch_bounds__(256, 1) mla_stage1_kernel(const __grid_constan
 
   if (warp == 0) {
     run_producer<QM>(p, ms, ring, it0, it1, lane);
-  } else if (warp == 1) {
-    if (lane == 0) run_qk<QM>(p, ms, ring, ring + L::kQOff, tmem, it0, it1);
-    __syncwarp();
-  } else if (warp == 2) {
-    if (lane == 0) run_pv<QM>(p, ms, ring, ring + L::kPOff, tmem, it0, it1);
-    __syncwarp();
-  } else if (warp == 3) {
+  } else if (warp == 1 || warp == 3) {
+    run_qk<QM>(p, ms, ring, ring + L::kQOff, tmem, it0, it1, warp == 3 ? 1 : 0, lane);
+  } else if (warp == 2 || warp == 9) {
+    run_pv<QM>(p, ms, ring, ring + L::kPOff, tmem, it0, it1, warp == 9 ? 1 : 0, lane);
+  } else if (warp == 8) {
     run_qprep<QM>(p, ms, smem + L::kQOff, it0, it1, lane);
   } else {
     run_softmax<QM>(p, ms, smem, smem + L::kPOff, tmem, it0, it1, threadIdx.x - 128);
@@ -723,7 +769,7 @@ static cudaError_t launch_t(const Stage1Params& p, int num_ctas, cudaStream_t st
   cudaError_t e = cudaFuncSetAttribute(mla_stage1_kernel<QM>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  mla_stage1_kernel<QM><<<num_ctas, 256, smem, stream>>>(p);
+  mla_stage1_kernel<QM><<<num_ctas, kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
