@@ -23,6 +23,9 @@ __global__ void __launch_bounds__(256) mla_stage2_kernel(const Stage2Params p) {
   const int lane = threadIdx.x & 31;
   const int job = gw >> 4, h = gw & 15;
   if (job >= p.num_jobs) return;
+  // Launched as a programmatic dependent of stage 1: wait here until stage 1
+  // has completed and its partials are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const MergeJob J = p.jobs[job];
   uint16_t* out = p.out + (static_cast<int64_t>(J.b) * kHeads + h) * kVDim;
   float acc[16];
@@ -68,8 +71,19 @@ __global__ void __launch_bounds__(256) mla_stage2_kernel(const Stage2Params p) {
 cudaError_t launch_stage2(const Stage2Params& p, cudaStream_t stream) {
   if (p.num_jobs <= 0) return cudaSuccess;
   const int warps = p.num_jobs * kHeads;
-  mla_stage2_kernel<<<(warps + 7) / 8, 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  // Programmatic dependent launch: the merge grid is scheduled while stage 1
+  // drains, instead of after a full launch gap.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((warps + 7) / 8);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mla_stage2_kernel, p);
 }
 
 }  // namespace mla
