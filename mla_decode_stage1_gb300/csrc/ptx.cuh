@@ -205,11 +205,12 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) 
 // ------------------------------------------------------------- descriptors
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading
 // and stride byte offsets (all >> 4), descriptor version 1 at bit 46, swizzle
-// mode in bits 61-63 (2 = 128-byte, 4 = 64-byte swizzle).  Base offset 0:
+// mode in bits 61-63 (2 = 128-byte, 4 = 64-byte, 6 = 32-byte swizzle).  Base offset 0:
 // every operand tile starts on its swizzle-atom boundary; K steps inside an
 // atom only move the start address.
 constexpr uint32_t kSwizzle128B = 2;
 constexpr uint32_t kSwizzle64B = 4;
+constexpr uint32_t kSwizzle32B = 6;
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes,
                                               uint32_t sbo_bytes, uint32_t swizzle) {
   uint64_t d = 0;

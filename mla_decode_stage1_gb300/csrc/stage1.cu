@@ -31,8 +31,9 @@
 // the per-tensor scales folded into one score factor and into l.  A bf16 q
 // meeting fp8 KV is split into q_hi + q_lo (two e4m3 terms with a per-request
 // scale, ~bf16 precision) that share one UMMA with N = 32.  p is likewise
-// split into p_hi + 2^-4 p_lo e4m3 terms, stacked as the 32 rows of one PV
-// operand so that one UMMA accumulates both parts (TMEM columns 0-15, 16-31).
+// split into p_hi + 2^-4 p_lo e4m3 terms, stacked as the 32 columns of one
+// MN-major PV operand (one 32-byte row per token) so that one UMMA
+// accumulates both parts (TMEM columns 0-15, 16-31).
 // bf16 KV runs kind::f16 with bf16 q and bf16 p.
 
 #include <cstddef>
@@ -258,11 +259,13 @@ __device__ void run_qk(const Stage1Params& p, Misc* ms, uint32_t ring, uint32_t 
     const uint32_t d = tmem + kColS + 64 * sb + 32 * half;
     const int k0 = half * (L::kKSteps / 2), k1 = k0 + L::kKSteps / 2;
     if (lane == 0) {
+    // descriptors built once per tile; a K step only moves the start address
+    const uint64_t a0 = smem_desc(tile, 16, gs, kSwizzle64B);
+    const uint64_t b0 = smem_desc(qaddr, 16, 1024, kSwizzle128B);
 #pragma unroll 3
     for (int kk = k0; kk < k1; ++kk) {
-      const uint64_t a = smem_desc(tile + (kk >> 1) * cs + (kk & 1) * 32, 16, gs, kSwizzle64B);
-      const uint64_t b =
-          smem_desc(qaddr + (kk >> 2) * L::kQAtomBytes + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+      const uint64_t a = a0 + (((kk >> 1) * cs + (kk & 1) * 32) >> 4);
+      const uint64_t b = b0 + (((kk >> 2) * L::kQAtomBytes + (kk & 3) * 32) >> 4);
       if constexpr (L::kKv8)
         umma_f8f6f4(d, a, b, idesc, kk != k0);
       else
@@ -299,21 +302,24 @@ __device__ void run_pv(const Stage1Params& p, Misc* ms, uint32_t ring, uint32_t 
     if (lane == 0) {
     for (int c = 2 * half; c < 2 * half + 2; ++c) {
       const uint32_t d = tmem + kColO + L::kOCols * c;
+      // B = P^T, MN-major with the 32-byte swizzle: one 32-byte row per token
+      // (fp8: 16 heads of p_hi then 16 of p_lo; bf16: 16 heads), 8-token
+      // groups of 256 bytes.
+      const uint64_t b0 = smem_desc(pa, 256, 256, kSwizzle32B);
       if constexpr (L::kKv8) {
-        constexpr uint32_t idesc = make_idesc(0, 0, true, false, 128, 32);
-        const uint32_t blk = tile + (2 * c) * cs;                 // 128 dims = 2 chunks
+        constexpr uint32_t idesc = make_idesc(0, 0, true, true, 128, 32);
+        const uint64_t a0 = smem_desc(tile + (2 * c) * cs, cs, gs, kSwizzle64B);  // 2 chunks
         for (int kk = 0; kk < 4; ++kk) {                          // 32 tokens = 4 groups
-          const uint64_t a = smem_desc(blk + kk * 4 * gs, cs, gs, kSwizzle64B);
-          const uint64_t b = smem_desc(pa + kk * 32, 16, 1024, kSwizzle128B);  // p_hi ; p_lo
+          const uint64_t a = a0 + ((kk * 4 * gs) >> 4);
+          const uint64_t b = b0 + ((kk * 1024) >> 4);
           umma_f8f6f4(d, a, b, idesc, (first && kk == 0) ? 0u : 1u);
         }
       } else {
-        constexpr uint32_t idesc = make_idesc(1, 1, true, false, 128, 16);
-        const uint32_t blk = tile + (4 * c) * cs;                 // 128 dims = 4 chunks
+        constexpr uint32_t idesc = make_idesc(1, 1, true, true, 128, 16);
+        const uint64_t a0 = smem_desc(tile + (4 * c) * cs, cs, gs, kSwizzle64B);  // 4 chunks
         for (int kk = 0; kk < 8; ++kk) {                          // 16 tokens = 2 groups
-          const uint64_t a = smem_desc(blk + kk * 2 * gs, cs, gs, kSwizzle64B);
-          const uint64_t b =
-              smem_desc(pa + (kk >> 2) * 2048 + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+          const uint64_t a = a0 + ((kk * 2 * gs) >> 4);
+          const uint64_t b = b0 + ((kk * 512) >> 4);
           umma_f16(d, a, b, idesc, (first && kk == 0) ? 0u : 1u);
         }
       }
@@ -598,8 +604,12 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
       // P buffer (g & 1) is free once PV of tile g-2 completed.
       if (g >= 2)
         wait_or_flag(smem_u32(&ms->pv_done[sb]), ((g >> 1) - 1) & 1u, p.err, kErrSoftmax, abort);
-      uint8_t* pbuf = pgen + sb * L::kPBytes;
+      // This token's row of P^T: 32 bytes, two 16-byte halves swapped on
+      // every other group of 4 tokens (32-byte swizzle: bit 4 ^= bit 7).
+      uint8_t* prow = pgen + sb * L::kPBytes + tid * 32;
+      const uint32_t flip = ((tid >> 2) & 1u) << 4;
       if constexpr (L::kKv8) {
+        uint32_t hw[4], lw[4];
 #pragma unroll
         for (int h = 0; h < 16; h += 2) {
           const __nv_fp8x2_storage_t hi =
@@ -608,18 +618,22 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
           const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
               make_float2((pv[h] - hf.x) * kPLoScale, (pv[h + 1] - hf.y) * kPLoScale),
               __NV_SATFINITE, __NV_E4M3);
-          pbuf[sw128(h, tid)] = static_cast<uint8_t>(hi & 0xFF);
-          pbuf[sw128(h + 1, tid)] = static_cast<uint8_t>(hi >> 8);
-          pbuf[2048 + sw128(h, tid)] = static_cast<uint8_t>(lo & 0xFF);
-          pbuf[2048 + sw128(h + 1, tid)] = static_cast<uint8_t>(lo >> 8);
+          const int wd = h >> 2, sh = (h & 2) * 8;
+          if ((h & 2) == 0) { hw[wd] = 0; lw[wd] = 0; }
+          hw[wd] |= static_cast<uint32_t>(hi) << sh;
+          lw[wd] |= static_cast<uint32_t>(lo) << sh;
         }
+        *reinterpret_cast<uint4*>(prow + (0u ^ flip)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *reinterpret_cast<uint4*>(prow + (16u ^ flip)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
       } else {
-        const uint32_t atom = tid >> 6, x = (tid & 63) * 2;
+        uint32_t bw[8];
 #pragma unroll
-        for (int h = 0; h < 16; ++h) {
-          const __nv_bfloat16 v = __float2bfloat16_rn(pv[h]);
-          *reinterpret_cast<__nv_bfloat16*>(pbuf + atom * 2048 + sw128(h, x)) = v;
+        for (int h = 0; h < 16; h += 2) {
+          const __nv_bfloat162 v = __floats2bfloat162_rn(pv[h], pv[h + 1]);
+          bw[h >> 1] = *reinterpret_cast<const uint32_t*>(&v);
         }
+        *reinterpret_cast<uint4*>(prow + (0u ^ flip)) = make_uint4(bw[0], bw[1], bw[2], bw[3]);
+        *reinterpret_cast<uint4*>(prow + (16u ^ flip)) = make_uint4(bw[4], bw[5], bw[6], bw[7]);
       }
       if (nvalid < kTile) {
         // Tail tile: rows past the range may hold anything (stale tiles,
