@@ -30,6 +30,7 @@ int qmode_of(int q_dtype, int kv_dtype) {
   if (q_dtype == MLA_DTYPE_FP8_E4M3 && kv_dtype == MLA_DTYPE_FP8_E4M3) return mla::kQFp8KvFp8;
   if (q_dtype == MLA_DTYPE_BF16 && kv_dtype == MLA_DTYPE_FP8_E4M3) return mla::kQBf16KvFp8;
   if (q_dtype == MLA_DTYPE_FP8_E4M3 && kv_dtype == MLA_DTYPE_BF16) return mla::kQFp8KvBf16;
+  if (q_dtype == MLA_DTYPE_BF16 && kv_dtype == MLA_DTYPE_MXFP4) return mla::kQBf16KvMx;
   return -1;
 }
 
@@ -167,6 +168,29 @@ bool make_kv_map(CUtensorMap* map, const void* kv, int kv_dtype, int64_t rows, i
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// MXFP4 pool: packed rows of 288 bytes as a 3-D tensor {144 B, row, half};
+// a box of box_rows rows lands as [half][row][144 B] (no swizzle).  Scale
+// rows (stride a multiple of 16, >= 32 bytes): 32-byte boxes, [row][32 B].
+bool make_mx_maps(CUtensorMap* kvmap, CUtensorMap* scmap, const void* kv, const uint8_t* e8m0,
+                  int64_t e8m0_stride, int64_t rows, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {144, static_cast<cuuint64_t>(rows), 2};
+  const cuuint64_t strides[2] = {288, 144};
+  const cuuint32_t box[3] = {144, static_cast<cuuint32_t>(box_rows), 2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  if (enc(kvmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(kv), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  const cuuint64_t sdims[2] = {32, static_cast<cuuint64_t>(rows)};
+  const cuuint64_t sstr[1] = {static_cast<cuuint64_t>(e8m0_stride)};
+  const cuuint32_t sbox[2] = {32, static_cast<cuuint32_t>(box_rows)};
+  return enc(scmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(e8m0), sdims, sstr,
+             sbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 }  // namespace
@@ -278,8 +302,6 @@ mla_status mla_decode_run(mla_plan* plan, const void* q, const float* q_scale, c
                           int64_t kv_e8m0_row_stride, int64_t kv_pool_rows,
                           const int32_t* kv_indices, void* workspace, size_t workspace_bytes,
                           void* out, float* lse, mla_stream_t stream_) {
-  (void)kv_e8m0;
-  (void)kv_e8m0_row_stride;
   if (plan == nullptr || q == nullptr || kv == nullptr || out == nullptr || workspace == nullptr)
     return MLA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(out, 16) || !aligned(workspace, 256))
@@ -287,6 +309,10 @@ mla_status mla_decode_run(mla_plan* plan, const void* q, const float* q_scale, c
   if (kv_pool_rows < 1 || kv_pool_rows > INT32_MAX) return MLA_ERR_INVALID_ARG;
   if (plan->q_dtype == MLA_DTYPE_FP8_E4M3 && q_scale == nullptr) return MLA_ERR_INVALID_ARG;
   if (plan->kv_dtype == MLA_DTYPE_FP8_E4M3 && kv_scale == nullptr) return MLA_ERR_INVALID_ARG;
+  if (plan->kv_dtype == MLA_DTYPE_MXFP4) {
+    if (kv_e8m0 == nullptr || !aligned(kv_e8m0, 16)) return MLA_ERR_INVALID_ARG;
+    if (kv_e8m0_row_stride < 32 || kv_e8m0_row_stride % 16 != 0) return MLA_ERR_UNSUPPORTED;
+  }
   if (workspace_bytes < plan->ws_bytes) return MLA_ERR_WORKSPACE;
   // Identity table: one TMA box of 128 rows per tile.  Page table: one box
   // per 8-row group (a group never straddles a page).
@@ -296,10 +322,18 @@ mla_status mla_decode_run(mla_plan* plan, const void* q, const float* q_scale, c
     box_rows = 8;
     if (kv_pool_rows % plan->page_size != 0) return MLA_ERR_INVALID_ARG;
   }
+  // bytes per row of the tile the UMMAs read (MXFP4 is dequantised to e4m3)
   const uint32_t row_bytes = mla::kQkDim * (plan->kv_dtype == MLA_DTYPE_BF16 ? 2 : 1);
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-  if (plan->tmap_ptr != kv || plan->tmap_rows != kv_pool_rows || plan->tmap_box_rows != box_rows) {
-    if (!make_kv_map(&plan->tmap, kv, plan->kv_dtype, kv_pool_rows, box_rows)) return MLA_ERR_CUDA;
+  if (plan->tmap_ptr != kv || plan->tmap_rows != kv_pool_rows || plan->tmap_box_rows != box_rows ||
+      plan->tmap_sc_ptr != kv_e8m0 || plan->tmap_sc_stride != kv_e8m0_row_stride) {
+    const bool ok = plan->kv_dtype == MLA_DTYPE_MXFP4
+                        ? make_mx_maps(&plan->tmap, &plan->tmap_sc, kv, kv_e8m0, kv_e8m0_row_stride,
+                                       kv_pool_rows, box_rows)
+                        : make_kv_map(&plan->tmap, kv, plan->kv_dtype, kv_pool_rows, box_rows);
+    if (!ok) return MLA_ERR_CUDA;
+    plan->tmap_sc_ptr = kv_e8m0;
+    plan->tmap_sc_stride = kv_e8m0_row_stride;
     plan->tmap_ptr = kv;
     plan->tmap_rows = kv_pool_rows;
     plan->tmap_box_rows = box_rows;
@@ -317,6 +351,7 @@ mla_status mla_decode_run(mla_plan* plan, const void* q, const float* q_scale, c
   if (plan->num_ctas > 0) {
     mla::Stage1Params p{};
     p.tmap_kv = plan->tmap;
+    p.tmap_sc = plan->tmap_sc;
     p.q = q;
     p.q_scale = q_scale;
     p.kv_scale = kv_scale;

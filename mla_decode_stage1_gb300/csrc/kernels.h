@@ -25,7 +25,7 @@ constexpr float kPLoScale = 16.0f;    // the low part of p is stored x2^4
 // Device error word bits (one per pipeline role that gave up a wait).
 enum : int32_t {
   kErrProducer = 1, kErrMma = 2, kErrSoftmax = 4, kErrQPrep = 8, kErrDrain = 16,
-  kErrBadPage = 32
+  kErrBadPage = 32, kErrDequant = 64
 };
 
 // One work item: a contiguous token range of one request.
@@ -50,11 +50,15 @@ enum QMode : int {
   kQBf16KvBf16 = 0,   // kind::f16, B = q (16 rows)
   kQFp8KvFp8 = 1,     // kind::f8f6f4, B = q bytes (16 rows)
   kQBf16KvFp8 = 2,    // kind::f8f6f4, B = [q_hi ; q_lo] e4m3 (32 rows)
-  kQFp8KvBf16 = 3     // kind::f16, q decoded to bf16 (exact), B = 16 rows
+  kQFp8KvBf16 = 3,    // kind::f16, q decoded to bf16 (exact), B = 16 rows
+  kQBf16KvMx = 4      // MXFP4 KV dequantised in shared memory to e4m3 with a per-token
+                      // power of two; then as kQBf16KvFp8
 };
 
 struct Stage1Params {
-  CUtensorMap tmap_kv;          // KV pool as [chunk 64 B][row][64 B], 64-byte swizzle
+  CUtensorMap tmap_kv;          // KV pool as [chunk 64 B][row][64 B], 64-byte swizzle;
+                                // MXFP4: packed rows as [half 144 B][row][144 B]
+  CUtensorMap tmap_sc;          // MXFP4 only: e8m0 scale rows, 32-byte boxes
   const void* q;                // [bs,16,576]
   const float* q_scale;         // device [1] (fp8 q) or null
   const float* kv_scale;        // device [1] (fp8 kv) or null

@@ -28,5 +28,8 @@ struct mla_plan {
   const void* tmap_ptr = nullptr;
   int64_t tmap_rows = -1;
   int32_t tmap_box_rows = -1;
+  CUtensorMap tmap_sc;
+  const void* tmap_sc_ptr = nullptr;
+  int64_t tmap_sc_stride = -1;
   cudaEvent_t ev_before = nullptr, ev_after = nullptr;
 };

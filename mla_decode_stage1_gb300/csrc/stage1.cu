@@ -49,8 +49,10 @@ namespace mla {
 
 template <int QM>
 struct Layout {
-  static constexpr bool kKv8 = (QM == kQFp8KvFp8 || QM == kQBf16KvFp8);
-  static constexpr int kNq = (QM == kQBf16KvFp8) ? 32 : 16;        // UMMA N of QK^T
+  static constexpr bool kMx = (QM == kQBf16KvMx);                  // MXFP4 KV, dequantised
+  static constexpr bool kKv8 = (QM == kQFp8KvFp8 || QM == kQBf16KvFp8 || kMx);
+  static constexpr int kNq = (QM == kQBf16KvFp8 || kMx) ? 32 : 16;  // UMMA N of QK^T
+  static constexpr int kThreads = kMx ? 448 : 320;                  // + 4 dequant warps
   static constexpr int kElem = kKv8 ? 1 : 2;
   static constexpr int kRowBytes = kQkDim * kElem;                  // 576 | 1152
   static constexpr int kChunks = kRowBytes / 64;                    // 64-byte column chunks
@@ -61,14 +63,17 @@ struct Layout {
   static constexpr int kQAtomBytes = kNq * 128;
   static constexpr int kQBytes = kQAtoms * kQAtomBytes;
   static constexpr int kPBytes = 4096;
+  static constexpr int kScBytes = kMx ? kTile * 32 : 0;             // e8m0 rows per tile slot
+  static constexpr int kRawRowBytes = kQkDim / 2;                   // packed MXFP4 row
   static constexpr uint32_t kOCols = kKv8 ? 32 : 16;               // TMEM columns per O block
   static constexpr int kMiscBytes = 2048;
   static constexpr int kMaxSmem = 232448;
   static constexpr int kNumTiles =
-      (kMaxSmem - 1024 - 2 * kQBytes - 2 * kPBytes - kMiscBytes) / kTileBytes;
+      (kMaxSmem - 1024 - 2 * kQBytes - 2 * kPBytes - kMiscBytes) / (kTileBytes + kScBytes);
   static constexpr int kQOff = kNumTiles * kTileBytes;
   static constexpr int kPOff = kQOff + 2 * kQBytes;
-  static constexpr int kMiscOff = kPOff + 2 * kPBytes;
+  static constexpr int kScOff = kPOff + 2 * kPBytes;
+  static constexpr int kMiscOff = kScOff + kNumTiles * kScBytes;
   static constexpr int kSmemBytes = kMiscOff + kMiscBytes + 1024;
   static_assert(kNumTiles >= 1 && kNumTiles <= 4, "tile ring");
   static_assert(kSmemBytes <= kMaxSmem, "shared memory over budget");
@@ -83,6 +88,10 @@ struct Misc {
   float qscale[2][2];
   uint32_t tmem_base;
   int32_t abort_sm;                  // set by a softmax thread whose bounded wait gave up
+  // MXFP4 only
+  uint64_t deq[4];                   // tile slot dequantised (128 dequant threads)
+  int32_t abort_dq;                  // set by a dequant thread whose bounded wait gave up
+  float uexp[2][128];                // per-token power of two u_t = r_t - 127 of a slot
 };
 static_assert(sizeof(Misc) <= 2048, "misc region");
 static_assert(offsetof(Misc, red) % 16 == 0, "reduction scratch is read as float4");
@@ -92,7 +101,6 @@ static_assert(offsetof(Misc, red) % 16 == 0, "reduction scratch is read as float
 // blocks of kOCols columns (fp8 KV: 16 heads of p_hi, then 16 of p_lo).
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColS = 0, kColO = 128;
-constexpr int kThreads = 320;     // 10 warps
 
 // Byte offset of (row, byte x) inside a 128-byte-wide K-major operand with
 // the 128-byte swizzle (8-row / 1024-byte atoms, 16-byte chunks XOR row%8).
@@ -205,10 +213,23 @@ __device__ void run_producer(const Stage1Params& p, Misc* ms, uint32_t ring, int
     if (!ok) break;
     const int row = box_row(p, f, lane);
     const uint32_t full = smem_u32(&ms->full[s]);
-    if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(f.nbox) * box_bytes);
-    __syncwarp();
-    if (lane < f.nbox)
-      tma_load_3d(ring + s * L::kTileBytes + lane * box_bytes, &p.tmap_kv, full, 0, row, 0, pol);
+    if constexpr (L::kMx) {
+      // packed rows into the upper half of the tile slot, scale rows beside
+      const uint32_t raw_bytes = p.box_rows * L::kRawRowBytes, sc_bytes = p.box_rows * 32u;
+      if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(f.nbox) * (raw_bytes + sc_bytes));
+      __syncwarp();
+      if (lane < f.nbox) {
+        tma_load_3d(ring + s * L::kTileBytes + L::kTileBytes / 2 + lane * raw_bytes, &p.tmap_kv,
+                    full, 0, row, 0, pol);
+        tma_load_2d(ring + L::kScOff + s * L::kScBytes + lane * sc_bytes, &p.tmap_sc, full, 0, row,
+                    pol);
+      }
+    } else {
+      if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(f.nbox) * box_bytes);
+      __syncwarp();
+      if (lane < f.nbox)
+        tma_load_3d(ring + s * L::kTileBytes + lane * box_bytes, &p.tmap_kv, full, 0, row, 0, pol);
+    }
     cur.advance();
     ++t;
   }
@@ -250,8 +271,9 @@ __device__ void run_qk(const Stage1Params& p, Misc* ms, uint32_t ring, uint32_t 
     if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ms->s_empty[sb]), ((t >> 1) & 1u) ^ 1u,
                                            p.err, kErrMma)))
       break;
-    if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ms->full[s]), (t / L::kNumTiles) & 1u,
-                                           p.err, kErrMma)))
+    // the tile is ready once it landed (MXFP4: once it was dequantised)
+    const uint32_t ready = L::kMx ? smem_u32(&ms->deq[s]) : smem_u32(&ms->full[s]);
+    if (!__all_sync(0xffffffffu, mbar_wait(ready, (t / L::kNumTiles) & 1u, p.err, kErrMma)))
       break;
     tc_fence_after();
     const uint32_t tile = ring + s * L::kTileBytes;
@@ -334,6 +356,86 @@ __device__ void run_pv(const Stage1Params& p, Misc* ms, uint32_t ring, uint32_t 
   mbar_wait(smem_u32(&ms->drain[2 + half]), 0, p.err, kErrDrain);
 }
 
+// ------------------------------------------------------ MXFP4 dequantise
+// e4m3 bytes of m * 2^k for the eight e2m1 magnitudes m = {0, .5, 1, 1.5, 2,
+// 3, 4, 6} (byte c of {lo, hi} = code c).  k <= 0; 2^k below 2^-126 flushes
+// the block to zero (it is then below 2^-126 of the row's largest block).
+__device__ __forceinline__ void e2m1_e4m3_table(int k, uint32_t& lo, uint32_t& hi) {
+  const float f = k >= -126 ? __int_as_float((k + 127) << 23) : 0.0f;
+  const uint32_t a = __nv_cvt_float2_to_fp8x2(make_float2(0.0f, 0.5f * f), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t b = __nv_cvt_float2_to_fp8x2(make_float2(1.0f * f, 1.5f * f), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t c = __nv_cvt_float2_to_fp8x2(make_float2(2.0f * f, 3.0f * f), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t d = __nv_cvt_float2_to_fp8x2(make_float2(4.0f * f, 6.0f * f), __NV_SATFINITE, __NV_E4M3);
+  lo = a | (b << 16);
+  hi = c | (d << 16);
+}
+
+// Eight packed e2m1 codes (nibble n = element n) -> eight e4m3 bytes: the
+// magnitude through the table (byte permute), the sign from bit 3.
+__device__ __forceinline__ uint2 e2m1x8_to_e4m3(uint32_t w, uint32_t lo, uint32_t hi) {
+  const uint32_t m0 = __byte_perm(lo, hi, w & 0x7777u);
+  const uint32_t m1 = __byte_perm(lo, hi, (w >> 16) & 0x7777u);
+  const uint32_t s0 = __byte_perm(0u, 0x80808080u, (w >> 1) & 0x4444u);
+  const uint32_t s1 = __byte_perm(0u, 0x80808080u, (w >> 17) & 0x4444u);
+  return make_uint2(m0 | s0, m1 | s1);
+}
+
+// Four warps turn the packed MXFP4 rows of a tile slot into the e4m3 tile the
+// UMMAs read (thread t = token t).  With r_t the largest e8m0 exponent of the
+// token, block b becomes e2m1 * 2^(E_b - r_t): exact in e4m3 while
+// E_b - r_t >= -8.  The remaining factor 2^(r_t - 127) of the token is left
+// to the softmax (u_t = r_t - 127 in shared memory).  The packed rows sit in
+// the upper half of the same slot, so every thread reads its whole row before
+// any thread writes.
+template <int QM>
+__device__ void run_dequant(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, int it0, int it1,
+                            int t) {
+  using L = Layout<QM>;
+  volatile int32_t* abort = &ms->abort_dq;
+  const uint32_t cs = p.chunk_stride, gs = p.group_stride;
+  const int br = p.box_rows;
+  TileCursor c;
+  c.init(p.items, it0, it1);
+  while (!c.done()) {
+    const uint32_t tt = c.t, s = tt % L::kNumTiles;
+    if (!mbar_wait(smem_u32(&ms->full[s]), (tt / L::kNumTiles) & 1u, p.err, kErrDequant)) *abort = 1;
+    uint8_t* tile = ring_gen + s * L::kTileBytes;
+    const uint8_t* raw = tile + L::kTileBytes / 2 + (t / br) * (br * L::kRawRowBytes) + (t % br) * 144;
+    uint4 rv[18];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) {
+      rv[i] = reinterpret_cast<const uint4*>(raw)[i];
+      rv[9 + i] = reinterpret_cast<const uint4*>(raw + br * 144)[i];
+    }
+    const uint4* scp = reinterpret_cast<const uint4*>(ring_gen + L::kScOff + s * L::kScBytes + t * 32);
+    const uint4 e0 = scp[0], e1 = scp[1];
+    named_bar_sync(3, 128);
+    if (*abort) return;
+    const uint32_t ew[5] = {e0.x, e0.y, e0.z, e0.w, e1.x};
+    int r = 0;
+#pragma unroll
+    for (int b = 0; b < 18; ++b) r = max(r, static_cast<int>((ew[b >> 2] >> ((b & 3) * 8)) & 0xFFu));
+    ms->uexp[s][t] = static_cast<float>(r - 127);
+    uint8_t* rowp = tile + (t >> 3) * gs + (t & 7) * 64;
+    const uint32_t swz = ((t & 7) >> 1) & 3u;           // 64-byte swizzle of this row
+#pragma unroll
+    for (int b = 0; b < 18; ++b) {
+      const int e = static_cast<int>((ew[b >> 2] >> ((b & 3) * 8)) & 0xFFu);
+      uint32_t lo, hi;
+      e2m1_e4m3_table(e - r, lo, hi);
+      const uint2 o0 = e2m1x8_to_e4m3(rv[b].x, lo, hi), o1 = e2m1x8_to_e4m3(rv[b].y, lo, hi);
+      const uint2 o2 = e2m1x8_to_e4m3(rv[b].z, lo, hi), o3 = e2m1x8_to_e4m3(rv[b].w, lo, hi);
+      uint8_t* dst = rowp + (b >> 1) * cs;              // 64 dims per chunk, 2 blocks
+      const uint32_t c0 = (b & 1) * 2;
+      *reinterpret_cast<uint4*>(dst + ((c0 ^ swz) << 4)) = make_uint4(o0.x, o0.y, o1.x, o1.y);
+      *reinterpret_cast<uint4*>(dst + (((c0 + 1) ^ swz) << 4)) = make_uint4(o2.x, o2.y, o3.x, o3.y);
+    }
+    fence_proxy_async_smem();
+    mbar_arrive(smem_u32(&ms->deq[s]));
+    c.advance();
+  }
+}
+
 // Softmax threads share named barriers, so a thread must never leave alone:
 // a wait that gives up raises the group's abort flag and the thread carries
 // on to the next named barrier, after which the whole group leaves.
@@ -359,7 +461,7 @@ __device__ void run_qprep(const Stage1Params& p, Misc* ms, uint8_t* qgen, int it
     const int b = p.items[it].b;
     uint8_t* dst = qgen + qb * L::kQBytes;
     float c_hi = 0.f, c_lo = 0.f;
-    if constexpr (QM == kQBf16KvFp8) {
+    if constexpr (QM == kQBf16KvFp8 || QM == kQBf16KvMx) {
       const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
                                                         static_cast<int64_t>(b) * kHeads * kQkDim);
       float amax = 0.f;
@@ -404,7 +506,7 @@ __device__ void run_qprep(const Stage1Params& p, Misc* ms, uint8_t* qgen, int it
         *reinterpret_cast<uint2*>(base + sw128(h, x)) = make_uint2(hw[0], hw[1]);
         *reinterpret_cast<uint2*>(base + sw128(16 + h, x)) = make_uint2(lw[0], lw[1]);
       }
-      const float kvs = __ldg(p.kv_scale);
+      const float kvs = (QM == kQBf16KvMx) ? 1.0f : __ldg(p.kv_scale);
       c_hi = s_hi * kvs * kSmScale * kLog2e;
       c_lo = s_hi * (1.0f / 16.0f) * kvs * kSmScale * kLog2e;
     } else if constexpr (QM == kQFp8KvFp8) {
@@ -554,6 +656,16 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
       mbar_arrive(smem_u32(&ms->s_empty[sb]));
       const int nvalid = min(kTile, w.tok_end - (w.tok_begin + j * kTile));
       const bool valid = tid < nvalid;
+      // MXFP4: the token's scores carry its factor 2^u; the running max and
+      // P use s + u (the factor of its V row), l uses s: P' = p 2^u.
+      float gl = 1.0f;                                   // 2^-u, turns P' back into p
+      if constexpr (L::kMx) {
+        const int u = static_cast<int>(ms->uexp[g % L::kNumTiles][tid]);
+        const float f = u >= -126 ? __int_as_float((u + 127) << 23) : 0.0f;
+        gl = (valid && u <= 126) ? __int_as_float((127 - u) << 23) : 0.0f;
+#pragma unroll
+        for (int h = 0; h < 16; ++h) s[h] = s[h] * f + static_cast<float>(u);
+      }
 #pragma unroll
       for (int h = 0; h < 16; ++h) s[h] = valid ? s[h] : -INFINITY;
       float mt[16];
@@ -599,7 +711,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
 #pragma unroll
       for (int h = 0; h < 16; ++h) {
         pv[h] = valid ? ex2(s[h] - m[h] + kPOff) : 0.0f;
-        l[h] += pv[h];
+        l[h] += L::kMx ? pv[h] * gl : pv[h];
       }
       // P buffer (g & 1) is free once PV of tile g-2 completed.
       if (g >= 2)
@@ -639,7 +751,8 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
         // Tail tile: rows past the range may hold anything (stale tiles,
         // unused page slots); zero their V bytes so that 0 * V stays 0.
         const uint32_t s2 = g % L::kNumTiles;
-        wait_or_flag(smem_u32(&ms->full[s2]), (g / L::kNumTiles) & 1u, p.err, kErrSoftmax, abort);
+        wait_or_flag(L::kMx ? smem_u32(&ms->deq[s2]) : smem_u32(&ms->full[s2]),
+                     (g / L::kNumTiles) & 1u, p.err, kErrSoftmax, abort);
         if (!valid) {
           uint8_t* row = ring_gen + s2 * L::kTileBytes + (tid >> 3) * gs + (tid & 7) * 64;
           for (int c = 0; c < L::kVChunks; ++c)
@@ -660,7 +773,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
     reduce16<false>(l, lt, ms->red[g & 1u], qw, lane);
     if (*abort) return;
     // fp8 V entered the UMMAs as raw e4m3: its per-tensor scale is applied here.
-    const float vscale = L::kKv8 ? __ldg(p.kv_scale) : 1.0f;
+    const float vscale = (L::kKv8 && !L::kMx) ? __ldg(p.kv_scale) : 1.0f;
     float inv[16];
 #pragma unroll
     for (int h = 0; h < 16; ++h) inv[h] = vscale / lt[h];
@@ -710,7 +823,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
 
 // -------------------------------------------------------------------- kernel
 template <int QM>
-__global__ void __launch_bounds__(kThreads, 1) mla_stage1_kernel(const __grid_constant__ Stage1Params p) {
+__global__ void __launch_bounds__(Layout<QM>::kThreads, 1) mla_stage1_kernel(const __grid_constant__ Stage1Params p) {
   using L = Layout<QM>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -734,6 +847,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_stage1_kernel(const __grid_co
       mbar_init(smem_u32(&ms->q_empty[i]), 3);       // both QK^T issuers + softmax
     }
     for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&ms->drain[i]), 1);
+    for (int i = 0; i < L::kNumTiles; ++i) mbar_init(smem_u32(&ms->deq[i]), 128);
+    ms->abort_dq = 0;
     ms->abort_sm = 0;
     fence_mbar_init();
   }
@@ -755,6 +870,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_stage1_kernel(const __grid_co
     run_pv<QM>(p, ms, ring, ring + L::kPOff, tmem, it0, it1, warp == 9 ? 1 : 0, lane);
   } else if (warp == 8) {
     run_qprep<QM>(p, ms, smem + L::kQOff, it0, it1, lane);
+  } else if (warp >= 10) {
+    if constexpr (L::kMx) run_dequant<QM>(p, ms, smem, it0, it1, threadIdx.x - 320);
   } else {
     run_softmax<QM>(p, ms, smem, smem + L::kPOff, tmem, it0, it1, threadIdx.x - 128);
   }
@@ -773,6 +890,7 @@ int stage1_smem_bytes(int qmode) {
     case kQFp8KvFp8: return Layout<kQFp8KvFp8>::kSmemBytes;
     case kQBf16KvFp8: return Layout<kQBf16KvFp8>::kSmemBytes;
     case kQFp8KvBf16: return Layout<kQFp8KvBf16>::kSmemBytes;
+    case kQBf16KvMx: return Layout<kQBf16KvMx>::kSmemBytes;
   }
   return -1;
 }
@@ -783,7 +901,7 @@ static cudaError_t launch_t(const Stage1Params& p, int num_ctas, cudaStream_t st
   cudaError_t e = cudaFuncSetAttribute(mla_stage1_kernel<QM>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  mla_stage1_kernel<QM><<<num_ctas, kThreads, smem, stream>>>(p);
+  mla_stage1_kernel<QM><<<num_ctas, Layout<QM>::kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -793,6 +911,7 @@ cudaError_t launch_stage1(int qmode, const Stage1Params& p, int num_ctas, cudaSt
     case kQFp8KvFp8: return launch_t<kQFp8KvFp8>(p, num_ctas, stream);
     case kQBf16KvFp8: return launch_t<kQBf16KvFp8>(p, num_ctas, stream);
     case kQFp8KvBf16: return launch_t<kQFp8KvBf16>(p, num_ctas, stream);
+    case kQBf16KvMx: return launch_t<kQBf16KvMx>(p, num_ctas, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -13,7 +13,9 @@ follow the facts the pages state):
     scale amax/448 (the fp8 quantiser of submission 668813, runtime helpers);
   * KV rows ~ N(0,1) over 576 dims, stored bf16, fp8-e4m3 with scale
     amax/448, or MXFP4 (288 packed bytes + one e8m0 scale per 32 values,
-    layout of the MXFP4 stage-1 kernel of submission 668813);
+    layout of the MXFP4 stage-1 kernel of submission 668813; the scale rows
+    are padded to 32 bytes, a row stride of at least 18 being all the pages
+    fix);
   * dense packing, regular or per-request lengths through kv_indptr; page
     tables either the identity or a seeded permutation of all pages.
 
@@ -85,7 +87,10 @@ def quant_fp8_per_tensor(x: torch.Tensor):
     return q.view(torch.uint8), scale.to(torch.float32)
 
 
-def quant_mxfp4_rows(x: torch.Tensor, scale_stride: int = QK_DIM // 32):
+MX_SCALE_STRIDE = 32   # e8m0 bytes per row: 18 used, padded to a 16-byte multiple
+
+
+def quant_mxfp4_rows(x: torch.Tensor, scale_stride: int = MX_SCALE_STRIDE):
     """Encode rows of 576 values as MXFP4: (packed uint8 [rows,288],
     e8m0 uint8 [rows, scale_stride]).  Scale bytes past 18 are 0x7F."""
     rows = x.shape[0]
@@ -108,7 +113,7 @@ def quant_mxfp4_rows(x: torch.Tensor, scale_stride: int = QK_DIM // 32):
 
 def make_workload(*, bs: int, lengths, page_size: int = 1, q_dtype: str = "bf16",
                   kv_dtype: str = "bf16", permute_pages: bool = False, seed: int = 0,
-                  device="cpu", scale_stride: int = QK_DIM // 32, name: str = "custom",
+                  device="cpu", scale_stride: int = MX_SCALE_STRIDE, name: str = "custom",
                   q_std: float = 1.0, extra_pool_pages: int = 0) -> Workload:
     """Build a seeded workload.  `lengths` is a list of token counts (0 allowed).
     Pages hold `page_size` tokens; the last page of a request may be partial

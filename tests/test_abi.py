@@ -98,9 +98,11 @@ def test_run_rejects_bad_arguments_without_launching(mla):
 
 
 def test_unsupported_combinations(mla):
-    with pytest.raises(mla.MlaError) as e:
-        plan(mla, [0, 4], qd="mxfp4", kd="fp8")
-    assert e.value.status == 2
+    for qd, kd in (("mxfp4", "fp8"), ("fp8", "mxfp4"), ("mxfp4", "mxfp4")):
+        with pytest.raises(mla.MlaError) as e:
+            plan(mla, [0, 4], qd=qd, kd=kd)
+        assert e.value.status == 2
+    plan(mla, [0, 4], qd="bf16", kd="mxfp4")     # supported
 
 
 def lengths_of(indptr, last, ps):

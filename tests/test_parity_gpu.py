@@ -158,3 +158,53 @@ def test_large_benchmark_configs_sampled(name):
     rng = np.random.default_rng(7)
     sel = sorted(rng.choice(w.bs, size=6, replace=False).tolist() + [0, w.bs - 1])
     check(w, select=sel)
+
+
+@pytest.mark.parametrize("page_size,permute", [(1, False), (16, True)])
+def test_mxfp4_ragged(page_size, permute):
+    from mla_decode_stage1_gb300 import synth
+    lengths = [1, 127, 128, 129, 700, 0, 2049]
+    w = synth.make_workload(bs=len(lengths), lengths=lengths, page_size=page_size, q_dtype="bf16",
+                            kv_dtype="mxfp4", permute_pages=permute, seed=41)
+    check(w)
+
+
+def test_mxfp4_wide_scale_rows_and_few_ctas():
+    from mla_decode_stage1_gb300 import synth
+    lengths = [300, 1024, 5, 2000]
+    w = synth.make_workload(bs=4, lengths=lengths, page_size=1, q_dtype="bf16", kv_dtype="mxfp4",
+                            seed=42, scale_stride=48)
+    check(w, num_sms=2)
+    check(w, num_splits=3)
+
+
+def test_mxfp4_spread_block_exponents():
+    # scale exponents spread over 8 binades inside a token: still exact
+    from mla_decode_stage1_gb300 import synth
+    w = synth.make_workload(bs=2, lengths=[500, 77], page_size=1, q_dtype="bf16",
+                            kv_dtype="mxfp4", seed=43)
+    g = torch.Generator().manual_seed(5)
+    w.kv_e8m0[:, :18] = (120 + torch.randint(0, 9, (w.kv_e8m0.shape[0], 18), generator=g)).to(torch.uint8)
+    check(w)
+
+
+def test_mxfp4_unsupported_scale_stride():
+    mla = _mla()
+    from mla_decode_stage1_gb300 import synth
+    w = synth.make_workload(bs=1, lengths=[64], page_size=1, q_dtype="bf16", kv_dtype="mxfp4",
+                            seed=44, scale_stride=18)
+    plan = mla.mla_decode_plan(w.kv_indptr, None, page_size=1, q_dtype="bf16", kv_dtype="mxfp4")
+    d = w.to("cuda")
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
+    out = torch.empty(1, 16, 512, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(mla.MlaError) as e:
+        mla.mla_decode_run(plan, d.q, d.kv, out, workspace=ws, kv_e8m0=d.kv_e8m0)
+    assert e.value.status == 2
+
+
+def test_mxfp4_benchmark_config_sampled():
+    from mla_decode_stage1_gb300 import synth
+    w = synth.make_config("bs256_varkv_mxfp4", device="cuda")
+    rng = np.random.default_rng(8)
+    sel = sorted(rng.choice(w.bs, size=6, replace=False).tolist() + [0, w.bs - 1])
+    check(w, select=sel)
