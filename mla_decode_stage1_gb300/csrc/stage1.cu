@@ -65,16 +65,20 @@ struct Layout {
   static constexpr int kPBytes = 4096;
   static constexpr int kScBytes = kMx ? kTile * 32 : 0;             // e8m0 rows per tile slot
   static constexpr int kRawRowBytes = kQkDim / 2;                   // packed MXFP4 row
+  static constexpr bool kQ8 = (QM == kQFp8KvFp8 || QM == kQFp8KvBf16);
+  static constexpr int kQSrcBytes = kHeads * kQkDim * (kQ8 ? 1 : 2);  // one request's q
   static constexpr uint32_t kOCols = kKv8 ? 32 : 16;               // TMEM columns per O block
   static constexpr int kMiscBytes = 2048;
   static constexpr int kMaxSmem = 232448;
   static constexpr int kNumTiles =
-      (kMaxSmem - 1024 - 2 * kQBytes - 2 * kPBytes - kMiscBytes) / (kTileBytes + kScBytes);
+      (kMaxSmem - 1024 - 2 * kQBytes - 2 * kPBytes - kMiscBytes - kQSrcBytes) /
+      (kTileBytes + kScBytes);
   static constexpr int kQOff = kNumTiles * kTileBytes;
   static constexpr int kPOff = kQOff + 2 * kQBytes;
   static constexpr int kScOff = kPOff + 2 * kPBytes;
   static constexpr int kMiscOff = kScOff + kNumTiles * kScBytes;
-  static constexpr int kSmemBytes = kMiscOff + kMiscBytes + 1024;
+  static constexpr int kQStageOff = kMiscOff + kMiscBytes;           // raw q of the next item
+  static constexpr int kSmemBytes = kQStageOff + kQSrcBytes + 1024;
   static_assert(kNumTiles >= 1 && kNumTiles <= 4, "tile ring");
   static_assert(kSmemBytes <= kMaxSmem, "shared memory over budget");
   static_assert(kTileBytes % 1024 == 0 && kQBytes % 1024 == 0, "operand alignment");
@@ -91,6 +95,7 @@ struct Misc {
   // MXFP4 only
   uint64_t deq[4];                   // tile slot dequantised (128 dequant threads)
   int32_t abort_dq;                  // set by a dequant thread whose bounded wait gave up
+  uint64_t q_stage;                  // raw q of the next item landed in the staging buffer
   float uexp[2][128];                // per-token power of two u_t = r_t - 127 of a slot
 };
 static_assert(sizeof(Misc) <= 2048, "misc region");
@@ -448,26 +453,37 @@ __device__ __forceinline__ void wait_or_flag(uint32_t bar, uint32_t parity, int3
 // One warp writes q of the next item into a free q buffer in the UMMA operand
 // layout (K-major, 128-byte swizzle) and publishes the score factors.
 template <int QM>
-__device__ void run_qprep(const Stage1Params& p, Misc* ms, uint8_t* qgen, int it0, int it1,
-                          int lane) {
+__device__ void run_qprep(const Stage1Params& p, Misc* ms, uint8_t* qgen, uint8_t* stage, int it0,
+                          int it1, int lane) {
   using L = Layout<QM>;
   constexpr float kSmScale = 1.0f / 24.0f;          // 1/sqrt(576)
+  // one bulk copy brings a request's q into the staging buffer; the next
+  // request's copy starts as soon as this one has been converted
+  const uint32_t stage_bar = smem_u32(&ms->q_stage);
+  auto fetch = [&](int it) {
+    if (lane == 0) {
+      const int bb = p.items[it].b;
+      mbar_arrive_expect_tx(stage_bar, L::kQSrcBytes);
+      bulk_load(smem_u32(stage), static_cast<const uint8_t*>(p.q) + static_cast<int64_t>(bb) * L::kQSrcBytes,
+                L::kQSrcBytes, stage_bar);
+    }
+  };
+  if (it0 < it1) fetch(it0);
   int k = 0;
   for (int it = it0; it < it1; ++it, ++k) {
     const uint32_t qb = k & 1;
     if (!__all_sync(0xffffffffu,
                     mbar_wait(smem_u32(&ms->q_empty[qb]), ((k >> 1) & 1) ^ 1, p.err, kErrQPrep)))
       return;
-    const int b = p.items[it].b;
+    if (!__all_sync(0xffffffffu, mbar_wait(stage_bar, k & 1, p.err, kErrQPrep))) return;
     uint8_t* dst = qgen + qb * L::kQBytes;
     float c_hi = 0.f, c_lo = 0.f;
     if constexpr (QM == kQBf16KvFp8 || QM == kQBf16KvMx) {
-      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
-                                                        static_cast<int64_t>(b) * kHeads * kQkDim);
+      const uint4* src = reinterpret_cast<const uint4*>(stage);
       float amax = 0.f;
 #pragma unroll 4
       for (int i = 0; i < 36; ++i) {
-        const uint4 v = __ldg(src + lane + 32 * i);
+        const uint4 v = src[lane + 32 * i];
         const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -483,7 +499,7 @@ __device__ void run_qprep(const Stage1Params& p, Misc* ms, uint8_t* qgen, int it
       for (int i = 0; i < 36; ++i) {
         const int vid = lane + 32 * i;
         const int h = vid / 72, d0 = (vid % 72) * 8;
-        const uint4 v = __ldg(src + vid);
+        const uint4 v = src[vid];
         const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v);
         uint32_t hw[2], lw[2];
 #pragma unroll
@@ -510,13 +526,12 @@ __device__ void run_qprep(const Stage1Params& p, Misc* ms, uint8_t* qgen, int it
       c_hi = s_hi * kvs * kSmScale * kLog2e;
       c_lo = s_hi * (1.0f / 16.0f) * kvs * kSmScale * kLog2e;
     } else if constexpr (QM == kQFp8KvFp8) {
-      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.q) +
-                                                        static_cast<int64_t>(b) * kHeads * kQkDim);
+      const uint4* src = reinterpret_cast<const uint4*>(stage);
 #pragma unroll 6
       for (int i = 0; i < 18; ++i) {
         const int vid = lane + 32 * i;
         const int h = vid / 36, d0 = (vid % 36) * 16;
-        const uint4 v = __ldg(src + vid);
+        const uint4 v = src[vid];
         *reinterpret_cast<uint4*>(dst + (d0 >> 7) * L::kQAtomBytes + sw128(h, d0 & 127)) = v;
       }
       c_hi = __ldg(p.q_scale) * __ldg(p.kv_scale) * kSmScale * kLog2e;
@@ -528,14 +543,9 @@ __device__ void run_qprep(const Stage1Params& p, Misc* ms, uint8_t* qgen, int it
         const int h = vid / 72, d0 = (vid % 72) * 8;
         uint4 v;
         if constexpr (QM == kQBf16KvBf16) {
-          v = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
-                                                   static_cast<int64_t>(b) * kHeads * kQkDim) +
-                    vid);
+          v = reinterpret_cast<const uint4*>(stage)[vid];
         } else {
-          const uint2 raw = __ldg(reinterpret_cast<const uint2*>(
-                                      static_cast<const uint8_t*>(p.q) +
-                                      static_cast<int64_t>(b) * kHeads * kQkDim) +
-                                  vid);
+          const uint2 raw = reinterpret_cast<const uint2*>(stage)[vid];
           uint32_t wv[4];
           const uint32_t rr[2] = {raw.x, raw.y};
 #pragma unroll
@@ -554,7 +564,8 @@ __device__ void run_qprep(const Stage1Params& p, Misc* ms, uint8_t* qgen, int it
       c_hi = (QM == kQFp8KvBf16 ? __ldg(p.q_scale) : 1.0f) * kSmScale * kLog2e;
     }
     fence_proxy_async_smem();
-    __syncwarp();
+    __syncwarp();                                     // every lane is done with the stage
+    if (it + 1 < it1) fetch(it + 1);
     if (lane == 0) {
       ms->qscale[qb][0] = c_hi;
       ms->qscale[qb][1] = c_lo;
@@ -848,6 +859,7 @@ __global__ void __launch_bounds__(Layout<QM>::kThreads, 1) mla_stage1_kernel(con
     }
     for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&ms->drain[i]), 1);
     for (int i = 0; i < L::kNumTiles; ++i) mbar_init(smem_u32(&ms->deq[i]), 128);
+    mbar_init(smem_u32(&ms->q_stage), 1);
     ms->abort_dq = 0;
     ms->abort_sm = 0;
     fence_mbar_init();
@@ -869,7 +881,7 @@ __global__ void __launch_bounds__(Layout<QM>::kThreads, 1) mla_stage1_kernel(con
   } else if (warp == 2 || warp == 9) {
     run_pv<QM>(p, ms, ring, ring + L::kPOff, tmem, it0, it1, warp == 9 ? 1 : 0, lane);
   } else if (warp == 8) {
-    run_qprep<QM>(p, ms, smem + L::kQOff, it0, it1, lane);
+    run_qprep<QM>(p, ms, smem + L::kQOff, smem + L::kQStageOff, it0, it1, lane);
   } else if (warp >= 10) {
     if constexpr (L::kMx) run_dequant<QM>(p, ms, smem, it0, it1, threadIdx.x - 320);
   } else {
