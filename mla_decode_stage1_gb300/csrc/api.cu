@@ -168,16 +168,17 @@ bool make_kv_map(CUtensorMap* map, const void* kv, int kv_dtype, int64_t rows, i
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// MXFP4 pool: packed rows of 288 bytes as a 3-D tensor {144 B, row, half};
-// a box of box_rows rows lands as [half][row][144 B] (no swizzle).  Scale
-// rows (stride a multiple of 16, >= 32 bytes): 32-byte boxes, [row][32 B].
+// MXFP4 pool: packed rows of 288 bytes as a 3-D tensor {32 B, row, chunk}
+// (chunk = the 64 values of two scale blocks); a box of box_rows rows lands
+// chunk-major as [chunk][row][32 B] (no swizzle).  Scale rows (stride a
+// multiple of 16, >= 32 bytes): 32-byte boxes, [row][32 B].
 bool make_mx_maps(CUtensorMap* kvmap, CUtensorMap* scmap, const void* kv, const uint8_t* e8m0,
                   int64_t e8m0_stride, int64_t rows, int box_rows) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return false;
-  const cuuint64_t dims[3] = {144, static_cast<cuuint64_t>(rows), 2};
-  const cuuint64_t strides[2] = {288, 144};
-  const cuuint32_t box[3] = {144, static_cast<cuuint32_t>(box_rows), 2};
+  const cuuint64_t dims[3] = {32, static_cast<cuuint64_t>(rows), 9};
+  const cuuint64_t strides[2] = {288, 32};
+  const cuuint32_t box[3] = {32, static_cast<cuuint32_t>(box_rows), 9};
   const cuuint32_t estr[3] = {1, 1, 1};
   if (enc(kvmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(kv), dims, strides, box, estr,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -322,6 +323,8 @@ mla_status mla_decode_run(mla_plan* plan, const void* q, const float* q_scale, c
     box_rows = 8;
     if (kv_pool_rows % plan->page_size != 0) return MLA_ERR_INVALID_ARG;
   }
+  // MXFP4 rows are dequantised in place box by box: always 8-row boxes
+  if (plan->kv_dtype == MLA_DTYPE_MXFP4) box_rows = 8;
   // bytes per row of the tile the UMMAs read (MXFP4 is dequantised to e4m3)
   const uint32_t row_bytes = mla::kQkDim * (plan->kv_dtype == MLA_DTYPE_BF16 ? 2 : 1);
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);

@@ -52,7 +52,12 @@ struct Layout {
   static constexpr bool kMx = (QM == kQBf16KvMx);                  // MXFP4 KV, dequantised
   static constexpr bool kKv8 = (QM == kQFp8KvFp8 || QM == kQBf16KvFp8 || kMx);
   static constexpr int kNq = (QM == kQBf16KvFp8 || kMx) ? 32 : 16;  // UMMA N of QK^T
-  static constexpr int kThreads = kMx ? 448 : 320;                  // + 4 dequant warps
+  // Warps: producer, 2 QK^T issuers, PV issuer(s), 4 softmax warps per head
+  // group, then either 4 dequant warps that also prepare q (MXFP4: 12 warps,
+  // register cap 168) or a q warp (14 warps: two head groups of 8 heads).
+  static constexpr int kHeadGroups = kMx ? 1 : 2;
+  static constexpr int kThreads = kMx ? 384 : 448;
+  static constexpr int kPvIssuers = kMx ? 1 : 2;
   static constexpr int kElem = kKv8 ? 1 : 2;
   static constexpr int kRowBytes = kQkDim * kElem;                  // 576 | 1152
   static constexpr int kChunks = kRowBytes / 64;                    // 64-byte column chunks
@@ -94,9 +99,11 @@ struct Misc {
   int32_t abort_sm;                  // set by a softmax thread whose bounded wait gave up
   // MXFP4 only
   uint64_t deq[4];                   // tile slot dequantised (128 dequant threads)
+  uint64_t deq_a[4];                 // its dims 0-319 dequantised (first QK^T K-half)
   int32_t abort_dq;                  // set by a dequant thread whose bounded wait gave up
   uint64_t q_stage;                  // raw q of the next item landed in the staging buffer
   float uexp[2][128];                // per-token power of two u_t = r_t - 127 of a slot
+  float qred[4];                     // per-warp |q| maxima (q prepared by the dequant warps)
 };
 static_assert(sizeof(Misc) <= 2048, "misc region");
 static_assert(offsetof(Misc, red) % 16 == 0, "reduction scratch is read as float4");
@@ -219,13 +226,14 @@ __device__ void run_producer(const Stage1Params& p, Misc* ms, uint32_t ring, int
     const int row = box_row(p, f, lane);
     const uint32_t full = smem_u32(&ms->full[s]);
     if constexpr (L::kMx) {
-      // packed rows into the upper half of the tile slot, scale rows beside
+      // packed rows of box i into the upper half of box i's e4m3 region,
+      // scale rows beside the slot
       const uint32_t raw_bytes = p.box_rows * L::kRawRowBytes, sc_bytes = p.box_rows * 32u;
       if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(f.nbox) * (raw_bytes + sc_bytes));
       __syncwarp();
       if (lane < f.nbox) {
-        tma_load_3d(ring + s * L::kTileBytes + L::kTileBytes / 2 + lane * raw_bytes, &p.tmap_kv,
-                    full, 0, row, 0, pol);
+        tma_load_3d(ring + s * L::kTileBytes + lane * box_bytes + raw_bytes, &p.tmap_kv, full, 0,
+                    row, 0, pol);
         tma_load_2d(ring + L::kScOff + s * L::kScBytes + lane * sc_bytes, &p.tmap_sc, full, 0, row,
                     pol);
       }
@@ -276,8 +284,10 @@ __device__ void run_qk(const Stage1Params& p, Misc* ms, uint32_t ring, uint32_t 
     if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ms->s_empty[sb]), ((t >> 1) & 1u) ^ 1u,
                                            p.err, kErrMma)))
       break;
-    // the tile is ready once it landed (MXFP4: once it was dequantised)
-    const uint32_t ready = L::kMx ? smem_u32(&ms->deq[s]) : smem_u32(&ms->full[s]);
+    // the tile is ready once it landed (MXFP4: once the dims of this K-half
+    // were dequantised)
+    const uint32_t ready = !L::kMx ? smem_u32(&ms->full[s])
+                           : half == 0 ? smem_u32(&ms->deq_a[s]) : smem_u32(&ms->deq[s]);
     if (!__all_sync(0xffffffffu, mbar_wait(ready, (t / L::kNumTiles) & 1u, p.err, kErrMma)))
       break;
     tc_fence_after();
@@ -309,11 +319,13 @@ __device__ void run_qk(const Stage1Params& p, Misc* ms, uint32_t ring, uint32_t 
 }
 
 // PV issuer: O^T[128 dims of block c] (+)= V^T . P^T.  V^T is the tile read
-// MN-major: 64-dim atoms at cs (LBO), 8-token groups at gs (SBO).
+// MN-major: 64-dim atoms at cs (LBO), 8-token groups at gs (SBO).  Issuer
+// `half` owns O blocks 2*half, 2*half+1 (two issuers) or all four (one).
 template <int QM>
 __device__ void run_pv(const Stage1Params& p, Misc* ms, uint32_t ring, uint32_t pbase,
                        uint32_t tmem, int it0, int it1, int half, int lane) {
   using L = Layout<QM>;
+  constexpr int kBlocks = 4 / L::kPvIssuers;
   const uint32_t cs = p.chunk_stride, gs = p.group_stride;
   TileCursor pc;
   pc.init(p.items, it0, it1);
@@ -327,7 +339,7 @@ __device__ void run_pv(const Stage1Params& p, Misc* ms, uint32_t ring, uint32_t 
     const uint32_t pa = pbase + pb * L::kPBytes;
     const bool first = pc.j == 0;
     if (lane == 0) {
-    for (int c = 2 * half; c < 2 * half + 2; ++c) {
+    for (int c = kBlocks * half; c < kBlocks * half + kBlocks; ++c) {
       const uint32_t d = tmem + kColO + L::kOCols * c;
       // B = P^T, MN-major with the 32-byte swizzle: one 32-byte row per token
       // (fp8: 16 heads of p_hi then 16 of p_lo; bf16: 16 heads), 8-token
@@ -366,6 +378,14 @@ __device__ void run_pv(const Stage1Params& p, Misc* ms, uint32_t ring, uint32_t 
 // 3, 4, 6} (byte c of {lo, hi} = code c).  k <= 0; 2^k below 2^-126 flushes
 // the block to zero (it is then below 2^-126 of the row's largest block).
 __device__ __forceinline__ void e2m1_e4m3_table(int k, uint32_t& lo, uint32_t& hi) {
+  if (k >= -5) {
+    // every nonzero entry stays a normal e4m3 number, so scaling by 2^k only
+    // moves the exponent field (bits 3-6): add 8k to each nonzero byte
+    // (no byte is below 8|k|, so nothing borrows across bytes)
+    lo = 0x3C383000u + static_cast<uint32_t>(k) * 0x08080800u;
+    hi = 0x4C484440u + static_cast<uint32_t>(k) * 0x08080808u;
+    return;
+  }
   const float f = k >= -126 ? __int_as_float((k + 127) << 23) : 0.0f;
   const uint32_t a = __nv_cvt_float2_to_fp8x2(make_float2(0.0f, 0.5f * f), __NV_SATFINITE, __NV_E4M3);
   const uint32_t b = __nv_cvt_float2_to_fp8x2(make_float2(1.0f * f, 1.5f * f), __NV_SATFINITE, __NV_E4M3);
@@ -376,68 +396,196 @@ __device__ __forceinline__ void e2m1_e4m3_table(int k, uint32_t& lo, uint32_t& h
 }
 
 // Eight packed e2m1 codes (nibble n = element n) -> eight e4m3 bytes: the
-// magnitude through the table (byte permute), the sign from bit 3.
+// magnitude through the table (byte permute with the sign bits cleared), the
+// sign from bit 3 of each nibble.  That bit is the msb of byte n/2 of w << 4
+// (n even) or of w (n odd), so a byte permute that replicates msbs turns it
+// into a 0x00 / 0xFF mask per output byte.
 __device__ __forceinline__ uint2 e2m1x8_to_e4m3(uint32_t w, uint32_t lo, uint32_t hi) {
-  const uint32_t m0 = __byte_perm(lo, hi, w & 0x7777u);
-  const uint32_t m1 = __byte_perm(lo, hi, (w >> 16) & 0x7777u);
-  const uint32_t s0 = __byte_perm(0u, 0x80808080u, (w >> 1) & 0x4444u);
-  const uint32_t s1 = __byte_perm(0u, 0x80808080u, (w >> 17) & 0x4444u);
-  return make_uint2(m0 | s0, m1 | s1);
+  const uint32_t sel = w & 0x77777777u;
+  const uint32_t m0 = prmt(lo, hi, sel), m1 = prmt(lo, hi, sel >> 16);
+  const uint32_t w4 = w << 4;
+  const uint32_t s0 = prmt(w4, w, 0xD9C8u), s1 = prmt(w4, w, 0xFBEAu);
+  return make_uint2(m0 | (s0 & 0x80808080u), m1 | (s1 & 0x80808080u));
+}
+
+// ----------------------------------------------------- q staging helpers
+// One bulk copy brings q of item `it` (all 16 heads) into the staging buffer.
+template <int QM>
+__device__ __forceinline__ void q_fetch(const Stage1Params& p, Misc* ms, uint8_t* stage, int it) {
+  using L = Layout<QM>;
+  const uint32_t bar = smem_u32(&ms->q_stage);
+  const int bb = p.items[it].b;
+  mbar_arrive_expect_tx(bar, L::kQSrcBytes);
+  bulk_load(smem_u32(stage), static_cast<const uint8_t*>(p.q) + static_cast<int64_t>(bb) * L::kQSrcBytes,
+            L::kQSrcBytes, bar);
+}
+
+// Eight bf16 q values (vector `vid` of the [16 heads][576] q) -> their e4m3
+// q_hi = rn(q / s_hi) and q_lo = rn(16 (q - q_hi s_hi) / s_hi) bytes, stored
+// as rows h and 16 + h of the K-major, 128-byte-swizzled q operand.
+__device__ __forceinline__ void q_split_store(const uint4 v, int vid, float s_hi, float inv_hi,
+                                              uint8_t* dst, int atom_bytes) {
+  const int h = vid / 72, d0 = (vid % 72) * 8;
+  const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+  uint32_t hw[2], lw[2];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 f = __bfloat1622float2(h2[e]);
+    const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+        make_float2(f.x * inv_hi, f.y * inv_hi), __NV_SATFINITE, __NV_E4M3);
+    const float2 hf = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(hi, __NV_E4M3)));
+    const float rx = (f.x - hf.x * s_hi) * inv_hi * 16.0f;
+    const float ry = (f.y - hf.y * s_hi) * inv_hi * 16.0f;
+    const __nv_fp8x2_storage_t lo =
+        __nv_cvt_float2_to_fp8x2(make_float2(rx, ry), __NV_SATFINITE, __NV_E4M3);
+    const int wd = e >> 1, sh = (e & 1) * 16;
+    if ((e & 1) == 0) { hw[wd] = 0; lw[wd] = 0; }
+    hw[wd] |= static_cast<uint32_t>(hi) << sh;
+    lw[wd] |= static_cast<uint32_t>(lo) << sh;
+  }
+  const int atom = d0 >> 7, x = d0 & 127;
+  uint8_t* base = dst + atom * atom_bytes;
+  *reinterpret_cast<uint2*>(base + sw128(h, x)) = make_uint2(hw[0], hw[1]);
+  *reinterpret_cast<uint2*>(base + sw128(16 + h, x)) = make_uint2(lw[0], lw[1]);
+}
+
+// MXFP4 variant: the four dequant warps (128 threads, named barrier 3)
+// prepare q of item `it` (ordinal k) into q buffer k & 1, then start the copy
+// of the next item's q.  Returns false once the group gave up.
+template <int QM>
+__device__ bool qprep_group(const Stage1Params& p, Misc* ms, uint8_t* qgen, uint8_t* stage, int it,
+                            int k, int it1, int t) {
+  using L = Layout<QM>;
+  constexpr float kSmScale = 1.0f / 24.0f;          // 1/sqrt(576)
+  constexpr int kVec = L::kQSrcBytes / 16 / 128;    // 16-byte vectors per thread
+  volatile int32_t* abort = &ms->abort_dq;
+  const uint32_t qb = k & 1;
+  if (!mbar_wait(smem_u32(&ms->q_empty[qb]), ((k >> 1) & 1) ^ 1, p.err, kErrQPrep)) *abort = 1;
+  if (!mbar_wait(smem_u32(&ms->q_stage), k & 1, p.err, kErrQPrep)) *abort = 1;
+  const uint4* src = reinterpret_cast<const uint4*>(stage);
+  uint4 v[kVec];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < kVec; ++i) {
+    v[i] = src[t + 128 * i];
+    const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v[i]);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(h2[e]);
+      amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if ((t & 31) == 0) ms->qred[t >> 5] = amax;
+  named_bar_sync(3, 128);
+  if (*abort) return false;
+  amax = fmaxf(fmaxf(fmaxf(ms->qred[0], ms->qred[1]), fmaxf(ms->qred[2], ms->qred[3])), 1e-30f);
+  const float s_hi = amax / 448.0f, inv_hi = 448.0f / amax;
+  uint8_t* dst = qgen + qb * L::kQBytes;
+#pragma unroll
+  for (int i = 0; i < kVec; ++i) q_split_store(v[i], t + 128 * i, s_hi, inv_hi, dst, L::kQAtomBytes);
+  fence_proxy_async_smem();
+  named_bar_sync(3, 128);                           // staging buffer and qred free again
+  if (t == 0) {
+    if (it + 1 < it1) q_fetch<QM>(p, ms, stage, it + 1);
+    ms->qscale[qb][0] = s_hi * kSmScale * kLog2e;
+    ms->qscale[qb][1] = s_hi * (1.0f / 16.0f) * kSmScale * kLog2e;
+    mbar_arrive(smem_u32(&ms->q_full[qb]));
+  }
+  return true;
 }
 
 // Four warps turn the packed MXFP4 rows of a tile slot into the e4m3 tile the
 // UMMAs read (thread t = token t).  With r_t the largest e8m0 exponent of the
 // token, block b becomes e2m1 * 2^(E_b - r_t): exact in e4m3 while
 // E_b - r_t >= -8.  The remaining factor 2^(r_t - 127) of the token is left
-// to the softmax (u_t = r_t - 127 in shared memory).  The packed rows sit in
-// the upper half of the same slot, so every thread reads its whole row before
-// any thread writes.
+// to the softmax (u_t = r_t - 127 in shared memory).
+//
+// In place, without holding a row in registers: 8-row box i of the slot owns
+// bytes [i*4608, (i+1)*4608) of e4m3 rows ([chunk c][8 rows][64 B], chunk c =
+// dims 64c..64c+63) and its packed rows land chunk-major in the upper half,
+// [chunk c][8 rows][32 B] at 2304 + 256c.  Packed chunk c therefore lies in
+// e4m3 chunk floor(4.5 + c/2) >= c, so writing e4m3 chunk c only overwrites
+// packed chunks the box's 8 threads (one quarter of a warp) have already
+// read: a warp barrier between the reads and the writes of each chunk is
+// enough.
+//
+// The same threads prepare q: item 0's before the first tile, item k+1's
+// right after the first tile of item k (its q buffer is free by then: QK^T
+// of item k-1 has been issued on tiles this group already dequantised).
 template <int QM>
-__device__ void run_dequant(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, int it0, int it1,
-                            int t) {
+__device__ void run_dequant(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, uint8_t* qgen,
+                            uint8_t* stage, int it0, int it1, int t) {
   using L = Layout<QM>;
+  static_assert(L::kRowBytes * 8 == 4608 && L::kRawRowBytes * 8 == 2304, "box layout");
   volatile int32_t* abort = &ms->abort_dq;
-  const uint32_t cs = p.chunk_stride, gs = p.group_stride;
-  const int br = p.box_rows;
+  if (it0 >= it1) return;
+  if (t == 0) q_fetch<QM>(p, ms, stage, it0);
+  if (!qprep_group<QM>(p, ms, qgen, stage, it0, 0, it1, t)) return;
+  // this thread's row: box t/8, row t%8 (8-row boxes)
+  const uint32_t box_off = (t >> 3) * 4608u, r8 = t & 7u;
+  const uint32_t swz = (r8 >> 1) & 3u;                 // 64-byte swizzle of this row
   TileCursor c;
   c.init(p.items, it0, it1);
   while (!c.done()) {
     const uint32_t tt = c.t, s = tt % L::kNumTiles;
     if (!mbar_wait(smem_u32(&ms->full[s]), (tt / L::kNumTiles) & 1u, p.err, kErrDequant)) *abort = 1;
-    uint8_t* tile = ring_gen + s * L::kTileBytes;
-    const uint8_t* raw = tile + L::kTileBytes / 2 + (t / br) * (br * L::kRawRowBytes) + (t % br) * 144;
-    uint4 rv[18];
-#pragma unroll
-    for (int i = 0; i < 9; ++i) {
-      rv[i] = reinterpret_cast<const uint4*>(raw)[i];
-      rv[9 + i] = reinterpret_cast<const uint4*>(raw + br * 144)[i];
-    }
-    const uint4* scp = reinterpret_cast<const uint4*>(ring_gen + L::kScOff + s * L::kScBytes + t * 32);
-    const uint4 e0 = scp[0], e1 = scp[1];
     named_bar_sync(3, 128);
     if (*abort) return;
-    const uint32_t ew[5] = {e0.x, e0.y, e0.z, e0.w, e1.x};
+    uint8_t* box = ring_gen + s * L::kTileBytes + box_off;
+    const uint8_t* raw = box + 2304u + r8 * 32u;
+    const uint8_t* sc = ring_gen + L::kScOff + s * L::kScBytes + t * 32;
     int r = 0;
+    {
+      const uint4 e0 = reinterpret_cast<const uint4*>(sc)[0];
+      const uint32_t e1 = reinterpret_cast<const uint32_t*>(sc)[4];
+      const uint32_t ew[5] = {e0.x, e0.y, e0.z, e0.w, e1};
 #pragma unroll
-    for (int b = 0; b < 18; ++b) r = max(r, static_cast<int>((ew[b >> 2] >> ((b & 3) * 8)) & 0xFFu));
+      for (int b = 0; b < 18; ++b)
+        r = max(r, static_cast<int>((ew[b >> 2] >> ((b & 3) * 8)) & 0xFFu));
+    }
     ms->uexp[s][t] = static_cast<float>(r - 127);
-    uint8_t* rowp = tile + (t >> 3) * gs + (t & 7) * 64;
-    const uint32_t swz = ((t & 7) >> 1) & 3u;           // 64-byte swizzle of this row
-#pragma unroll
-    for (int b = 0; b < 18; ++b) {
-      const int e = static_cast<int>((ew[b >> 2] >> ((b & 3) * 8)) & 0xFFu);
-      uint32_t lo, hi;
-      e2m1_e4m3_table(e - r, lo, hi);
-      const uint2 o0 = e2m1x8_to_e4m3(rv[b].x, lo, hi), o1 = e2m1x8_to_e4m3(rv[b].y, lo, hi);
-      const uint2 o2 = e2m1x8_to_e4m3(rv[b].z, lo, hi), o3 = e2m1x8_to_e4m3(rv[b].w, lo, hi);
-      uint8_t* dst = rowp + (b >> 1) * cs;              // 64 dims per chunk, 2 blocks
-      const uint32_t c0 = (b & 1) * 2;
-      *reinterpret_cast<uint4*>(dst + ((c0 ^ swz) << 4)) = make_uint4(o0.x, o0.y, o1.x, o1.y);
-      *reinterpret_cast<uint4*>(dst + (((c0 + 1) ^ swz) << 4)) = make_uint4(o2.x, o2.y, o3.x, o3.y);
+    uint8_t* row = box + r8 * 64u;
+    // packed chunk ch+1 and its two scale bytes are read while chunk ch is
+    // converted (reading early is always safe; only writes must wait)
+    uint4 na = reinterpret_cast<const uint4*>(raw)[0];
+    uint4 nb = reinterpret_cast<const uint4*>(raw)[1];
+    uint32_t neb = reinterpret_cast<const uint16_t*>(sc)[0];
+#pragma unroll 1
+    for (int ch = 0; ch < 9; ++ch) {
+      const uint4 a = na, b = nb;
+      const uint32_t eb = neb;                          // e8m0 of blocks 2ch, 2ch+1
+      if (ch < 8) {
+        na = reinterpret_cast<const uint4*>(raw + (ch + 1) * 256)[0];
+        nb = reinterpret_cast<const uint4*>(raw + (ch + 1) * 256)[1];
+        neb = reinterpret_cast<const uint16_t*>(sc)[ch + 1];
+      }
+      __syncwarp();                                     // the box read packed chunk ch
+      uint32_t lo0, hi0, lo1, hi1;
+      e2m1_e4m3_table(static_cast<int>(eb & 0xFFu) - r, lo0, hi0);
+      e2m1_e4m3_table(static_cast<int>(eb >> 8) - r, lo1, hi1);
+      const uint2 o0 = e2m1x8_to_e4m3(a.x, lo0, hi0), o1 = e2m1x8_to_e4m3(a.y, lo0, hi0);
+      const uint2 o2 = e2m1x8_to_e4m3(a.z, lo0, hi0), o3 = e2m1x8_to_e4m3(a.w, lo0, hi0);
+      const uint2 o4 = e2m1x8_to_e4m3(b.x, lo1, hi1), o5 = e2m1x8_to_e4m3(b.y, lo1, hi1);
+      const uint2 o6 = e2m1x8_to_e4m3(b.z, lo1, hi1), o7 = e2m1x8_to_e4m3(b.w, lo1, hi1);
+      uint8_t* dst = row + ch * 512;
+      *reinterpret_cast<uint4*>(dst + ((0u ^ swz) << 4)) = make_uint4(o0.x, o0.y, o1.x, o1.y);
+      *reinterpret_cast<uint4*>(dst + ((1u ^ swz) << 4)) = make_uint4(o2.x, o2.y, o3.x, o3.y);
+      *reinterpret_cast<uint4*>(dst + ((2u ^ swz) << 4)) = make_uint4(o4.x, o4.y, o5.x, o5.y);
+      *reinterpret_cast<uint4*>(dst + ((3u ^ swz) << 4)) = make_uint4(o6.x, o6.y, o7.x, o7.y);
+      if (ch == 4) {
+        // dims 0-319 done: the first QK^T K-half (dims 0-287) may start
+        fence_proxy_async_smem();
+        mbar_arrive(smem_u32(&ms->deq_a[s]));
+      }
     }
     fence_proxy_async_smem();
     mbar_arrive(smem_u32(&ms->deq[s]));
+    const bool first = c.j == 0;
+    const int it = c.it, k = c.k;
     c.advance();
+    if (first && it + 1 < it1 && !qprep_group<QM>(p, ms, qgen, stage, it + 1, k + 1, it1, t)) return;
   }
 }
 
@@ -461,12 +609,7 @@ __device__ void run_qprep(const Stage1Params& p, Misc* ms, uint8_t* qgen, uint8_
   // request's copy starts as soon as this one has been converted
   const uint32_t stage_bar = smem_u32(&ms->q_stage);
   auto fetch = [&](int it) {
-    if (lane == 0) {
-      const int bb = p.items[it].b;
-      mbar_arrive_expect_tx(stage_bar, L::kQSrcBytes);
-      bulk_load(smem_u32(stage), static_cast<const uint8_t*>(p.q) + static_cast<int64_t>(bb) * L::kQSrcBytes,
-                L::kQSrcBytes, stage_bar);
-    }
+    if (lane == 0) q_fetch<QM>(p, ms, stage, it);
   };
   if (it0 < it1) fetch(it0);
   int k = 0;
@@ -498,29 +641,7 @@ __device__ void run_qprep(const Stage1Params& p, Misc* ms, uint8_t* qgen, uint8_
 #pragma unroll 4
       for (int i = 0; i < 36; ++i) {
         const int vid = lane + 32 * i;
-        const int h = vid / 72, d0 = (vid % 72) * 8;
-        const uint4 v = src[vid];
-        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v);
-        uint32_t hw[2], lw[2];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = __bfloat1622float2(h2[e]);
-          const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
-              make_float2(f.x * inv_hi, f.y * inv_hi), __NV_SATFINITE, __NV_E4M3);
-          const float2 hf = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(hi, __NV_E4M3)));
-          const float rx = (f.x - hf.x * s_hi) * inv_hi * 16.0f;
-          const float ry = (f.y - hf.y * s_hi) * inv_hi * 16.0f;
-          const __nv_fp8x2_storage_t lo =
-              __nv_cvt_float2_to_fp8x2(make_float2(rx, ry), __NV_SATFINITE, __NV_E4M3);
-          const int wd = e >> 1, sh = (e & 1) * 16;
-          if ((e & 1) == 0) { hw[wd] = 0; lw[wd] = 0; }
-          hw[wd] |= static_cast<uint32_t>(hi) << sh;
-          lw[wd] |= static_cast<uint32_t>(lo) << sh;
-        }
-        const int atom = d0 >> 7, x = d0 & 127;
-        uint8_t* base = dst + atom * L::kQAtomBytes;
-        *reinterpret_cast<uint2*>(base + sw128(h, x)) = make_uint2(hw[0], hw[1]);
-        *reinterpret_cast<uint2*>(base + sw128(16 + h, x)) = make_uint2(lw[0], lw[1]);
+        q_split_store(src[vid], vid, s_hi, inv_hi, dst, L::kQAtomBytes);
       }
       const float kvs = (QM == kQBf16KvMx) ? 1.0f : __ldg(p.kv_scale);
       c_hi = s_hi * kvs * kSmScale * kLog2e;
@@ -575,117 +696,117 @@ __device__ void run_qprep(const Stage1Params& p, Misc* ms, uint8_t* qgen, uint8_
 }
 
 // ------------------------------------------------------ softmax / epilogue
-// Reduce 16 per-thread values over the 128 softmax threads (op = max or
-// sum).  A 16-shuffle transpose-reduce leaves head h(lane) in lanes 2j, 2j+1;
-// four warp results meet in shared memory.
-template <bool kMax>
-__device__ __forceinline__ void reduce16(float (&v)[16], float (&out)[16], float (*red)[16],
-                                         int qw, int lane) {
+// Reduce kH per-thread values (heads h0..h0+kH-1) over the 128 threads of a
+// head group (op = max or sum).  A transpose-reduce over the lane bits
+// 16, 8, ... leaves one head per group of lanes after log2(kH) shuffle
+// stages; the four warp results meet in shared memory behind the group's
+// named barrier `bar`.
+template <bool kMax, int kH>
+__device__ __forceinline__ void reduce_heads(const float (&v)[kH], float (&out)[kH],
+                                             float (*red)[16], int h0, int qw, int lane, int bar) {
   auto op = [](float a, float b) { return kMax ? fmaxf(a, b) : a + b; };
-  float r8[8], r4[4], r2[2], r1;
-  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+  constexpr int kStages = kH == 16 ? 4 : 3;
+  float buf[kH];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float send = b4 ? v[i] : v[i + 8], keep = b4 ? v[i + 8] : v[i];
-    r8[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+  for (int i = 0; i < kH; ++i) buf[i] = v[i];
+  int h = 0;
+#pragma unroll
+  for (int st = 0; st < kStages; ++st) {
+    const int half = kH >> (st + 1), off = 16 >> st;
+    const bool up = lane & off;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = up ? buf[i] : buf[i + half], keep = up ? buf[i + half] : buf[i];
+      buf[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, off));
+    }
+    if (up) h += half;
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float send = b3 ? r8[i] : r8[i + 4], keep = b3 ? r8[i + 4] : r8[i];
-    r4[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 8));
-  }
+  for (int off = 16 >> kStages; off >= 1; off >>= 1)
+    buf[0] = op(buf[0], __shfl_xor_sync(0xffffffffu, buf[0], off));
+  if ((lane & ((32 >> kStages) - 1)) == 0) red[qw][h0 + h] = buf[0];
+  named_bar_sync(bar, 128);
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const float send = b2 ? r4[i] : r4[i + 2], keep = b2 ? r4[i + 2] : r4[i];
-    r2[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 4));
-  }
-  {
-    const float send = b1 ? r2[0] : r2[1], keep = b1 ? r2[1] : r2[0];
-    r1 = op(keep, __shfl_xor_sync(0xffffffffu, send, 2));
-  }
-  r1 = op(r1, __shfl_xor_sync(0xffffffffu, r1, 1));
-  const int h = (b4 ? 8 : 0) + (b3 ? 4 : 0) + (b2 ? 2 : 0) + (b1 ? 1 : 0);
-  if ((lane & 1) == 0) red[qw][h] = r1;
-  named_bar_sync(1, 128);
-#pragma unroll
-  for (int i = 0; i < 16; i += 4) {
-    float4 a = *reinterpret_cast<const float4*>(&red[0][i]);
-    float4 bq = *reinterpret_cast<const float4*>(&red[1][i]);
-    float4 cq = *reinterpret_cast<const float4*>(&red[2][i]);
-    float4 dq = *reinterpret_cast<const float4*>(&red[3][i]);
-    out[i + 0] = op(op(a.x, bq.x), op(cq.x, dq.x));
-    out[i + 1] = op(op(a.y, bq.y), op(cq.y, dq.y));
-    out[i + 2] = op(op(a.z, bq.z), op(cq.z, dq.z));
-    out[i + 3] = op(op(a.w, bq.w), op(cq.w, dq.w));
-  }
+  for (int i = 0; i < kH; ++i)
+    out[i] = op(op(red[0][h0 + i], red[1][h0 + i]), op(red[2][h0 + i], red[3][h0 + i]));
 }
 
+// Softmax warps: kHeadGroups groups of four warps (one per TMEM lane
+// quadrant); thread tq of a group owns token tq of every tile (its TMEM lane)
+// and heads h0..h0+kH-1.  Per tile: S from TMEM, the running max, the lazy
+// rescale of O, p = exp2(s - m + 4) into l and into the P operand.  After an
+// item's last tile, the epilogue normalises O and writes it out.
 template <int QM>
 __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, uint8_t* pgen,
                             uint32_t tmem, int it0, int it1, int tid) {
   using L = Layout<QM>;
+  constexpr int kHG = L::kHeadGroups, kH = 16 / kHG;
   volatile int32_t* abort = &ms->abort_sm;
-  const int qw = tid >> 5, lane = tid & 31;
+  const int hg = tid >> 7, tq = tid & 127;
+  const int h0 = kH * hg, bar = 1 + hg;
+  const int qw = tq >> 5, lane = tq & 31;
   const uint32_t tl = tmem + (static_cast<uint32_t>(qw * 32) << 16);   // this warp's lanes
   uint32_t g = 0;
   const uint32_t cs = p.chunk_stride, gs = p.group_stride;
   int k = 0;
-  float m[16], l[16];
+  float m[kH], l[kH];
   for (int it = it0; it < it1; ++it, ++k) {
     const WorkItem w = p.items[it];
     const uint32_t qb = k & 1;
     wait_or_flag(smem_u32(&ms->q_full[qb]), (k >> 1) & 1, p.err, kErrSoftmax, abort);
     const float c_hi = ms->qscale[qb][0], c_lo = ms->qscale[qb][1];
-    named_bar_sync(1, 128);
+    named_bar_sync(bar, 128);
     if (*abort) return;
-    if (tid == 0) mbar_arrive(smem_u32(&ms->q_empty[qb]));
+    if (tq == 0) mbar_arrive(smem_u32(&ms->q_empty[qb]));
     const int ntile = (w.tok_end - w.tok_begin + kTile - 1) / kTile;
     for (int j = 0; j < ntile; ++j, ++g) {
       const uint32_t sb = g & 1u;
       wait_or_flag(smem_u32(&ms->s_full[sb]), (g >> 1) & 1u, p.err, kErrSoftmax, abort);
       tc_fence_after();
-      float s[16];
+      float s[kH];
       {
-        const uint32_t sc = tl + kColS + 64 * sb;
-        float a0[16], a1[16];
-        tmem_ld16(sc, a0);
-        tmem_ld16(sc + 32, a1);
+        // S^T columns of buffer sb: two K-halves of 32 columns; with kNq = 32
+        // heads 0-15 of the q_hi term, then of the q_lo term
+        const uint32_t sc = tl + kColS + 64 * sb + h0;
+        float a0[kH], a1[kH];
+        tmem_ld(sc, a0);
+        tmem_ld(sc + 32, a1);
         if constexpr (L::kNq == 32) {
-          float b0[16], b1[16];
-          tmem_ld16(sc + 16, b0);
-          tmem_ld16(sc + 48, b1);
+          float b0[kH], b1[kH];
+          tmem_ld(sc + 16, b0);
+          tmem_ld(sc + 48, b1);
           tmem_wait_ld();
 #pragma unroll
-          for (int h = 0; h < 16; ++h) s[h] = (a0[h] + a1[h]) * c_hi + (b0[h] + b1[h]) * c_lo;
+          for (int h = 0; h < kH; ++h) s[h] = (a0[h] + a1[h]) * c_hi + (b0[h] + b1[h]) * c_lo;
         } else {
           tmem_wait_ld();
 #pragma unroll
-          for (int h = 0; h < 16; ++h) s[h] = (a0[h] + a1[h]) * c_hi;
+          for (int h = 0; h < kH; ++h) s[h] = (a0[h] + a1[h]) * c_hi;
         }
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&ms->s_empty[sb]));
       const int nvalid = min(kTile, w.tok_end - (w.tok_begin + j * kTile));
-      const bool valid = tid < nvalid;
+      const bool valid = tq < nvalid;
       // MXFP4: the token's scores carry its factor 2^u; the running max and
       // P use s + u (the factor of its V row), l uses s: P' = p 2^u.
       float gl = 1.0f;                                   // 2^-u, turns P' back into p
       if constexpr (L::kMx) {
-        const int u = static_cast<int>(ms->uexp[g % L::kNumTiles][tid]);
+        const int u = static_cast<int>(ms->uexp[g % L::kNumTiles][tq]);
         const float f = u >= -126 ? __int_as_float((u + 127) << 23) : 0.0f;
         gl = (valid && u <= 126) ? __int_as_float((127 - u) << 23) : 0.0f;
 #pragma unroll
-        for (int h = 0; h < 16; ++h) s[h] = s[h] * f + static_cast<float>(u);
+        for (int h = 0; h < kH; ++h) s[h] = s[h] * f + static_cast<float>(u);
       }
 #pragma unroll
-      for (int h = 0; h < 16; ++h) s[h] = valid ? s[h] : -INFINITY;
-      float mt[16];
-      reduce16<true>(s, mt, ms->red[g & 1u], qw, lane);
+      for (int h = 0; h < kH; ++h) s[h] = valid ? s[h] : -INFINITY;
+      float mt[kH];
+      reduce_heads<true, kH>(s, mt, ms->red[g & 1u], h0, qw, lane, bar);
       if (*abort) return;
       bool resc = false;
-      float alpha[16];
+      float alpha[kH];
 #pragma unroll
-      for (int h = 0; h < 16; ++h) {
+      for (int h = 0; h < kH; ++h) {
         alpha[h] = 1.0f;
         if (j == 0) {
           m[h] = mt[h];
@@ -697,30 +818,30 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
         }
       }
       if (resc) {
-        // The running max moved by more than kTau: scale O (both parts) once
-        // the previous tile's PV has landed in TMEM.
+        // The running max moved by more than kTau: scale this group's O
+        // columns (both parts) once the previous tile's PV has landed.
         const uint32_t gp = g - 1;
         wait_or_flag(smem_u32(&ms->pv_done[gp & 1u]), (gp >> 1) & 1u, p.err, kErrSoftmax, abort);
         tc_fence_after();
         const int nparts = L::kKv8 ? 2 : 1;
         for (int part = 0; part < nparts; ++part) {
           for (int c = 0; c < 4; ++c) {
-            const uint32_t col = kColO + L::kOCols * c + 16 * part;
-            float o[16];
-            tmem_ld16(tl + col, o);
+            const uint32_t col = kColO + L::kOCols * c + 16 * part + h0;
+            float o[kH];
+            tmem_ld(tl + col, o);
             tmem_wait_ld();
 #pragma unroll
-            for (int h = 0; h < 16; ++h) o[h] *= alpha[h];
-            tmem_st16(tl + col, o);
+            for (int h = 0; h < kH; ++h) o[h] *= alpha[h];
+            tmem_st(tl + col, o);
           }
         }
         tmem_wait_st();
 #pragma unroll
-        for (int h = 0; h < 16; ++h) l[h] *= alpha[h];
+        for (int h = 0; h < kH; ++h) l[h] *= alpha[h];
       }
-      float pv[16];
+      float pv[kH];
 #pragma unroll
-      for (int h = 0; h < 16; ++h) {
+      for (int h = 0; h < kH; ++h) {
         pv[h] = valid ? ex2(s[h] - m[h] + kPOff) : 0.0f;
         l[h] += L::kMx ? pv[h] * gl : pv[h];
       }
@@ -729,12 +850,13 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
         wait_or_flag(smem_u32(&ms->pv_done[sb]), ((g >> 1) - 1) & 1u, p.err, kErrSoftmax, abort);
       // This token's row of P^T: 32 bytes, two 16-byte halves swapped on
       // every other group of 4 tokens (32-byte swizzle: bit 4 ^= bit 7).
-      uint8_t* prow = pgen + sb * L::kPBytes + tid * 32;
-      const uint32_t flip = ((tid >> 2) & 1u) << 4;
+      uint8_t* prow = pgen + sb * L::kPBytes + tq * 32;
+      const uint32_t flip = ((tq >> 2) & 1u) << 4;
       if constexpr (L::kKv8) {
-        uint32_t hw[4], lw[4];
+        // fp8: p_hi of heads 0-15 in bytes 0-15, p_lo in bytes 16-31
+        uint32_t hw[kH / 4], lw[kH / 4];
 #pragma unroll
-        for (int h = 0; h < 16; h += 2) {
+        for (int h = 0; h < kH; h += 2) {
           const __nv_fp8x2_storage_t hi =
               __nv_cvt_float2_to_fp8x2(make_float2(pv[h], pv[h + 1]), __NV_SATFINITE, __NV_E4M3);
           const float2 hf = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(hi, __NV_E4M3)));
@@ -746,17 +868,27 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
           hw[wd] |= static_cast<uint32_t>(hi) << sh;
           lw[wd] |= static_cast<uint32_t>(lo) << sh;
         }
-        *reinterpret_cast<uint4*>(prow + (0u ^ flip)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-        *reinterpret_cast<uint4*>(prow + (16u ^ flip)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        if constexpr (kH == 16) {
+          *reinterpret_cast<uint4*>(prow + (0u ^ flip)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(prow + (16u ^ flip)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        } else {
+          *reinterpret_cast<uint2*>(prow + ((8u * hg) ^ flip)) = make_uint2(hw[0], hw[1]);
+          *reinterpret_cast<uint2*>(prow + ((16u + 8u * hg) ^ flip)) = make_uint2(lw[0], lw[1]);
+        }
       } else {
-        uint32_t bw[8];
+        // bf16: heads 0-15, 2 bytes each
+        uint32_t bw[kH / 2];
 #pragma unroll
-        for (int h = 0; h < 16; h += 2) {
+        for (int h = 0; h < kH; h += 2) {
           const __nv_bfloat162 v = __floats2bfloat162_rn(pv[h], pv[h + 1]);
           bw[h >> 1] = *reinterpret_cast<const uint32_t*>(&v);
         }
-        *reinterpret_cast<uint4*>(prow + (0u ^ flip)) = make_uint4(bw[0], bw[1], bw[2], bw[3]);
-        *reinterpret_cast<uint4*>(prow + (16u ^ flip)) = make_uint4(bw[4], bw[5], bw[6], bw[7]);
+        if constexpr (kH == 16) {
+          *reinterpret_cast<uint4*>(prow + (0u ^ flip)) = make_uint4(bw[0], bw[1], bw[2], bw[3]);
+          *reinterpret_cast<uint4*>(prow + (16u ^ flip)) = make_uint4(bw[4], bw[5], bw[6], bw[7]);
+        } else {
+          *reinterpret_cast<uint4*>(prow + ((16u * hg) ^ flip)) = make_uint4(bw[0], bw[1], bw[2], bw[3]);
+        }
       }
       if (nvalid < kTile) {
         // Tail tile: rows past the range may hold anything (stale tiles,
@@ -765,8 +897,9 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
         wait_or_flag(L::kMx ? smem_u32(&ms->deq[s2]) : smem_u32(&ms->full[s2]),
                      (g / L::kNumTiles) & 1u, p.err, kErrSoftmax, abort);
         if (!valid) {
-          uint8_t* row = ring_gen + s2 * L::kTileBytes + (tid >> 3) * gs + (tid & 7) * 64;
-          for (int c = 0; c < L::kVChunks; ++c)
+          uint8_t* row = ring_gen + s2 * L::kTileBytes + (tq >> 3) * gs + (tq & 7) * 64;
+          constexpr int kZc = L::kVChunks / kHG;       // chunks zeroed by each group
+          for (int c = hg * kZc; c < (hg + 1) * kZc; ++c)
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               reinterpret_cast<uint4*>(row + c * cs)[i] = make_uint4(0, 0, 0, 0);
@@ -780,54 +913,55 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
     const uint32_t gl = g - 1;
     wait_or_flag(smem_u32(&ms->pv_done[gl & 1u]), (gl >> 1) & 1u, p.err, kErrSoftmax, abort);
     tc_fence_after();
-    float lt[16];
-    reduce16<false>(l, lt, ms->red[g & 1u], qw, lane);
+    float lt[kH];
+    reduce_heads<false, kH>(l, lt, ms->red[g & 1u], h0, qw, lane, bar);
     if (*abort) return;
     // fp8 V entered the UMMAs as raw e4m3: its per-tensor scale is applied here.
     const float vscale = (L::kKv8 && !L::kMx) ? __ldg(p.kv_scale) : 1.0f;
-    float inv[16];
+    float inv[kH];
 #pragma unroll
-    for (int h = 0; h < 16; ++h) inv[h] = vscale / lt[h];
+    for (int h = 0; h < kH; ++h) inv[h] = vscale / lt[h];
     const int slot = w.slot;
     for (int c = 0; c < 4; ++c) {
-      float oh[16];
-      tmem_ld16(tl + kColO + L::kOCols * c, oh);
+      float oh[kH];
+      tmem_ld(tl + kColO + L::kOCols * c + h0, oh);
       if constexpr (L::kKv8) {
-        float ol[16];
-        tmem_ld16(tl + kColO + L::kOCols * c + 16, ol);
+        float ol[kH];
+        tmem_ld(tl + kColO + L::kOCols * c + 16 + h0, ol);
         tmem_wait_ld();
 #pragma unroll
-        for (int h = 0; h < 16; ++h) oh[h] = (oh[h] + ol[h] * (1.0f / kPLoScale)) * inv[h];
+        for (int h = 0; h < kH; ++h) oh[h] = (oh[h] + ol[h] * (1.0f / kPLoScale)) * inv[h];
       } else {
         tmem_wait_ld();
 #pragma unroll
-        for (int h = 0; h < 16; ++h) oh[h] *= inv[h];
+        for (int h = 0; h < kH; ++h) oh[h] *= inv[h];
       }
-      const int d = c * 128 + tid;
+      const int d = c * 128 + tq;
       if (slot >= 0) {
-        float* po = p.part_o + static_cast<int64_t>(slot) * kHeads * kVDim + d;
+        float* po = p.part_o + (static_cast<int64_t>(slot) * kHeads + h0) * kVDim + d;
 #pragma unroll
-        for (int h = 0; h < 16; ++h) po[h * kVDim] = oh[h];
+        for (int h = 0; h < kH; ++h) po[h * kVDim] = oh[h];
       } else {
-        uint16_t* po = p.out + static_cast<int64_t>(w.b) * kHeads * kVDim + d;
+        uint16_t* po = p.out + (static_cast<int64_t>(w.b) * kHeads + h0) * kVDim + d;
 #pragma unroll
-        for (int h = 0; h < 16; ++h) {
+        for (int h = 0; h < kH; ++h) {
           const __nv_bfloat16 v = __float2bfloat16_rn(oh[h]);
           po[h * kVDim] = *reinterpret_cast<const uint16_t*>(&v);
         }
       }
     }
     tc_fence_before();
-    if (tid < 16) {
+    if (tq < kH) {
       float mh = 0.f, lh = 1.f;
 #pragma unroll
-      for (int h = 0; h < 16; ++h)
-        if (h == tid) { mh = m[h]; lh = lt[h]; }
+      for (int h = 0; h < kH; ++h)
+        if (h == tq) { mh = m[h]; lh = lt[h]; }
       const float lse2 = mh + __log2f(lh) - kPOff;
+      const int hh = h0 + tq;
       if (slot >= 0)
-        p.part_lse[static_cast<int64_t>(slot) * kHeads + tid] = lse2;
+        p.part_lse[static_cast<int64_t>(slot) * kHeads + hh] = lse2;
       else if (p.lse != nullptr)
-        p.lse[static_cast<int64_t>(w.b) * kHeads + tid] = lse2 * kLn2;
+        p.lse[static_cast<int64_t>(w.b) * kHeads + hh] = lse2 * kLn2;
     }
   }
 }
@@ -847,18 +981,21 @@ __global__ void __launch_bounds__(Layout<QM>::kThreads, 1) mla_stage1_kernel(con
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::kNumTiles; ++i) {
       mbar_init(smem_u32(&ms->full[i]), 1);
-      mbar_init(smem_u32(&ms->empty[i]), 2);         // both PV issuers
+      mbar_init(smem_u32(&ms->empty[i]), L::kPvIssuers);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&ms->s_full[i]), 2);        // both QK^T issuers
-      mbar_init(smem_u32(&ms->s_empty[i]), 128);
-      mbar_init(smem_u32(&ms->p_full[i]), 128);
-      mbar_init(smem_u32(&ms->pv_done[i]), 2);       // both PV issuers
+      mbar_init(smem_u32(&ms->s_empty[i]), 128 * L::kHeadGroups);
+      mbar_init(smem_u32(&ms->p_full[i]), 128 * L::kHeadGroups);
+      mbar_init(smem_u32(&ms->pv_done[i]), L::kPvIssuers);
       mbar_init(smem_u32(&ms->q_full[i]), 1);
-      mbar_init(smem_u32(&ms->q_empty[i]), 3);       // both QK^T issuers + softmax
+      mbar_init(smem_u32(&ms->q_empty[i]), 2 + L::kHeadGroups);  // QK^T issuers + softmax groups
     }
     for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&ms->drain[i]), 1);
-    for (int i = 0; i < L::kNumTiles; ++i) mbar_init(smem_u32(&ms->deq[i]), 128);
+    for (int i = 0; i < L::kNumTiles; ++i) {
+      mbar_init(smem_u32(&ms->deq[i]), 128);
+      mbar_init(smem_u32(&ms->deq_a[i]), 128);
+    }
     mbar_init(smem_u32(&ms->q_stage), 1);
     ms->abort_dq = 0;
     ms->abort_sm = 0;
@@ -878,14 +1015,15 @@ __global__ void __launch_bounds__(Layout<QM>::kThreads, 1) mla_stage1_kernel(con
     run_producer<QM>(p, ms, ring, it0, it1, lane);
   } else if (warp == 1 || warp == 3) {
     run_qk<QM>(p, ms, ring, ring + L::kQOff, tmem, it0, it1, warp == 3 ? 1 : 0, lane);
-  } else if (warp == 2 || warp == 9) {
-    run_pv<QM>(p, ms, ring, ring + L::kPOff, tmem, it0, it1, warp == 9 ? 1 : 0, lane);
-  } else if (warp == 8) {
-    run_qprep<QM>(p, ms, smem + L::kQOff, smem + L::kQStageOff, it0, it1, lane);
-  } else if (warp >= 10) {
-    if constexpr (L::kMx) run_dequant<QM>(p, ms, smem, it0, it1, threadIdx.x - 320);
-  } else {
+  } else if (warp == 2 || (!L::kMx && warp == 13)) {
+    run_pv<QM>(p, ms, ring, ring + L::kPOff, tmem, it0, it1, warp == 13 ? 1 : 0, lane);
+  } else if (warp < 4 + 4 * L::kHeadGroups) {
     run_softmax<QM>(p, ms, smem, smem + L::kPOff, tmem, it0, it1, threadIdx.x - 128);
+  } else if constexpr (L::kMx) {
+    run_dequant<QM>(p, ms, smem, smem + L::kQOff, smem + L::kQStageOff, it0, it1,
+                    threadIdx.x - 256);
+  } else {
+    run_qprep<QM>(p, ms, smem + L::kQOff, smem + L::kQStageOff, it0, it1, lane);
   }
 
   tc_fence_before();
