@@ -219,18 +219,28 @@ __device__ void run_producer(const Stage1Params& p, Misc* ms, uint32_t ring, int
     f1 = box_fetch(p, ahead, lane);
     ahead.advance();
     const uint32_t s = t % L::kNumTiles, ph = (t / L::kNumTiles) & 1u;
-    // every lane waits: a lone lane-0 wait followed by a broadcast cost
-    // about 1500 cycles of reconvergence per tile on GB300
+    const uint32_t full = smem_u32(&ms->full[s]);
+    const uint32_t raw_bytes = p.box_rows * L::kRawRowBytes, sc_bytes = p.box_rows * 32u;
+    // Before waiting for the slot to be free: resolve the rows and arm the
+    // slot's next full phase with the bytes to come.  That arrive must fall
+    // in the next phase, so the slot's previous tile must have landed first
+    // (it has, in the steady state); the armed phase cannot complete before
+    // the copies, which are only issued once the slot is free.
+    // Every lane waits: a lone lane-0 wait followed by a broadcast cost
+    // about 1500 cycles of reconvergence per tile on GB300.
+    const int row = box_row(p, f, lane);
+    if (t >= static_cast<uint32_t>(L::kNumTiles)) {
+      ok = __all_sync(0xffffffffu, mbar_wait(full, ph ^ 1u, p.err, kErrProducer));
+      if (!ok) break;
+    }
+    if (lane == 0)
+      mbar_arrive_expect_tx(full, static_cast<uint32_t>(f.nbox) *
+                                      (L::kMx ? raw_bytes + sc_bytes : box_bytes));
     ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ms->empty[s]), ph ^ 1u, p.err, kErrProducer));
     if (!ok) break;
-    const int row = box_row(p, f, lane);
-    const uint32_t full = smem_u32(&ms->full[s]);
     if constexpr (L::kMx) {
       // packed rows of box i into the upper half of box i's e4m3 region,
       // scale rows beside the slot
-      const uint32_t raw_bytes = p.box_rows * L::kRawRowBytes, sc_bytes = p.box_rows * 32u;
-      if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(f.nbox) * (raw_bytes + sc_bytes));
-      __syncwarp();
       if (lane < f.nbox) {
         tma_load_3d(ring + s * L::kTileBytes + lane * box_bytes + raw_bytes, &p.tmap_kv, full, 0,
                     row, 0, pol);
@@ -238,8 +248,6 @@ __device__ void run_producer(const Stage1Params& p, Misc* ms, uint32_t ring, int
                     pol);
       }
     } else {
-      if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(f.nbox) * box_bytes);
-      __syncwarp();
       if (lane < f.nbox)
         tma_load_3d(ring + s * L::kTileBytes + lane * box_bytes, &p.tmap_kv, full, 0, row, 0, pol);
     }
@@ -800,21 +808,32 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
       }
 #pragma unroll
       for (int h = 0; h < kH; ++h) s[h] = valid ? s[h] : -INFINITY;
-      float mt[kH];
-      reduce_heads<true, kH>(s, mt, ms->red[g & 1u], h0, qw, lane, bar);
+      // The running max only moves when some score of the tile exceeds it by
+      // more than kTau (always on an item's first tile).  One barrier vote
+      // settles that; only then is the tile max reduced over the group.
+      bool over = j == 0;
+#pragma unroll
+      for (int h = 0; h < kH; ++h) over |= s[h] > m[h] + kTau;
+      over = named_bar_any(4 + hg, 128, over);
       if (*abort) return;
       bool resc = false;
       float alpha[kH];
 #pragma unroll
-      for (int h = 0; h < kH; ++h) {
-        alpha[h] = 1.0f;
-        if (j == 0) {
-          m[h] = mt[h];
-          l[h] = 0.0f;
-        } else if (mt[h] > m[h] + kTau) {
-          alpha[h] = ex2(m[h] - mt[h]);
-          m[h] = mt[h];
-          resc = true;
+      for (int h = 0; h < kH; ++h) alpha[h] = 1.0f;
+      if (over) {
+        float mt[kH];
+        reduce_heads<true, kH>(s, mt, ms->red[g & 1u], h0, qw, lane, bar);
+        if (*abort) return;
+#pragma unroll
+        for (int h = 0; h < kH; ++h) {
+          if (j == 0) {
+            m[h] = mt[h];
+            l[h] = 0.0f;
+          } else if (mt[h] > m[h] + kTau) {
+            alpha[h] = ex2(m[h] - mt[h]);
+            m[h] = mt[h];
+            resc = true;
+          }
         }
       }
       if (resc) {
