@@ -104,6 +104,7 @@ struct Misc {
   uint64_t q_stage;                  // raw q of the next item landed in the staging buffer
   float uexp[2][128];                // per-token power of two u_t = r_t - 127 of a slot
   float qred[4];                     // per-warp |q| maxima (q prepared by the dequant warps)
+  uint2 e2m1_tab[16];                // e4m3 tables for 2^k, k = index - 14 (k <= -14: all 0)
 };
 static_assert(sizeof(Misc) <= 2048, "misc region");
 static_assert(offsetof(Misc, red) % 16 == 0, "reduction scratch is read as float4");
@@ -385,15 +386,10 @@ __device__ void run_pv(const Stage1Params& p, Misc* ms, uint32_t ring, uint32_t 
 // e4m3 bytes of m * 2^k for the eight e2m1 magnitudes m = {0, .5, 1, 1.5, 2,
 // 3, 4, 6} (byte c of {lo, hi} = code c).  k <= 0; 2^k below 2^-126 flushes
 // the block to zero (it is then below 2^-126 of the row's largest block).
+// A block uses one of 15 tables (k = 0 .. -14; from k = -14 down every entry
+// rounds to 0, below half the smallest e4m3 subnormal); the dequant warps
+// build them once per CTA.
 __device__ __forceinline__ void e2m1_e4m3_table(int k, uint32_t& lo, uint32_t& hi) {
-  if (k >= -5) {
-    // every nonzero entry stays a normal e4m3 number, so scaling by 2^k only
-    // moves the exponent field (bits 3-6): add 8k to each nonzero byte
-    // (no byte is below 8|k|, so nothing borrows across bytes)
-    lo = 0x3C383000u + static_cast<uint32_t>(k) * 0x08080800u;
-    hi = 0x4C484440u + static_cast<uint32_t>(k) * 0x08080808u;
-    return;
-  }
   const float f = k >= -126 ? __int_as_float((k + 127) << 23) : 0.0f;
   const uint32_t a = __nv_cvt_float2_to_fp8x2(make_float2(0.0f, 0.5f * f), __NV_SATFINITE, __NV_E4M3);
   const uint32_t b = __nv_cvt_float2_to_fp8x2(make_float2(1.0f * f, 1.5f * f), __NV_SATFINITE, __NV_E4M3);
@@ -530,6 +526,13 @@ __device__ void run_dequant(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
   volatile int32_t* abort = &ms->abort_dq;
   if (it0 >= it1) return;
   if (t == 0) q_fetch<QM>(p, ms, stage, it0);
+  if (t < 15) {
+    uint32_t lo, hi;
+    e2m1_e4m3_table(t - 14, lo, hi);
+    ms->e2m1_tab[t] = make_uint2(lo, hi);
+  }
+  // (qprep_group and every tile begin with a group barrier, so the tables
+  // are visible before their first use)
   if (!qprep_group<QM>(p, ms, qgen, stage, it0, 0, it1, t)) return;
   // this thread's row: box t/8, row t%8 (8-row boxes)
   const uint32_t box_off = (t >> 3) * 4608u, r8 = t & 7u;
@@ -570,9 +573,9 @@ __device__ void run_dequant(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
         neb = reinterpret_cast<const uint16_t*>(sc)[ch + 1];
       }
       __syncwarp();                                     // the box read packed chunk ch
-      uint32_t lo0, hi0, lo1, hi1;
-      e2m1_e4m3_table(static_cast<int>(eb & 0xFFu) - r, lo0, hi0);
-      e2m1_e4m3_table(static_cast<int>(eb >> 8) - r, lo1, hi1);
+      const uint2 t0 = ms->e2m1_tab[max(static_cast<int>(eb & 0xFFu) - r, -14) + 14];
+      const uint2 t1 = ms->e2m1_tab[max(static_cast<int>(eb >> 8) - r, -14) + 14];
+      const uint32_t lo0 = t0.x, hi0 = t0.y, lo1 = t1.x, hi1 = t1.y;
       const uint2 o0 = e2m1x8_to_e4m3(a.x, lo0, hi0), o1 = e2m1x8_to_e4m3(a.y, lo0, hi0);
       const uint2 o2 = e2m1x8_to_e4m3(a.z, lo0, hi0), o3 = e2m1x8_to_e4m3(a.w, lo0, hi0);
       const uint2 o4 = e2m1x8_to_e4m3(b.x, lo1, hi1), o5 = e2m1x8_to_e4m3(b.y, lo1, hi1);
