@@ -18,12 +18,13 @@
 //  * PV reuses the very same shared-memory bytes as an MN-major operand:
 //    O^T[512 x 16] += V^T[512 x 128 tok] . P^T, four M=128 blocks in TMEM;
 //  * a tcgen05.mma costs the issuing thread about the same time whatever
-//    its N, so QK^T and PV are issued by two different warps that run side
-//    by side: warps 1 and 3 each issue half of the QK^T K-steps into their
-//    own S accumulator, warps 2 and 9 issue PV for O blocks 0-1 and 2-3;
-//    warp 0 is the TMA producer, warp 8
-//    prepares q for the next item, warps 4-7 do the softmax and the
-//    epilogue (one thread per token / per output dim, TMEM lane = thread);
+//    its N, so QK^T and PV are issued by separate warps that run side by
+//    side: warps 1 and 3 each issue half of the QK^T K-steps into their own
+//    S accumulator; warps 2 and 13 issue PV for O blocks 0-1 and 2-3 (MXFP4:
+//    warp 2 alone).  Warp 0 is the TMA producer, warp 12 prepares q for the
+//    next item (MXFP4: warps 12-15 dequantise tiles and prepare q), and
+//    warps 4-11 do the softmax and the epilogue in two groups of 8 heads
+//    (one thread per token / per output dim, TMEM lane = thread);
 //  * every mbarrier wait is bounded (see mbar_wait) and reports into the
 //    device error word instead of hanging.
 //
@@ -52,11 +53,11 @@ struct Layout {
   static constexpr bool kMx = (QM == kQBf16KvMx);                  // MXFP4 KV, dequantised
   static constexpr bool kKv8 = (QM == kQFp8KvFp8 || QM == kQBf16KvFp8 || kMx);
   static constexpr int kNq = (QM == kQBf16KvFp8 || kMx) ? 32 : 16;  // UMMA N of QK^T
-  // Warps: producer, 2 QK^T issuers, PV issuer(s), 4 softmax warps per head
-  // group, then either 4 dequant warps that also prepare q (MXFP4: 12 warps,
-  // register cap 168) or a q warp (14 warps: two head groups of 8 heads).
-  static constexpr int kHeadGroups = kMx ? 1 : 2;
-  static constexpr int kThreads = kMx ? 384 : 448;
+  // Warps: producer, 2 QK^T issuers, PV issuer(s), two head groups of four
+  // softmax warps (8 heads each), then either a q warp (14 warps) or, for
+  // MXFP4, 4 dequant warps that also prepare q (16 warps, register cap 128).
+  static constexpr int kHeadGroups = 2;
+  static constexpr int kThreads = kMx ? 512 : 448;
   static constexpr int kPvIssuers = kMx ? 1 : 2;
   static constexpr int kElem = kKv8 ? 1 : 2;
   static constexpr int kRowBytes = kQkDim * kElem;                  // 576 | 1152
@@ -1043,7 +1044,7 @@ __global__ void __launch_bounds__(Layout<QM>::kThreads, 1) mla_stage1_kernel(con
     run_softmax<QM>(p, ms, smem, smem + L::kPOff, tmem, it0, it1, threadIdx.x - 128);
   } else if constexpr (L::kMx) {
     run_dequant<QM>(p, ms, smem, smem + L::kQOff, smem + L::kQStageOff, it0, it1,
-                    threadIdx.x - 256);
+                    threadIdx.x - 384);
   } else {
     run_qprep<QM>(p, ms, smem + L::kQOff, smem + L::kQStageOff, it0, it1, lane);
   }
