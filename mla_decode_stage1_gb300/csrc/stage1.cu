@@ -101,6 +101,7 @@ struct Misc {
   // MXFP4 only
   uint64_t deq[4];                   // tile slot dequantised (128 dequant threads)
   uint64_t deq_a[4];                 // its dims 0-319 dequantised (first QK^T K-half)
+  uint64_t upper_free[4];            // PV no longer reads the slot's upper box halves
   int32_t abort_dq;                  // set by a dequant thread whose bounded wait gave up
   uint64_t q_stage;                  // raw q of the next item landed in the staging buffer
   float uexp[2][128];                // per-token power of two u_t = r_t - 127 of a slot
@@ -238,7 +239,10 @@ __device__ void run_producer(const Stage1Params& p, Misc* ms, uint32_t ring, int
     if (lane == 0)
       mbar_arrive_expect_tx(full, static_cast<uint32_t>(f.nbox) *
                                       (L::kMx ? raw_bytes + sc_bytes : box_bytes));
-    ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ms->empty[s]), ph ^ 1u, p.err, kErrProducer));
+    // (MXFP4: the packed rows land in the upper box halves, free once PV has
+    // read O blocks 2-3; the dequantisation waits for the whole slot)
+    ok = __all_sync(0xffffffffu, mbar_wait(L::kMx ? smem_u32(&ms->upper_free[s]) : smem_u32(&ms->empty[s]),
+                                           ph ^ 1u, p.err, kErrProducer));
     if (!ok) break;
     if constexpr (L::kMx) {
       // packed rows of box i into the upper half of box i's e4m3 region,
@@ -349,7 +353,12 @@ __device__ void run_pv(const Stage1Params& p, Misc* ms, uint32_t ring, uint32_t 
     const uint32_t pa = pbase + pb * L::kPBytes;
     const bool first = pc.j == 0;
     if (lane == 0) {
-    for (int c = kBlocks * half; c < kBlocks * half + kBlocks; ++c) {
+    for (int i = 0; i < kBlocks; ++i) {
+      // MXFP4 (one issuer): O blocks 2-3 first.  Their V chunks 4-7 and the
+      // rope chunk 8 are the upper half of every 8-row box, where the next
+      // packed rows land, so the producer may refill the slot as soon as
+      // they are read; blocks 0-1 follow.
+      const int c = L::kMx ? (i + 2) & 3 : kBlocks * half + i;
       const uint32_t d = tmem + kColO + L::kOCols * c;
       // B = P^T, MN-major with the 32-byte swizzle: one 32-byte row per token
       // (fp8: 16 heads of p_hi then 16 of p_lo; bf16: 16 heads), 8-token
@@ -372,6 +381,7 @@ __device__ void run_pv(const Stage1Params& p, Misc* ms, uint32_t ring, uint32_t 
           umma_f16(d, a, b, idesc, (first && kk == 0) ? 0u : 1u);
         }
       }
+      if (L::kMx && i == 1) tc_commit(smem_u32(&ms->upper_free[s]));
     }
     tc_commit(smem_u32(&ms->pv_done[pb]));
     tc_commit(smem_u32(&ms->empty[s]));      // QK^T of this tile completed before P existed
@@ -543,6 +553,10 @@ __device__ void run_dequant(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
   while (!c.done()) {
     const uint32_t tt = c.t, s = tt % L::kNumTiles;
     if (!mbar_wait(smem_u32(&ms->full[s]), (tt / L::kNumTiles) & 1u, p.err, kErrDequant)) *abort = 1;
+    // e4m3 rows are written over the whole slot: PV of its previous tile
+    // must have finished (the packed rows only needed the upper halves)
+    if (!mbar_wait(smem_u32(&ms->empty[s]), ((tt / L::kNumTiles) & 1u) ^ 1u, p.err, kErrDequant))
+      *abort = 1;
     named_bar_sync(3, 128);
     if (*abort) return;
     uint8_t* box = ring_gen + s * L::kTileBytes + box_off;
@@ -1018,6 +1032,7 @@ __global__ void __launch_bounds__(Layout<QM>::kThreads, 1) mla_stage1_kernel(con
     for (int i = 0; i < L::kNumTiles; ++i) {
       mbar_init(smem_u32(&ms->deq[i]), 128);
       mbar_init(smem_u32(&ms->deq_a[i]), 128);
+      mbar_init(smem_u32(&ms->upper_free[i]), 1);
     }
     mbar_init(smem_u32(&ms->q_stage), 1);
     ms->abort_dq = 0;
