@@ -104,8 +104,9 @@ struct Misc {
   uint64_t upper_free[4];            // PV no longer reads the slot's upper box halves
   int32_t abort_dq;                  // set by a dequant thread whose bounded wait gave up
   uint64_t q_stage;                  // raw q of the next item landed in the staging buffer
+  uint64_t q_stage_free;             // the softmax warps converted the first item's q
   float uexp[2][128];                // per-token power of two u_t = r_t - 127 of a slot
-  float qred[4];                     // per-warp |q| maxima (q prepared by the dequant warps)
+  float qred[8];                     // per-warp |q| maxima (q prepared by a warp group)
   uint2 e2m1_tab[16];                // e4m3 tables for 2^k, k = index - 14 (k <= -14: all 0)
 };
 static_assert(sizeof(Misc) <= 2048, "misc region");
@@ -464,6 +465,81 @@ __device__ __forceinline__ void q_split_store(const uint4 v, int vid, float s_hi
   *reinterpret_cast<uint2*>(base + sw128(16 + h, x)) = make_uint2(lw[0], lw[1]);
 }
 
+// Writes q of one request from the staging buffer into q buffer `dst` (the
+// UMMA B operand) with n threads (this is thread i, n a multiple of 32) and
+// returns the two score factors.  A bf16 q meeting fp8 or MXFP4 KV is split
+// into two e4m3 terms with one scale for the request, which needs |q|max
+// over all n threads: warp shuffles, then (n > 32) ms->qred and named
+// barrier `bar`.  The caller fences and publishes the buffer.
+template <int QM>
+__device__ __forceinline__ void q_convert(const Stage1Params& p, Misc* ms, const uint8_t* stage,
+                                          uint8_t* dst, int i, int n, int bar, float& c_hi,
+                                          float& c_lo) {
+  using L = Layout<QM>;
+  constexpr float kSmScale = 1.0f / 24.0f;          // 1/sqrt(576)
+  c_lo = 0.f;
+  if constexpr (QM == kQBf16KvFp8 || QM == kQBf16KvMx) {
+    constexpr int kV = L::kQSrcBytes / 16;           // 16-byte vectors of 8 bf16
+    const uint4* src = reinterpret_cast<const uint4*>(stage);
+    float amax = 0.f;
+    for (int v = i; v < kV; v += n) {
+      const uint4 x = src[v];
+      const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&x);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(h2[e]);
+        amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if (n > 32) {
+      if ((i & 31) == 0) ms->qred[i >> 5] = amax;
+      named_bar_sync(bar, n);
+      amax = 0.f;
+      for (int w = 0; w < n / 32; ++w) amax = fmaxf(amax, ms->qred[w]);
+    }
+    amax = fmaxf(amax, 1e-30f);
+    const float s_hi = amax / 448.0f, inv_hi = 448.0f / amax;
+    for (int v = i; v < kV; v += n) q_split_store(src[v], v, s_hi, inv_hi, dst, L::kQAtomBytes);
+    const float kvs = (QM == kQBf16KvMx) ? 1.0f : __ldg(p.kv_scale);
+    c_hi = s_hi * kvs * kSmScale * kLog2e;
+    c_lo = c_hi * (1.0f / 16.0f);
+  } else if constexpr (QM == kQFp8KvFp8) {
+    const uint4* src = reinterpret_cast<const uint4*>(stage);
+    for (int v = i; v < kHeads * 36; v += n) {       // 36 vectors of 16 e4m3 per head
+      const int h = v / 36, d0 = (v % 36) * 16;
+      *reinterpret_cast<uint4*>(dst + (d0 >> 7) * L::kQAtomBytes + sw128(h, d0 & 127)) = src[v];
+    }
+    c_hi = __ldg(p.q_scale) * __ldg(p.kv_scale) * kSmScale * kLog2e;
+  } else {
+    // bf16 operand for kind::f16; fp8 q is decoded exactly to bf16 first.
+    for (int v = i; v < kHeads * 72; v += n) {       // 72 vectors of 8 values per head
+      const int h = v / 72, d0 = (v % 72) * 8;
+      uint4 x;
+      if constexpr (QM == kQBf16KvBf16) {
+        x = reinterpret_cast<const uint4*>(stage)[v];
+      } else {
+        const uint2 raw = reinterpret_cast<const uint2*>(stage)[v];
+        uint32_t wv[4];
+        const uint32_t rr[2] = {raw.x, raw.y};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const __nv_fp8x2_storage_t pr =
+              static_cast<__nv_fp8x2_storage_t>((rr[e >> 1] >> ((e & 1) * 16)) & 0xFFFFu);
+          const float2 f = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3)));
+          const __nv_bfloat162 bb = __float22bfloat162_rn(f);
+          wv[e] = *reinterpret_cast<const uint32_t*>(&bb);
+        }
+        x = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+      }
+      const int atom = d0 >> 6, xb = (d0 & 63) * 2;
+      *reinterpret_cast<uint4*>(dst + atom * L::kQAtomBytes + sw128(h, xb)) = x;
+    }
+    c_hi = (QM == kQFp8KvBf16 ? __ldg(p.q_scale) : 1.0f) * kSmScale * kLog2e;
+  }
+}
+
 // MXFP4 variant: the four dequant warps (128 threads, named barrier 3)
 // prepare q of item `it` (ordinal k) into q buffer k & 1, then start the copy
 // of the next item's q.  Returns false once the group gave up.
@@ -471,41 +547,20 @@ template <int QM>
 __device__ bool qprep_group(const Stage1Params& p, Misc* ms, uint8_t* qgen, uint8_t* stage, int it,
                             int k, int it1, int t) {
   using L = Layout<QM>;
-  constexpr float kSmScale = 1.0f / 24.0f;          // 1/sqrt(576)
-  constexpr int kVec = L::kQSrcBytes / 16 / 128;    // 16-byte vectors per thread
   volatile int32_t* abort = &ms->abort_dq;
   const uint32_t qb = k & 1;
   if (!mbar_wait(smem_u32(&ms->q_empty[qb]), ((k >> 1) & 1) ^ 1, p.err, kErrQPrep)) *abort = 1;
   if (!mbar_wait(smem_u32(&ms->q_stage), k & 1, p.err, kErrQPrep)) *abort = 1;
-  const uint4* src = reinterpret_cast<const uint4*>(stage);
-  uint4 v[kVec];
-  float amax = 0.f;
-#pragma unroll
-  for (int i = 0; i < kVec; ++i) {
-    v[i] = src[t + 128 * i];
-    const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v[i]);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 f = __bfloat1622float2(h2[e]);
-      amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  if ((t & 31) == 0) ms->qred[t >> 5] = amax;
   named_bar_sync(3, 128);
   if (*abort) return false;
-  amax = fmaxf(fmaxf(fmaxf(ms->qred[0], ms->qred[1]), fmaxf(ms->qred[2], ms->qred[3])), 1e-30f);
-  const float s_hi = amax / 448.0f, inv_hi = 448.0f / amax;
-  uint8_t* dst = qgen + qb * L::kQBytes;
-#pragma unroll
-  for (int i = 0; i < kVec; ++i) q_split_store(v[i], t + 128 * i, s_hi, inv_hi, dst, L::kQAtomBytes);
+  float c_hi, c_lo;
+  q_convert<QM>(p, ms, stage, qgen + qb * L::kQBytes, t, 128, 3, c_hi, c_lo);
   fence_proxy_async_smem();
   named_bar_sync(3, 128);                           // staging buffer and qred free again
   if (t == 0) {
     if (it + 1 < it1) q_fetch<QM>(p, ms, stage, it + 1);
-    ms->qscale[qb][0] = s_hi * kSmScale * kLog2e;
-    ms->qscale[qb][1] = s_hi * (1.0f / 16.0f) * kSmScale * kLog2e;
+    ms->qscale[qb][0] = c_hi;
+    ms->qscale[qb][1] = c_lo;
     mbar_arrive(smem_u32(&ms->q_full[qb]));
   }
   return true;
@@ -624,96 +679,35 @@ __device__ __forceinline__ void wait_or_flag(uint32_t bar, uint32_t parity, int3
 }
 
 // -------------------------------------------------------------- q prepare
-// One warp writes q of the next item into a free q buffer in the UMMA operand
-// layout (K-major, 128-byte swizzle) and publishes the score factors.
+// One bulk copy per request brings q into the staging buffer.  The first
+// item's q gates the first QK^T, so the softmax warps (idle until then)
+// convert it together; this warp converts the q of every later item into the
+// free q buffer, off the critical path, and starts the next copy as soon as
+// the staging buffer is free.
 template <int QM>
 __device__ void run_qprep(const Stage1Params& p, Misc* ms, uint8_t* qgen, uint8_t* stage, int it0,
                           int it1, int lane) {
   using L = Layout<QM>;
-  constexpr float kSmScale = 1.0f / 24.0f;          // 1/sqrt(576)
-  // one bulk copy brings a request's q into the staging buffer; the next
-  // request's copy starts as soon as this one has been converted
   const uint32_t stage_bar = smem_u32(&ms->q_stage);
-  auto fetch = [&](int it) {
-    if (lane == 0) q_fetch<QM>(p, ms, stage, it);
-  };
-  if (it0 < it1) fetch(it0);
-  int k = 0;
-  for (int it = it0; it < it1; ++it, ++k) {
+  if (it0 >= it1) return;
+  if (lane == 0) q_fetch<QM>(p, ms, stage, it0);
+  if (it0 + 1 >= it1) return;
+  // the softmax warps are done with the first item's staged q
+  if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ms->q_stage_free), 0, p.err, kErrQPrep))) return;
+  if (lane == 0) q_fetch<QM>(p, ms, stage, it0 + 1);
+  int k = 1;
+  for (int it = it0 + 1; it < it1; ++it, ++k) {
     const uint32_t qb = k & 1;
     if (!__all_sync(0xffffffffu,
                     mbar_wait(smem_u32(&ms->q_empty[qb]), ((k >> 1) & 1) ^ 1, p.err, kErrQPrep)))
       return;
     if (!__all_sync(0xffffffffu, mbar_wait(stage_bar, k & 1, p.err, kErrQPrep))) return;
-    uint8_t* dst = qgen + qb * L::kQBytes;
-    float c_hi = 0.f, c_lo = 0.f;
-    if constexpr (QM == kQBf16KvFp8 || QM == kQBf16KvMx) {
-      const uint4* src = reinterpret_cast<const uint4*>(stage);
-      float amax = 0.f;
-#pragma unroll 4
-      for (int i = 0; i < 36; ++i) {
-        const uint4 v = src[lane + 32 * i];
-        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = __bfloat1622float2(h2[e]);
-          amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      amax = fmaxf(amax, 1e-30f);
-      const float s_hi = amax / 448.0f, inv_hi = 448.0f / amax;
-#pragma unroll 4
-      for (int i = 0; i < 36; ++i) {
-        const int vid = lane + 32 * i;
-        q_split_store(src[vid], vid, s_hi, inv_hi, dst, L::kQAtomBytes);
-      }
-      const float kvs = (QM == kQBf16KvMx) ? 1.0f : __ldg(p.kv_scale);
-      c_hi = s_hi * kvs * kSmScale * kLog2e;
-      c_lo = s_hi * (1.0f / 16.0f) * kvs * kSmScale * kLog2e;
-    } else if constexpr (QM == kQFp8KvFp8) {
-      const uint4* src = reinterpret_cast<const uint4*>(stage);
-#pragma unroll 6
-      for (int i = 0; i < 18; ++i) {
-        const int vid = lane + 32 * i;
-        const int h = vid / 36, d0 = (vid % 36) * 16;
-        const uint4 v = src[vid];
-        *reinterpret_cast<uint4*>(dst + (d0 >> 7) * L::kQAtomBytes + sw128(h, d0 & 127)) = v;
-      }
-      c_hi = __ldg(p.q_scale) * __ldg(p.kv_scale) * kSmScale * kLog2e;
-    } else {
-      // bf16 operand for kind::f16; fp8 q is decoded exactly to bf16 first.
-#pragma unroll 4
-      for (int i = 0; i < 36; ++i) {
-        const int vid = lane + 32 * i;
-        const int h = vid / 72, d0 = (vid % 72) * 8;
-        uint4 v;
-        if constexpr (QM == kQBf16KvBf16) {
-          v = reinterpret_cast<const uint4*>(stage)[vid];
-        } else {
-          const uint2 raw = reinterpret_cast<const uint2*>(stage)[vid];
-          uint32_t wv[4];
-          const uint32_t rr[2] = {raw.x, raw.y};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const __nv_fp8x2_storage_t pr =
-                static_cast<__nv_fp8x2_storage_t>((rr[e >> 1] >> ((e & 1) * 16)) & 0xFFFFu);
-            const float2 f = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3)));
-            const __nv_bfloat162 bb = __float22bfloat162_rn(f);
-            wv[e] = *reinterpret_cast<const uint32_t*>(&bb);
-          }
-          v = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-        }
-        const int atom = d0 >> 6, x = (d0 & 63) * 2;
-        *reinterpret_cast<uint4*>(dst + atom * L::kQAtomBytes + sw128(h, x)) = v;
-      }
-      c_hi = (QM == kQFp8KvBf16 ? __ldg(p.q_scale) : 1.0f) * kSmScale * kLog2e;
-    }
+    float c_hi, c_lo;
+    q_convert<QM>(p, ms, stage, qgen + qb * L::kQBytes, lane, 32, 0, c_hi, c_lo);
     fence_proxy_async_smem();
     __syncwarp();                                     // every lane is done with the stage
-    if (it + 1 < it1) fetch(it + 1);
     if (lane == 0) {
+      if (it + 1 < it1) q_fetch<QM>(p, ms, stage, it + 1);
       ms->qscale[qb][0] = c_hi;
       ms->qscale[qb][1] = c_lo;
       mbar_arrive(smem_u32(&ms->q_full[qb]));
@@ -764,7 +758,8 @@ __device__ __forceinline__ void reduce_heads(const float (&v)[kH], float (&out)[
 // item's last tile, the epilogue normalises O and writes it out.
 template <int QM>
 __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, uint8_t* pgen,
-                            uint32_t tmem, int it0, int it1, int tid) {
+                            uint8_t* qgen, uint8_t* stage, uint32_t tmem, int it0, int it1,
+                            int tid) {
   using L = Layout<QM>;
   constexpr int kHG = L::kHeadGroups, kH = 16 / kHG;
   volatile int32_t* abort = &ms->abort_sm;
@@ -774,6 +769,26 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
   const uint32_t tl = tmem + (static_cast<uint32_t>(qw * 32) << 16);   // this warp's lanes
   uint32_t g = 0;
   const uint32_t cs = p.chunk_stride, gs = p.group_stride;
+  if constexpr (!L::kMx) {
+    if (it0 < it1) {
+      // The first item's q gates the first QK^T: all softmax threads convert
+      // it (into q buffer 0) while they would otherwise wait for S.
+      constexpr int kN = 128 * kHG;
+      wait_or_flag(smem_u32(&ms->q_stage), 0, p.err, kErrSoftmax, abort);
+      named_bar_sync(6, kN);
+      if (*abort) return;
+      float c_hi, c_lo;
+      q_convert<QM>(p, ms, stage, qgen, tid, kN, 6, c_hi, c_lo);
+      fence_proxy_async_smem();
+      named_bar_sync(6, kN);
+      if (tid == 0) {
+        ms->qscale[0][0] = c_hi;
+        ms->qscale[0][1] = c_lo;
+        mbar_arrive(smem_u32(&ms->q_full[0]));
+        mbar_arrive(smem_u32(&ms->q_stage_free));
+      }
+    }
+  }
   int k = 0;
   float m[kH], l[kH];
   for (int it = it0; it < it1; ++it, ++k) {
@@ -1035,6 +1050,7 @@ __global__ void __launch_bounds__(Layout<QM>::kThreads, 1) mla_stage1_kernel(con
       mbar_init(smem_u32(&ms->upper_free[i]), 1);
     }
     mbar_init(smem_u32(&ms->q_stage), 1);
+    mbar_init(smem_u32(&ms->q_stage_free), 1);
     ms->abort_dq = 0;
     ms->abort_sm = 0;
     fence_mbar_init();
@@ -1056,7 +1072,8 @@ __global__ void __launch_bounds__(Layout<QM>::kThreads, 1) mla_stage1_kernel(con
   } else if (warp == 2 || (!L::kMx && warp == 13)) {
     run_pv<QM>(p, ms, ring, ring + L::kPOff, tmem, it0, it1, warp == 13 ? 1 : 0, lane);
   } else if (warp < 4 + 4 * L::kHeadGroups) {
-    run_softmax<QM>(p, ms, smem, smem + L::kPOff, tmem, it0, it1, threadIdx.x - 128);
+    run_softmax<QM>(p, ms, smem, smem + L::kPOff, smem + L::kQOff, smem + L::kQStageOff, tmem, it0,
+                    it1, threadIdx.x - 128);
   } else if constexpr (L::kMx) {
     run_dequant<QM>(p, ms, smem, smem + L::kQOff, smem + L::kQStageOff, it0, it1,
                     threadIdx.x - 384);

@@ -23,11 +23,12 @@ __global__ void __launch_bounds__(256) mla_stage2_kernel(const Stage2Params p) {
   const int lane = threadIdx.x & 31;
   const int job = gw >> 4, h = gw & 15;
   if (job >= p.num_jobs) return;
+  // The job table is plan data (not written by stage 1): read it first.
+  const MergeJob J = p.jobs[job];
+  uint16_t* out = p.out + (static_cast<int64_t>(J.b) * kHeads + h) * kVDim;
   // Launched as a programmatic dependent of stage 1: wait here until stage 1
   // has completed and its partials are visible.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const MergeJob J = p.jobs[job];
-  uint16_t* out = p.out + (static_cast<int64_t>(J.b) * kHeads + h) * kVDim;
   float acc[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
@@ -37,19 +38,32 @@ __global__ void __launch_bounds__(256) mla_stage2_kernel(const Stage2Params p) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   if (M != -INFINITY) {
-    for (int s = 0; s < J.count; ++s) {
-      const int64_t row = static_cast<int64_t>(J.first + s) * kHeads + h;
-      const float w = ex2(p.part_lse[row] - M);
-      if (w == 0.0f) continue;
-      wsum += w;
-      const float4* src = reinterpret_cast<const float4*>(p.part_o + row * kVDim);
+    // Partials go two at a time so that the loads of both rows are in flight
+    // together; a partial whose weight is 0 adds exactly nothing (a select,
+    // not a branch, so that no load waits on the weight).
+    for (int s = 0; s < J.count; s += 2) {
+      const int n = min(2, J.count - s);
+      float w[2];
+      float4 v[2][4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float4 v = src[lane + 32 * i];
-        acc[4 * i + 0] += w * v.x;
-        acc[4 * i + 1] += w * v.y;
-        acc[4 * i + 2] += w * v.z;
-        acc[4 * i + 3] += w * v.w;
+      for (int u = 0; u < 2; ++u) {
+        const int64_t row = static_cast<int64_t>(J.first + s + (u < n ? u : 0)) * kHeads + h;
+        w[u] = u < n ? ex2(p.part_lse[row] - M) : 0.0f;
+        const float4* src = reinterpret_cast<const float4*>(p.part_o + row * kVDim);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[u][i] = src[lane + 32 * i];
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        wsum += w[u];
+        const bool live = w[u] > 0.0f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[4 * i + 0] += live ? w[u] * v[u][i].x : 0.0f;
+          acc[4 * i + 1] += live ? w[u] * v[u][i].y : 0.0f;
+          acc[4 * i + 2] += live ? w[u] * v[u][i].z : 0.0f;
+          acc[4 * i + 3] += live ? w[u] * v[u][i].w : 0.0f;
+        }
       }
     }
   }
