@@ -17,6 +17,7 @@
 
 using mla::MergeJob;
 using mla::WorkItem;
+using mla::CtaHead;
 
 
 namespace {
@@ -112,8 +113,8 @@ void layout_workspace(mla_plan* P) {
   size_t off = 0;
   P->off_err = off;
   off = align256(off + 16);
-  P->off_indptr = off;
-  off = align256(off + sizeof(int32_t) * P->cta_indptr.size());
+  P->off_indptr = off;                                       // CtaHead per CTA
+  off = align256(off + sizeof(CtaHead) * (P->cta_indptr.size() - 1));
   P->off_items = off;
   off = align256(off + sizeof(WorkItem) * P->items.size());
   P->off_jobs = off;
@@ -124,8 +125,13 @@ void layout_workspace(mla_plan* P) {
   off = align256(off + sizeof(float) * static_cast<size_t>(P->num_partials) * mla::kHeads);
   P->ws_bytes = std::max<size_t>(off, 256);
   P->table.assign(P->off_part_o, 0);
-  std::memcpy(P->table.data() + P->off_indptr, P->cta_indptr.data(),
-              sizeof(int32_t) * P->cta_indptr.size());
+  for (size_t c = 0; c + 1 < P->cta_indptr.size(); ++c) {
+    CtaHead h{};
+    h.it0 = P->cta_indptr[c];
+    h.it1 = P->cta_indptr[c + 1];
+    if (h.it0 < h.it1) h.first = P->items[h.it0];
+    std::memcpy(P->table.data() + P->off_indptr + c * sizeof(CtaHead), &h, sizeof(h));
+  }
   if (!P->items.empty())
     std::memcpy(P->table.data() + P->off_items, P->items.data(), sizeof(WorkItem) * P->items.size());
   if (!P->jobs.empty())
@@ -360,7 +366,7 @@ mla_status mla_decode_run(mla_plan* plan, const void* q, const float* q_scale, c
     p.kv_scale = kv_scale;
     p.kv_indices = kv_indices;
     p.items = reinterpret_cast<const WorkItem*>(ws + plan->off_items);
-    p.cta_indptr = reinterpret_cast<const int32_t*>(ws + plan->off_indptr);
+    p.heads = reinterpret_cast<const CtaHead*>(ws + plan->off_indptr);
     p.part_o = part_o;
     p.part_lse = part_lse;
     p.out = static_cast<uint16_t*>(out);

@@ -40,6 +40,15 @@ struct WorkItem {
 };
 static_assert(sizeof(WorkItem) == 32, "work item is two int4");
 
+// Per-CTA head: its item range and a copy of its first item, so that one
+// load gives a CTA everything its first tile needs.
+struct CtaHead {
+  int32_t it0, it1;   // items [it0, it1) of the work-item array
+  int32_t pad0, pad1;
+  WorkItem first;     // items[it0] (unused when it0 == it1)
+};
+static_assert(sizeof(CtaHead) == 48, "CTA head is three int4");
+
 // One stage-2 job: merge `count` consecutive partials of request b (count 0:
 // the request is empty, write zeros and -inf).
 struct MergeJob {
@@ -64,7 +73,7 @@ struct Stage1Params {
   const float* kv_scale;        // device [1] (fp8 kv) or null
   const int32_t* kv_indices;    // page table or null (identity)
   const WorkItem* items;
-  const int32_t* cta_indptr;
+  const CtaHead* heads;         // [num_ctas]
   float* part_o;                // [num_partials,16,512] fp32, normalised
   float* part_lse;              // [num_partials,16] log2 domain
   uint16_t* out;                // [bs,16,512] bf16 bits

@@ -132,14 +132,21 @@ struct TileCursor {
   int j, ntile;          // tile within the item
   uint32_t t;            // tile ordinal within the CTA
   WorkItem w;
-  __device__ __forceinline__ void init(const WorkItem* items_, int it0, int it1_) {
+  // `first` is a copy of items_[it0] (the CTA head), so starting costs no load
+  __device__ __forceinline__ void init(const WorkItem* items_, int it0, int it1_,
+                                       const WorkItem& first) {
     items = items_;
     it = it0;
     it1 = it1_;
     k = 0;
     j = 0;
     t = 0;
-    load();
+    if (it < it1) {
+      w = first;
+      ntile = (w.tok_end - w.tok_begin + kTile - 1) / kTile;
+    } else {
+      ntile = 0;
+    }
   }
   __device__ __forceinline__ void load() {
     if (it < it1) {
@@ -204,12 +211,12 @@ __device__ __forceinline__ int box_row(const Stage1Params& p, const BoxFetch& f,
 // fetched two tiles ahead of the tile being issued.
 template <int QM>
 __device__ void run_producer(const Stage1Params& p, Misc* ms, uint32_t ring, int it0, int it1,
-                             int lane) {
+                             const WorkItem& first, int lane) {
   using L = Layout<QM>;
   const uint64_t pol = l2_policy_evict_first();
   const uint32_t box_bytes = static_cast<uint32_t>(p.box_rows) * L::kRowBytes;
   TileCursor cur, ahead;
-  cur.init(p.items, it0, it1);
+  cur.init(p.items, it0, it1, first);
   ahead = cur;
   BoxFetch f0 = box_fetch(p, ahead, lane);
   ahead.advance();
@@ -279,13 +286,14 @@ __device__ void run_producer(const Stage1Params& p, Misc* ms, uint32_t ring, int
 // groups at gs.
 template <int QM>
 __device__ void run_qk(const Stage1Params& p, Misc* ms, uint32_t ring, uint32_t qbase,
-                       uint32_t tmem, int it0, int it1, int half, int lane) {
+                       uint32_t tmem, int it0, int it1, const WorkItem& first, int half,
+                       int lane) {
   using L = Layout<QM>;
   constexpr uint32_t idesc = L::kKv8 ? make_idesc(0, 0, false, false, 128, L::kNq)
                                      : make_idesc(1, 1, false, false, 128, 16);
   const uint32_t cs = p.chunk_stride, gs = p.group_stride;
   TileCursor qc;
-  qc.init(p.items, it0, it1);
+  qc.init(p.items, it0, it1, first);
   int q_ready = -1;
   while (!qc.done()) {
     const uint32_t t = qc.t, sb = t & 1u, s = t % L::kNumTiles;
@@ -338,12 +346,13 @@ __device__ void run_qk(const Stage1Params& p, Misc* ms, uint32_t ring, uint32_t 
 // `half` owns O blocks 2*half, 2*half+1 (two issuers) or all four (one).
 template <int QM>
 __device__ void run_pv(const Stage1Params& p, Misc* ms, uint32_t ring, uint32_t pbase,
-                       uint32_t tmem, int it0, int it1, int half, int lane) {
+                       uint32_t tmem, int it0, int it1, const WorkItem& first, int half,
+                       int lane) {
   using L = Layout<QM>;
   constexpr int kBlocks = 4 / L::kPvIssuers;
   const uint32_t cs = p.chunk_stride, gs = p.group_stride;
   TileCursor pc;
-  pc.init(p.items, it0, it1);
+  pc.init(p.items, it0, it1, first);
   while (!pc.done()) {
     const uint32_t t = pc.t, pb = t & 1u, s = t % L::kNumTiles;
     if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ms->p_full[pb]), (t >> 1) & 1u, p.err,
@@ -425,12 +434,11 @@ __device__ __forceinline__ uint2 e2m1x8_to_e4m3(uint32_t w, uint32_t lo, uint32_
 }
 
 // ----------------------------------------------------- q staging helpers
-// One bulk copy brings q of item `it` (all 16 heads) into the staging buffer.
+// One bulk copy brings q of request `bb` (all 16 heads) into the staging buffer.
 template <int QM>
-__device__ __forceinline__ void q_fetch(const Stage1Params& p, Misc* ms, uint8_t* stage, int it) {
+__device__ __forceinline__ void q_fetch(const Stage1Params& p, Misc* ms, uint8_t* stage, int bb) {
   using L = Layout<QM>;
   const uint32_t bar = smem_u32(&ms->q_stage);
-  const int bb = p.items[it].b;
   mbar_arrive_expect_tx(bar, L::kQSrcBytes);
   bulk_load(smem_u32(stage), static_cast<const uint8_t*>(p.q) + static_cast<int64_t>(bb) * L::kQSrcBytes,
             L::kQSrcBytes, bar);
@@ -558,7 +566,7 @@ __device__ bool qprep_group(const Stage1Params& p, Misc* ms, uint8_t* qgen, uint
   fence_proxy_async_smem();
   named_bar_sync(3, 128);                           // staging buffer and qred free again
   if (t == 0) {
-    if (it + 1 < it1) q_fetch<QM>(p, ms, stage, it + 1);
+    if (it + 1 < it1) q_fetch<QM>(p, ms, stage, p.items[it + 1].b);
     ms->qscale[qb][0] = c_hi;
     ms->qscale[qb][1] = c_lo;
     mbar_arrive(smem_u32(&ms->q_full[qb]));
@@ -586,12 +594,12 @@ __device__ bool qprep_group(const Stage1Params& p, Misc* ms, uint8_t* qgen, uint
 // of item k-1 has been issued on tiles this group already dequantised).
 template <int QM>
 __device__ void run_dequant(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, uint8_t* qgen,
-                            uint8_t* stage, int it0, int it1, int t) {
+                            uint8_t* stage, int it0, int it1, const WorkItem& first, int t) {
   using L = Layout<QM>;
   static_assert(L::kRowBytes * 8 == 4608 && L::kRawRowBytes * 8 == 2304, "box layout");
   volatile int32_t* abort = &ms->abort_dq;
   if (it0 >= it1) return;
-  if (t == 0) q_fetch<QM>(p, ms, stage, it0);
+  if (t == 0) q_fetch<QM>(p, ms, stage, first.b);
   if (t < 15) {
     uint32_t lo, hi;
     e2m1_e4m3_table(t - 14, lo, hi);
@@ -604,7 +612,7 @@ __device__ void run_dequant(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
   const uint32_t box_off = (t >> 3) * 4608u, r8 = t & 7u;
   const uint32_t swz = (r8 >> 1) & 3u;                 // 64-byte swizzle of this row
   TileCursor c;
-  c.init(p.items, it0, it1);
+  c.init(p.items, it0, it1, first);
   while (!c.done()) {
     const uint32_t tt = c.t, s = tt % L::kNumTiles;
     if (!mbar_wait(smem_u32(&ms->full[s]), (tt / L::kNumTiles) & 1u, p.err, kErrDequant)) *abort = 1;
@@ -686,15 +694,15 @@ __device__ __forceinline__ void wait_or_flag(uint32_t bar, uint32_t parity, int3
 // the staging buffer is free.
 template <int QM>
 __device__ void run_qprep(const Stage1Params& p, Misc* ms, uint8_t* qgen, uint8_t* stage, int it0,
-                          int it1, int lane) {
+                          int it1, const WorkItem& first, int lane) {
   using L = Layout<QM>;
   const uint32_t stage_bar = smem_u32(&ms->q_stage);
   if (it0 >= it1) return;
-  if (lane == 0) q_fetch<QM>(p, ms, stage, it0);
+  if (lane == 0) q_fetch<QM>(p, ms, stage, first.b);
   if (it0 + 1 >= it1) return;
   // the softmax warps are done with the first item's staged q
   if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ms->q_stage_free), 0, p.err, kErrQPrep))) return;
-  if (lane == 0) q_fetch<QM>(p, ms, stage, it0 + 1);
+  if (lane == 0) q_fetch<QM>(p, ms, stage, p.items[it0 + 1].b);
   int k = 1;
   for (int it = it0 + 1; it < it1; ++it, ++k) {
     const uint32_t qb = k & 1;
@@ -707,7 +715,7 @@ __device__ void run_qprep(const Stage1Params& p, Misc* ms, uint8_t* qgen, uint8_
     fence_proxy_async_smem();
     __syncwarp();                                     // every lane is done with the stage
     if (lane == 0) {
-      if (it + 1 < it1) q_fetch<QM>(p, ms, stage, it + 1);
+      if (it + 1 < it1) q_fetch<QM>(p, ms, stage, p.items[it + 1].b);
       ms->qscale[qb][0] = c_hi;
       ms->qscale[qb][1] = c_lo;
       mbar_arrive(smem_u32(&ms->q_full[qb]));
@@ -759,7 +767,7 @@ __device__ __forceinline__ void reduce_heads(const float (&v)[kH], float (&out)[
 template <int QM>
 __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, uint8_t* pgen,
                             uint8_t* qgen, uint8_t* stage, uint32_t tmem, int it0, int it1,
-                            int tid) {
+                            const WorkItem& first, int tid) {
   using L = Layout<QM>;
   constexpr int kHG = L::kHeadGroups, kH = 16 / kHG;
   volatile int32_t* abort = &ms->abort_sm;
@@ -792,7 +800,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
   int k = 0;
   float m[kH], l[kH];
   for (int it = it0; it < it1; ++it, ++k) {
-    const WorkItem w = p.items[it];
+    const WorkItem w = it == it0 ? first : p.items[it];
     const uint32_t qb = k & 1;
     wait_or_flag(smem_u32(&ms->q_full[qb]), (k >> 1) & 1, p.err, kErrSoftmax, abort);
     const float c_hi = ms->qscale[qb][0], c_lo = ms->qscale[qb][1];
@@ -974,30 +982,30 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
 #pragma unroll
     for (int h = 0; h < kH; ++h) inv[h] = vscale / lt[h];
     const int slot = w.slot;
+    // O^T of this thread's dim in all four blocks: every TMEM load is issued
+    // before one wait
+    float oh[4][kH], ol[4][kH];
+#pragma unroll
     for (int c = 0; c < 4; ++c) {
-      float oh[kH];
-      tmem_ld(tl + kColO + L::kOCols * c + h0, oh);
-      if constexpr (L::kKv8) {
-        float ol[kH];
-        tmem_ld(tl + kColO + L::kOCols * c + 16 + h0, ol);
-        tmem_wait_ld();
+      tmem_ld(tl + kColO + L::kOCols * c + h0, oh[c]);
+      if constexpr (L::kKv8) tmem_ld(tl + kColO + L::kOCols * c + 16 + h0, ol[c]);
+    }
+    tmem_wait_ld();
 #pragma unroll
-        for (int h = 0; h < kH; ++h) oh[h] = (oh[h] + ol[h] * (1.0f / kPLoScale)) * inv[h];
-      } else {
-        tmem_wait_ld();
+    for (int c = 0; c < 4; ++c) {
 #pragma unroll
-        for (int h = 0; h < kH; ++h) oh[h] *= inv[h];
-      }
+      for (int h = 0; h < kH; ++h)
+        oh[c][h] = L::kKv8 ? (oh[c][h] + ol[c][h] * (1.0f / kPLoScale)) * inv[h] : oh[c][h] * inv[h];
       const int d = c * 128 + tq;
       if (slot >= 0) {
         float* po = p.part_o + (static_cast<int64_t>(slot) * kHeads + h0) * kVDim + d;
 #pragma unroll
-        for (int h = 0; h < kH; ++h) po[h * kVDim] = oh[h];
+        for (int h = 0; h < kH; ++h) po[h * kVDim] = oh[c][h];
       } else {
         uint16_t* po = p.out + (static_cast<int64_t>(w.b) * kHeads + h0) * kVDim + d;
 #pragma unroll
         for (int h = 0; h < kH; ++h) {
-          const __nv_bfloat16 v = __float2bfloat16_rn(oh[h]);
+          const __nv_bfloat16 v = __float2bfloat16_rn(oh[c][h]);
           po[h * kVDim] = *reinterpret_cast<const uint16_t*>(&v);
         }
       }
@@ -1028,7 +1036,9 @@ __global__ void __launch_bounds__(Layout<QM>::kThreads, 1) mla_stage1_kernel(con
   const uint32_t ring = smem_u32(smem);
   Misc* ms = reinterpret_cast<Misc*>(smem + L::kMiscOff);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int it0 = p.cta_indptr[blockIdx.x], it1 = p.cta_indptr[blockIdx.x + 1];
+  const CtaHead& head = p.heads[blockIdx.x];
+  const int it0 = head.it0, it1 = head.it1;
+  const WorkItem first = head.first;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::kNumTiles; ++i) {
@@ -1066,19 +1076,19 @@ __global__ void __launch_bounds__(Layout<QM>::kThreads, 1) mla_stage1_kernel(con
   const uint32_t tmem = ms->tmem_base;
 
   if (warp == 0) {
-    run_producer<QM>(p, ms, ring, it0, it1, lane);
+    run_producer<QM>(p, ms, ring, it0, it1, first, lane);
   } else if (warp == 1 || warp == 3) {
-    run_qk<QM>(p, ms, ring, ring + L::kQOff, tmem, it0, it1, warp == 3 ? 1 : 0, lane);
+    run_qk<QM>(p, ms, ring, ring + L::kQOff, tmem, it0, it1, first, warp == 3 ? 1 : 0, lane);
   } else if (warp == 2 || (!L::kMx && warp == 13)) {
-    run_pv<QM>(p, ms, ring, ring + L::kPOff, tmem, it0, it1, warp == 13 ? 1 : 0, lane);
+    run_pv<QM>(p, ms, ring, ring + L::kPOff, tmem, it0, it1, first, warp == 13 ? 1 : 0, lane);
   } else if (warp < 4 + 4 * L::kHeadGroups) {
     run_softmax<QM>(p, ms, smem, smem + L::kPOff, smem + L::kQOff, smem + L::kQStageOff, tmem, it0,
-                    it1, threadIdx.x - 128);
+                    it1, first, threadIdx.x - 128);
   } else if constexpr (L::kMx) {
-    run_dequant<QM>(p, ms, smem, smem + L::kQOff, smem + L::kQStageOff, it0, it1,
+    run_dequant<QM>(p, ms, smem, smem + L::kQOff, smem + L::kQStageOff, it0, it1, first,
                     threadIdx.x - 384);
   } else {
-    run_qprep<QM>(p, ms, smem + L::kQOff, smem + L::kQStageOff, it0, it1, lane);
+    run_qprep<QM>(p, ms, smem + L::kQOff, smem + L::kQStageOff, it0, it1, first, lane);
   }
 
   tc_fence_before();
