@@ -641,8 +641,7 @@ __device__ void run_dequant(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
     uint4 na = reinterpret_cast<const uint4*>(raw)[0];
     uint4 nb = reinterpret_cast<const uint4*>(raw)[1];
     uint32_t neb = reinterpret_cast<const uint16_t*>(sc)[0];
-#pragma unroll 1
-    for (int ch = 0; ch < 9; ++ch) {
+    auto chunk = [&](int ch, bool sync) {
       const uint4 a = na, b = nb;
       const uint32_t eb = neb;                          // e8m0 of blocks 2ch, 2ch+1
       if (ch < 8) {
@@ -650,7 +649,7 @@ __device__ void run_dequant(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
         nb = reinterpret_cast<const uint4*>(raw + (ch + 1) * 256)[1];
         neb = reinterpret_cast<const uint16_t*>(sc)[ch + 1];
       }
-      __syncwarp();                                     // the box read packed chunk ch
+      if (sync) __syncwarp();                           // the box read the packed chunks
       const uint2 t0 = ms->e2m1_tab[max(static_cast<int>(eb & 0xFFu) - r, -14) + 14];
       const uint2 t1 = ms->e2m1_tab[max(static_cast<int>(eb >> 8) - r, -14) + 14];
       const uint32_t lo0 = t0.x, hi0 = t0.y, lo1 = t1.x, hi1 = t1.y;
@@ -663,6 +662,16 @@ __device__ void run_dequant(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
       *reinterpret_cast<uint4*>(dst + ((1u ^ swz) << 4)) = make_uint4(o2.x, o2.y, o3.x, o3.y);
       *reinterpret_cast<uint4*>(dst + ((2u ^ swz) << 4)) = make_uint4(o4.x, o4.y, o5.x, o5.y);
       *reinterpret_cast<uint4*>(dst + ((3u ^ swz) << 4)) = make_uint4(o6.x, o6.y, o7.x, o7.y);
+    };
+    // e4m3 chunks 0-3 lie below every packed chunk: no barrier.  From chunk
+    // 4 on, e4m3 chunk ch overwrites packed chunks 2ch-9 and 2ch-8, which
+    // the box's threads read (one chunk ahead) in earlier iterations: a warp
+    // barrier before each write orders those reads first.
+#pragma unroll 1
+    for (int ch = 0; ch < 4; ++ch) chunk(ch, false);
+#pragma unroll 1
+    for (int ch = 4; ch < 9; ++ch) {
+      chunk(ch, true);
       if (ch == 4) {
         // dims 0-319 done: the first QK^T K-half (dims 0-287) may start
         fence_proxy_async_smem();
