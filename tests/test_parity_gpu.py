@@ -188,6 +188,18 @@ def test_mxfp4_spread_block_exponents():
     check(w)
 
 
+def test_mxfp4_very_spread_block_exponents():
+    # exponents spread over 30 binades inside a token: blocks more than 8
+    # binades below the row's largest are rounded to e4m3 subnormals or to 0
+    # (they are then below 2^-8 of that block, far inside the tolerance)
+    from mla_decode_stage1_gb300 import synth
+    w = synth.make_workload(bs=3, lengths=[300, 129, 1000], page_size=8, permute_pages=True,
+                            q_dtype="bf16", kv_dtype="mxfp4", seed=45)
+    g = torch.Generator().manual_seed(6)
+    w.kv_e8m0[:, :18] = (100 + torch.randint(0, 31, (w.kv_e8m0.shape[0], 18), generator=g)).to(torch.uint8)
+    check(w)
+
+
 def test_mxfp4_unsupported_scale_stride():
     mla = _mla()
     from mla_decode_stage1_gb300 import synth
