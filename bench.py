@@ -56,6 +56,36 @@ def dist_env():
     return world, rank, local
 
 
+def rank_seed(base_seed, rank):
+    """Seed of a rank's own batch: every rank decodes a different batch of
+    the same shape (batch-sharded replicas)."""
+    return base_seed + 1000 * rank
+
+
+def reduce_over_ranks(dist, max_values, sum_values, device="cpu"):
+    """Max over ranks of the times (the slowest rank sets the job's time) and
+    sum over ranks of the work counts.  Without a process group (dist is None)
+    the values are returned as they are."""
+    max_values = [float(v) for v in max_values]
+    sum_values = [float(v) for v in sum_values]
+    if dist is None:
+        return max_values, sum_values
+    import torch
+    out = []
+    for vals, op in ((max_values, dist.ReduceOp.MAX), (sum_values, dist.ReduceOp.SUM)):
+        if vals:
+            t = torch.tensor(vals, dtype=torch.float64, device=device)
+            dist.all_reduce(t, op=op)
+            vals = t.tolist()
+        out.append(vals)
+    return out[0], out[1]
+
+
+def aggregate_gbs(total_bytes, ms):
+    """Whole-job throughput: the bytes of all ranks over the slowest rank's time."""
+    return total_bytes / (ms * 1e-3) / 1e9
+
+
 def config_meta(name, w):
     from mla_decode_stage1_gb300 import synth
     c = synth.CONFIGS[name]
@@ -228,7 +258,7 @@ def main():
         lengths = (lengths * ((args.bs + len(lengths) - 1) // len(lengths)))[: args.bs]
     w = synth.make_workload(bs=len(lengths), lengths=lengths,
                             page_size=c["page_size"], q_dtype=c["q_dtype"], kv_dtype=c["kv_dtype"],
-                            permute_pages=c["permute_pages"], seed=c["seed"] + 1000 * rank,
+                            permute_pages=c["permute_pages"], seed=rank_seed(c["seed"], rank),
                             device=dev, name=args.config)
     d = w.to(dev)
     torch.cuda.empty_cache()
@@ -292,10 +322,9 @@ def main():
     mla.mla_decode_check(plan, ws)
     step_ms = sum(a.elapsed_time(b) for a, b in ev) / K
     s1_ms = sum(a.elapsed_time(b) for a, b in ev_s1) / K
-    if dist is not None:
-        t = torch.tensor([step_ms, s1_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms, s1_ms = float(t[0]), float(t[1])
+    # the job's time is the slowest rank's; its work is every rank's batch
+    (step_ms, s1_ms), (total_bytes,) = reduce_over_ranks(dist, [step_ms, s1_ms], [alg_bytes],
+                                                         device=dev)
     clocks = clk.summary()
 
     # end to end through the public API: pinned host inputs -> device, decode,
@@ -334,11 +363,8 @@ def main():
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = e0.elapsed_time(e1) / E
-        if dist is not None:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t[0])
-        e2e = {"value": world * alg_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+        (e2e_ms,), _ = reduce_over_ranks(dist, [e2e_ms], [], device=dev)
+        e2e = {"value": aggregate_gbs(total_bytes, e2e_ms), "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                "steps": E}
         del dev_in, host
@@ -351,7 +377,7 @@ def main():
     peak, peak_kind = load_peaks()
     achieved = alg_bytes / (s1_ms * 1e-3) / 1e9
     traffic = stage1_traffic(args.config)
-    gbs = world * alg_bytes / (step_ms * 1e-3) / 1e9
+    gbs = aggregate_gbs(total_bytes, step_ms)
     line = {
         "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": max(3, args.warmup), "ms_per_step": step_ms, "us_per_call": step_ms * 1e3,
