@@ -81,9 +81,11 @@ typedef struct {
  *   kv_last_page_len_host [batch_size] int32 tokens used in each request's
  *                         last page (1..page_size), or NULL for full pages.
  *   batch_size            >= 1.
- *   page_size             tokens per page: 1, or a power of two >= 8.
- *                         page_size 1 requires the identity page table
- *                         (kv_indices == NULL at run time).
+ *   page_size             tokens per page, >= 1.  With a page table, a
+ *                         multiple of 8 lets one TMA box copy 8 rows of a
+ *                         page; other sizes (bf16 / fp8 KV) copy every row
+ *                         on its own.  MXFP4 KV with a page table needs a
+ *                         multiple of 8 (MLA_ERR_UNSUPPORTED at run time).
  *   q_dtype               MLA_DTYPE_BF16 or MLA_DTYPE_FP8_E4M3.
  *   kv_dtype              MLA_DTYPE_BF16, MLA_DTYPE_FP8_E4M3 or MLA_DTYPE_MXFP4.
  *   num_splits            0: the planner balances 128-token tiles over the

@@ -24,7 +24,6 @@ namespace {
 
 constexpr size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
 
 int qmode_of(int q_dtype, int kv_dtype) {
   if (q_dtype == MLA_DTYPE_BF16 && kv_dtype == MLA_DTYPE_BF16) return mla::kQBf16KvBf16;
@@ -321,13 +320,20 @@ mla_status mla_decode_run(mla_plan* plan, const void* q, const float* q_scale, c
     if (kv_e8m0_row_stride < 32 || kv_e8m0_row_stride % 16 != 0) return MLA_ERR_UNSUPPORTED;
   }
   if (workspace_bytes < plan->ws_bytes) return MLA_ERR_WORKSPACE;
-  // Identity table: one TMA box of 128 rows per tile.  Page table: one box
-  // per 8-row group (a group never straddles a page).
+  // Identity table: one TMA box of 128 rows per tile.  Page table with a
+  // page size that is a multiple of 8: one box per 8-row group (a group never
+  // straddles a page).  Other page sizes (bf16 / fp8 KV): every row is
+  // gathered on its own (cp.async), laid out as for the identity table.
   int box_rows = mla::kTile;
+  int gather = 0;
   if (kv_indices != nullptr) {
-    if (!is_pow2(plan->page_size) || plan->page_size < 8) return MLA_ERR_UNSUPPORTED;
-    box_rows = 8;
     if (kv_pool_rows % plan->page_size != 0) return MLA_ERR_INVALID_ARG;
+    if (plan->page_size % 8 == 0)
+      box_rows = 8;
+    else if (plan->kv_dtype == MLA_DTYPE_MXFP4)
+      return MLA_ERR_UNSUPPORTED;
+    else
+      gather = 1;
   }
   // MXFP4 rows are dequantised in place box by box: always 8-row boxes
   if (plan->kv_dtype == MLA_DTYPE_MXFP4) box_rows = 8;
@@ -374,6 +380,8 @@ mla_status mla_decode_run(mla_plan* plan, const void* q, const float* q_scale, c
     p.err = err;
     p.page_size = plan->page_size;
     p.box_rows = box_rows;
+    p.gather = gather;
+    p.kv = static_cast<const uint8_t*>(kv);
     p.chunk_stride = static_cast<uint32_t>(box_rows) * 64u;    // [group][chunk][rows][64 B]
     p.group_stride = box_rows == 8 ? row_bytes * 8u : 512u;
     p.pool_rows = kv_pool_rows;

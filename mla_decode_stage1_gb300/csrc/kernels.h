@@ -81,6 +81,9 @@ struct Stage1Params {
   int32_t* err;                 // device error word
   int32_t page_size;
   int32_t box_rows;             // rows per TMA box: 128 (identity table) or 8 (page table)
+  int32_t gather;               // 1: page size not a multiple of 8 (bf16 / fp8 KV); rows are
+                                // gathered one by one with cp.async instead of TMA boxes
+  const uint8_t* kv;            // KV pool base (gather mode)
   uint32_t chunk_stride;        // smem bytes between 64-byte column chunks of a tile
   uint32_t group_stride;        // smem bytes between 8-row groups of a tile
   int64_t pool_rows;

@@ -86,6 +86,18 @@ __device__ __forceinline__ int32_t ld_nc_early(const int32_t* ptr) {
   return v;
 }
 
+// ------------------------------------------------------------ cp.async rows
+// 16-byte asynchronous copy global -> shared (cached in L1, so that the other
+// 16-byte pieces of the same line hit there).
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+// One arrival on `bar` once every cp.async this thread issued so far has
+// completed (the barrier's expected count includes it).
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 // ------------------------------------------------------------------- proxies
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -21,10 +21,11 @@
 //    its N, so QK^T and PV are issued by separate warps that run side by
 //    side: warps 1 and 3 each issue half of the QK^T K-steps into their own
 //    S accumulator; warps 2 and 13 issue PV for O blocks 0-1 and 2-3 (MXFP4:
-//    warp 2 alone).  Warp 0 is the TMA producer, warp 12 prepares q for the
-//    next item (MXFP4: warps 12-15 dequantise tiles and prepare q), and
-//    warps 4-11 do the softmax and the epilogue in two groups of 8 heads
-//    (one thread per token / per output dim, TMEM lane = thread);
+//    warp 2 alone).  Warp 0 is the TMA producer; warps 4-11 do the softmax
+//    and the epilogue in two groups of 8 heads (one thread per token / per
+//    output dim, TMEM lane = thread) and convert the first item's q; warp
+//    12 converts the q of later items (MXFP4: warps 12-15 dequantise the
+//    packed rows in place and prepare every item's q);
 //  * every mbarrier wait is bounded (see mbar_wait) and reports into the
 //    device error word instead of hanging.
 //
@@ -98,15 +99,15 @@ struct Misc {
   float qscale[2][2];
   uint32_t tmem_base;
   int32_t abort_sm;                  // set by a softmax thread whose bounded wait gave up
+  uint64_t q_stage;                  // raw q of the next item landed in the staging buffer
+  uint64_t q_stage_free;             // the softmax warps converted the first item's q
+  float qred[8];                     // per-warp |q| maxima (q prepared by a warp group)
   // MXFP4 only
   uint64_t deq[4];                   // tile slot dequantised (128 dequant threads)
   uint64_t deq_a[4];                 // its dims 0-319 dequantised (first QK^T K-half)
   uint64_t upper_free[4];            // PV no longer reads the slot's upper box halves
   int32_t abort_dq;                  // set by a dequant thread whose bounded wait gave up
-  uint64_t q_stage;                  // raw q of the next item landed in the staging buffer
-  uint64_t q_stage_free;             // the softmax warps converted the first item's q
   float uexp[2][128];                // per-token power of two u_t = r_t - 127 of a slot
-  float qred[8];                     // per-warp |q| maxima (q prepared by a warp group)
   uint2 e2m1_tab[16];                // e4m3 tables for 2^k, k = index - 14 (k <= -14: all 0)
 };
 static_assert(sizeof(Misc) <= 2048, "misc region");
@@ -225,6 +226,58 @@ __device__ void run_producer(const Stage1Params& p, Misc* ms, uint32_t ring, int
   bool ok = true;
   uint32_t t = 0;
   while (!cur.done() && ok) {
+    if (!L::kMx && p.gather) {
+      // Page size not a multiple of 8: lane l copies rows l, l+32, l+64,
+      // l+96 of the tile, each through its own page-table entry, in 16-byte
+      // pieces into the identity-table layout ([chunk][128 rows][64 B], the
+      // 64-byte swizzle), then arrives on the tile's barrier once its copies
+      // have landed (32 arrivals per tile).  (Lanes on consecutive pieces of
+      // one row, with the pool rows staged in shared memory, measured 2x
+      // slower; a row's chunks are 8 KB apart there, so its pieces share
+      // banks.)
+      const uint32_t s = t % L::kNumTiles, ph = (t / L::kNumTiles) & 1u;
+      const uint32_t full = smem_u32(&ms->full[s]);
+      const int t0 = cur.t0(), nvalid = cur.nvalid();
+      int32_t page[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {       // loaded before the waits, used after
+        const int r = lane + 32 * j;
+        page[j] = r < nvalid ? ld_nc_early(p.kv_indices + cur.w.page_base + (t0 + r) / p.page_size)
+                             : 0;
+      }
+      // (the slot's previous tile must have landed before these arrivals)
+      if (t >= static_cast<uint32_t>(L::kNumTiles)) {
+        ok = __all_sync(0xffffffffu, mbar_wait(full, ph ^ 1u, p.err, kErrProducer));
+        if (!ok) break;
+      }
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ms->empty[s]), ph ^ 1u, p.err, kErrProducer));
+      if (!ok) break;
+      const uint32_t tile = ring + s * L::kTileBytes;
+      const uint32_t cs = p.chunk_stride, gs = p.group_stride;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int r = lane + 32 * j;
+        if (r >= nvalid) continue;
+        int pg = page[j];
+        if (pg < 0 || static_cast<int64_t>(pg + 1) * p.page_size > p.pool_rows) {
+          atomicOr(p.err, kErrBadPage);
+          pg = 0;
+        }
+        const int64_t grow = static_cast<int64_t>(pg) * p.page_size + (t0 + r) % p.page_size;
+        const uint8_t* src = p.kv + grow * L::kRowBytes;
+        const uint32_t dst = tile + (r >> 3) * gs + (r & 7) * 64u;
+        const uint32_t swz = ((r & 7) >> 1) & 3u;
+#pragma unroll 3
+        for (int c = 0; c < L::kChunks; ++c)
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            cp_async_16(dst + c * cs + ((q ^ swz) << 4), src + c * 64 + q * 16);
+      }
+      cp_async_arrive(full);
+      cur.advance();
+      ++t;
+      continue;
+    }
     const BoxFetch f = f0;
     f0 = f1;
     f1 = box_fetch(p, ahead, lane);
@@ -314,6 +367,7 @@ __device__ void run_qk(const Stage1Params& p, Misc* ms, uint32_t ring, uint32_t 
     if (!__all_sync(0xffffffffu, mbar_wait(ready, (t / L::kNumTiles) & 1u, p.err, kErrMma)))
       break;
     tc_fence_after();
+    if (p.gather) fence_proxy_async_smem();   // rows copied by cp.async (generic proxy)
     const uint32_t tile = ring + s * L::kTileBytes;
     const uint32_t qaddr = qbase + (qc.k & 1) * L::kQBytes;
     const uint32_t d = tmem + kColS + 64 * sb + 32 * half;
@@ -359,6 +413,7 @@ __device__ void run_pv(const Stage1Params& p, Misc* ms, uint32_t ring, uint32_t 
                                            kErrMma)))
       break;
     tc_fence_after();
+    if (p.gather) fence_proxy_async_smem();   // V rows copied by cp.async (generic proxy)
     const uint32_t tile = ring + s * L::kTileBytes;
     const uint32_t pa = pbase + pb * L::kPBytes;
     const bool first = pc.j == 0;
@@ -1051,7 +1106,7 @@ __global__ void __launch_bounds__(Layout<QM>::kThreads, 1) mla_stage1_kernel(con
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::kNumTiles; ++i) {
-      mbar_init(smem_u32(&ms->full[i]), 1);
+      mbar_init(smem_u32(&ms->full[i]), p.gather ? 32 : 1);   // gather: one per producer lane
       mbar_init(smem_u32(&ms->empty[i]), L::kPvIssuers);
     }
     for (int i = 0; i < 2; ++i) {

@@ -81,8 +81,10 @@ def test_ragged_contiguous(q_dtype, kv_dtype):
 
 
 @pytest.mark.parametrize("q_dtype,kv_dtype", COMBOS)
-@pytest.mark.parametrize("page_size", [8, 16, 256])
+@pytest.mark.parametrize("page_size", [1, 2, 3, 4, 8, 12, 16, 24, 256])
 def test_paged_permuted_partial_pages(q_dtype, kv_dtype, page_size):
+    # page sizes that are multiples of 8 use one TMA box per 8-row group,
+    # the others gather every row through its own page-table entry
     from mla_decode_stage1_gb300 import synth
     lengths = [5, 700, 1, 0, 2049, 383]
     w = synth.make_workload(bs=len(lengths), lengths=lengths, page_size=page_size,
