@@ -199,3 +199,12 @@ def test_workspace_size_covers_partials(mla):
     info = pl.info()
     assert info.num_partials == 32
     assert pl.workspace_bytes >= 32 * 16 * 512 * 4 + 32 * 16 * 4
+
+
+def test_all_empty_batch_has_no_ctas_and_only_fill_jobs(mla):
+    # no tile to stream: stage 1 is not launched; stage 2 writes out = 0 and
+    # lse = -inf for every request
+    pl = plan(mla, np.array([0, 0, 0, 0]), ps=1)
+    info = pl.info()
+    assert info.num_ctas == 0 and info.num_items == 0 and info.num_partials == 0
+    assert info.num_merge_jobs == 3

@@ -222,3 +222,44 @@ def test_mxfp4_benchmark_config_sampled():
     rng = np.random.default_rng(8)
     sel = sorted(rng.choice(w.bs, size=6, replace=False).tolist() + [0, w.bs - 1])
     check(w, select=sel)
+
+
+def test_split_merge_repeated_launches_same_workspace():
+    # the plan's table is uploaded on the first launch into a workspace only;
+    # later launches reuse it and must give identical results
+    mla = _mla()
+    from mla_decode_stage1_gb300 import synth
+    lengths = [900, 0, 4096, 130, 2500]
+    w = synth.make_workload(bs=len(lengths), lengths=lengths, page_size=8, q_dtype="bf16",
+                            kv_dtype="fp8", permute_pages=True, seed=46)
+    plan = mla.mla_decode_plan(w.kv_indptr, w.kv_last_page_len, page_size=8, q_dtype="bf16",
+                               kv_dtype="fp8", num_splits=3)
+    assert plan.info().num_partials > 0
+    d = w.to("cuda")
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(4):
+        out = torch.full((w.bs, 16, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+        lse = torch.full((w.bs, 16), float("nan"), dtype=torch.float32, device="cuda")
+        mla.mla_decode_run(plan, d.q, d.kv, out, workspace=ws, q_scale=d.q_scale,
+                           kv_scale=d.kv_scale, kv_indices=d.kv_indices, lse=lse)
+        outs.append((out.clone(), lse.clone()))
+    mla.mla_decode_check(plan, ws)
+    for o, l in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
+    o_ref, l_ref = oracle.mla_decode(**synth.oracle_args(w))
+    o = outs[-1][0].float().cpu().numpy().astype(np.float64)
+    lse = outs[-1][1].cpu().numpy().astype(np.float64)
+    compare(o, lse, o_ref, l_ref, "fp8", w.lengths)
+
+
+@pytest.mark.parametrize("kv_dtype", ["fp8", "mxfp4"])
+def test_one_long_request_over_every_sm(kv_dtype):
+    # one request cut into as many items as there are CTAs: stage 2 merges
+    # well over a hundred partials per head
+    from mla_decode_stage1_gb300 import synth
+    n = 40000
+    w = synth.make_workload(bs=2, lengths=[n, 0], page_size=1, q_dtype="bf16",
+                            kv_dtype=kv_dtype, seed=47)
+    plan = check(w)
+    assert plan.info().num_partials >= 100
