@@ -10,6 +10,8 @@
 //
 // One warp per (request, head); a lane owns 16 of the 512 dims as four
 // float4 columns, so every partial row is read as coalesced 512-byte lines.
+// Up to four partials are loaded together with their lse values, so that a
+// request split in at most four takes one round trip to memory.
 
 #include <cuda_bf16.h>
 
@@ -33,37 +35,57 @@ __global__ void __launch_bounds__(256) mla_stage2_kernel(const Stage2Params p) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
   float M = -INFINITY, wsum = 0.0f;
-  for (int s = lane; s < J.count; s += 32)
-    M = fmaxf(M, p.part_lse[static_cast<int64_t>(J.first + s) * kHeads + h]);
+  // Adds partials [s0, s0 + n) (n <= 4) with weights 2^(lse - M); a partial
+  // whose weight is 0 adds exactly nothing (a select, not a branch, so that
+  // no load waits on the weight).
+  auto add = [&](int s0, int n, const float (&ls)[4], const float4 (&v)[4][4]) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  if (M != -INFINITY) {
-    // Partials go two at a time so that the loads of both rows are in flight
-    // together; a partial whose weight is 0 adds exactly nothing (a select,
-    // not a branch, so that no load waits on the weight).
-    for (int s = 0; s < J.count; s += 2) {
-      const int n = min(2, J.count - s);
-      float w[2];
-      float4 v[2][4];
+    for (int u = 0; u < 4; ++u) {
+      const float w = (u < n) ? ex2(ls[u] - M) : 0.0f;
+      wsum += w;
+      const bool live = w > 0.0f;
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int64_t row = static_cast<int64_t>(J.first + s + (u < n ? u : 0)) * kHeads + h;
-        w[u] = u < n ? ex2(p.part_lse[row] - M) : 0.0f;
-        const float4* src = reinterpret_cast<const float4*>(p.part_o + row * kVDim);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) v[u][i] = src[lane + 32 * i];
+      for (int i = 0; i < 4; ++i) {
+        acc[4 * i + 0] += live ? w * v[u][i].x : 0.0f;
+        acc[4 * i + 1] += live ? w * v[u][i].y : 0.0f;
+        acc[4 * i + 2] += live ? w * v[u][i].z : 0.0f;
+        acc[4 * i + 3] += live ? w * v[u][i].w : 0.0f;
       }
+    }
+  };
+  // Loads of up to four partials (lse and this lane's 16 dims) in flight together.
+  auto load = [&](int s0, int n, float (&ls)[4], float4 (&v)[4][4]) {
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        wsum += w[u];
-        const bool live = w[u] > 0.0f;
+    for (int u = 0; u < 4; ++u) {
+      const int64_t row = static_cast<int64_t>(J.first + s0 + (u < n ? u : 0)) * kHeads + h;
+      ls[u] = p.part_lse[row];
+      const float4* src = reinterpret_cast<const float4*>(p.part_o + row * kVDim);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          acc[4 * i + 0] += live ? w[u] * v[u][i].x : 0.0f;
-          acc[4 * i + 1] += live ? w[u] * v[u][i].y : 0.0f;
-          acc[4 * i + 2] += live ? w[u] * v[u][i].z : 0.0f;
-          acc[4 * i + 3] += live ? w[u] * v[u][i].w : 0.0f;
-        }
+      for (int i = 0; i < 4; ++i) v[u][i] = src[lane + 32 * i];
+    }
+  };
+  if (J.count == 0) {
+    // empty request: no partial to read (out = 0, lse = -inf below)
+  } else if (J.count <= 4) {
+    // the common case: one round trip for every lse and every row
+    float ls[4];
+    float4 v[4][4];
+    load(0, J.count, ls, v);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) M = u < J.count ? fmaxf(M, ls[u]) : M;
+    if (M != -INFINITY) add(0, J.count, ls, v);
+  } else {
+    for (int s = lane; s < J.count; s += 32)
+      M = fmaxf(M, p.part_lse[static_cast<int64_t>(J.first + s) * kHeads + h]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    if (M != -INFINITY) {
+      for (int s = 0; s < J.count; s += 4) {
+        float ls[4];
+        float4 v[4][4];
+        const int n = min(4, J.count - s);
+        load(s, n, ls, v);
+        add(s, n, ls, v);
       }
     }
   }
