@@ -41,7 +41,7 @@ class Workload:
     page_size: int
     q_dtype: str            # 'bf16' | 'fp8'
     kv_dtype: str           # 'bf16' | 'fp8' | 'mxfp4'
-    q: torch.Tensor         # [bs,16,576] bf16, or uint8 (e4m3 bytes)
+    q: torch.Tensor         # [bs*q_len,16,576] bf16, or uint8 (e4m3 bytes)
     kv: torch.Tensor        # [rows,576] bf16 | uint8 e4m3 bytes | uint8 [rows,288] packed
     kv_indptr: torch.Tensor  # int32 [bs+1], in pages
     lengths: list            # tokens per request
@@ -51,6 +51,7 @@ class Workload:
     kv_indices: torch.Tensor | None = None  # int32 page ids (None = identity)
     kv_last_page_len: torch.Tensor | None = None  # int32 [bs]
     meta: dict = field(default_factory=dict)
+    q_len: int = 1          # query tokens per request (q row b*q_len + t)
 
     @property
     def pool_rows(self) -> int:
@@ -65,8 +66,8 @@ class Workload:
     def algorithmic_bytes(self) -> int:
         """KV + Q + O bytes of one decode call (the page table, lse and
         split partials are not counted)."""
-        qb = self.bs * HEADS * QK_DIM * (2 if self.q_dtype == "bf16" else 1)
-        ob = self.bs * HEADS * V_DIM * 2
+        qb = self.bs * self.q_len * HEADS * QK_DIM * (2 if self.q_dtype == "bf16" else 1)
+        ob = self.bs * self.q_len * HEADS * V_DIM * 2
         return self.total_tokens() * self.kv_bytes_per_token() + qb + ob
 
     def to(self, device) -> "Workload":
@@ -75,7 +76,8 @@ class Workload:
         return Workload(self.name, self.bs, self.page_size, self.q_dtype, self.kv_dtype,
                         mv(self.q), mv(self.kv), mv(self.kv_indptr), list(self.lengths),
                         mv(self.q_scale), mv(self.kv_scale), mv(self.kv_e8m0),
-                        mv(self.kv_indices), mv(self.kv_last_page_len), dict(self.meta))
+                        mv(self.kv_indices), mv(self.kv_last_page_len), dict(self.meta),
+                        self.q_len)
 
 
 def quant_fp8_per_tensor(x: torch.Tensor):
@@ -114,8 +116,9 @@ def quant_mxfp4_rows(x: torch.Tensor, scale_stride: int = MX_SCALE_STRIDE):
 def make_workload(*, bs: int, lengths, page_size: int = 1, q_dtype: str = "bf16",
                   kv_dtype: str = "bf16", permute_pages: bool = False, seed: int = 0,
                   device="cpu", scale_stride: int = MX_SCALE_STRIDE, name: str = "custom",
-                  q_std: float = 1.0, extra_pool_pages: int = 0) -> Workload:
+                  q_std: float = 1.0, extra_pool_pages: int = 0, q_len: int = 1) -> Workload:
     """Build a seeded workload.  `lengths` is a list of token counts (0 allowed).
+    q_len query tokens per request give q rows [bs*q_len, 16, 576].
     Pages hold `page_size` tokens; the last page of a request may be partial
     (kv_last_page_len).  permute_pages scatters every request's pages through
     a seeded permutation of the whole pool."""
@@ -131,7 +134,7 @@ def make_workload(*, bs: int, lengths, page_size: int = 1, q_dtype: str = "bf16"
     last = torch.tensor([n - (p - 1) * page_size if p > 0 else page_size
                          for n, p in zip(lengths, npages)], dtype=torch.int32)
 
-    q32 = torch.randn(bs, HEADS, QK_DIM, generator=g, device=device) * q_std
+    q32 = torch.randn(bs * q_len, HEADS, QK_DIM, generator=g, device=device) * q_std
     kv32 = torch.randn(rows, QK_DIM, generator=g, device=device)
     if permute_pages:
         perm = torch.randperm(total_pages, generator=g, device=device).to(torch.int32)
@@ -164,7 +167,7 @@ def make_workload(*, bs: int, lengths, page_size: int = 1, q_dtype: str = "bf16"
                     q=q.contiguous(), kv=kv.contiguous(), kv_indptr=indptr, lengths=lengths,
                     q_scale=w_q_scale, kv_scale=kv_scale, kv_e8m0=e8m0,
                     kv_indices=indices, kv_last_page_len=last if need_last else None,
-                    meta={"seed": seed, "permute_pages": permute_pages})
+                    meta={"seed": seed, "permute_pages": permute_pages}, q_len=q_len)
 
 
 # The five benchmark shapes: batch, KV length, storage formats and paging of
@@ -221,5 +224,5 @@ def oracle_args(w: Workload, select=None, num_splits: int = 0) -> dict:
                 kv_scale=1.0 if w.kv_scale is None else float(host(w.kv_scale)[0]),
                 e8m0=None if e8 is None else e8.numpy(),
                 e8m0_stride=0 if e8 is None else int(e8.shape[1]),
-                num_splits=num_splits,
+                num_splits=num_splits, q_len=w.q_len,
                 select=None if select is None else np.asarray(select, dtype=np.int32))

@@ -52,6 +52,9 @@ def _load():
         lib.oracle_mla_decode.argtypes = [i32, i32, i32, i32, P, dbl, P, dbl, P, i64,
                                           P, P, P, i32, P, i32, i32, P, P]
         lib.oracle_mla_decode.restype = i32
+        lib.oracle_mla_decode_q.argtypes = [i32, i32, i32, i32, i32, P, dbl, P, dbl, P, i64,
+                                            P, P, P, i32, P, i32, i32, P, P]
+        lib.oracle_mla_decode_q.restype = i32
         _lib = lib
     return _lib
 
@@ -107,11 +110,15 @@ def dequant_kv(kv_dtype: int, kv, kv_scale: float = 1.0, e8m0=None, e8m0_stride:
 def mla_decode(*, bs: int, page_size: int, q_dtype: int, kv_dtype: int, q, kv,
                kv_indptr, kv_indices=None, kv_last_page_len=None, q_scale: float = 1.0,
                kv_scale: float = 1.0, e8m0=None, e8m0_stride: int = 0,
-               num_splits: int = 0, select=None, nthreads: int | None = None):
-    """Reference decode.  Returns (o [n,16,512] fp64, lse [n,16] fp64) for the
-    selected requests (all of them when ``select`` is None).
+               num_splits: int = 0, select=None, nthreads: int | None = None, q_len: int = 1):
+    """Reference decode.  Returns (o [n*q_len,16,512] fp64, lse [n*q_len,16]
+    fp64) for the selected requests (all of them when ``select`` is None), row
+    i*q_len + t holding query token t of the i-th selected request.
 
-    q: raw bf16 bit patterns (uint16) or e4m3 bytes (uint8), shape [bs,16,576].
+    q: raw bf16 bit patterns (uint16) or e4m3 bytes (uint8), shape
+    [bs*q_len,16,576] (row b*q_len + t = query token t of request b).  Query
+    token t of a request with n tokens attends to its first n - q_len + 1 + t
+    tokens (causal over the last q_len positions).
     kv: raw rows (bf16 bits / e4m3 bytes / 288 packed MXFP4 bytes per row).
     kv_indptr is in pages; kv_indices None means the identity page table.
     """
@@ -123,12 +130,14 @@ def mla_decode(*, bs: int, page_size: int, q_dtype: int, kv_dtype: int, q, kv,
     ix = _c(kv_indices, np.int32)
     ll = _c(kv_last_page_len, np.int32)
     sel = _c(select, np.int32)
-    n = bs if sel is None else sel.size
+    n = (bs if sel is None else sel.size) * int(q_len)
     o = np.empty((n, HEADS, V_DIM), dtype=np.float64)
     lse = np.empty((n, HEADS), dtype=np.float64)
     if nthreads is None:
         nthreads = os.cpu_count() or 1
-    rc = lib.oracle_mla_decode(bs, page_size, q_dtype, kv_dtype, _ptr(qa), float(q_scale),
+    assert qa.size == bs * int(q_len) * HEADS * QK_DIM, "q must hold bs * q_len rows"
+    rc = lib.oracle_mla_decode_q(bs, int(q_len), page_size, q_dtype, kv_dtype, _ptr(qa),
+                               float(q_scale),
                                _ptr(ka), float(kv_scale), _ptr(ea), int(e8m0_stride),
                                _ptr(ip), _ptr(ix), _ptr(ll), int(num_splits), _ptr(sel),
                                0 if sel is None else sel.size, int(nthreads), _ptr(o), _ptr(lse))

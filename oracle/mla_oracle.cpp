@@ -27,11 +27,22 @@
 //   e8m0 0xFF decodes to NaN; an empty request gives o = 0, lse = -inf;
 //   lse is the natural log-sum-exp of the scaled scores.
 //
+// Several query tokens per request (q_len > 1): the pages run one query
+// token per request (max_seqlen_qo = 1 in the metadata calls of submission
+// 668813, whose causal flag is set) and name four query tokens only in the
+// route selection of submission 695854.  The reading taken: the q_len query
+// tokens are the last q_len positions of the sequence, already in the KV
+// cache, and attend causally, so that query token i of a request with n
+// tokens sees tokens [0, n - q_len + 1 + i); a query token that sees no
+// token gives o = 0, lse = -inf.  q and the outputs are laid out
+// [request][query token][head].
+//
 // Everything is fp64.  Inputs are decoded exactly (every bf16 / e4m3 / e2m1 x
 // e8m0 value is exactly representable in a double).  No blocking, no fusion:
 // scores, max, exponentials, sum and the weighted sum of V rows are computed
 // one after the other as the definition states.
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -98,8 +109,9 @@ struct Problem {
   const int32_t* last_len;  // [bs] tokens used in the last page, or null
 };
 
-double q_value(const Problem& P, int b, int h, int d) {
-  const int64_t i = (static_cast<int64_t>(b) * kHeads + h) * kQkDim + d;
+// Element d of head h of q row `qr` (row = request * q_len + query token).
+double q_value(const Problem& P, int64_t qr, int h, int d) {
+  const int64_t i = (qr * kHeads + h) * kQkDim + d;
   if (P.q_dtype == DT_BF16) return dec_bf16(static_cast<const uint16_t*>(P.q)[i]);
   return dec_e4m3(static_cast<const uint8_t*>(P.q)[i]) * P.q_scale;
 }
@@ -136,17 +148,17 @@ std::vector<int64_t> token_rows(const Problem& P, int b) {
   return rows;
 }
 
-// One (request, head) over a token sub-range [t0, t1): the definition.
+// One (q row, head) over a token sub-range [t0, t1): the definition.
 //   s_j = (1/sqrt(576)) * sum_{d<576} q[h,d] k_j[d]
 //   M = max_j s_j ; w_j = exp(s_j - M) ; l = sum_j w_j
 //   o = sum_j w_j v_j / l  (v_j = first 512 dims of k_j) ; lse = M + ln l
-void attend(const Problem& P, int b, int h, const std::vector<int64_t>& rows,
+void attend(const Problem& P, int64_t qr, int h, const std::vector<int64_t>& rows,
             int64_t t0, int64_t t1, double* o, double* lse) {
   for (int d = 0; d < kVDim; ++d) o[d] = 0.0;
   if (t1 <= t0) { *lse = kNegInf; return; }
   const double sm_scale = 1.0 / std::sqrt(static_cast<double>(kQkDim));
   double q[kQkDim];
-  for (int d = 0; d < kQkDim; ++d) q[d] = q_value(P, b, h, d);
+  for (int d = 0; d < kQkDim; ++d) q[d] = q_value(P, qr, h, d);
   std::vector<double> s(t1 - t0);
   for (int64_t j = t0; j < t1; ++j) {
     double acc = 0.0;
@@ -170,14 +182,13 @@ void attend(const Problem& P, int b, int h, const std::vector<int64_t>& rows,
 // each, then merge with the log-sum-exp weights of its stage-2 kernel
 // (written here in natural log):  L = max_s lse_s,
 //   o = sum_s exp(lse_s - L) o_s / sum_s exp(lse_s - L),  lse = L + ln(sum).
-void attend_split(const Problem& P, int b, int h, const std::vector<int64_t>& rows,
-                  int S, double* o, double* lse) {
-  const int64_t n = static_cast<int64_t>(rows.size());
+void attend_split(const Problem& P, int64_t qr, int h, const std::vector<int64_t>& rows,
+                  int64_t n, int S, double* o, double* lse) {
   const int64_t per = (n + S - 1) / S;
   std::vector<double> os(static_cast<size_t>(S) * kVDim), ls(S);
   for (int s = 0; s < S; ++s) {
     const int64_t a = std::min<int64_t>(per * s, n), e = std::min<int64_t>(per * s + per, n);
-    attend(P, b, h, rows, a, e, &os[static_cast<size_t>(s) * kVDim], &ls[s]);
+    attend(P, qr, h, rows, a, e, &os[static_cast<size_t>(s) * kVDim], &ls[s]);
   }
   double L = kNegInf;
   for (int s = 0; s < S; ++s) L = std::fmax(L, ls[s]);
@@ -224,19 +235,22 @@ int oracle_dequant_kv(int kv_dtype, const void* kv, double kv_scale,
   return 0;
 }
 
-// Full decode.  For each selected request (all of them when `select` is null)
-// writes o[i, 16, 512] and lse[i, 16] in fp64.  num_splits <= 1 computes the
-// definition directly; num_splits > 1 uses the split/merge mode.
+// Full decode with q_len query tokens per request.  For each selected
+// request (all of them when `select` is null) and each of its query tokens
+// writes o[(i * q_len + t), 16, 512] and lse[(i * q_len + t), 16] in fp64.
+// num_splits <= 1 computes the definition directly; num_splits > 1 uses the
+// split/merge mode over each query token's visible tokens.
 // Returns 0, or 1 on bad arguments.
-int oracle_mla_decode(int bs, int page_size, int q_dtype, int kv_dtype,
-                      const void* q, double q_scale,
-                      const void* kv, double kv_scale,
-                      const uint8_t* e8m0, int64_t e8m0_stride,
-                      const int32_t* kv_indptr, const int32_t* kv_indices,
-                      const int32_t* last_page_len,
-                      int num_splits, const int32_t* select, int nselect,
-                      int nthreads, double* o, double* lse) {
-  if (bs < 0 || page_size < 1 || q_dtype < 0 || q_dtype > 1 || kv_dtype < 0 || kv_dtype > 2)
+int oracle_mla_decode_q(int bs, int q_len, int page_size, int q_dtype, int kv_dtype,
+                        const void* q, double q_scale,
+                        const void* kv, double kv_scale,
+                        const uint8_t* e8m0, int64_t e8m0_stride,
+                        const int32_t* kv_indptr, const int32_t* kv_indices,
+                        const int32_t* last_page_len,
+                        int num_splits, const int32_t* select, int nselect,
+                        int nthreads, double* o, double* lse) {
+  if (bs < 0 || q_len < 1 || page_size < 1 || q_dtype < 0 || q_dtype > 1 || kv_dtype < 0 ||
+      kv_dtype > 2)
     return 1;
   if (kv_dtype == DT_MXFP4 && (e8m0 == nullptr || e8m0_stride < kQkDim / kMxBlock)) return 1;
   Problem P{bs, page_size, q_dtype, kv_dtype, q, q_scale, kv, kv_scale,
@@ -245,20 +259,26 @@ int oracle_mla_decode(int bs, int page_size, int q_dtype, int kv_dtype,
   if (select)
     for (int i = 0; i < nselect; ++i)
       if (select[i] < 0 || select[i] >= bs) return 1;
-  const int64_t units = static_cast<int64_t>(nreq) * kHeads;
+  const int64_t units = static_cast<int64_t>(nreq) * q_len * kHeads;
   std::atomic<int64_t> next(0);
   auto worker = [&]() {
     for (;;) {
       const int64_t u = next.fetch_add(1);
       if (u >= units) break;
-      const int i = static_cast<int>(u / kHeads), h = static_cast<int>(u % kHeads);
+      const int64_t row = u / kHeads;                      // output row i * q_len + t
+      const int i = static_cast<int>(row / q_len), t = static_cast<int>(row % q_len);
+      const int h = static_cast<int>(u % kHeads);
       const int b = select ? select[i] : i;
       const std::vector<int64_t> rows = token_rows(P, b);
+      const int64_t n = static_cast<int64_t>(rows.size());
+      // query token t sees the first n - q_len + 1 + t tokens
+      const int64_t vis = std::max<int64_t>(0, std::min<int64_t>(n, n - q_len + 1 + t));
+      const int64_t qr = static_cast<int64_t>(b) * q_len + t;
       double* oo = o + u * kVDim;
       if (num_splits > 1)
-        attend_split(P, b, h, rows, num_splits, oo, lse + u);
+        attend_split(P, qr, h, rows, vis, num_splits, oo, lse + u);
       else
-        attend(P, b, h, rows, 0, static_cast<int64_t>(rows.size()), oo, lse + u);
+        attend(P, qr, h, rows, 0, vis, oo, lse + u);
     }
   };
   if (nthreads < 1) nthreads = 1;
@@ -267,6 +287,20 @@ int oracle_mla_decode(int bs, int page_size, int q_dtype, int kv_dtype,
   worker();
   for (auto& th : pool) th.join();
   return 0;
+}
+
+// One query token per request: o[i, 16, 512], lse[i, 16].
+int oracle_mla_decode(int bs, int page_size, int q_dtype, int kv_dtype,
+                      const void* q, double q_scale,
+                      const void* kv, double kv_scale,
+                      const uint8_t* e8m0, int64_t e8m0_stride,
+                      const int32_t* kv_indptr, const int32_t* kv_indices,
+                      const int32_t* last_page_len,
+                      int num_splits, const int32_t* select, int nselect,
+                      int nthreads, double* o, double* lse) {
+  return oracle_mla_decode_q(bs, 1, page_size, q_dtype, kv_dtype, q, q_scale, kv, kv_scale,
+                             e8m0, e8m0_stride, kv_indptr, kv_indices, last_page_len,
+                             num_splits, select, nselect, nthreads, o, lse);
 }
 
 }  // extern "C"

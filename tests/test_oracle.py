@@ -312,3 +312,81 @@ def test_brute_force_small_mixed():
         W = np.exp(S - M)
         assert np.allclose(o[b], W @ K[:, :DV] / W.sum(1, keepdims=True), rtol=1e-12, atol=1e-12)
         assert np.allclose(lse[b], (M + np.log(W.sum(1, keepdims=True)))[:, 0], rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------- several query tokens
+
+def _qlen_problem(seed=11, page_size=4, q_len=3, lengths=(0, 1, 2, 5, 40)):
+    rng = np.random.default_rng(seed)
+    lengths = list(lengths)
+    bs = len(lengths)
+    npages = [(n + page_size - 1) // page_size for n in lengths]
+    total = sum(npages) + 2
+    q_bits, _ = rand_bf16(rng, (bs * q_len, H, D))
+    kv_bits, _ = rand_bf16(rng, (total * page_size, D))
+    perm = rng.permutation(total).astype(np.int32)[: sum(npages)]
+    indptr = np.zeros(bs + 1, np.int32)
+    indptr[1:] = np.cumsum(npages)
+    last = np.array([n - (p - 1) * page_size if p else page_size for n, p in zip(lengths, npages)],
+                    np.int32)
+    return dict(bs=bs, page_size=page_size, q_len=q_len, lengths=lengths, q=q_bits, kv=kv_bits,
+                indptr=indptr, indices=perm, last=last)
+
+
+def test_qlen_rows_are_single_token_decodes_of_causal_prefixes():
+    # query token t of a request with n tokens is a one-token decode of the
+    # request cut to its first n - q_len + 1 + t tokens (same pages)
+    P = _qlen_problem()
+    o, lse = oracle.mla_decode(bs=P["bs"], page_size=P["page_size"], q_dtype=BF16, kv_dtype=BF16,
+                               q=P["q"], kv=P["kv"], kv_indptr=P["indptr"],
+                               kv_indices=P["indices"], kv_last_page_len=P["last"], nthreads=4,
+                               q_len=P["q_len"])
+    ps, ql = P["page_size"], P["q_len"]
+    assert o.shape == (P["bs"] * ql, H, DV)
+    for b, n in enumerate(P["lengths"]):
+        for t in range(ql):
+            vis = max(0, n - ql + 1 + t)
+            npg = (vis + ps - 1) // ps
+            p0 = int(P["indptr"][b])
+            ip = np.array([p0, p0 + npg], np.int32)
+            last = np.array([vis - (npg - 1) * ps if npg else ps], np.int32)
+            o1, l1 = oracle.mla_decode(bs=1, page_size=ps, q_dtype=BF16, kv_dtype=BF16,
+                                       q=P["q"][b * ql + t], kv=P["kv"], kv_indptr=ip,
+                                       kv_indices=P["indices"][: p0 + npg] if npg else P["indices"],
+                                       kv_last_page_len=last, nthreads=1)
+            r = b * ql + t
+            np.testing.assert_array_equal(o[r], o1[0])
+            np.testing.assert_array_equal(lse[r], l1[0])
+
+
+def test_qlen_token_without_visible_kv_is_empty_and_last_sees_all():
+    P = _qlen_problem(lengths=(1, 2, 7), q_len=4)
+    o, lse = oracle.mla_decode(bs=P["bs"], page_size=P["page_size"], q_dtype=BF16, kv_dtype=BF16,
+                               q=P["q"], kv=P["kv"], kv_indptr=P["indptr"],
+                               kv_indices=P["indices"], kv_last_page_len=P["last"], nthreads=4,
+                               q_len=4)
+    for b, n in enumerate(P["lengths"]):
+        for t in range(4):
+            r = b * 4 + t
+            if n - 4 + 1 + t <= 0:
+                assert np.all(o[r] == 0) and np.all(np.isneginf(lse[r]))
+            else:
+                assert np.all(np.isfinite(lse[r]))
+    # the last query token of each request attends to every token: with its q
+    # row, that is the plain one-token decode of the whole request
+    q_last = P["q"].reshape(P["bs"], 4, H, D)[:, 3]
+    o1, l1 = oracle.mla_decode(bs=P["bs"], page_size=P["page_size"], q_dtype=BF16, kv_dtype=BF16,
+                               q=q_last, kv=P["kv"], kv_indptr=P["indptr"],
+                               kv_indices=P["indices"], kv_last_page_len=P["last"], nthreads=4)
+    np.testing.assert_array_equal(o[3::4], o1)
+    np.testing.assert_array_equal(lse[3::4], l1)
+
+
+def test_qlen_split_merge_invariance():
+    P = _qlen_problem(lengths=(3, 40, 17), q_len=2)
+    kw = dict(bs=P["bs"], page_size=P["page_size"], q_dtype=BF16, kv_dtype=BF16, q=P["q"],
+              kv=P["kv"], kv_indptr=P["indptr"], kv_indices=P["indices"],
+              kv_last_page_len=P["last"], nthreads=4, q_len=2)
+    o, lse = oracle.mla_decode(**kw)
+    o3, l3 = oracle.mla_decode(num_splits=3, **kw)
+    assert np.allclose(o3, o, atol=1e-13, rtol=0) and np.allclose(l3, lse, atol=1e-12, rtol=0)
