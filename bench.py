@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--bs", type=int, default=0,
                     help="override the batch size of the configuration (profiling runs)")
+    ap.add_argument("--q-len", type=int, default=1,
+                    help="query tokens per request (causal over the last q_len positions)")
     return ap.parse_args()
 
 
@@ -94,7 +96,8 @@ def config_meta(name, w):
             "q_dtype": w.q_dtype, "kv_dtype": w.kv_dtype, "page_size": w.page_size,
             "page_table": "permuted" if w.kv_indices is not None else "identity",
             "heads": 16, "qk_dim": 576, "v_dim": 512,
-            "parallelism": "batch-sharded replicas (one batch per GPU)"}
+            "parallelism": "batch-sharded replicas (one batch per GPU)",
+            **({"q_len": w.q_len} if w.q_len > 1 else {})}
 
 
 def load_peaks():
@@ -186,7 +189,7 @@ def cpu_baseline(w, target_s=8.0):
     elapsed = 0.0
     done = 0
     nbytes = 0
-    per_req_qo = 16 * 576 * (2 if w.q_dtype == "bf16" else 1) + 16 * 512 * 2
+    per_req_qo = w.q_len * (16 * 576 * (2 if w.q_dtype == "bf16" else 1) + 16 * 512 * 2)
     start = 0
     while elapsed < target_s and done < w.bs:
         sel = list(range(start, min(start + n, w.bs)))
@@ -259,15 +262,15 @@ def main():
     w = synth.make_workload(bs=len(lengths), lengths=lengths,
                             page_size=c["page_size"], q_dtype=c["q_dtype"], kv_dtype=c["kv_dtype"],
                             permute_pages=c["permute_pages"], seed=rank_seed(c["seed"], rank),
-                            device=dev, name=args.config)
+                            device=dev, name=args.config, q_len=args.q_len)
     d = w.to(dev)
     torch.cuda.empty_cache()
     plan = mla.mla_decode_plan(w.kv_indptr, w.kv_last_page_len, page_size=w.page_size,
-                               q_dtype=w.q_dtype, kv_dtype=w.kv_dtype)
+                               q_dtype=w.q_dtype, kv_dtype=w.kv_dtype, q_len=w.q_len)
     info = plan.info()
     ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=dev)
-    out = torch.empty(w.bs, 16, 512, dtype=torch.bfloat16, device=dev)
-    lse = torch.empty(w.bs, 16, dtype=torch.float32, device=dev)
+    out = torch.empty(w.bs * w.q_len, 16, 512, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(w.bs * w.q_len, 16, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     kw = dict(workspace=ws, q_scale=d.q_scale, kv_scale=d.kv_scale, kv_e8m0=d.kv_e8m0,
               kv_indices=d.kv_indices, lse=lse)
@@ -376,7 +379,8 @@ def main():
 
     peak, peak_kind = load_peaks()
     achieved = alg_bytes / (s1_ms * 1e-3) / 1e9
-    traffic = stage1_traffic(args.config)
+    # the committed DRAM counts are for the configuration as named
+    traffic = stage1_traffic(args.config) if not args.bs and args.q_len == 1 else None
     gbs = aggregate_gbs(total_bytes, step_ms)
     line = {
         "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": K,

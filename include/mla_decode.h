@@ -55,6 +55,8 @@ typedef enum {
 
 typedef struct mla_plan mla_plan;
 
+#define MLA_MAX_Q_LEN 64   /* query tokens per request accepted by mla_decode_plan_q */
+
 typedef struct {
   int32_t batch_size;
   int32_t page_size;
@@ -65,6 +67,7 @@ typedef struct {
   int64_t total_tokens;
   int64_t total_tiles;       /* 128-token tiles over all requests */
   size_t workspace_bytes;
+  int32_t q_len;             /* query tokens per request */
 } mla_plan_info;
 
 /*
@@ -105,6 +108,34 @@ mla_status mla_decode_plan(const int32_t* kv_indptr_host, const int32_t* kv_last
                            mla_dtype kv_dtype, int32_t num_splits, int32_t num_sms,
                            mla_plan** plan_out);
 
+/*
+ * mla_decode_plan_q -- mla_decode_plan for q_len query tokens per request
+ * (speculative or multi-token decode).  mla_decode_plan is this call with
+ * q_len = 1.
+ *
+ * The pages run one query token per request (max_seqlen_qo = 1 in the
+ * metadata calls of submission 668813, with the causal flag set) and name
+ * four query tokens in the route selection of submission 695854.  The
+ * reading implemented: the q_len query tokens are the last q_len positions
+ * of each sequence, already in the KV cache, and attend causally, so that
+ * query token t of a request with n tokens attends to its first
+ * n - q_len + 1 + t tokens (none: out = 0, lse = -inf).
+ *
+ * q, out and lse then hold batch_size * q_len rows, row b * q_len + t for
+ * query token t of request b ([batch, q_len, 16, ...] contiguous).  The
+ * balanced plan gives every query token its own group of CTAs, each group
+ * balanced over all requests, so that the q_len passes over a request's KV
+ * run side by side and all but one are served from L2.
+ *
+ * Arguments as for mla_decode_plan, plus q_len in [1, MLA_MAX_Q_LEN].
+ * Errors: as mla_decode_plan; MLA_ERR_INVALID_ARG for q_len out of range or
+ * batch_size * q_len * 16 above INT32_MAX.
+ */
+mla_status mla_decode_plan_q(const int32_t* kv_indptr_host, const int32_t* kv_last_page_len_host,
+                             int32_t batch_size, int32_t q_len, int32_t page_size,
+                             mla_dtype q_dtype, mla_dtype kv_dtype, int32_t num_splits,
+                             int32_t num_sms, mla_plan** plan_out);
+
 /* Bytes of device workspace mla_decode_run needs for this plan (work table,
  * split partials, error word).  Errors: MLA_ERR_INVALID_ARG on NULL. */
 mla_status mla_plan_workspace_size(const mla_plan* plan, size_t* bytes);
@@ -127,7 +158,8 @@ void mla_plan_destroy(mla_plan* plan);
  * enqueued on `stream`.  The role of aiter's mla_decode_fwd on the pages.
  *
  *   q          [batch,16,576] contiguous, bf16 or e4m3 bytes (plan's q_dtype);
- *              16-byte aligned.
+ *              16-byte aligned.  A plan made with q_len > 1 takes
+ *              [batch,q_len,16,576] (and out / lse likewise).
  *   q_scale    device fp32 [1]; required when q is e4m3, ignored otherwise.
  *   kv         KV pool, kv_pool_rows rows of 576 bf16 / 576 e4m3 bytes /
  *              288 packed MXFP4 bytes, contiguous; row r of page p is

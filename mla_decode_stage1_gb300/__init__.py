@@ -19,7 +19,7 @@ HEADS, QK_DIM, V_DIM, TILE = 16, 576, 512, 128
 DTYPES = {"bf16": 0, "fp8": 1, "mxfp4": 2}
 STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED", 3: "MLA_ERR_WORKSPACE",
           4: "MLA_ERR_CUDA", 5: "MLA_ERR_DEVICE_TIMEOUT"}
-EXPORTS = ("mla_decode_plan", "mla_plan_workspace_size", "mla_plan_get_info", "mla_plan_get_work",
+EXPORTS = ("mla_decode_plan", "mla_decode_plan_q", "mla_plan_workspace_size", "mla_plan_get_info", "mla_plan_get_work",
            "mla_plan_destroy", "mla_decode_run", "mla_decode_check", "mla_status_string",
            "mla_plan_set_stage1_events", "mla_decode_run_noalloc")
 
@@ -35,7 +35,7 @@ class PlanInfo(ctypes.Structure):
                 ("num_ctas", ctypes.c_int32), ("num_items", ctypes.c_int32),
                 ("num_partials", ctypes.c_int32), ("num_merge_jobs", ctypes.c_int32),
                 ("total_tokens", ctypes.c_int64), ("total_tiles", ctypes.c_int64),
-                ("workspace_bytes", ctypes.c_size_t)]
+                ("workspace_bytes", ctypes.c_size_t), ("q_len", ctypes.c_int32)]
 
 
 def _load():
@@ -46,6 +46,8 @@ def _load():
     P, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
     lib.mla_decode_plan.argtypes = [P, P, i32, i32, ctypes.c_int, ctypes.c_int, i32, i32,
                                     ctypes.POINTER(P)]
+    lib.mla_decode_plan_q.argtypes = [P, P, i32, i32, i32, ctypes.c_int, ctypes.c_int, i32, i32,
+                                      ctypes.POINTER(P)]
     lib.mla_plan_workspace_size.argtypes = [P, ctypes.POINTER(sz)]
     lib.mla_plan_get_info.argtypes = [P, ctypes.POINTER(PlanInfo)]
     lib.mla_plan_get_work.argtypes = [P, P, P]
@@ -92,6 +94,7 @@ class Plan:
     def __init__(self, handle, q_dtype, kv_dtype, page_size):
         self._h = handle
         self.q_dtype, self.kv_dtype, self.page_size = q_dtype, kv_dtype, page_size
+        self.q_len = 1
 
     @property
     def handle(self):
@@ -132,17 +135,27 @@ class Plan:
 
 def mla_decode_plan(kv_indptr, kv_last_page_len=None, *, page_size: int, q_dtype: str,
                     kv_dtype: str, num_splits: int = 0, num_sms: int = 0,
-                    batch_size: int | None = None) -> Plan:
+                    batch_size: int | None = None, q_len: int = 1) -> Plan:
     """Plan a batch from the HOST kv_indptr (in pages) and optional last-page
-    lengths.  num_sms=0 queries the current CUDA device."""
+    lengths.  num_sms=0 queries the current CUDA device.  q_len > 1 plans
+    q_len query tokens per request (mla_decode_plan_q): q, out and lse then
+    hold [bs, q_len, 16, ...] rows."""
     ind, ind_p = _i32_array(kv_indptr)
     last, last_p = _i32_array(kv_last_page_len)
     bs = len(ind) - 1 if batch_size is None else int(batch_size)
     h = ctypes.c_void_p()
-    _check("mla_decode_plan", _lib.mla_decode_plan(ind_p, last_p, bs, int(page_size),
-                                                   DTYPES[q_dtype], DTYPES[kv_dtype],
-                                                   int(num_splits), int(num_sms), ctypes.byref(h)))
+    if int(q_len) == 1:
+        _check("mla_decode_plan", _lib.mla_decode_plan(ind_p, last_p, bs, int(page_size),
+                                                       DTYPES[q_dtype], DTYPES[kv_dtype],
+                                                       int(num_splits), int(num_sms),
+                                                       ctypes.byref(h)))
+    else:
+        _check("mla_decode_plan_q", _lib.mla_decode_plan_q(ind_p, last_p, bs, int(q_len),
+                                                           int(page_size), DTYPES[q_dtype],
+                                                           DTYPES[kv_dtype], int(num_splits),
+                                                           int(num_sms), ctypes.byref(h)))
     plan = Plan(h, q_dtype, kv_dtype, int(page_size))
+    plan.q_len = int(q_len)
     plan._keep = (ind, last)
     return plan
 
@@ -165,7 +178,8 @@ def mla_decode_run(plan: Plan, q, kv, out, *, workspace, q_scale=None, kv_scale=
     q [bs,16,576] bf16 or uint8 (e4m3 bytes); kv [rows,576] bf16 / uint8 e4m3
     bytes, or [rows,288] uint8 packed MXFP4; out [bs,16,512] bf16; lse
     [bs,16] fp32 or None; workspace a uint8 CUDA tensor of at least
-    plan.workspace_bytes; scales are fp32 CUDA tensors of one element.
+    plan.workspace_bytes; scales are fp32 CUDA tensors of one element.  With
+    a plan for q_len query tokens, q, out and lse hold bs * q_len rows.
     """
     for name, t in (("q", q), ("kv", kv), ("out", out), ("workspace", workspace)):
         if t is None or not t.is_cuda or not t.is_contiguous():

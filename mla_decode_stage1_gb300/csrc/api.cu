@@ -34,20 +34,23 @@ int qmode_of(int q_dtype, int kv_dtype) {
   return -1;
 }
 
-// Items of the balanced plan: the T tiles of all requests, in request order,
-// cut into G nearly equal contiguous ranges (one per CTA).
-void plan_balanced(mla_plan* P, const std::vector<int64_t>& tiles, const std::vector<int32_t>& len,
-                   const std::vector<int32_t>& page_base, const std::vector<int32_t>& npages,
-                   int32_t G) {
-  const int64_t T = P->total_tiles;
-  P->num_ctas = G;
-  P->cta_indptr.assign(1, 0);
-  int32_t b = 0;
-  int64_t in_req = 0;  // tiles of request b already assigned
+// Items of the balanced plan over the requests listed in `order`: their
+// tiles, in that order, cut into G nearly equal contiguous ranges, one per
+// CTA; the CTAs are appended to the plan.
+void plan_balanced(mla_plan* P, const std::vector<int32_t>& order, const std::vector<int64_t>& tiles,
+                   const std::vector<int32_t>& len, const std::vector<int32_t>& page_base,
+                   const std::vector<int32_t>& npages, int32_t G) {
+  int64_t T = 0;
+  for (const int32_t r : order) T += tiles[r];
+  if (G > T) G = static_cast<int32_t>(T);
+  P->num_ctas += G;
+  size_t k = 0;        // position in `order`
+  int64_t in_req = 0;  // tiles of request order[k] already assigned
   for (int32_t i = 0; i < G; ++i) {
     int64_t need = (T * (i + 1)) / G - (T * i) / G;
     while (need > 0) {
-      while (tiles[b] - in_req == 0) { ++b; in_req = 0; }
+      while (tiles[order[k]] - in_req == 0) { ++k; in_req = 0; }
+      const int32_t b = order[k];
       const int64_t take = std::min(need, tiles[b] - in_req);
       WorkItem w{};
       w.b = b;
@@ -203,14 +206,15 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 extern "C" {
 
-mla_status mla_decode_plan(const int32_t* kv_indptr_host, const int32_t* kv_last_page_len_host,
-                           int32_t batch_size, int32_t page_size, mla_dtype q_dtype,
-                           mla_dtype kv_dtype, int32_t num_splits, int32_t num_sms,
-                           mla_plan** plan_out) {
+mla_status mla_decode_plan_q(const int32_t* kv_indptr_host, const int32_t* kv_last_page_len_host,
+                             int32_t batch_size, int32_t q_len, int32_t page_size,
+                             mla_dtype q_dtype, mla_dtype kv_dtype, int32_t num_splits,
+                             int32_t num_sms, mla_plan** plan_out) {
   if (plan_out == nullptr) return MLA_ERR_INVALID_ARG;
   *plan_out = nullptr;
   if (kv_indptr_host == nullptr || batch_size < 1 || page_size < 1 || num_splits < 0 ||
-      num_sms < 0)
+      num_sms < 0 || q_len < 1 || q_len > MLA_MAX_Q_LEN ||
+      static_cast<int64_t>(batch_size) * q_len > INT32_MAX / mla::kHeads)
     return MLA_ERR_INVALID_ARG;
   if (q_dtype < MLA_DTYPE_BF16 || q_dtype > MLA_DTYPE_MXFP4 || kv_dtype < MLA_DTYPE_BF16 ||
       kv_dtype > MLA_DTYPE_MXFP4)
@@ -218,8 +222,12 @@ mla_status mla_decode_plan(const int32_t* kv_indptr_host, const int32_t* kv_last
   const int qmode = qmode_of(q_dtype, kv_dtype);
   if (qmode < 0) return MLA_ERR_UNSUPPORTED;
   if (kv_indptr_host[0] < 0) return MLA_ERR_INVALID_ARG;
-  std::vector<int32_t> len(batch_size), page_base(batch_size), npages(batch_size);
-  std::vector<int64_t> tiles(batch_size);
+  // Query token t of request b is "virtual request" r = b * q_len + t (its
+  // q, out and lse row): it attends to the request's first n - q_len + 1 + t
+  // tokens, through the request's pages.
+  const int32_t nv = batch_size * q_len;
+  std::vector<int32_t> len(nv), page_base(nv), npages(nv);
+  std::vector<int64_t> tiles(nv);
   int64_t total_tok = 0, total_tiles = 0;
   for (int32_t b = 0; b < batch_size; ++b) {
     const int64_t np = static_cast<int64_t>(kv_indptr_host[b + 1]) - kv_indptr_host[b];
@@ -231,12 +239,15 @@ mla_status mla_decode_plan(const int32_t* kv_indptr_host, const int32_t* kv_last
       n -= page_size - last;
     }
     if (n > INT32_MAX - mla::kTile) return MLA_ERR_INVALID_ARG;
-    len[b] = static_cast<int32_t>(n);
-    page_base[b] = kv_indptr_host[b];
-    npages[b] = static_cast<int32_t>(np);
-    tiles[b] = (n + mla::kTile - 1) / mla::kTile;
-    total_tok += n;
-    total_tiles += tiles[b];
+    for (int32_t t = 0; t < q_len; ++t) {
+      const int32_t r = b * q_len + t;
+      len[r] = static_cast<int32_t>(std::max<int64_t>(0, n - q_len + 1 + t));
+      page_base[r] = kv_indptr_host[b];
+      npages[r] = static_cast<int32_t>(np);
+      tiles[r] = (len[r] + mla::kTile - 1) / mla::kTile;
+      total_tok += len[r];
+      total_tiles += tiles[r];
+    }
   }
   if (num_sms == 0) {
     int dev = 0;
@@ -246,7 +257,8 @@ mla_status mla_decode_plan(const int32_t* kv_indptr_host, const int32_t* kv_last
   }
   mla_plan* P = new (std::nothrow) mla_plan();
   if (P == nullptr) return MLA_ERR_INVALID_ARG;
-  P->bs = batch_size;
+  P->bs = nv;
+  P->q_len = q_len;
   P->page_size = page_size;
   P->num_splits = num_splits;
   P->q_dtype = q_dtype;
@@ -254,10 +266,28 @@ mla_status mla_decode_plan(const int32_t* kv_indptr_host, const int32_t* kv_last
   P->qmode = qmode;
   P->total_tokens = total_tok;
   P->total_tiles = total_tiles;
+  P->cta_indptr.assign(1, 0);
   if (num_splits == 0) {
     const int32_t G = static_cast<int32_t>(std::min<int64_t>(num_sms, total_tiles));
-    if (G > 0) plan_balanced(P, tiles, len, page_base, npages, G);
-    else P->cta_indptr.assign(1, 0);
+    std::vector<int32_t> order;
+    if (q_len == 1 || G < q_len) {
+      // query-token-major order: the q_len passes over a request's KV stay
+      // close in time when the CTAs are too few to group them
+      for (int32_t t = 0; t < q_len; ++t)
+        for (int32_t b = 0; b < batch_size; ++b) order.push_back(b * q_len + t);
+      plan_balanced(P, order, tiles, len, page_base, npages, G);
+    } else {
+      // one group of CTAs per query token, each balanced over every request:
+      // CTA i of each group reads the same KV at about the same time, so the
+      // other q_len - 1 passes are served from L2
+      for (int32_t t = 0; t < q_len; ++t) {
+        order.clear();
+        for (int32_t b = 0; b < batch_size; ++b) order.push_back(b * q_len + t);
+        const int32_t Gt = static_cast<int32_t>((static_cast<int64_t>(G) * (t + 1)) / q_len -
+                                                (static_cast<int64_t>(G) * t) / q_len);
+        plan_balanced(P, order, tiles, len, page_base, npages, Gt);
+      }
+    }
   } else {
     plan_fixed(P, tiles, len, page_base, npages, num_splits);
   }
@@ -265,6 +295,14 @@ mla_status mla_decode_plan(const int32_t* kv_indptr_host, const int32_t* kv_last
   layout_workspace(P);
   *plan_out = P;
   return MLA_OK;
+}
+
+mla_status mla_decode_plan(const int32_t* kv_indptr_host, const int32_t* kv_last_page_len_host,
+                           int32_t batch_size, int32_t page_size, mla_dtype q_dtype,
+                           mla_dtype kv_dtype, int32_t num_splits, int32_t num_sms,
+                           mla_plan** plan_out) {
+  return mla_decode_plan_q(kv_indptr_host, kv_last_page_len_host, batch_size, 1, page_size,
+                           q_dtype, kv_dtype, num_splits, num_sms, plan_out);
 }
 
 mla_status mla_plan_workspace_size(const mla_plan* plan, size_t* bytes) {
@@ -275,7 +313,8 @@ mla_status mla_plan_workspace_size(const mla_plan* plan, size_t* bytes) {
 
 mla_status mla_plan_get_info(const mla_plan* plan, mla_plan_info* info) {
   if (plan == nullptr || info == nullptr) return MLA_ERR_INVALID_ARG;
-  info->batch_size = plan->bs;
+  info->batch_size = plan->bs / plan->q_len;
+  info->q_len = plan->q_len;
   info->page_size = plan->page_size;
   info->num_ctas = plan->num_ctas;
   info->num_items = static_cast<int32_t>(plan->items.size());

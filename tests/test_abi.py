@@ -208,3 +208,52 @@ def test_all_empty_batch_has_no_ctas_and_only_fill_jobs(mla):
     info = pl.info()
     assert info.num_ctas == 0 and info.num_items == 0 and info.num_partials == 0
     assert info.num_merge_jobs == 3
+
+
+# ------------------------------------------------- several query tokens
+
+def plan_q(mla, indptr, q_len, last=None, ps=1, S=0, sms=148):
+    return mla.mla_decode_plan(np.asarray(indptr, np.int32), last, page_size=ps, q_dtype="bf16",
+                               kv_dtype="fp8", num_splits=S, num_sms=sms, q_len=q_len)
+
+
+def virtual_lengths(lengths, q_len):
+    return [max(0, n - q_len + 1 + t) for n in lengths for t in range(q_len)]
+
+
+@pytest.mark.parametrize("q_len,S,sms", [(2, 0, 152), (3, 0, 12), (4, 0, 3), (3, 2, 152)])
+def test_qlen_plan_covers_causal_prefixes(mla, q_len, S, sms):
+    # query token t of request b is row b*q_len + t and covers the request's
+    # first n - q_len + 1 + t tokens
+    lens = [0, 1, 2, 3, 300, 1000, 4096, 129]
+    indptr = np.concatenate([[0], np.cumsum(lens)])
+    pl = plan_q(mla, indptr, q_len, S=S, sms=sms)
+    info = pl.info()
+    assert info.batch_size == len(lens) and info.q_len == q_len
+    check_partition(pl, virtual_lengths(lens, q_len))
+
+
+def test_qlen_plan_groups_ctas_by_query_token(mla):
+    # every query token gets its own group of CTAs, each balanced over all
+    # requests, so CTA i of each group reads the same KV ranges
+    q_len, sms, bs, kv = 3, 12, 8, 2048
+    indptr = np.arange(bs + 1) * kv
+    pl = plan_q(mla, indptr, q_len, sms=sms)
+    ind, items = pl.work()
+    info = pl.info()
+    assert info.num_ctas == sms
+    per = sms // q_len
+    for c in range(sms):
+        toks = {int(r) % q_len for r, _, _, _ in items[ind[c]:ind[c + 1]]}
+        assert toks == {c // per}
+    for i in range(per):
+        ranges = [[(int(r) // q_len, int(t0)) for r, t0, _, _ in items[ind[g * per + i]:ind[g * per + i + 1]]]
+                  for g in range(q_len)]
+        assert ranges[0] == ranges[1] == ranges[2]
+
+
+def test_qlen_plan_rejects_bad_q_len(mla):
+    for q_len in (0, -1, 65):
+        with pytest.raises(mla.MlaError) as e:
+            plan_q(mla, [0, 10], q_len)
+        assert e.value.status == 1

@@ -30,11 +30,12 @@ def run_gpu(w, num_splits=0, num_sms=0):
     from mla_decode_stage1_gb300 import synth  # noqa: F401
     plan = mla.mla_decode_plan(w.kv_indptr, w.kv_last_page_len, page_size=w.page_size,
                                q_dtype=w.q_dtype, kv_dtype=w.kv_dtype, num_splits=num_splits,
-                               num_sms=num_sms)
+                               num_sms=num_sms, q_len=w.q_len)
     d = w.to("cuda")
     ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
-    out = torch.full((w.bs, 16, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
-    lse = torch.full((w.bs, 16), float("nan"), dtype=torch.float32, device="cuda")
+    rows = w.bs * w.q_len
+    out = torch.full((rows, 16, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((rows, 16), float("nan"), dtype=torch.float32, device="cuda")
     mla.mla_decode_run(plan, d.q, d.kv, out, workspace=ws, q_scale=d.q_scale,
                        kv_scale=d.kv_scale, kv_e8m0=d.kv_e8m0, kv_indices=d.kv_indices, lse=lse)
     mla.mla_decode_check(plan, ws)
@@ -64,7 +65,12 @@ def check(w, num_splits=0, num_sms=0, select=None):
     o, lse, plan = run_gpu(w, num_splits=num_splits, num_sms=num_sms)
     sel = list(range(w.bs)) if select is None else list(select)
     o_ref, l_ref = oracle.mla_decode(**synth.oracle_args(w, select=sel))
-    compare(o[sel], lse[sel], o_ref, l_ref, w.kv_dtype, [w.lengths[i] for i in sel])
+    # rows b*q_len + t; query token t of a request with n tokens sees the
+    # first n - q_len + 1 + t of them
+    ql = w.q_len
+    rows = [b * ql + t for b in sel for t in range(ql)]
+    seen = [max(0, w.lengths[b] - ql + 1 + t) for b in sel for t in range(ql)]
+    compare(o[rows], lse[rows], o_ref, l_ref, w.kv_dtype, seen)
     return plan
 
 
@@ -263,3 +269,38 @@ def test_one_long_request_over_every_sm(kv_dtype):
                             kv_dtype=kv_dtype, seed=47)
     plan = check(w)
     assert plan.info().num_partials >= 100
+
+
+# ------------------------------------------------- several query tokens
+
+@pytest.mark.parametrize("q_dtype,kv_dtype", COMBOS + [("bf16", "mxfp4")])
+@pytest.mark.parametrize("q_len", [2, 4])
+def test_qlen_causal_decode(q_dtype, kv_dtype, q_len):
+    # requests shorter than q_len leave their first query tokens empty
+    from mla_decode_stage1_gb300 import synth
+    lengths = [1, 3, 130, 0, 1000, 2049]
+    page = 8 if kv_dtype == "mxfp4" else 4
+    w = synth.make_workload(bs=len(lengths), lengths=lengths, page_size=page, q_dtype=q_dtype,
+                            kv_dtype=kv_dtype, permute_pages=True, seed=48, q_len=q_len)
+    check(w)
+
+
+@pytest.mark.parametrize("num_splits,num_sms", [(3, 0), (0, 5), (0, 2)])
+def test_qlen_splits_and_few_ctas(num_splits, num_sms):
+    from mla_decode_stage1_gb300 import synth
+    lengths = [700, 5, 4096, 129]
+    w = synth.make_workload(bs=4, lengths=lengths, page_size=16, q_dtype="fp8", kv_dtype="fp8",
+                            permute_pages=True, seed=49, q_len=3)
+    check(w, num_splits=num_splits, num_sms=num_sms)
+
+
+def test_qlen_large_batch_sampled():
+    # bs=64 x 8192 tokens, two query tokens, in the balanced launch the
+    # planner picks (one CTA group per query token)
+    _mla()
+    from mla_decode_stage1_gb300 import synth
+    w = synth.make_workload(bs=64, lengths=[8192] * 64, page_size=8, q_dtype="bf16",
+                            kv_dtype="fp8", permute_pages=True, seed=50, q_len=2, device="cuda")
+    rng = np.random.default_rng(9)
+    sel = sorted(rng.choice(w.bs, size=4, replace=False).tolist() + [0, w.bs - 1])
+    check(w, select=sel)
