@@ -304,3 +304,35 @@ def test_qlen_large_batch_sampled():
     rng = np.random.default_rng(9)
     sel = sorted(rng.choice(w.bs, size=4, replace=False).tolist() + [0, w.bs - 1])
     check(w, select=sel)
+
+
+# ------------------------------------------------- seeded random sweep
+
+def _random_case(seed):
+    rng = np.random.default_rng(1000 + seed)
+    q_dtype, kv_dtype = [("bf16", "bf16"), ("bf16", "fp8"), ("fp8", "fp8"), ("fp8", "bf16"),
+                         ("bf16", "mxfp4")][rng.integers(5)]
+    bs = int(rng.integers(1, 9))
+    lengths = [int(x) for x in rng.choice([0, 1, 2, 127, 128, 129, 255, 300, 1000, 2500], size=bs)]
+    if kv_dtype == "mxfp4":
+        page_size = int(rng.choice([1, 8, 16, 64]))
+    else:
+        page_size = int(rng.choice([1, 2, 3, 8, 16, 40, 64]))
+    permute = page_size > 1 and bool(rng.integers(2))
+    q_len = int(rng.choice([1, 1, 2, 3]))
+    mode = int(rng.integers(3))
+    num_splits = int(rng.integers(1, 5)) if mode == 1 else 0
+    num_sms = int(rng.integers(1, 12)) if mode == 2 else 0
+    return dict(bs=bs, lengths=lengths, page_size=page_size, q_dtype=q_dtype, kv_dtype=kv_dtype,
+                permute_pages=permute, q_len=q_len), num_splits, num_sms
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_sweep(seed):
+    # formats, lengths (empty, partial tiles), page sizes (row gather and
+    # 8-row boxes), page permutation, several query tokens, fixed splits and
+    # few-CTA plans drawn from one seed; every output against the oracle
+    from mla_decode_stage1_gb300 import synth
+    kw, num_splits, num_sms = _random_case(seed)
+    w = synth.make_workload(seed=60 + seed, **kw)
+    check(w, num_splits=num_splits, num_sms=num_sms)
