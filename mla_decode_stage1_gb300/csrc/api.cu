@@ -122,9 +122,9 @@ void layout_workspace(mla_plan* P) {
   P->off_jobs = off;
   off = align256(off + sizeof(MergeJob) * P->jobs.size());
   P->off_part_o = off;
-  off = align256(off + sizeof(float) * static_cast<size_t>(P->num_partials) * mla::kHeads * mla::kVDim);
+  off = align256(off + sizeof(float) * static_cast<size_t>(P->num_partials) * P->rows * mla::kVDim);
   P->off_part_lse = off;
-  off = align256(off + sizeof(float) * static_cast<size_t>(P->num_partials) * mla::kHeads);
+  off = align256(off + sizeof(float) * static_cast<size_t>(P->num_partials) * P->rows);
   P->ws_bytes = std::max<size_t>(off, 256);
   P->table.assign(P->off_part_o, 0);
   for (size_t c = 0; c + 1 < P->cta_indptr.size(); ++c) {
@@ -222,11 +222,15 @@ mla_status mla_decode_plan_q(const int32_t* kv_indptr_host, const int32_t* kv_la
   const int qmode = qmode_of(q_dtype, kv_dtype);
   if (qmode < 0) return MLA_ERR_UNSUPPORTED;
   if (kv_indptr_host[0] < 0) return MLA_ERR_INVALID_ARG;
-  // Query token t of request b is "virtual request" r = b * q_len + t (its
-  // q, out and lse row): it attends to the request's first n - q_len + 1 + t
-  // tokens, through the request's pages.
-  const int32_t nv = batch_size * q_len;
-  std::vector<int32_t> len(nv), page_base(nv), npages(nv);
+  // Two query tokens with fp8 q and KV run natively: both tokens' 32 q rows
+  // share every tile (kQFp8KvFp8x2, query token t sees vis0 + t tokens).
+  // Otherwise query token t of request b is "virtual request" r = b * q_len + t
+  // (its q, out and lse row): it attends to the request's first
+  // n - q_len + 1 + t tokens, through the request's pages.
+  const bool native2 = q_len == 2 && qmode == mla::kQFp8KvFp8;
+  const int32_t qv = native2 ? 1 : q_len;          // virtual requests per request
+  const int32_t nv = batch_size * qv;
+  std::vector<int32_t> len(nv), page_base(nv), npages(nv), vis0(nv, 0);
   std::vector<int64_t> tiles(nv);
   int64_t total_tok = 0, total_tiles = 0;
   for (int32_t b = 0; b < batch_size; ++b) {
@@ -239,9 +243,10 @@ mla_status mla_decode_plan_q(const int32_t* kv_indptr_host, const int32_t* kv_la
       n -= page_size - last;
     }
     if (n > INT32_MAX - mla::kTile) return MLA_ERR_INVALID_ARG;
-    for (int32_t t = 0; t < q_len; ++t) {
-      const int32_t r = b * q_len + t;
-      len[r] = static_cast<int32_t>(std::max<int64_t>(0, n - q_len + 1 + t));
+    for (int32_t t = 0; t < qv; ++t) {
+      const int32_t r = b * qv + t;
+      len[r] = static_cast<int32_t>(native2 ? n : std::max<int64_t>(0, n - q_len + 1 + t));
+      vis0[r] = static_cast<int32_t>(std::max<int64_t>(0, n - 1));
       page_base[r] = kv_indptr_host[b];
       npages[r] = static_cast<int32_t>(np);
       tiles[r] = (len[r] + mla::kTile - 1) / mla::kTile;
@@ -258,23 +263,25 @@ mla_status mla_decode_plan_q(const int32_t* kv_indptr_host, const int32_t* kv_la
   mla_plan* P = new (std::nothrow) mla_plan();
   if (P == nullptr) return MLA_ERR_INVALID_ARG;
   P->bs = nv;
+  P->nreq = batch_size;
+  P->rows = native2 ? 2 * mla::kHeads : mla::kHeads;
   P->q_len = q_len;
   P->page_size = page_size;
   P->num_splits = num_splits;
   P->q_dtype = q_dtype;
   P->kv_dtype = kv_dtype;
-  P->qmode = qmode;
+  P->qmode = native2 ? mla::kQFp8KvFp8x2 : qmode;
   P->total_tokens = total_tok;
   P->total_tiles = total_tiles;
   P->cta_indptr.assign(1, 0);
   if (num_splits == 0) {
     const int32_t G = static_cast<int32_t>(std::min<int64_t>(num_sms, total_tiles));
     std::vector<int32_t> order;
-    if (q_len == 1 || G < q_len) {
+    if (qv == 1 || G < qv) {
       // query-token-major order: the q_len passes over a request's KV stay
       // close in time when the CTAs are too few to group them
-      for (int32_t t = 0; t < q_len; ++t)
-        for (int32_t b = 0; b < batch_size; ++b) order.push_back(b * q_len + t);
+      for (int32_t t = 0; t < qv; ++t)
+        for (int32_t b = 0; b < batch_size; ++b) order.push_back(b * qv + t);
       plan_balanced(P, order, tiles, len, page_base, npages, G);
     } else {
       // one group of CTAs per query token, each balanced over every request:
@@ -291,6 +298,7 @@ mla_status mla_decode_plan_q(const int32_t* kv_indptr_host, const int32_t* kv_la
   } else {
     plan_fixed(P, tiles, len, page_base, npages, num_splits);
   }
+  for (WorkItem& w : P->items) w.vis0 = vis0[w.b];
   assign_slots(P, len);
   layout_workspace(P);
   *plan_out = P;
@@ -313,7 +321,7 @@ mla_status mla_plan_workspace_size(const mla_plan* plan, size_t* bytes) {
 
 mla_status mla_plan_get_info(const mla_plan* plan, mla_plan_info* info) {
   if (plan == nullptr || info == nullptr) return MLA_ERR_INVALID_ARG;
-  info->batch_size = plan->bs / plan->q_len;
+  info->batch_size = plan->nreq;
   info->q_len = plan->q_len;
   info->page_size = plan->page_size;
   info->num_ctas = plan->num_ctas;
@@ -439,6 +447,7 @@ mla_status mla_decode_run(mla_plan* plan, const void* q, const float* q_scale, c
     s.out = static_cast<uint16_t*>(out);
     s.lse = lse;
     s.num_jobs = static_cast<int32_t>(plan->jobs.size());
+    s.rows = plan->rows;
     if (mla::launch_stage2(s, stream) != cudaSuccess) return MLA_ERR_CUDA;
   }
   return MLA_OK;

@@ -36,7 +36,9 @@ struct WorkItem {
   int32_t slot;       // partial slot, or -1: write out/lse directly
   int32_t page_base;  // kv_indptr[b]: first page-table entry of the request
   int32_t npages;     // page-table entries of the request
-  int32_t pad0, pad1;
+  int32_t vis0;       // two query tokens per request: tokens query token 0 sees
+                      // (query token t sees vis0 + t); unused with one token
+  int32_t pad1;
 };
 static_assert(sizeof(WorkItem) == 32, "work item is two int4");
 
@@ -60,8 +62,10 @@ enum QMode : int {
   kQFp8KvFp8 = 1,     // kind::f8f6f4, B = q bytes (16 rows)
   kQBf16KvFp8 = 2,    // kind::f8f6f4, B = [q_hi ; q_lo] e4m3 (32 rows)
   kQFp8KvBf16 = 3,    // kind::f16, q decoded to bf16 (exact), B = 16 rows
-  kQBf16KvMx = 4      // MXFP4 KV dequantised in shared memory to e4m3 with a per-token
+  kQBf16KvMx = 4,     // MXFP4 KV dequantised in shared memory to e4m3 with a per-token
                       // power of two; then as kQBf16KvFp8
+  kQFp8KvFp8x2 = 5    // two query tokens per request, fp8 q and KV: kind::f8f6f4,
+                      // B = 32 q rows (token-major), causal over the last two positions
 };
 
 struct Stage1Params {
@@ -91,6 +95,7 @@ struct Stage1Params {
 
 struct Stage2Params {
   const MergeJob* jobs;
+  int32_t rows;                 // output rows per request: 16 heads x query tokens
   const float* part_o;
   const float* part_lse;
   uint16_t* out;

@@ -13,6 +13,8 @@
 struct mla_plan {
   int32_t bs = 0, page_size = 0, num_splits = 0;   // bs: rows of q (requests x q_len)
   int32_t q_len = 1;                                 // query tokens per request
+  int32_t nreq = 0;                                  // requests of the batch
+  int32_t rows = 16;                                 // output rows per planned request (16 x tokens it holds)
   int q_dtype = 0, kv_dtype = 0, qmode = 0;
   int32_t num_ctas = 0, num_partials = 0;
   int64_t total_tokens = 0, total_tiles = 0;

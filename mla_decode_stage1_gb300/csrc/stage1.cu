@@ -52,12 +52,17 @@ namespace mla {
 template <int QM>
 struct Layout {
   static constexpr bool kMx = (QM == kQBf16KvMx);                  // MXFP4 KV, dequantised
-  static constexpr bool kKv8 = (QM == kQFp8KvFp8 || QM == kQBf16KvFp8 || kMx);
-  static constexpr int kNq = (QM == kQBf16KvFp8 || kMx) ? 32 : 16;  // UMMA N of QK^T
+  static constexpr bool kKv8 =
+      (QM == kQFp8KvFp8 || QM == kQBf16KvFp8 || kMx || QM == kQFp8KvFp8x2);
+  static constexpr int kQL = (QM == kQFp8KvFp8x2) ? 2 : 1;         // query tokens per request
+  static constexpr int kRows = kHeads * kQL;                        // q rows, token-major
+  static constexpr bool kHiLo = (QM == kQBf16KvFp8 || kMx);         // q as two e4m3 terms
+  static constexpr int kNq = kRows * (kHiLo ? 2 : 1);               // UMMA N of QK^T
   // Warps: producer, 2 QK^T issuers, PV issuer(s), two head groups of four
   // softmax warps (8 heads each), then either a q warp (14 warps) or, for
   // MXFP4, 4 dequant warps that also prepare q (16 warps, register cap 128).
   static constexpr int kHeadGroups = 2;
+  static constexpr int kH = kRows / kHeadGroups;                    // q rows per softmax thread
   static constexpr int kThreads = kMx ? 512 : 448;
   static constexpr int kPvIssuers = kMx ? 1 : 2;
   static constexpr int kElem = kKv8 ? 1 : 2;
@@ -69,13 +74,16 @@ struct Layout {
   static constexpr int kQAtoms = kKv8 ? 5 : 9;                      // 128-byte K atoms of q
   static constexpr int kQAtomBytes = kNq * 128;
   static constexpr int kQBytes = kQAtoms * kQAtomBytes;
-  static constexpr int kPBytes = 4096;
+  static constexpr int kPRow = 2 * kRows;                           // P bytes per token
+  static constexpr int kPBytes = kTile * kPRow;
   static constexpr int kScBytes = kMx ? kTile * 32 : 0;             // e8m0 rows per tile slot
   static constexpr int kRawRowBytes = kQkDim / 2;                   // packed MXFP4 row
-  static constexpr bool kQ8 = (QM == kQFp8KvFp8 || QM == kQFp8KvBf16);
-  static constexpr int kQSrcBytes = kHeads * kQkDim * (kQ8 ? 1 : 2);  // one request's q
-  static constexpr uint32_t kOCols = kKv8 ? 32 : 16;               // TMEM columns per O block
-  static constexpr int kMiscBytes = 2048;
+  static constexpr bool kQ8 = (QM == kQFp8KvFp8 || QM == kQFp8KvBf16 || QM == kQFp8KvFp8x2);
+  static constexpr int kQSrcBytes = kRows * kQkDim * (kQ8 ? 1 : 2);  // one request's q
+  static constexpr uint32_t kOCols = kRows * (kKv8 ? 2 : 1);       // TMEM columns per O block
+  // TMEM: S^T at 0 (2 buffers x 2 K-halves x 32 columns), O^T from 128
+  static constexpr uint32_t kTmemCols = 128 + 4 * kOCols <= 256 ? 256 : 512;
+  static constexpr int kMiscBytes = 2560;
   static constexpr int kMaxSmem = 232448;
   static constexpr int kNumTiles =
       (kMaxSmem - 1024 - 2 * kQBytes - 2 * kPBytes - kMiscBytes - kQSrcBytes) /
@@ -89,13 +97,14 @@ struct Layout {
   static_assert(kNumTiles >= 1 && kNumTiles <= 4, "tile ring");
   static_assert(kSmemBytes <= kMaxSmem, "shared memory over budget");
   static_assert(kTileBytes % 1024 == 0 && kQBytes % 1024 == 0, "operand alignment");
+  static_assert(kNq <= 32, "S^T columns per K-half");
 };
 
 // Misc region: barriers, reduction scratch, q scales, TMEM address.
 struct Misc {
   uint64_t full[4], empty[4];
   uint64_t s_full[2], s_empty[2], p_full[2], pv_done[2], q_full[2], q_empty[2], drain[4];
-  alignas(16) float red[2][4][16];   // read back as float4
+  alignas(16) float red[2][4][32];   // per-warp partial max / sum of every q row
   float qscale[2][2];
   uint32_t tmem_base;
   int32_t abort_sm;                  // set by a softmax thread whose bounded wait gave up
@@ -110,13 +119,12 @@ struct Misc {
   float uexp[2][128];                // per-token power of two u_t = r_t - 127 of a slot
   uint2 e2m1_tab[16];                // e4m3 tables for 2^k, k = index - 14 (k <= -14: all 0)
 };
-static_assert(sizeof(Misc) <= 2048, "misc region");
+static_assert(sizeof(Misc) <= 2560, "misc region");
 static_assert(offsetof(Misc, red) % 16 == 0, "reduction scratch is read as float4");
 
 // TMEM columns: S^T as 2 buffers x 2 K-halves x 32 columns [0,128) (the two
 // QK^T issuers each accumulate half of the 576 dims), then O^T: four 128-dim
-// blocks of kOCols columns (fp8 KV: 16 heads of p_hi, then 16 of p_lo).
-constexpr uint32_t kTmemCols = 256;
+// blocks of kOCols columns (fp8 KV: the q rows of p_hi, then of p_lo).
 constexpr uint32_t kColS = 0, kColO = 128;
 
 // Byte offset of (row, byte x) inside a 128-byte-wide K-major operand with
@@ -425,24 +433,26 @@ __device__ void run_pv(const Stage1Params& p, Misc* ms, uint32_t ring, uint32_t 
       // they are read; blocks 0-1 follow.
       const int c = L::kMx ? (i + 2) & 3 : kBlocks * half + i;
       const uint32_t d = tmem + kColO + L::kOCols * c;
-      // B = P^T, MN-major with the 32-byte swizzle: one 32-byte row per token
-      // (fp8: 16 heads of p_hi then 16 of p_lo; bf16: 16 heads), 8-token
-      // groups of 256 bytes.
-      const uint64_t b0 = smem_desc(pa, 256, 256, kSwizzle32B);
+      // B = P^T, MN-major: one kPRow-byte row per token (fp8: the q rows of
+      // p_hi then of p_lo; bf16: the q rows), 8-token groups of 8 rows, with
+      // the swizzle of the row width (32 or 64 bytes).
+      constexpr uint32_t kPGroup = 8 * L::kPRow;
+      const uint64_t b0 =
+          smem_desc(pa, kPGroup, kPGroup, L::kPRow == 64 ? kSwizzle64B : kSwizzle32B);
       if constexpr (L::kKv8) {
-        constexpr uint32_t idesc = make_idesc(0, 0, true, true, 128, 32);
+        constexpr uint32_t idesc = make_idesc(0, 0, true, true, 128, L::kOCols);
         const uint64_t a0 = smem_desc(tile + (2 * c) * cs, cs, gs, kSwizzle64B);  // 2 chunks
         for (int kk = 0; kk < 4; ++kk) {                          // 32 tokens = 4 groups
           const uint64_t a = a0 + ((kk * 4 * gs) >> 4);
-          const uint64_t b = b0 + ((kk * 1024) >> 4);
+          const uint64_t b = b0 + ((kk * 4 * kPGroup) >> 4);
           umma_f8f6f4(d, a, b, idesc, (first && kk == 0) ? 0u : 1u);
         }
       } else {
-        constexpr uint32_t idesc = make_idesc(1, 1, true, true, 128, 16);
+        constexpr uint32_t idesc = make_idesc(1, 1, true, true, 128, L::kOCols);
         const uint64_t a0 = smem_desc(tile + (4 * c) * cs, cs, gs, kSwizzle64B);  // 4 chunks
         for (int kk = 0; kk < 8; ++kk) {                          // 16 tokens = 2 groups
           const uint64_t a = a0 + ((kk * 2 * gs) >> 4);
-          const uint64_t b = b0 + ((kk * 512) >> 4);
+          const uint64_t b = b0 + ((kk * 2 * kPGroup) >> 4);
           umma_f16(d, a, b, idesc, (first && kk == 0) ? 0u : 1u);
         }
       }
@@ -568,9 +578,9 @@ __device__ __forceinline__ void q_convert(const Stage1Params& p, Misc* ms, const
     const float kvs = (QM == kQBf16KvMx) ? 1.0f : __ldg(p.kv_scale);
     c_hi = s_hi * kvs * kSmScale * kLog2e;
     c_lo = c_hi * (1.0f / 16.0f);
-  } else if constexpr (QM == kQFp8KvFp8) {
+  } else if constexpr (QM == kQFp8KvFp8 || QM == kQFp8KvFp8x2) {
     const uint4* src = reinterpret_cast<const uint4*>(stage);
-    for (int v = i; v < kHeads * 36; v += n) {       // 36 vectors of 16 e4m3 per head
+    for (int v = i; v < L::kRows * 36; v += n) {     // 36 vectors of 16 e4m3 per q row
       const int h = v / 36, d0 = (v % 36) * 16;
       *reinterpret_cast<uint4*>(dst + (d0 >> 7) * L::kQAtomBytes + sw128(h, d0 & 127)) = src[v];
     }
@@ -795,7 +805,7 @@ __device__ void run_qprep(const Stage1Params& p, Misc* ms, uint8_t* qgen, uint8_
 // named barrier `bar`.
 template <bool kMax, int kH>
 __device__ __forceinline__ void reduce_heads(const float (&v)[kH], float (&out)[kH],
-                                             float (*red)[16], int h0, int qw, int lane, int bar) {
+                                             float (*red)[32], int h0, int qw, int lane, int bar) {
   auto op = [](float a, float b) { return kMax ? fmaxf(a, b) : a + b; };
   constexpr int kStages = kH == 16 ? 4 : 3;
   float buf[kH];
@@ -825,15 +835,16 @@ __device__ __forceinline__ void reduce_heads(const float (&v)[kH], float (&out)[
 
 // Softmax warps: kHeadGroups groups of four warps (one per TMEM lane
 // quadrant); thread tq of a group owns token tq of every tile (its TMEM lane)
-// and heads h0..h0+kH-1.  Per tile: S from TMEM, the running max, the lazy
-// rescale of O, p = exp2(s - m + 4) into l and into the P operand.  After an
-// item's last tile, the epilogue normalises O and writes it out.
+// and q rows h0..h0+kH-1 (one query token: 8 of its heads, or with two query
+// tokens all 16 heads of token hg).  Per tile: S from TMEM, the running max,
+// the lazy rescale of O, p = exp2(s - m + 4) into l and into the P operand.
+// After an item's last tile, the epilogue normalises O and writes it out.
 template <int QM>
 __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, uint8_t* pgen,
                             uint8_t* qgen, uint8_t* stage, uint32_t tmem, int it0, int it1,
                             const WorkItem& first, int tid) {
   using L = Layout<QM>;
-  constexpr int kHG = L::kHeadGroups, kH = 16 / kHG;
+  constexpr int kHG = L::kHeadGroups, kH = L::kH;
   volatile int32_t* abort = &ms->abort_sm;
   const int hg = tid >> 7, tq = tid & 127;
   const int h0 = kH * hg, bar = 1 + hg;
@@ -878,16 +889,16 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
       tc_fence_after();
       float s[kH];
       {
-        // S^T columns of buffer sb: two K-halves of 32 columns; with kNq = 32
-        // heads 0-15 of the q_hi term, then of the q_lo term
+        // S^T columns of buffer sb: two K-halves of 32 columns; q split in two
+        // terms puts the rows of q_hi first, then those of q_lo
         const uint32_t sc = tl + kColS + 64 * sb + h0;
         float a0[kH], a1[kH];
         tmem_ld(sc, a0);
         tmem_ld(sc + 32, a1);
-        if constexpr (L::kNq == 32) {
+        if constexpr (L::kHiLo) {
           float b0[kH], b1[kH];
-          tmem_ld(sc + 16, b0);
-          tmem_ld(sc + 48, b1);
+          tmem_ld(sc + L::kRows, b0);
+          tmem_ld(sc + 32 + L::kRows, b1);
           tmem_wait_ld();
 #pragma unroll
           for (int h = 0; h < kH; ++h) s[h] = (a0[h] + a1[h]) * c_hi + (b0[h] + b1[h]) * c_lo;
@@ -901,6 +912,10 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
       mbar_arrive(smem_u32(&ms->s_empty[sb]));
       const int nvalid = min(kTile, w.tok_end - (w.tok_begin + j * kTile));
       const bool valid = tq < nvalid;
+      // two query tokens: query token hg sees the request's first vis0 + hg
+      // tokens (causal over the last two positions)
+      bool vis = valid;
+      if constexpr (L::kQL > 1) vis = valid && w.tok_begin + j * kTile + tq < w.vis0 + hg;
       // MXFP4: the token's scores carry its factor 2^u; the running max and
       // P use s + u (the factor of its V row), l uses s: P' = p 2^u.
       float gl = 1.0f;                                   // 2^-u, turns P' back into p
@@ -912,7 +927,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
         for (int h = 0; h < kH; ++h) s[h] = s[h] * f + static_cast<float>(u);
       }
 #pragma unroll
-      for (int h = 0; h < kH; ++h) s[h] = valid ? s[h] : -INFINITY;
+      for (int h = 0; h < kH; ++h) s[h] = vis ? s[h] : -INFINITY;
       // The running max only moves when some score of the tile exceeds it by
       // more than kTau (always on an item's first tile).  One barrier vote
       // settles that; only then is the tile max reduced over the group.
@@ -950,7 +965,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
         const int nparts = L::kKv8 ? 2 : 1;
         for (int part = 0; part < nparts; ++part) {
           for (int c = 0; c < 4; ++c) {
-            const uint32_t col = kColO + L::kOCols * c + 16 * part + h0;
+            const uint32_t col = kColO + L::kOCols * c + L::kRows * part + h0;
             float o[kH];
             tmem_ld(tl + col, o);
             tmem_wait_ld();
@@ -966,18 +981,21 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
       float pv[kH];
 #pragma unroll
       for (int h = 0; h < kH; ++h) {
-        pv[h] = valid ? ex2(s[h] - m[h] + kPOff) : 0.0f;
+        pv[h] = vis ? ex2(s[h] - m[h] + kPOff) : 0.0f;
         l[h] += L::kMx ? pv[h] * gl : pv[h];
       }
       // P buffer (g & 1) is free once PV of tile g-2 completed.
       if (g >= 2)
         wait_or_flag(smem_u32(&ms->pv_done[sb]), ((g >> 1) - 1) & 1u, p.err, kErrSoftmax, abort);
-      // This token's row of P^T: 32 bytes, two 16-byte halves swapped on
-      // every other group of 4 tokens (32-byte swizzle: bit 4 ^= bit 7).
-      uint8_t* prow = pgen + sb * L::kPBytes + tq * 32;
+      // This token's row of P^T.  32-byte rows: two 16-byte halves swapped
+      // on every other group of 4 tokens (32-byte swizzle: bit 4 ^= bit 7).
+      // 64-byte rows (two query tokens): 16-byte chunk c at c ^ ((tq >> 1) & 3)
+      // (64-byte swizzle), 8-token groups of 512 bytes.
+      uint8_t* prow = pgen + sb * L::kPBytes + tq * L::kPRow;
       const uint32_t flip = ((tq >> 2) & 1u) << 4;
+      const uint32_t sw64 = (tq >> 1) & 3u;
       if constexpr (L::kKv8) {
-        // fp8: p_hi of heads 0-15 in bytes 0-15, p_lo in bytes 16-31
+        // fp8: p_hi of the q rows, then p_lo of the q rows (one byte each)
         uint32_t hw[kH / 4], lw[kH / 4];
 #pragma unroll
         for (int h = 0; h < kH; h += 2) {
@@ -992,9 +1010,12 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
           hw[wd] |= static_cast<uint32_t>(hi) << sh;
           lw[wd] |= static_cast<uint32_t>(lo) << sh;
         }
-        if constexpr (kH == 16) {
-          *reinterpret_cast<uint4*>(prow + (0u ^ flip)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-          *reinterpret_cast<uint4*>(prow + (16u ^ flip)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        if constexpr (L::kPRow == 64) {
+          // [p_hi token 0 | p_hi token 1 | p_lo token 0 | p_lo token 1]
+          *reinterpret_cast<uint4*>(prow + ((static_cast<uint32_t>(hg) ^ sw64) << 4)) =
+              make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(prow + (((2u + hg) ^ sw64) << 4)) =
+              make_uint4(lw[0], lw[1], lw[2], lw[3]);
         } else {
           *reinterpret_cast<uint2*>(prow + ((8u * hg) ^ flip)) = make_uint2(hw[0], hw[1]);
           *reinterpret_cast<uint2*>(prow + ((16u + 8u * hg) ^ flip)) = make_uint2(lw[0], lw[1]);
@@ -1007,12 +1028,8 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
           const __nv_bfloat162 v = __floats2bfloat162_rn(pv[h], pv[h + 1]);
           bw[h >> 1] = *reinterpret_cast<const uint32_t*>(&v);
         }
-        if constexpr (kH == 16) {
-          *reinterpret_cast<uint4*>(prow + (0u ^ flip)) = make_uint4(bw[0], bw[1], bw[2], bw[3]);
-          *reinterpret_cast<uint4*>(prow + (16u ^ flip)) = make_uint4(bw[4], bw[5], bw[6], bw[7]);
-        } else {
-          *reinterpret_cast<uint4*>(prow + ((16u * hg) ^ flip)) = make_uint4(bw[0], bw[1], bw[2], bw[3]);
-        }
+        static_assert(L::kPRow == 32, "bf16 P rows: one query token");
+        *reinterpret_cast<uint4*>(prow + ((16u * hg) ^ flip)) = make_uint4(bw[0], bw[1], bw[2], bw[3]);
       }
       if (nvalid < kTile) {
         // Tail tile: rows past the range may hold anything (stale tiles,
@@ -1045,33 +1062,60 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
     float inv[kH];
 #pragma unroll
     for (int h = 0; h < kH; ++h) inv[h] = vscale / lt[h];
-    const int slot = w.slot;
-    // O^T of this thread's dim in all four blocks: every TMEM load is issued
-    // before one wait
-    float oh[4][kH], ol[4][kH];
+    if constexpr (L::kQL > 1) {
+      // a query token may see none of the item's tokens (l = 0): O = 0
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      tmem_ld(tl + kColO + L::kOCols * c + h0, oh[c]);
-      if constexpr (L::kKv8) tmem_ld(tl + kColO + L::kOCols * c + 16 + h0, ol[c]);
+      for (int h = 0; h < kH; ++h) inv[h] = lt[h] > 0.0f ? inv[h] : 0.0f;
     }
-    tmem_wait_ld();
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-#pragma unroll
-      for (int h = 0; h < kH; ++h)
-        oh[c][h] = L::kKv8 ? (oh[c][h] + ol[c][h] * (1.0f / kPLoScale)) * inv[h] : oh[c][h] * inv[h];
+    const int slot = w.slot;
+    // rows of this group's q rows in the partial slot or in out (request b's
+    // rows are b * kRows .. : [query token][head])
+    const int64_t row0 = (slot >= 0 ? static_cast<int64_t>(slot) : static_cast<int64_t>(w.b)) *
+                             L::kRows + h0;
+    auto store_block = [&](int c, float (&o)[kH]) {
       const int d = c * 128 + tq;
       if (slot >= 0) {
-        float* po = p.part_o + (static_cast<int64_t>(slot) * kHeads + h0) * kVDim + d;
+        float* po = p.part_o + row0 * kVDim + d;
 #pragma unroll
-        for (int h = 0; h < kH; ++h) po[h * kVDim] = oh[c][h];
+        for (int h = 0; h < kH; ++h) po[h * kVDim] = o[h];
       } else {
-        uint16_t* po = p.out + (static_cast<int64_t>(w.b) * kHeads + h0) * kVDim + d;
+        uint16_t* po = p.out + row0 * kVDim + d;
 #pragma unroll
         for (int h = 0; h < kH; ++h) {
-          const __nv_bfloat16 v = __float2bfloat16_rn(oh[c][h]);
+          const __nv_bfloat16 v = __float2bfloat16_rn(o[h]);
           po[h * kVDim] = *reinterpret_cast<const uint16_t*>(&v);
         }
+      }
+    };
+    if constexpr (kH <= 8) {
+      // O^T of this thread's dim in all four blocks: every TMEM load is
+      // issued before one wait
+      float oh[4][kH], ol[4][kH];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        tmem_ld(tl + kColO + L::kOCols * c + h0, oh[c]);
+        if constexpr (L::kKv8) tmem_ld(tl + kColO + L::kOCols * c + L::kRows + h0, ol[c]);
+      }
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+#pragma unroll
+        for (int h = 0; h < kH; ++h)
+          oh[c][h] = L::kKv8 ? (oh[c][h] + ol[c][h] * (1.0f / kPLoScale)) * inv[h] : oh[c][h] * inv[h];
+        store_block(c, oh[c]);
+      }
+    } else {
+      // 16 rows per thread: one block at a time (registers)
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float oh[kH], ol[kH];
+        tmem_ld(tl + kColO + L::kOCols * c + h0, oh);
+        if constexpr (L::kKv8) tmem_ld(tl + kColO + L::kOCols * c + L::kRows + h0, ol);
+        tmem_wait_ld();
+#pragma unroll
+        for (int h = 0; h < kH; ++h)
+          oh[h] = L::kKv8 ? (oh[h] + ol[h] * (1.0f / kPLoScale)) * inv[h] : oh[h] * inv[h];
+        store_block(c, oh);
       }
     }
     tc_fence_before();
@@ -1080,12 +1124,12 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
 #pragma unroll
       for (int h = 0; h < kH; ++h)
         if (h == tq) { mh = m[h]; lh = lt[h]; }
-      const float lse2 = mh + __log2f(lh) - kPOff;
-      const int hh = h0 + tq;
+      float lse2 = mh + __log2f(lh) - kPOff;
+      if constexpr (L::kQL > 1) lse2 = lh > 0.0f ? lse2 : -INFINITY;
       if (slot >= 0)
-        p.part_lse[static_cast<int64_t>(slot) * kHeads + hh] = lse2;
+        p.part_lse[row0 + tq] = lse2;
       else if (p.lse != nullptr)
-        p.lse[static_cast<int64_t>(w.b) * kHeads + hh] = lse2 * kLn2;
+        p.lse[row0 + tq] = lse2 * kLn2;
     }
   }
 }
@@ -1131,7 +1175,7 @@ __global__ void __launch_bounds__(Layout<QM>::kThreads, 1) mla_stage1_kernel(con
   }
   if (warp == 0 && lane == 0) prefetch_tensormap(&p.tmap_kv);
   if (warp == 1) {
-    tmem_alloc(smem_u32(&ms->tmem_base), kTmemCols);
+    tmem_alloc(smem_u32(&ms->tmem_base), L::kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -1159,7 +1203,7 @@ __global__ void __launch_bounds__(Layout<QM>::kThreads, 1) mla_stage1_kernel(con
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, L::kTmemCols);
   }
 }
 
@@ -1170,6 +1214,7 @@ int stage1_smem_bytes(int qmode) {
     case kQBf16KvFp8: return Layout<kQBf16KvFp8>::kSmemBytes;
     case kQFp8KvBf16: return Layout<kQFp8KvBf16>::kSmemBytes;
     case kQBf16KvMx: return Layout<kQBf16KvMx>::kSmemBytes;
+    case kQFp8KvFp8x2: return Layout<kQFp8KvFp8x2>::kSmemBytes;
   }
   return -1;
 }
@@ -1191,6 +1236,7 @@ cudaError_t launch_stage1(int qmode, const Stage1Params& p, int num_ctas, cudaSt
     case kQBf16KvFp8: return launch_t<kQBf16KvFp8>(p, num_ctas, stream);
     case kQFp8KvBf16: return launch_t<kQFp8KvBf16>(p, num_ctas, stream);
     case kQBf16KvMx: return launch_t<kQBf16KvMx>(p, num_ctas, stream);
+    case kQFp8KvFp8x2: return launch_t<kQFp8KvFp8x2>(p, num_ctas, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -8,7 +8,8 @@
 // Partials with lse = -inf carry no weight; a request with no partials is
 // empty and gets out = 0, lse = -inf.
 //
-// One warp per (request, head); a lane owns 16 of the 512 dims as four
+// One warp per (request, output row: head, or query token x head); a lane
+// owns 16 of the 512 dims as four
 // float4 columns, so every partial row is read as coalesced 512-byte lines.
 // Up to four partials are loaded together with their lse values, so that a
 // request split in at most four takes one round trip to memory.
@@ -23,11 +24,11 @@ namespace mla {
 __global__ void __launch_bounds__(256) mla_stage2_kernel(const Stage2Params p) {
   const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  const int job = gw >> 4, h = gw & 15;
+  const int job = gw / p.rows, h = gw % p.rows;   // h: output row of the request
   if (job >= p.num_jobs) return;
   // The job table is plan data (not written by stage 1): read it first.
   const MergeJob J = p.jobs[job];
-  uint16_t* out = p.out + (static_cast<int64_t>(J.b) * kHeads + h) * kVDim;
+  uint16_t* out = p.out + (static_cast<int64_t>(J.b) * p.rows + h) * kVDim;
   // Launched as a programmatic dependent of stage 1: wait here until stage 1
   // has completed and its partials are visible.
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -57,7 +58,7 @@ __global__ void __launch_bounds__(256) mla_stage2_kernel(const Stage2Params p) {
   auto load = [&](int s0, int n, float (&ls)[4], float4 (&v)[4][4]) {
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const int64_t row = static_cast<int64_t>(J.first + s0 + (u < n ? u : 0)) * kHeads + h;
+      const int64_t row = static_cast<int64_t>(J.first + s0 + (u < n ? u : 0)) * p.rows + h;
       ls[u] = p.part_lse[row];
       const float4* src = reinterpret_cast<const float4*>(p.part_o + row * kVDim);
 #pragma unroll
@@ -76,7 +77,7 @@ __global__ void __launch_bounds__(256) mla_stage2_kernel(const Stage2Params p) {
     if (M != -INFINITY) add(0, J.count, ls, v);
   } else {
     for (int s = lane; s < J.count; s += 32)
-      M = fmaxf(M, p.part_lse[static_cast<int64_t>(J.first + s) * kHeads + h]);
+      M = fmaxf(M, p.part_lse[static_cast<int64_t>(J.first + s) * p.rows + h]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     if (M != -INFINITY) {
@@ -100,13 +101,13 @@ __global__ void __launch_bounds__(256) mla_stage2_kernel(const Stage2Params p) {
     reinterpret_cast<uint2*>(out)[lane + 32 * i] = v;
   }
   if (lane == 0 && p.lse != nullptr)
-    p.lse[static_cast<int64_t>(J.b) * kHeads + h] =
+    p.lse[static_cast<int64_t>(J.b) * p.rows + h] =
         wsum > 0.0f ? (M + __log2f(wsum)) * kLn2 : -INFINITY;
 }
 
 cudaError_t launch_stage2(const Stage2Params& p, cudaStream_t stream) {
   if (p.num_jobs <= 0) return cudaSuccess;
-  const int warps = p.num_jobs * kHeads;
+  const int warps = p.num_jobs * p.rows;
   // Programmatic dependent launch: the merge grid is scheduled while stage 1
   // drains, instead of after a full launch gap.
   cudaLaunchConfig_t cfg = {};

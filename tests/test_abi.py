@@ -257,3 +257,17 @@ def test_qlen_plan_rejects_bad_q_len(mla):
         with pytest.raises(mla.MlaError) as e:
             plan_q(mla, [0, 10], q_len)
         assert e.value.status == 1
+
+
+@pytest.mark.parametrize("S,sms", [(0, 152), (0, 7), (3, 152)])
+def test_qlen2_fp8_plans_whole_requests(mla, S, sms):
+    # two query tokens with fp8 q and KV share every tile: the plan covers
+    # each request's tokens once, and a partial holds 32 rows (2 x 16 heads)
+    lens = [0, 1, 2, 300, 1000, 4096, 129]
+    indptr = np.concatenate([[0], np.cumsum(lens)])
+    pl = mla.mla_decode_plan(np.asarray(indptr, np.int32), None, page_size=1, q_dtype="fp8",
+                             kv_dtype="fp8", num_splits=S, num_sms=sms, q_len=2)
+    info = pl.info()
+    assert info.batch_size == len(lens) and info.q_len == 2
+    check_partition(pl, lens)
+    assert pl.workspace_bytes >= info.num_partials * 32 * (512 + 1) * 4

@@ -285,21 +285,45 @@ def test_qlen_causal_decode(q_dtype, kv_dtype, q_len):
     check(w)
 
 
+@pytest.mark.parametrize("q_len", [2, 3])
 @pytest.mark.parametrize("num_splits,num_sms", [(3, 0), (0, 5), (0, 2)])
-def test_qlen_splits_and_few_ctas(num_splits, num_sms):
+def test_qlen_splits_and_few_ctas(num_splits, num_sms, q_len):
+    # fp8 q + fp8 KV with two query tokens runs both tokens in one pass (32 q
+    # rows per tile); three tokens run as causal prefixes
     from mla_decode_stage1_gb300 import synth
-    lengths = [700, 5, 4096, 129]
-    w = synth.make_workload(bs=4, lengths=lengths, page_size=16, q_dtype="fp8", kv_dtype="fp8",
-                            permute_pages=True, seed=49, q_len=3)
+    lengths = [700, 5, 4096, 129, 1, 2, 128]
+    w = synth.make_workload(bs=len(lengths), lengths=lengths, page_size=16, q_dtype="fp8",
+                            kv_dtype="fp8", permute_pages=True, seed=49, q_len=q_len)
     check(w, num_splits=num_splits, num_sms=num_sms)
 
 
-def test_qlen_large_batch_sampled():
+def test_qlen2_fp8_token_zero_without_kv_in_an_item():
+    # items that hold only a request's last token leave query token 0 with no
+    # token to attend to in that item (partial lse = -inf, weight 0)
+    from mla_decode_stage1_gb300 import synth
+    lengths = [129, 257, 1, 2049]
+    w = synth.make_workload(bs=4, lengths=lengths, page_size=1, q_dtype="fp8", kv_dtype="fp8",
+                            seed=51, q_len=2)
+    check(w, num_splits=2)
+    check(w, num_sms=11)
+
+
+def test_qlen2_fp8_peaked_scores():
+    # large scores: the running max moves across tiles and the lazy rescale
+    # runs on 16-row groups
+    from mla_decode_stage1_gb300 import synth
+    w = synth.make_workload(bs=3, lengths=[1500, 640, 3000], page_size=8, q_dtype="fp8",
+                            kv_dtype="fp8", permute_pages=True, seed=52, q_len=2, q_std=6.0)
+    check(w, num_sms=2)
+
+
+@pytest.mark.parametrize("q_dtype", ["bf16", "fp8"])
+def test_qlen_large_batch_sampled(q_dtype):
     # bs=64 x 8192 tokens, two query tokens, in the balanced launch the
     # planner picks (one CTA group per query token)
     _mla()
     from mla_decode_stage1_gb300 import synth
-    w = synth.make_workload(bs=64, lengths=[8192] * 64, page_size=8, q_dtype="bf16",
+    w = synth.make_workload(bs=64, lengths=[8192] * 64, page_size=8, q_dtype=q_dtype,
                             kv_dtype="fp8", permute_pages=True, seed=50, q_len=2, device="cuda")
     rng = np.random.default_rng(9)
     sel = sorted(rng.choice(w.bs, size=4, replace=False).tolist() + [0, w.bs - 1])
