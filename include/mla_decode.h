@@ -122,10 +122,12 @@ mla_status mla_decode_plan(const int32_t* kv_indptr_host, const int32_t* kv_last
  * n - q_len + 1 + t tokens (none: out = 0, lse = -inf).
  *
  * q, out and lse then hold batch_size * q_len rows, row b * q_len + t for
- * query token t of request b ([batch, q_len, 16, ...] contiguous).  The
- * balanced plan gives every query token its own group of CTAs, each group
- * balanced over all requests, so that the q_len passes over a request's KV
- * run side by side and all but one are served from L2.
+ * query token t of request b ([batch, q_len, 16, ...] contiguous).  With
+ * q_len = 2 and fp8 q and KV, both query tokens share one pass over the KV
+ * (32 q rows per tile).  Otherwise every query token is planned as its own
+ * causal prefix; the balanced plan gives each query token its own group of
+ * CTAs, balanced over all requests, so that the q_len passes over a
+ * request's KV run side by side and all but one are served from L2.
  *
  * Arguments as for mla_decode_plan, plus q_len in [1, MLA_MAX_Q_LEN].
  * Errors: as mla_decode_plan; MLA_ERR_INVALID_ARG for q_len out of range or
