@@ -222,13 +222,15 @@ mla_status mla_decode_plan_q(const int32_t* kv_indptr_host, const int32_t* kv_la
   const int qmode = qmode_of(q_dtype, kv_dtype);
   if (qmode < 0) return MLA_ERR_UNSUPPORTED;
   if (kv_indptr_host[0] < 0) return MLA_ERR_INVALID_ARG;
-  // Two query tokens with fp8 q and KV run natively: both tokens' 32 q rows
-  // share every tile (kQFp8KvFp8x2, query token t sees vis0 + t tokens).
-  // Otherwise query token t of request b is "virtual request" r = b * q_len + t
-  // (its q, out and lse row): it attends to the request's first
-  // n - q_len + 1 + t tokens, through the request's pages.
-  const bool native2 = q_len == 2 && qmode == mla::kQFp8KvFp8;
-  const int32_t qv = native2 ? 1 : q_len;          // virtual requests per request
+  // With fp8 q and KV and an even q_len, query tokens run in pairs: pair p
+  // of request b is "virtual request" r = b * q_len / 2 + p, whose 32 q rows
+  // (tokens 2p, 2p+1) share every tile (kQFp8KvFp8x2); its first token sees
+  // vis0 = n - q_len + 1 + 2p tokens, its second one more.  Otherwise query
+  // token t of request b is virtual request r = b * q_len + t (its q, out
+  // and lse row): it attends to the request's first n - q_len + 1 + t
+  // tokens.  Either way through the request's own pages.
+  const bool pairs = q_len % 2 == 0 && qmode == mla::kQFp8KvFp8;
+  const int32_t qv = pairs ? q_len / 2 : q_len;    // virtual requests per request
   const int32_t nv = batch_size * qv;
   std::vector<int32_t> len(nv), page_base(nv), npages(nv), vis0(nv, 0);
   std::vector<int64_t> tiles(nv);
@@ -245,8 +247,9 @@ mla_status mla_decode_plan_q(const int32_t* kv_indptr_host, const int32_t* kv_la
     if (n > INT32_MAX - mla::kTile) return MLA_ERR_INVALID_ARG;
     for (int32_t t = 0; t < qv; ++t) {
       const int32_t r = b * qv + t;
-      len[r] = static_cast<int32_t>(native2 ? n : std::max<int64_t>(0, n - q_len + 1 + t));
-      vis0[r] = static_cast<int32_t>(std::max<int64_t>(0, n - 1));
+      const int64_t first_seen = n - q_len + 1 + (pairs ? 2 * t : t);
+      len[r] = static_cast<int32_t>(std::max<int64_t>(0, first_seen + (pairs ? 1 : 0)));
+      vis0[r] = static_cast<int32_t>(std::max<int64_t>(0, first_seen));
       page_base[r] = kv_indptr_host[b];
       npages[r] = static_cast<int32_t>(np);
       tiles[r] = (len[r] + mla::kTile - 1) / mla::kTile;
@@ -264,13 +267,13 @@ mla_status mla_decode_plan_q(const int32_t* kv_indptr_host, const int32_t* kv_la
   if (P == nullptr) return MLA_ERR_INVALID_ARG;
   P->bs = nv;
   P->nreq = batch_size;
-  P->rows = native2 ? 2 * mla::kHeads : mla::kHeads;
+  P->rows = pairs ? 2 * mla::kHeads : mla::kHeads;
   P->q_len = q_len;
   P->page_size = page_size;
   P->num_splits = num_splits;
   P->q_dtype = q_dtype;
   P->kv_dtype = kv_dtype;
-  P->qmode = native2 ? mla::kQFp8KvFp8x2 : qmode;
+  P->qmode = pairs ? mla::kQFp8KvFp8x2 : qmode;
   P->total_tokens = total_tok;
   P->total_tiles = total_tiles;
   P->cta_indptr.assign(1, 0);
@@ -284,14 +287,14 @@ mla_status mla_decode_plan_q(const int32_t* kv_indptr_host, const int32_t* kv_la
         for (int32_t b = 0; b < batch_size; ++b) order.push_back(b * qv + t);
       plan_balanced(P, order, tiles, len, page_base, npages, G);
     } else {
-      // one group of CTAs per query token, each balanced over every request:
-      // CTA i of each group reads the same KV at about the same time, so the
-      // other q_len - 1 passes are served from L2
-      for (int32_t t = 0; t < q_len; ++t) {
+      // one group of CTAs per query token (or pair), each balanced over
+      // every request: CTA i of each group reads the same KV at about the
+      // same time, so the other passes are served from L2
+      for (int32_t t = 0; t < qv; ++t) {
         order.clear();
-        for (int32_t b = 0; b < batch_size; ++b) order.push_back(b * q_len + t);
-        const int32_t Gt = static_cast<int32_t>((static_cast<int64_t>(G) * (t + 1)) / q_len -
-                                                (static_cast<int64_t>(G) * t) / q_len);
+        for (int32_t b = 0; b < batch_size; ++b) order.push_back(b * qv + t);
+        const int32_t Gt = static_cast<int32_t>((static_cast<int64_t>(G) * (t + 1)) / qv -
+                                                (static_cast<int64_t>(G) * t) / qv);
         plan_balanced(P, order, tiles, len, page_base, npages, Gt);
       }
     }

@@ -271,3 +271,15 @@ def test_qlen2_fp8_plans_whole_requests(mla, S, sms):
     assert info.batch_size == len(lens) and info.q_len == 2
     check_partition(pl, lens)
     assert pl.workspace_bytes >= info.num_partials * 32 * (512 + 1) * 4
+
+
+def test_even_qlen_fp8_plans_pairs_of_query_tokens(mla):
+    # q_len = 4 with fp8 q and KV: pair p of request b is planned request
+    # 2b + p, covering the tokens its second query token sees
+    lens = [0, 1, 3, 4, 300, 1000]
+    indptr = np.concatenate([[0], np.cumsum(lens)])
+    pl = mla.mla_decode_plan(np.asarray(indptr, np.int32), None, page_size=1, q_dtype="fp8",
+                             kv_dtype="fp8", num_sms=20, q_len=4)
+    pair_lens = [max(0, n - 4 + 2 + 2 * p) for n in lens for p in range(2)]
+    check_partition(pl, pair_lens)
+    assert pl.info().batch_size == len(lens) and pl.info().q_len == 4

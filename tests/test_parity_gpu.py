@@ -285,11 +285,11 @@ def test_qlen_causal_decode(q_dtype, kv_dtype, q_len):
     check(w)
 
 
-@pytest.mark.parametrize("q_len", [2, 3])
+@pytest.mark.parametrize("q_len", [2, 3, 4, 6])
 @pytest.mark.parametrize("num_splits,num_sms", [(3, 0), (0, 5), (0, 2)])
 def test_qlen_splits_and_few_ctas(num_splits, num_sms, q_len):
-    # fp8 q + fp8 KV with two query tokens runs both tokens in one pass (32 q
-    # rows per tile); three tokens run as causal prefixes
+    # fp8 q + fp8 KV with an even number of query tokens runs them in pairs
+    # (32 q rows per tile); three tokens run as causal prefixes
     from mla_decode_stage1_gb300 import synth
     lengths = [700, 5, 4096, 129, 1, 2, 128]
     w = synth.make_workload(bs=len(lengths), lengths=lengths, page_size=16, q_dtype="fp8",
