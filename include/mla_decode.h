@@ -122,11 +122,11 @@ mla_status mla_decode_plan(const int32_t* kv_indptr_host, const int32_t* kv_last
  * n - q_len + 1 + t tokens (none: out = 0, lse = -inf).
  *
  * q, out and lse then hold batch_size * q_len rows, row b * q_len + t for
- * query token t of request b ([batch, q_len, 16, ...] contiguous).  With
- * q_len = 2 and fp8 q and KV, both query tokens share one pass over the KV
- * (32 q rows per tile).  Otherwise every query token is planned as its own
- * causal prefix; the balanced plan gives each query token its own group of
- * CTAs, balanced over all requests, so that the q_len passes over a
+ * query token t of request b ([batch, q_len, 16, ...] contiguous).  With an
+ * even q_len and fp8 q and KV, query tokens 2p and 2p+1 share one pass over
+ * the KV (32 q rows per tile).  Otherwise every query token is planned as its
+ * own causal prefix.  The balanced plan gives each pass (pair or token) its
+ * own group of CTAs, balanced over all requests, so that the passes over a
  * request's KV run side by side and all but one are served from L2.
  *
  * Arguments as for mla_decode_plan, plus q_len in [1, MLA_MAX_Q_LEN].
