@@ -2,7 +2,8 @@
 //
 // What it computes (kernelindex.com, amd-mixed-mla submission 668813, MXFP4
 // qh16 stage-1 kernel; submission 695854, fp8 split stage-1 kernel): for one
-// token range of one request and all 16 heads at once, the scores
+// token range of one request and all 16 heads at once (all 32 q rows of two
+// query tokens in the two-token mode), the scores
 // s = q . k^T * (1/sqrt(576)) over 576 dims, an exp2-domain online softmax,
 // and the partial output O = softmax(s) . V with V the first 512 dims of the
 // same rows, plus the log-sum-exp of the range.
@@ -14,7 +15,7 @@
 //    [64-byte column chunk][8 rows][64 B] image with the 64-byte swizzle, so
 //    a page-8 table costs 16 TMA operations per tile and an identity table 1;
 //  * QK^T runs on the 5th-generation tensor cores with the tokens as M:
-//    S^T[128 tok x 16 heads] = K[128 x 576] . Q^T, accumulated in TMEM;
+//    S^T[128 tok x 16 q rows] = K[128 x 576] . Q^T, accumulated in TMEM;
 //  * PV reuses the very same shared-memory bytes as an MN-major operand:
 //    O^T[512 x 16] += V^T[512 x 128 tok] . P^T, four M=128 blocks in TMEM;
 //  * a tcgen05.mma costs the issuing thread about the same time whatever
@@ -22,7 +23,8 @@
 //    side: warps 1 and 3 each issue half of the QK^T K-steps into their own
 //    S accumulator; warps 2 and 13 issue PV for O blocks 0-1 and 2-3 (MXFP4:
 //    warp 2 alone).  Warp 0 is the TMA producer; warps 4-11 do the softmax
-//    and the epilogue in two groups of 8 heads (one thread per token / per
+//    and the epilogue in two groups of 8 heads (two-token mode: one group
+//    per query token, 16 heads each; one thread per token / per
 //    output dim, TMEM lane = thread) and convert the first item's q; warp
 //    12 converts the q of later items (MXFP4: warps 12-15 dequantise the
 //    packed rows in place and prepare every item's q);
@@ -59,7 +61,7 @@ struct Layout {
   static constexpr bool kHiLo = (QM == kQBf16KvFp8 || kMx);         // q as two e4m3 terms
   static constexpr int kNq = kRows * (kHiLo ? 2 : 1);               // UMMA N of QK^T
   // Warps: producer, 2 QK^T issuers, PV issuer(s), two head groups of four
-  // softmax warps (8 heads each), then either a q warp (14 warps) or, for
+  // softmax warps (kH q rows each), then either a q warp (14 warps) or, for
   // MXFP4, 4 dequant warps that also prepare q (16 warps, register cap 128).
   static constexpr int kHeadGroups = 2;
   static constexpr int kH = kRows / kHeadGroups;                    // q rows per softmax thread
@@ -499,7 +501,7 @@ __device__ __forceinline__ uint2 e2m1x8_to_e4m3(uint32_t w, uint32_t lo, uint32_
 }
 
 // ----------------------------------------------------- q staging helpers
-// One bulk copy brings q of request `bb` (all 16 heads) into the staging buffer.
+// One bulk copy brings q of request `bb` (all its q rows) into the staging buffer.
 template <int QM>
 __device__ __forceinline__ void q_fetch(const Stage1Params& p, Misc* ms, uint8_t* stage, int bb) {
   using L = Layout<QM>;
@@ -798,7 +800,7 @@ __device__ void run_qprep(const Stage1Params& p, Misc* ms, uint8_t* qgen, uint8_
 }
 
 // ------------------------------------------------------ softmax / epilogue
-// Reduce kH per-thread values (heads h0..h0+kH-1) over the 128 threads of a
+// Reduce kH per-thread values (q rows h0..h0+kH-1) over the 128 threads of a
 // head group (op = max or sum).  A transpose-reduce over the lane bits
 // 16, 8, ... leaves one head per group of lanes after log2(kH) shuffle
 // stages; the four warp results meet in shared memory behind the group's
@@ -1021,7 +1023,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
           *reinterpret_cast<uint2*>(prow + ((16u + 8u * hg) ^ flip)) = make_uint2(lw[0], lw[1]);
         }
       } else {
-        // bf16: heads 0-15, 2 bytes each
+        // bf16: the 16 heads, 2 bytes each
         uint32_t bw[kH / 2];
 #pragma unroll
         for (int h = 0; h < kH; h += 2) {
