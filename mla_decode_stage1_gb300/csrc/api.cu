@@ -35,36 +35,73 @@ int qmode_of(int q_dtype, int kv_dtype) {
 }
 
 // Items of the balanced plan over the requests listed in `order`: their
-// tiles, in that order, cut into G nearly equal contiguous ranges, one per
-// CTA; the CTAs are appended to the plan.
+// tiles, in that order, cut into at most G contiguous ranges, one per CTA,
+// appended to the plan.  A range costs 2 per tile plus 1 for every item past
+// its first: an item boundary inside a CTA (an epilogue before the next
+// item's first tile) costs about half a tile period.  The smallest maximum
+// cost that G greedy ranges reach is found by bisection.
 void plan_balanced(mla_plan* P, const std::vector<int32_t>& order, const std::vector<int64_t>& tiles,
                    const std::vector<int32_t>& len, const std::vector<int32_t>& page_base,
                    const std::vector<int32_t>& npages, int32_t G) {
   int64_t T = 0;
   for (const int32_t r : order) T += tiles[r];
   if (G > T) G = static_cast<int32_t>(T);
-  P->num_ctas += G;
-  size_t k = 0;        // position in `order`
-  int64_t in_req = 0;  // tiles of request order[k] already assigned
-  for (int32_t i = 0; i < G; ++i) {
-    int64_t need = (T * (i + 1)) / G - (T * i) / G;
-    while (need > 0) {
-      while (tiles[order[k]] - in_req == 0) { ++k; in_req = 0; }
-      const int32_t b = order[k];
-      const int64_t take = std::min(need, tiles[b] - in_req);
-      WorkItem w{};
-      w.b = b;
-      w.tok_begin = static_cast<int32_t>(in_req * mla::kTile);
-      w.tok_end = static_cast<int32_t>(std::min<int64_t>((in_req + take) * mla::kTile, len[b]));
-      w.slot = 0;
-      w.page_base = page_base[b];
-      w.npages = npages[b];
-      P->items.push_back(w);
-      in_req += take;
-      need -= take;
+  if (G <= 0) return;
+  // Greedy cut under a cost cap: each range takes tiles while its cost stays
+  // within `cap` (a range always takes at least one tile).  Calls emit(k,
+  // first tile, tiles taken, range index) per item and returns the ranges.
+  auto cut = [&](int64_t cap, auto&& emit) {
+    int32_t ranges = 0;
+    size_t k = 0;
+    int64_t in_req = 0;
+    while (true) {
+      while (k < order.size() && tiles[order[k]] - in_req == 0) { ++k; in_req = 0; }
+      if (k == order.size()) break;
+      int64_t cost = 0;
+      bool any = false;
+      while (k < order.size()) {
+        const int64_t left = tiles[order[k]] - in_req;
+        if (left == 0) { ++k; in_req = 0; continue; }
+        const int64_t item = any ? 1 : 0;
+        int64_t take = (cap - cost - item) / 2;
+        if (take <= 0) {
+          if (any) break;
+          take = 1;
+        }
+        take = std::min(take, left);
+        emit(order[k], in_req, take, ranges);
+        cost += 2 * take + item;
+        any = true;
+        in_req += take;
+        if (in_req < tiles[order[k]]) break;   // cap reached inside this request
+      }
+      ++ranges;
     }
-    P->cta_indptr.push_back(static_cast<int32_t>(P->items.size()));
+    return ranges;
+  };
+  auto none = [](int32_t, int64_t, int64_t, int32_t) {};
+  int64_t lo = (2 * T + G - 1) / G, hi = 2 * T + static_cast<int64_t>(order.size());
+  while (lo < hi) {
+    const int64_t mid = (lo + hi) / 2;
+    if (cut(mid, none) <= G) hi = mid; else lo = mid + 1;
   }
+  int32_t last = -1;
+  const int32_t used = cut(lo, [&](int32_t b, int64_t t0, int64_t take, int32_t range) {
+    if (range != last) {
+      if (last >= 0) P->cta_indptr.push_back(static_cast<int32_t>(P->items.size()));
+      last = range;
+    }
+    WorkItem w{};
+    w.b = b;
+    w.tok_begin = static_cast<int32_t>(t0 * mla::kTile);
+    w.tok_end = static_cast<int32_t>(std::min<int64_t>((t0 + take) * mla::kTile, len[b]));
+    w.slot = 0;
+    w.page_base = page_base[b];
+    w.npages = npages[b];
+    P->items.push_back(w);
+  });
+  P->cta_indptr.push_back(static_cast<int32_t>(P->items.size()));
+  P->num_ctas += used;
 }
 
 // Items of the fixed-split plan: request b cut into S ranges of

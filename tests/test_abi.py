@@ -147,6 +147,28 @@ def check_partition(pl, lengths):
     return ind, items
 
 
+def plan_costs(ind, items):
+    """Per CTA: 2 per tile plus 1 per item past its first (the planner's cost)."""
+    costs = []
+    for c in range(len(ind) - 1):
+        rng = items[ind[c]:ind[c + 1]]
+        costs.append(2 * sum((t1 - t0 + 127) // 128 for _, t0, t1, _ in rng) + len(rng) - 1)
+    return costs
+
+
+def uniform_split_max_cost(lengths, G):
+    """The same cost for G equal contiguous tile ranges (the plain split)."""
+    tiles = [(n + 127) // 128 for n in lengths]
+    owner = [b for b, t in enumerate(tiles) for _ in range(t)]
+    T = len(owner)
+    G = min(G, T)
+    worst = 0
+    for i in range(G):
+        seg = owner[T * i // G: T * (i + 1) // G]
+        worst = max(worst, 2 * len(seg) + len(set(seg)) - 1)
+    return worst
+
+
 @pytest.mark.parametrize("bs,kv,ps,sms", [(256, 8192, 8, 148), (256, 8192, 8, 152), (64, 8192, 8, 152),
                                           (32, 1024, 1, 152), (4, 1024, 1, 152), (3, 100, 1, 152)])
 def test_balanced_plan_regular(mla, bs, kv, ps, sms):
@@ -155,12 +177,21 @@ def test_balanced_plan_regular(mla, bs, kv, ps, sms):
     ind, items = check_partition(pl, [kv] * bs)
     info = pl.info()
     tiles = bs * ((kv + 127) // 128)
-    assert info.num_ctas == min(sms, tiles)
-    # tiles per CTA differ by at most one
-    per = []
-    for i in range(info.num_ctas):
-        per.append(sum((t1 - t0 + 127) // 128 for _, t0, t1, _ in items[ind[i]:ind[i + 1]]))
-    assert max(per) - min(per) <= 1 and sum(per) == tiles
+    assert 1 <= info.num_ctas <= min(sms, tiles)
+    costs = plan_costs(ind, items)
+    # never worse than the plain equal split, and within a tile and an item
+    # of the ideal share
+    assert max(costs) <= uniform_split_max_cost([kv] * bs, sms)
+    assert max(costs) <= -(-2 * tiles // min(sms, tiles)) + 3
+
+
+def test_balanced_plan_avoids_straddling_when_free(mla):
+    # 32 requests of 8 tiles on 152 SMs: two tiles of one request per CTA
+    # (128 CTAs, no CTA holds two requests) beats 1-2 tiles straddling them
+    indptr = np.arange(33) * 1024
+    pl = plan(mla, indptr, ps=1, sms=152)
+    ind, items = check_partition(pl, [1024] * 32)
+    assert pl.info().num_ctas == 128 and np.all(np.diff(ind) == 1)
 
 
 def test_balanced_plan_ragged_with_last_pages(mla):
