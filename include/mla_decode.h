@@ -93,7 +93,8 @@ typedef struct {
  *   kv_dtype              MLA_DTYPE_BF16, MLA_DTYPE_FP8_E4M3 or MLA_DTYPE_MXFP4.
  *   num_splits            0: the planner balances 128-token tiles over the
  *                         CTAs (a request may be cut anywhere on a tile
- *                         boundary); S > 0: every request is cut into S
+ *                         boundary), counting each extra request a CTA
+ *                         holds as half a tile; S > 0: every request is cut into S
  *                         contiguous ranges of ceil(tiles/S) tiles, one CTA
  *                         each, as the pages' fixed-split kernels do.
  *   num_sms               CTAs of the balanced plan; 0 = the SM count of the

@@ -40,6 +40,8 @@ int qmode_of(int q_dtype, int kv_dtype) {
 // its first: an item boundary inside a CTA (an epilogue before the next
 // item's first tile) costs about half a tile period.  The smallest maximum
 // cost that G greedy ranges reach is found by bisection.
+constexpr int64_t kItemCost = 1;   // an extra item in a CTA, in half tiles
+
 void plan_balanced(mla_plan* P, const std::vector<int32_t>& order, const std::vector<int64_t>& tiles,
                    const std::vector<int32_t>& len, const std::vector<int32_t>& page_base,
                    const std::vector<int32_t>& npages, int32_t G) {
@@ -62,7 +64,7 @@ void plan_balanced(mla_plan* P, const std::vector<int32_t>& order, const std::ve
       while (k < order.size()) {
         const int64_t left = tiles[order[k]] - in_req;
         if (left == 0) { ++k; in_req = 0; continue; }
-        const int64_t item = any ? 1 : 0;
+        const int64_t item = any ? kItemCost : 0;
         int64_t take = (cap - cost - item) / 2;
         if (take <= 0) {
           if (any) break;
@@ -80,7 +82,7 @@ void plan_balanced(mla_plan* P, const std::vector<int32_t>& order, const std::ve
     return ranges;
   };
   auto none = [](int32_t, int64_t, int64_t, int32_t) {};
-  int64_t lo = (2 * T + G - 1) / G, hi = 2 * T + static_cast<int64_t>(order.size());
+  int64_t lo = (2 * T + G - 1) / G, hi = 2 * T + kItemCost * static_cast<int64_t>(order.size());
   while (lo < hi) {
     const int64_t mid = (lo + hi) / 2;
     if (cut(mid, none) <= G) hi = mid; else lo = mid + 1;
