@@ -201,6 +201,19 @@ mla_status mla_decode_run(mla_plan* plan, const void* q, const float* q_scale, c
 mla_status mla_decode_check(const mla_plan* plan, void* workspace, mla_stream_t stream);
 
 /*
+ * mla_selftest_bounded_wait -- exercises the timeout path of the pipeline
+ * waits on the GPU.  It launches one warp that waits, with the same bounded
+ * wait every decode pipeline stage uses, on an mbarrier that nothing arrives
+ * on, for limit_us microseconds (1 .. 1000000).  The wait gives up and sets
+ * the producer bit of the workspace's device error word, and the kernel
+ * returns.  The next mla_decode_check then returns MLA_ERR_DEVICE_TIMEOUT and
+ * clears the word; the CUDA context stays usable.  Enqueued on `stream`.
+ * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_WORKSPACE, MLA_ERR_CUDA.
+ */
+mla_status mla_selftest_bounded_wait(const mla_plan* plan, void* workspace, size_t workspace_bytes,
+                                     uint32_t limit_us, mla_stream_t stream);
+
+/*
  * mla_decode_run_noalloc -- mla_decode_run without a caller-provided workspace.
  *
  * The pages have no counterpart of this call.  It is for callers that cannot

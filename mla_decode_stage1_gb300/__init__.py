@@ -21,7 +21,7 @@ STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED", 3: "M
           4: "MLA_ERR_CUDA", 5: "MLA_ERR_DEVICE_TIMEOUT"}
 EXPORTS = ("mla_decode_plan", "mla_decode_plan_q", "mla_plan_workspace_size", "mla_plan_get_info", "mla_plan_get_work",
            "mla_plan_destroy", "mla_decode_run", "mla_decode_check", "mla_status_string",
-           "mla_plan_set_stage1_events", "mla_decode_run_noalloc")
+           "mla_plan_set_stage1_events", "mla_decode_run_noalloc", "mla_selftest_bounded_wait")
 
 
 class MlaError(RuntimeError):
@@ -57,11 +57,13 @@ def _load():
     lib.mla_decode_check.argtypes = [P, P, P]
     lib.mla_plan_set_stage1_events.argtypes = [P, P, P]
     lib.mla_decode_run_noalloc.argtypes = [P, P, P, P, P, P, i64, i64, P, P, P, P]
+    lib.mla_selftest_bounded_wait.argtypes = [P, P, sz, ctypes.c_uint32, P]
     lib.mla_status_string.argtypes = [ctypes.c_int]
     lib.mla_status_string.restype = ctypes.c_char_p
     for name in ("mla_decode_plan", "mla_plan_workspace_size", "mla_plan_get_info",
                  "mla_plan_get_work", "mla_decode_run", "mla_decode_check",
-                 "mla_plan_set_stage1_events", "mla_decode_run_noalloc"):
+                 "mla_plan_set_stage1_events", "mla_decode_run_noalloc", "mla_decode_plan_q",
+                 "mla_selftest_bounded_wait"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
 
@@ -209,6 +211,15 @@ def mla_decode_run_noalloc(plan: Plan, q, kv, out, *, q_scale=None, kv_scale=Non
                                          _ptr(kv_indices), _ptr(out), _ptr(lse),
                                          _stream_ptr(stream))
     _check("mla_decode_run_noalloc", status)
+
+
+def mla_selftest_bounded_wait(plan: Plan, workspace, limit_us: int = 10000, stream=None) -> None:
+    """Enqueue one warp whose bounded wait on a barrier nothing arrives on runs
+    out after limit_us: the next mla_decode_check raises MlaError with
+    MLA_ERR_DEVICE_TIMEOUT (status 5) and clears the device error word."""
+    _check("mla_selftest_bounded_wait", _lib.mla_selftest_bounded_wait(
+        plan.handle, _ptr(workspace), workspace.numel() * workspace.element_size(),
+        int(limit_us), _stream_ptr(stream)))
 
 
 def mla_decode_check(plan: Plan, workspace, stream=None) -> None:

@@ -64,17 +64,21 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // false so that the caller can leave its loop instead of hanging the GPU.
 constexpr uint64_t kWaitLimitNs = 200ull * 1000ull * 1000ull;  // 200 ms
 
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* err,
-                                          int32_t code) {
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, int32_t* err,
+                                              int32_t code, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       atomicOr(err, code);
       return false;
     }
   }
   return true;
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* err,
+                                          int32_t code) {
+  return mbar_wait_for(bar, parity, err, code, kWaitLimitNs);
 }
 
 // Global load issued exactly where it is written (an asm volatile cannot be

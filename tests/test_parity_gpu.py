@@ -360,3 +360,35 @@ def test_random_sweep(seed):
     kw, num_splits, num_sms = _random_case(seed)
     w = synth.make_workload(seed=60 + seed, **kw)
     check(w, num_splits=num_splits, num_sms=num_sms)
+
+
+# ------------------------------------------------- failure detection
+
+def test_bounded_wait_times_out_and_context_survives():
+    # a pipeline wait on a barrier nothing arrives on gives up after its
+    # limit, the device error word reports it once, and the same context and
+    # workspace then decode correctly
+    mla = _mla()
+    import time
+    from mla_decode_stage1_gb300 import synth
+    w = synth.make_workload(bs=3, lengths=[300, 0, 1000], page_size=8, q_dtype="bf16",
+                            kv_dtype="fp8", permute_pages=True, seed=53)
+    plan = mla.mla_decode_plan(w.kv_indptr, w.kv_last_page_len, page_size=8, q_dtype="bf16",
+                               kv_dtype="fp8", num_splits=2)
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
+    t0 = time.perf_counter()
+    mla.mla_selftest_bounded_wait(plan, ws, limit_us=20000)
+    with pytest.raises(mla.MlaError) as e:
+        mla.mla_decode_check(plan, ws)
+    assert e.value.status == 5                      # MLA_ERR_DEVICE_TIMEOUT
+    assert time.perf_counter() - t0 >= 0.02          # it waited out its limit
+    mla.mla_decode_check(plan, ws)                  # the word was cleared
+    d = w.to("cuda")
+    out = torch.full((w.bs, 16, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(w.bs, 16, dtype=torch.float32, device="cuda")
+    mla.mla_decode_run(plan, d.q, d.kv, out, workspace=ws, q_scale=d.q_scale,
+                       kv_scale=d.kv_scale, kv_indices=d.kv_indices, lse=lse)
+    mla.mla_decode_check(plan, ws)
+    o_ref, l_ref = oracle.mla_decode(**synth.oracle_args(w))
+    compare(out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64),
+            o_ref, l_ref, "fp8", w.lengths)
