@@ -218,9 +218,9 @@ bool make_kv_map(CUtensorMap* map, const void* kv, int kv_dtype, int64_t rows, i
 // MXFP4 pool: packed rows of 288 bytes as a 3-D tensor {32 B, row, chunk}
 // (chunk = the 64 values of two scale blocks); a box of box_rows rows lands
 // chunk-major as [chunk][row][32 B] (no swizzle).  Scale rows (stride a
-// multiple of 16, >= 32 bytes): 32-byte boxes, [row][32 B].
+// multiple of 16, >= 32 bytes): 32-byte boxes of sc_rows rows, [row][32 B].
 bool make_mx_maps(CUtensorMap* kvmap, CUtensorMap* scmap, const void* kv, const uint8_t* e8m0,
-                  int64_t e8m0_stride, int64_t rows, int box_rows) {
+                  int64_t e8m0_stride, int64_t rows, int box_rows, int sc_rows) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return false;
   const cuuint64_t dims[3] = {32, static_cast<cuuint64_t>(rows), 9};
@@ -233,7 +233,7 @@ bool make_mx_maps(CUtensorMap* kvmap, CUtensorMap* scmap, const void* kv, const 
     return false;
   const cuuint64_t sdims[2] = {32, static_cast<cuuint64_t>(rows)};
   const cuuint64_t sstr[1] = {static_cast<cuuint64_t>(e8m0_stride)};
-  const cuuint32_t sbox[2] = {32, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t sbox[2] = {32, static_cast<cuuint32_t>(sc_rows)};
   return enc(scmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(e8m0), sdims, sstr,
              sbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -429,15 +429,20 @@ mla_status mla_decode_run(mla_plan* plan, const void* q, const float* q_scale, c
   // bytes per row of the tile the UMMAs read (MXFP4 is dequantised to e4m3)
   const uint32_t row_bytes = mla::kQkDim * (plan->kv_dtype == MLA_DTYPE_BF16 ? 2 : 1);
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  // MXFP4 with the identity table: a tile's 128 scale rows are contiguous, one box
+  const bool sc_one_box = plan->kv_dtype == MLA_DTYPE_MXFP4 && kv_indices == nullptr;
+  const int sc_rows = sc_one_box ? mla::kTile : box_rows;
   if (plan->tmap_ptr != kv || plan->tmap_rows != kv_pool_rows || plan->tmap_box_rows != box_rows ||
-      plan->tmap_sc_ptr != kv_e8m0 || plan->tmap_sc_stride != kv_e8m0_row_stride) {
+      plan->tmap_sc_ptr != kv_e8m0 || plan->tmap_sc_stride != kv_e8m0_row_stride ||
+      plan->tmap_sc_rows != sc_rows) {
     const bool ok = plan->kv_dtype == MLA_DTYPE_MXFP4
                         ? make_mx_maps(&plan->tmap, &plan->tmap_sc, kv, kv_e8m0, kv_e8m0_row_stride,
-                                       kv_pool_rows, box_rows)
+                                       kv_pool_rows, box_rows, sc_rows)
                         : make_kv_map(&plan->tmap, kv, plan->kv_dtype, kv_pool_rows, box_rows);
     if (!ok) return MLA_ERR_CUDA;
     plan->tmap_sc_ptr = kv_e8m0;
     plan->tmap_sc_stride = kv_e8m0_row_stride;
+    plan->tmap_sc_rows = sc_rows;
     plan->tmap_ptr = kv;
     plan->tmap_rows = kv_pool_rows;
     plan->tmap_box_rows = box_rows;
@@ -474,6 +479,7 @@ mla_status mla_decode_run(mla_plan* plan, const void* q, const float* q_scale, c
     p.chunk_stride = static_cast<uint32_t>(box_rows) * 64u;    // [group][chunk][rows][64 B]
     p.group_stride = box_rows == 8 ? row_bytes * 8u : 512u;
     p.pool_rows = kv_pool_rows;
+    p.sc_one_box = sc_one_box ? 1 : 0;
     if (plan->ev_before != nullptr && cudaEventRecord(plan->ev_before, stream) != cudaSuccess)
       return MLA_ERR_CUDA;
     if (mla::launch_stage1(plan->qmode, p, plan->num_ctas, stream) != cudaSuccess)

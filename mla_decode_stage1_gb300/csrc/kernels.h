@@ -71,7 +71,8 @@ enum QMode : int {
 struct Stage1Params {
   CUtensorMap tmap_kv;          // KV pool as [chunk 64 B][row][64 B], 64-byte swizzle;
                                 // MXFP4: packed rows as [half 144 B][row][144 B]
-  CUtensorMap tmap_sc;          // MXFP4 only: e8m0 scale rows, 32-byte boxes
+  CUtensorMap tmap_sc;          // MXFP4 only: e8m0 scale rows, 32-byte boxes of box_rows rows
+                                // (128 rows with sc_one_box)
   const void* q;                // [bs,16,576]
   const float* q_scale;         // device [1] (fp8 q) or null
   const float* kv_scale;        // device [1] (fp8 kv) or null
@@ -91,6 +92,7 @@ struct Stage1Params {
   uint32_t chunk_stride;        // smem bytes between 64-byte column chunks of a tile
   uint32_t group_stride;        // smem bytes between 8-row groups of a tile
   int64_t pool_rows;
+  int32_t sc_one_box;           // MXFP4, identity table: a tile's 128 scale rows in one box
 };
 
 struct Stage2Params {

@@ -34,5 +34,6 @@ struct mla_plan {
   CUtensorMap tmap_sc;
   const void* tmap_sc_ptr = nullptr;
   int64_t tmap_sc_stride = -1;
+  int32_t tmap_sc_rows = -1;
   cudaEvent_t ev_before = nullptr, ev_after = nullptr;
 };

@@ -308,8 +308,10 @@ __device__ void run_producer(const Stage1Params& p, Misc* ms, uint32_t ring, int
       if (!ok) break;
     }
     if (lane == 0)
-      mbar_arrive_expect_tx(full, static_cast<uint32_t>(f.nbox) *
-                                      (L::kMx ? raw_bytes + sc_bytes : box_bytes));
+      mbar_arrive_expect_tx(full, L::kMx && p.sc_one_box
+                                      ? static_cast<uint32_t>(f.nbox) * raw_bytes + kTile * 32u
+                                      : static_cast<uint32_t>(f.nbox) *
+                                            (L::kMx ? raw_bytes + sc_bytes : box_bytes));
     // (MXFP4: the packed rows land in the upper box halves, free once PV has
     // read O blocks 2-3; the dequantisation waits for the whole slot)
     ok = __all_sync(0xffffffffu, mbar_wait(L::kMx ? smem_u32(&ms->upper_free[s]) : smem_u32(&ms->empty[s]),
@@ -317,13 +319,17 @@ __device__ void run_producer(const Stage1Params& p, Misc* ms, uint32_t ring, int
     if (!ok) break;
     if constexpr (L::kMx) {
       // packed rows of box i into the upper half of box i's e4m3 region,
-      // scale rows beside the slot
+      // scale rows beside the slot: one box per 8 rows, or (identity table)
+      // all 128 in one box, which takes 15 copy operations off every tile
       if (lane < f.nbox) {
         tma_load_3d(ring + s * L::kTileBytes + lane * box_bytes + raw_bytes, &p.tmap_kv, full, 0,
                     row, 0, pol);
-        tma_load_2d(ring + L::kScOff + s * L::kScBytes + lane * sc_bytes, &p.tmap_sc, full, 0, row,
-                    pol);
+        if (!p.sc_one_box)
+          tma_load_2d(ring + L::kScOff + s * L::kScBytes + lane * sc_bytes, &p.tmap_sc, full, 0,
+                      row, pol);
       }
+      if (p.sc_one_box && lane == 0)
+        tma_load_2d(ring + L::kScOff + s * L::kScBytes, &p.tmap_sc, full, 0, row, pol);
     } else {
       if (lane < f.nbox)
         tma_load_3d(ring + s * L::kTileBytes + lane * box_bytes, &p.tmap_kv, full, 0, row, 0, pol);
