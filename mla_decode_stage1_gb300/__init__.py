@@ -163,13 +163,14 @@ def mla_decode_plan(kv_indptr, kv_last_page_len=None, *, page_size: int, q_dtype
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    # a plain int: ctypes converts it for the void* parameter
+    return None if t is None else t.data_ptr()
 
 
 def _stream_ptr(stream):
     import torch
     s = torch.cuda.current_stream() if stream is None else stream
-    return ctypes.c_void_p(s.cuda_stream)
+    return s.cuda_stream
 
 
 def mla_decode_run(plan: Plan, q, kv, out, *, workspace, q_scale=None, kv_scale=None,
@@ -184,15 +185,16 @@ def mla_decode_run(plan: Plan, q, kv, out, *, workspace, q_scale=None, kv_scale=
     a plan for q_len query tokens, q, out and lse hold bs * q_len rows.
     """
     for name, t in (("q", q), ("kv", kv), ("out", out), ("workspace", workspace)):
-        if t is None or not t.is_cuda or not t.is_contiguous():
+        if t is None or not (t.is_cuda and t.is_contiguous()):
             raise ValueError(f"{name} must be a contiguous CUDA tensor")
-    rows = int(kv.shape[0]) if kv_pool_rows is None else int(kv_pool_rows)
-    stride = 0 if kv_e8m0 is None else int(kv_e8m0.stride(0))
-    status = _lib.mla_decode_run(plan.handle, _ptr(q), _ptr(q_scale), _ptr(kv), _ptr(kv_scale),
-                                 _ptr(kv_e8m0), stride, rows, _ptr(kv_indices), _ptr(workspace),
-                                 workspace.numel() * workspace.element_size(), _ptr(out),
+    rows = kv.shape[0] if kv_pool_rows is None else int(kv_pool_rows)
+    stride = 0 if kv_e8m0 is None else kv_e8m0.stride(0)
+    status = _lib.mla_decode_run(plan.handle, q.data_ptr(), _ptr(q_scale), kv.data_ptr(),
+                                 _ptr(kv_scale), _ptr(kv_e8m0), stride, rows, _ptr(kv_indices),
+                                 workspace.data_ptr(), workspace.nbytes, out.data_ptr(),
                                  _ptr(lse), _stream_ptr(stream))
-    _check("mla_decode_run", status)
+    if status:
+        _check("mla_decode_run", status)
 
 
 def mla_decode_run_noalloc(plan: Plan, q, kv, out, *, q_scale=None, kv_scale=None,
