@@ -392,3 +392,38 @@ def test_bounded_wait_times_out_and_context_survives():
     o_ref, l_ref = oracle.mla_decode(**synth.oracle_args(w))
     compare(out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64),
             o_ref, l_ref, "fp8", w.lengths)
+
+
+def test_decode_call_captures_in_a_cuda_graph():
+    # after one run has uploaded the plan's table into the workspace, a call
+    # only launches kernels on the stream: it can be captured in a CUDA graph
+    # and replayed (stage 2 keeps its programmatic dependency on stage 1)
+    mla = _mla()
+    from mla_decode_stage1_gb300 import synth
+    w = synth.make_workload(bs=5, lengths=[700, 1, 0, 3000, 129], page_size=8, q_dtype="fp8",
+                            kv_dtype="fp8", permute_pages=True, seed=54)
+    plan = mla.mla_decode_plan(w.kv_indptr, w.kv_last_page_len, page_size=8, q_dtype="fp8",
+                               kv_dtype="fp8", num_sms=8)
+    d = w.to("cuda")
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
+    out = torch.empty(w.bs, 16, 512, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(w.bs, 16, dtype=torch.float32, device="cuda")
+    kw = dict(workspace=ws, q_scale=d.q_scale, kv_scale=d.kv_scale, kv_indices=d.kv_indices,
+              lse=lse)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        mla.mla_decode_run(plan, d.q, d.kv, out, stream=s, **kw)      # uploads the table
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        mla.mla_decode_run(plan, d.q, d.kv, out, stream=s, **kw)
+    out.fill_(float("nan"))
+    lse.fill_(float("nan"))
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    mla.mla_decode_check(plan, ws)
+    o_ref, l_ref = oracle.mla_decode(**synth.oracle_args(w))
+    compare(out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64),
+            o_ref, l_ref, "fp8", w.lengths)
