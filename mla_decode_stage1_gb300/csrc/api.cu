@@ -141,6 +141,7 @@ void assign_slots(mla_plan* P, const std::vector<int32_t>& len) {
       first[b] = next;
       P->jobs.push_back(MergeJob{b, next, nitems[b], 0});
       next += nitems[b];
+      P->max_parts = std::max(P->max_parts, nitems[b]);
     } else if (len[b] == 0) {
       P->jobs.push_back(MergeJob{b, 0, 0, 0});
     }
@@ -496,6 +497,7 @@ mla_status mla_decode_run(mla_plan* plan, const void* q, const float* q_scale, c
     s.lse = lse;
     s.num_jobs = static_cast<int32_t>(plan->jobs.size());
     s.rows = plan->rows;
+    s.wide = plan->max_parts > 8 ? 1 : 0;
     if (mla::launch_stage2(s, stream) != cudaSuccess) return MLA_ERR_CUDA;
   }
   return MLA_OK;

@@ -98,6 +98,7 @@ struct Stage1Params {
 struct Stage2Params {
   const MergeJob* jobs;
   int32_t rows;                 // output rows per request: 16 heads x query tokens
+  int32_t wide;                 // 1: some request has many partials (one CTA per row)
   const float* part_o;
   const float* part_lse;
   uint16_t* out;

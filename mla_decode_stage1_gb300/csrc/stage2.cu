@@ -105,13 +105,93 @@ __global__ void __launch_bounds__(256) mla_stage2_kernel(const Stage2Params p) {
         wsum > 0.0f ? (M + __log2f(wsum)) * kLn2 : -INFINITY;
 }
 
+// Wide merge, for plans where a request has many partials (one long request
+// spread over every SM): one CTA of 8 warps per (request, output row, quarter
+// of the 512 dims), so that a lane owns one float4 of every partial row and a
+// warp keeps 16 partials in flight per round trip to memory.  The 256
+// threads find M = max_s lse_s together; warp w adds partials w, w + 8, ...
+// with weights 2^(lse_s - M); the eight partial sums meet in shared memory.
+constexpr int kWideSplit = 4;                 // CTAs per output row (128 dims each)
+constexpr int kWideBatch = 16;                // partials per warp per round trip
+
+__global__ void __launch_bounds__(256) mla_stage2_wide_kernel(const Stage2Params p) {
+  __shared__ float red_m[8], red_w[8];
+  __shared__ float4 red_acc[8][32];
+  const int quarter = blockIdx.x % kWideSplit, rowid = blockIdx.x / kWideSplit;
+  const int job = rowid / p.rows, h = rowid % p.rows;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (job >= p.num_jobs) return;
+  const MergeJob J = p.jobs[job];
+  const int col = quarter * 32 + lane;        // this lane's float4 column (dims 4 col ..)
+  uint16_t* out = p.out + (static_cast<int64_t>(J.b) * p.rows + h) * kVDim;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  float M = -INFINITY;
+  for (int s = tid; s < J.count; s += 256)
+    M = fmaxf(M, p.part_lse[static_cast<int64_t>(J.first + s) * p.rows + h]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if (lane == 0) red_m[warp] = M;
+  __syncthreads();
+  M = red_m[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) M = fmaxf(M, red_m[w]);
+  float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  float wsum = 0.0f;
+  if (M != -INFINITY) {
+    for (int s0 = warp; s0 < J.count; s0 += 8 * kWideBatch) {
+      float ls[kWideBatch];
+      float4 v[kWideBatch];
+#pragma unroll
+      for (int u = 0; u < kWideBatch; ++u) {
+        const int s = s0 + 8 * u;
+        const int64_t row = static_cast<int64_t>(J.first + (s < J.count ? s : s0)) * p.rows + h;
+        ls[u] = s < J.count ? p.part_lse[row] : -INFINITY;
+        v[u] = reinterpret_cast<const float4*>(p.part_o + row * kVDim)[col];
+      }
+#pragma unroll
+      for (int u = 0; u < kWideBatch; ++u) {
+        const float w = ex2(ls[u] - M);         // 0 for a missing or empty partial
+        wsum += w;
+        const bool live = w > 0.0f;
+        acc.x += live ? w * v[u].x : 0.0f;
+        acc.y += live ? w * v[u].y : 0.0f;
+        acc.z += live ? w * v[u].z : 0.0f;
+        acc.w += live ? w * v[u].w : 0.0f;
+      }
+    }
+  }
+  if (lane == 0) red_w[warp] = wsum;           // every lane added the same weights
+  red_acc[warp][lane] = acc;
+  __syncthreads();
+  if (tid < 32) {
+    float4 a = red_acc[0][tid];
+    float W = red_w[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) {
+      const float4 b = red_acc[w][tid];
+      a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+      W += red_w[w];
+    }
+    const float inv = W > 0.0f ? 1.0f / W : 0.0f;
+    const __nv_bfloat162 x = __floats2bfloat162_rn(a.x * inv, a.y * inv);
+    const __nv_bfloat162 y = __floats2bfloat162_rn(a.z * inv, a.w * inv);
+    uint2 o2;
+    o2.x = *reinterpret_cast<const uint32_t*>(&x);
+    o2.y = *reinterpret_cast<const uint32_t*>(&y);
+    reinterpret_cast<uint2*>(out)[quarter * 32 + tid] = o2;
+    if (quarter == 0 && tid == 0 && p.lse != nullptr)
+      p.lse[static_cast<int64_t>(J.b) * p.rows + h] = W > 0.0f ? (M + __log2f(W)) * kLn2 : -INFINITY;
+  }
+}
+
 cudaError_t launch_stage2(const Stage2Params& p, cudaStream_t stream) {
   if (p.num_jobs <= 0) return cudaSuccess;
   const int warps = p.num_jobs * p.rows;
+  const bool wide = p.wide != 0;
   // Programmatic dependent launch: the merge grid is scheduled while stage 1
   // drains, instead of after a full launch gap.
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((warps + 7) / 8);
+  cfg.gridDim = dim3(wide ? warps * kWideSplit : (warps + 7) / 8);
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
@@ -120,7 +200,8 @@ cudaError_t launch_stage2(const Stage2Params& p, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mla_stage2_kernel, p);
+  return wide ? cudaLaunchKernelEx(&cfg, mla_stage2_wide_kernel, p)
+              : cudaLaunchKernelEx(&cfg, mla_stage2_kernel, p);
 }
 
 }  // namespace mla

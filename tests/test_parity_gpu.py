@@ -427,3 +427,15 @@ def test_decode_call_captures_in_a_cuda_graph():
     o_ref, l_ref = oracle.mla_decode(**synth.oracle_args(w))
     compare(out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64),
             o_ref, l_ref, "fp8", w.lengths)
+
+
+@pytest.mark.parametrize("q_len", [1, 2])
+def test_many_partials_per_request_wide_merge(q_len):
+    # more than 8 partials per request: stage 2 merges with one CTA of eight
+    # warps per output row; empty requests and short ones in the same batch
+    from mla_decode_stage1_gb300 import synth
+    lengths = [5000, 0, 1, 130, 3000]
+    w = synth.make_workload(bs=len(lengths), lengths=lengths, page_size=8, q_dtype="fp8",
+                            kv_dtype="fp8", permute_pages=True, seed=55, q_len=q_len)
+    plan = check(w, num_splits=20)
+    assert plan.info().num_partials > 20
