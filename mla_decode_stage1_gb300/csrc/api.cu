@@ -497,7 +497,7 @@ mla_status mla_decode_run(mla_plan* plan, const void* q, const float* q_scale, c
     s.lse = lse;
     s.num_jobs = static_cast<int32_t>(plan->jobs.size());
     s.rows = plan->rows;
-    s.wide = plan->max_parts > 8 ? 1 : 0;
+    s.wide = plan->max_parts > 4 ? 1 : 0;   // the narrow merge takes up to 4 partials per round trip
     if (mla::launch_stage2(s, stream) != cudaSuccess) return MLA_ERR_CUDA;
   }
   return MLA_OK;

@@ -17,7 +17,7 @@ struct mla_plan {
   int32_t rows = 16;                                 // output rows per planned request (16 x tokens it holds)
   int q_dtype = 0, kv_dtype = 0, qmode = 0;
   int32_t num_ctas = 0, num_partials = 0;
-  int32_t max_parts = 0;   // most partials of one request (stage 2 goes wide above 8)
+  int32_t max_parts = 0;   // most partials of one request (stage 2 goes wide above 4)
   int64_t total_tokens = 0, total_tiles = 0;
   std::vector<int32_t> cta_indptr;
   std::vector<mla::WorkItem> items;

@@ -431,7 +431,7 @@ def test_decode_call_captures_in_a_cuda_graph():
 
 @pytest.mark.parametrize("q_len", [1, 2])
 def test_many_partials_per_request_wide_merge(q_len):
-    # more than 8 partials per request: stage 2 merges with one CTA of eight
+    # more than 4 partials per request: stage 2 merges with one CTA of eight
     # warps per output row; empty requests and short ones in the same batch
     from mla_decode_stage1_gb300 import synth
     lengths = [5000, 0, 1, 130, 3000]
