@@ -314,3 +314,55 @@ def test_even_qlen_fp8_plans_pairs_of_query_tokens(mla):
     pair_lens = [max(0, n - 4 + 2 + 2 * p) for n in lens for p in range(2)]
     check_partition(pl, pair_lens)
     assert pl.info().batch_size == len(lens) and pl.info().q_len == 4
+
+
+# ------------------------------------------------- randomized plan sweep
+
+def _random_batch(rng):
+    bs = int(rng.choice([1, 2, 5, 17, 64, 300]))
+    kind = rng.integers(0, 3)
+    if kind == 0:        # short requests, many empty
+        lens = rng.integers(0, 300, bs)
+    elif kind == 1:      # long requests
+        lens = rng.integers(1000, 20000, bs)
+    else:                # a mix with empties
+        lens = np.where(rng.random(bs) < 0.2, 0, rng.integers(1, 9000, bs))
+    return lens.astype(np.int64)
+
+
+@pytest.mark.parametrize("seed", range(120))
+def test_randomized_plans_partition_every_query_token(mla, seed):
+    """Any batch, page size, last-page layout, SM count, forced split and
+    q_len: the work table covers every planned request's visible tokens
+    exactly once, with consecutive partial slots and enough workspace.  The
+    balanced plan's most expensive CTA never costs more than with the plain
+    equal split of the tiles."""
+    rng = np.random.default_rng(1000 + seed)
+    lens = _random_batch(rng)
+    ps = int(rng.choice([1, 2, 3, 8, 16, 64, 256]))
+    npages = (lens + ps - 1) // ps
+    indptr = np.concatenate([[0], np.cumsum(npages)]).astype(np.int32)
+    use_last = ps > 1 and rng.random() < 0.7
+    last = (np.where(npages > 0, lens - (npages - 1) * ps, ps).astype(np.int32)
+            if use_last else None)
+    n = lens if use_last else npages * ps                   # tokens the plan sees
+    sms = int(rng.choice([1, 3, 17, 148, 152]))
+    S = int(rng.choice([0, 0, 0, 1, 2, 5, 32]))
+    q_len = int(rng.choice([1, 1, 2, 3, 4]))
+    qd, kd = [("bf16", "fp8"), ("fp8", "fp8"), ("bf16", "bf16"), ("bf16", "mxfp4")][rng.integers(0, 4)]
+    pl = mla.mla_decode_plan(indptr, last, page_size=ps, q_dtype=qd, kv_dtype=kd, num_splits=S,
+                             num_sms=sms, q_len=q_len)
+    info = pl.info()
+    assert info.batch_size == len(lens) and info.q_len == q_len
+    pairs = q_len % 2 == 0 and (qd, kd) == ("fp8", "fp8")
+    if pairs:
+        vlens = [max(0, int(x) - q_len + 2 + 2 * p) for x in n for p in range(q_len // 2)]
+    else:
+        vlens = virtual_lengths([int(x) for x in n], q_len)
+    ind, items = check_partition(pl, vlens)
+    if S == 0:
+        assert info.num_ctas <= sms
+    rows = 32 if pairs else 16
+    assert pl.workspace_bytes >= info.num_partials * rows * (512 + 1) * 4
+    if S == 0 and q_len == 1 and info.num_ctas > 0:
+        assert max(plan_costs(ind, items)) <= uniform_split_max_cost(vlens, sms)
