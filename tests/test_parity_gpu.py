@@ -259,6 +259,62 @@ def test_split_merge_repeated_launches_same_workspace():
     compare(o, lse, o_ref, l_ref, "fp8", w.lengths)
 
 
+@pytest.mark.parametrize("q_dtype,kv_dtype,q_len", [
+    ("bf16", "bf16", 1), ("bf16", "fp8", 1), ("fp8", "fp8", 1), ("fp8", "bf16", 1),
+    ("bf16", "mxfp4", 1), ("fp8", "fp8", 2)])
+def test_soak_interleaved_plans_are_deterministic(q_dtype, kv_dtype, q_len):
+    # 300 calls back to back on one stream, without synchronising: two plans
+    # of different batches interleaved, plan A alternating between two
+    # workspaces (its table is uploaded again on every switch).  No device
+    # wait may give up, every repeat must be bitwise identical to the plan's
+    # first result, and the first results must match the oracle.
+    mla = _mla()
+    from mla_decode_stage1_gb300 import synth
+    ps = 1 if kv_dtype == "mxfp4" else 8
+    rng = np.random.default_rng(70 + len(q_dtype) + len(kv_dtype) + q_len)
+    wa = synth.make_workload(bs=24, lengths=[int(x) for x in rng.integers(0, 3000, 24)], page_size=ps,
+                             q_dtype=q_dtype, kv_dtype=kv_dtype, permute_pages=ps > 1,
+                             q_len=q_len, seed=71)
+    wb = synth.make_workload(bs=5, lengths=[4000, 1, 0, 700, 129], page_size=ps, q_dtype=q_dtype,
+                             kv_dtype=kv_dtype, permute_pages=ps > 1, q_len=q_len, seed=72)
+    cases = []
+    for w, S in ((wa, 0), (wb, 3)):
+        plan = mla.mla_decode_plan(w.kv_indptr, w.kv_last_page_len, page_size=ps, q_dtype=q_dtype,
+                                   kv_dtype=kv_dtype, num_splits=S, q_len=q_len)
+        cases.append((w, plan, w.to("cuda")))
+    (wa, pa, da), (wb, pb, db) = cases
+    ws = [torch.empty(p.workspace_bytes, dtype=torch.uint8, device="cuda") for p in (pa, pa, pb)]
+    n_rep = 100
+    outs = {0: [], 1: [], 2: []}
+
+    def call(k, w, plan, d):
+        rows = w.bs * w.q_len
+        out = torch.empty((rows, 16, 512), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((rows, 16), dtype=torch.float32, device="cuda")
+        mla.mla_decode_run(plan, d.q, d.kv, out, workspace=ws[k], q_scale=d.q_scale,
+                           kv_scale=d.kv_scale, kv_e8m0=d.kv_e8m0, kv_indices=d.kv_indices, lse=lse)
+        outs[k].append((out, lse))
+
+    for _ in range(n_rep):
+        call(0, wa, pa, da)
+        call(2, wb, pb, db)
+        call(1, wa, pa, da)
+    torch.cuda.synchronize()
+    for k, plan in ((0, pa), (1, pa), (2, pb)):
+        mla.mla_decode_check(plan, ws[k])
+    first_a = outs[0][0]
+    for k in (0, 1, 2):
+        ref = outs[2][0] if k == 2 else first_a
+        for o, l in outs[k]:
+            assert torch.equal(o, ref[0]) and torch.equal(l, ref[1]), f"workspace {k}: result changed"
+    for w, (o, l) in ((wa, first_a), (wb, outs[2][0])):
+        o_ref, l_ref = oracle.mla_decode(**synth.oracle_args(w))
+        ql = w.q_len
+        seen = [max(0, w.lengths[b] - ql + 1 + t) for b in range(w.bs) for t in range(ql)]
+        compare(o.float().cpu().numpy().astype(np.float64), l.cpu().numpy().astype(np.float64),
+                o_ref, l_ref, w.kv_dtype, seen)
+
+
 @pytest.mark.parametrize("kv_dtype", ["fp8", "mxfp4"])
 def test_one_long_request_over_every_sm(kv_dtype):
     # one request cut into as many items as there are CTAs: stage 2 merges
