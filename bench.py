@@ -125,8 +125,96 @@ def stage1_traffic(workload):
     return float(entry["dram_bytes_per_launch"])
 
 
+class NvmlSampler:
+    """SM clock and clock-event reasons read through NVML (read only: no
+    setting is changed) about every millisecond in a thread, so that even a
+    timed region of a few milliseconds holds samples.  summary() keeps the
+    samples taken inside the window given to mark()."""
+
+    # NVML clock-event reason bits (nvml.h); the hardware power brake is a
+    # hardware slowdown too
+    REASONS = (("hw_slowdown", 0x8 | 0x80), ("hw_thermal_slowdown", 0x40),
+               ("sw_thermal_slowdown", 0x20), ("sw_power_cap", 0x4))
+    CLOCK_SM = 1
+
+    def __init__(self, index, uuid=None):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit_v2 failed")
+        self.dev = ctypes.c_void_p()
+        mx = ctypes.c_uint()
+        # the CUDA device by its UUID (NVML numbers devices on its own), else by index
+        found = uuid is not None and self.lib.nvmlDeviceGetHandleByUUID(
+            ("GPU-" + str(uuid)).encode(), ctypes.byref(self.dev)) == 0
+        if not found:
+            found = self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.dev)) == 0
+        if not found or self.lib.nvmlDeviceGetMaxClockInfo(self.dev, self.CLOCK_SM, ctypes.byref(mx)) != 0:
+            self.lib.nvmlShutdown()
+            raise OSError("NVML device query failed")
+        self.max_mhz = mx.value
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.samples, self.window, self.thread = [], None, None
+        self.stop = None
+
+    def _poll(self):
+        ct = self.ct
+        mhz, rs = ct.c_uint(), ct.c_ulonglong()
+        while not self.stop.is_set():
+            t = time.perf_counter()
+            if (self.lib.nvmlDeviceGetClockInfo(self.dev, self.CLOCK_SM, ct.byref(mhz)) == 0
+                    and self.reasons_fn(self.dev, ct.byref(rs)) == 0):
+                self.samples.append((t, mhz.value, rs.value))
+            time.sleep(0.0005)
+
+    def __enter__(self):
+        import threading
+        self.stop = threading.Event()
+        self.thread = threading.Thread(target=self._poll, daemon=True)
+        self.thread.start()
+        return self
+
+    def __exit__(self, *a):
+        self.stop.set()
+        self.thread.join(timeout=5)
+        self.lib.nvmlShutdown()
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def summary(self):
+        rows = self.samples
+        where = "whole sampling period"
+        if self.window is not None:
+            inside = [r for r in rows if self.window[0] <= r[0] <= self.window[1]]
+            if inside:
+                rows, where = inside, "timed region"
+        if not rows:
+            return None
+        sm = sorted(r[1] for r in rows)
+        reasons = sorted({name for r in rows for name, bit in self.REASONS if r[2] & bit})
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(rows), "source": "nvml", "window": where}
+
+
+def clock_sampler(index):
+    """The NVML sampler where the driver library loads, else nvidia-smi."""
+    try:
+        import torch
+        uuid = getattr(torch.cuda.get_device_properties(index), "uuid", None)
+    except Exception:
+        uuid = None
+    try:
+        return NvmlSampler(index, uuid)
+    except (OSError, AttributeError):
+        return ClockSampler(index)
+
+
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling during the timed region."""
+    """nvidia-smi clock / throttle sampling (100 ms interval) around the
+    timed region; the fallback when NVML cannot be loaded."""
 
     def __init__(self, index):
         self.index = index
@@ -156,6 +244,9 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
+    def mark(self, t0, t1):
+        pass
+
     def summary(self):
         if self.path is None or not os.path.exists(self.path):
             return None
@@ -175,7 +266,7 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i, v in enumerate(r[2]) if v.lower() == "active"})
         return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": rows[0][1], "reasons": reasons,
-                "samples": len(rows)}
+                "samples": len(rows), "source": "nvidia-smi", "window": "around the timed region"}
 
 
 def cpu_baseline(w, target_s=8.0):
@@ -297,11 +388,11 @@ def main():
     for a, b in ev_s1:   # torch creates the CUDA event on first record
         a.record(stream)
         b.record(stream)
-    with ClockSampler(local) as clk:
+    with clock_sampler(local) as clk:
         if dist is not None:
             dist.barrier()
         torch.cuda.synchronize()
-        t_wall = time.perf_counter()
+        t_start = time.perf_counter()
         for i in range(K):
             if flush:
                 scratch.fill_(1)
@@ -309,7 +400,9 @@ def main():
             step()
             ev[i][1].record(stream)
         torch.cuda.synchronize()
-        t_wall = time.perf_counter() - t_wall
+        t_end = time.perf_counter()
+        clk.mark(t_start, t_end)
+        t_wall = t_end - t_start
         if dist is not None:
             dist.barrier()
         # second pass: the stage-1 kernel alone, between events the library

@@ -59,3 +59,26 @@ def test_two_gloo_ranks_take_max_time_and_sum_work():
 def test_single_process_reduction_is_identity():
     assert bench.reduce_over_ranks(None, [1.5, 2.5], [7]) == ([1.5, 2.5], [7.0])
     assert bench.rank_seed(4, 0) == 4
+
+
+def test_nvml_clock_samples_are_kept_from_the_timed_window_only():
+    # the sampler's summary (no NVML call: the samples are injected) keeps the
+    # samples inside the timed window and decodes NVML's clock-event bits
+    s = bench.NvmlSampler.__new__(bench.NvmlSampler)
+    s.max_mhz = 2070
+    s.samples = [(0.5, 900, 0x1),           # idle, before the window
+                 (1.0, 2070, 0x4),          # sw power cap
+                 (1.2, 2040, 0x0),
+                 (1.5, 2070, 0x40),         # hw thermal slowdown
+                 (3.0, 500, 0x8 | 0x20)]    # after the window
+    s.window = (0.9, 2.0)
+    got = s.summary()
+    assert got["samples"] == 3 and got["window"] == "timed region"
+    assert got["sm_mhz"] == 2070 and got["sm_max_mhz"] == 2070
+    assert got["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
+    # a window that no sample falls in reports the whole sampling period
+    s.window = (10.0, 11.0)
+    got = s.summary()
+    assert got["samples"] == 5 and got["window"] == "whole sampling period"
+    assert got["reasons"] == ["hw_slowdown", "hw_thermal_slowdown", "sw_power_cap",
+                              "sw_thermal_slowdown"]
