@@ -82,3 +82,29 @@ def test_nvml_clock_samples_are_kept_from_the_timed_window_only():
     assert got["samples"] == 5 and got["window"] == "whole sampling period"
     assert got["reasons"] == ["hw_slowdown", "hw_thermal_slowdown", "sw_power_cap",
                               "sw_thermal_slowdown"]
+
+
+def test_reference_arm_prints_its_json_line():
+    # `bench.py --impl reference` (the fp64 oracle on the host cores) needs no
+    # GPU: one JSON line with the bench contract's keys and the reference
+    # arm's own (impl, cpu_baseline, an e2e with no copies)
+    import json
+    import subprocess
+    import sys
+    import __graft_entry__
+    __graft_entry__._builder().build()          # the package loads its library on import
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                        "--config", "bs4_kv1024_bf16", "--steps", "1", "--warmup", "0"],
+                       capture_output=True, text=True, timeout=300, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    d = json.loads(lines[-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
+    assert d["config"]["workload"] == "bs4_kv1024_bf16" and d["steps"] == 1
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
