@@ -82,7 +82,28 @@ void plan_balanced(mla_plan* P, const std::vector<int32_t>& order, const std::ve
     return ranges;
   };
   auto none = [](int32_t, int64_t, int64_t, int32_t) {};
-  int64_t lo = (2 * T + G - 1) / G, hi = 2 * T + kItemCost * static_cast<int64_t>(order.size());
+  // Bisection for the smallest cap whose greedy cut needs at most G ranges.
+  // Upper bound: the largest cost among the G ranges of the plain equal split
+  // of the tiles.  That split meets its own largest cost with G ranges, and a
+  // greedy cut under a cap needs the fewest ranges of any contiguous cut, so
+  // the bound is feasible and the search spans a few units, not 2T.
+  std::vector<int64_t> cum(order.size() + 1, 0);   // tiles before order[k]
+  std::vector<int32_t> nz(order.size() + 1, 0);    // requests with tiles before order[k]
+  for (size_t k = 0; k < order.size(); ++k) {
+    cum[k + 1] = cum[k] + tiles[order[k]];
+    nz[k + 1] = nz[k] + (tiles[order[k]] > 0 ? 1 : 0);
+  }
+  auto holder = [&](int64_t x) {                   // the request holding tile x
+    return static_cast<size_t>(std::upper_bound(cum.begin(), cum.end(), x) - cum.begin()) - 1;
+  };
+  int64_t hi = 2;
+  for (int32_t i = 0; i < G; ++i) {
+    const int64_t a = T * i / G, b = T * (i + 1) / G;
+    if (b <= a) continue;
+    const int64_t items = nz[holder(b - 1) + 1] - nz[holder(a)];
+    hi = std::max(hi, 2 * (b - a) + kItemCost * (items - 1));
+  }
+  int64_t lo = std::min<int64_t>((2 * T + G - 1) / G, hi);
   while (lo < hi) {
     const int64_t mid = (lo + hi) / 2;
     if (cut(mid, none) <= G) hi = mid; else lo = mid + 1;
