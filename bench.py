@@ -12,7 +12,11 @@ own batch of the same shape (batch-sharded replicas, no collective on the
 data path); timing is the max over ranks.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--config NAME] [--no-e2e] [--no-cpu-baseline]
+                  [--config NAME] [--no-e2e] [--no-cpu-baseline] [--no-per-config]
+
+The line's `value` is the configuration named by --config (default: the
+headline shape); `per_config` adds every configuration of the suite, each
+timed the same way in the same run with its own clock record.
 """
 from __future__ import annotations
 
@@ -48,6 +52,11 @@ def parse():
                     help="override the batch size of the configuration (profiling runs)")
     ap.add_argument("--q-len", type=int, default=1,
                     help="query tokens per request (causal over the last q_len positions)")
+    ap.add_argument("--per-config", dest="per_config", action="store_true", default=True,
+                    help="also measure every other configuration of the suite (default)")
+    ap.add_argument("--no-per-config", dest="per_config", action="store_false")
+    ap.add_argument("--per-config-steps", type=int, default=50,
+                    help="timed steps of each other configuration")
     return ap.parse_args()
 
 
@@ -89,7 +98,7 @@ def aggregate_gbs(total_bytes, ms):
 
 
 def config_meta(name, w):
-    from mla_decode_stage1_gb300 import synth
+    import workloads as synth
     c = synth.CONFIGS[name]
     return {"workload": name, "bs": w.bs,
             "kv_len": c["kv_len"] if c["kv_len"] is not None else "U[512,8192]",
@@ -273,7 +282,7 @@ def cpu_baseline(w, target_s=8.0):
     """The fp64 oracle, as it stands, on the host cores over a bounded sample
     of the workload's requests.  Returns (GB/s, cores, sample description)."""
     import oracle
-    from mla_decode_stage1_gb300 import synth
+    import workloads as synth
     cores = os.cpu_count() or 1
     n = max(1, min(w.bs, cores))
     args = synth.oracle_args(w)
@@ -300,7 +309,7 @@ def run_reference(args, world, rank):
     bounded sample of the same workload (rank 0 only)."""
     if rank != 0:
         return
-    from mla_decode_stage1_gb300 import synth
+    import workloads as synth
     w = synth.make_config(args.config, device="cpu")
     import oracle
     oargs = synth.oracle_args(w)
@@ -326,6 +335,112 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def build_workload(name, rank, dev, bs_override=0, q_len=1):
+    """The seeded workload of configuration `name` for this rank, on `dev`."""
+    import workloads as synth
+    c = synth.CONFIGS[name]
+    lengths = synth.config_lengths(name)
+    if bs_override:
+        lengths = (lengths * ((bs_override + len(lengths) - 1) // len(lengths)))[:bs_override]
+    return synth.make_workload(bs=len(lengths), lengths=lengths, page_size=c["page_size"],
+                               q_dtype=c["q_dtype"], kv_dtype=c["kv_dtype"],
+                               permute_pages=c["permute_pages"], seed=rank_seed(c["seed"], rank),
+                               device=dev, name=name, q_len=q_len)
+
+
+class Decoder:
+    """One configuration made ready to decode: its plan, workspace, outputs
+    and (for inputs smaller than twice the L2) the buffer that flushes L2."""
+
+    def __init__(self, mla, w, dev):
+        import torch
+        self.mla, self.w, self.d = mla, w, w.to(dev)
+        self.plan = mla.mla_decode_plan(w.kv_indptr, w.kv_last_page_len, page_size=w.page_size,
+                                        q_dtype=w.q_dtype, kv_dtype=w.kv_dtype, q_len=w.q_len)
+        self.info = self.plan.info()
+        self.ws = torch.empty(max(self.plan.workspace_bytes, 256), dtype=torch.uint8, device=dev)
+        self.out = torch.empty(w.bs * w.q_len, 16, 512, dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty(w.bs * w.q_len, 16, dtype=torch.float32, device=dev)
+        self.alg_bytes = w.algorithmic_bytes()
+        self.kv_bytes = w.total_tokens() * w.kv_bytes_per_token()
+        self.flush = self.kv_bytes < 2 * L2_BYTES
+        self.scratch = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if self.flush else None
+
+    def step(self, stream=None):
+        d = self.d
+        self.mla.mla_decode_run(self.plan, d.q, d.kv, self.out, workspace=self.ws, q_scale=d.q_scale,
+                                kv_scale=d.kv_scale, kv_e8m0=d.kv_e8m0, kv_indices=d.kv_indices,
+                                lse=self.lse, stream=stream)
+
+    def measure(self, K, warmup, dist, local):
+        """W untimed steps, then K steps timed with CUDA events on the
+        launching stream (L2 flushed before each step when the inputs fit
+        in it), bracketed by a barrier and a synchronize; then K more steps
+        with events the library records around the stage-1 launch alone.
+        Returns (ms per step, stage-1 ms, clocks, wall seconds), the times
+        already the max over ranks."""
+        import torch
+        stream = torch.cuda.current_stream()
+        for _ in range(max(3, warmup)):
+            if self.flush:
+                self.scratch.fill_(1)
+            self.step()
+        torch.cuda.synchronize()
+        self.mla.mla_decode_check(self.plan, self.ws)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)]
+        ev_s1 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(K)]
+        for a, b in ev_s1:   # torch creates the CUDA event on first record
+            a.record(stream)
+            b.record(stream)
+        with clock_sampler(local) as clk:
+            if dist is not None:
+                dist.barrier()
+            torch.cuda.synchronize()
+            t_start = time.perf_counter()
+            for i in range(K):
+                if self.flush:
+                    self.scratch.fill_(1)
+                ev[i][0].record(stream)
+                self.step()
+                ev[i][1].record(stream)
+            torch.cuda.synchronize()
+            t_end = time.perf_counter()
+            clk.mark(t_start, t_end)
+            if dist is not None:
+                dist.barrier()
+            # second pass: the stage-1 kernel alone, between events the library
+            # records around its launch (kept out of the headline loop because an
+            # event between the two kernels would serialise their launches)
+            for i in range(K):
+                if self.flush:
+                    self.scratch.fill_(1)
+                self.plan.set_stage1_events(*ev_s1[i])
+                self.step()
+            torch.cuda.synchronize()
+        self.plan.set_stage1_events(None, None)
+        self.mla.mla_decode_check(self.plan, self.ws)
+        step_ms = sum(a.elapsed_time(b) for a, b in ev) / K
+        s1_ms = sum(a.elapsed_time(b) for a, b in ev_s1) / K
+        (step_ms, s1_ms), _ = reduce_over_ranks(dist, [step_ms, s1_ms], [],
+                                                device=torch.device("cuda", local))
+        return step_ms, s1_ms, clk.summary(), t_end - t_start
+
+
+def config_entry(dec, step_ms, s1_ms, clocks, total_bytes, peak):
+    """The per-configuration figures of the bench line."""
+    gbs = aggregate_gbs(total_bytes, step_ms)
+    s1 = dec.alg_bytes / (s1_ms * 1e-3) / 1e9
+    return {"us_per_call": step_ms * 1e3, "GBps": gbs,
+            "pct_of_8TBps": 100.0 * (dec.alg_bytes / (step_ms * 1e-3) / 1e9) / NOMINAL_HBM_GBS,
+            "stage1_us": s1_ms * 1e3, "stage1_GBps": s1, "stage1_frac": s1 / peak,
+            "algorithmic_bytes": dec.alg_bytes, "num_ctas": dec.info.num_ctas,
+            "num_partials": dec.info.num_partials,
+            "l2": "flushed between steps (2x L2 write)" if dec.flush else "inputs larger than L2",
+            "clocks": clocks}
+
+
 def main():
     args = parse()
     world, rank, local = dist_env()
@@ -335,7 +450,7 @@ def main():
 
     import torch
     import mla_decode_stage1_gb300 as mla
-    from mla_decode_stage1_gb300 import synth
+    import workloads as synth
 
     dist = None
     if world > 1:
@@ -344,90 +459,29 @@ def main():
         dist.init_process_group("nccl")
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    peak, peak_kind = load_peaks()
 
     # every rank owns one batch of the configured shape (weak scaling)
-    c = synth.CONFIGS[args.config]
-    lengths = synth.config_lengths(args.config)
-    if args.bs:
-        lengths = (lengths * ((args.bs + len(lengths) - 1) // len(lengths)))[: args.bs]
-    w = synth.make_workload(bs=len(lengths), lengths=lengths,
-                            page_size=c["page_size"], q_dtype=c["q_dtype"], kv_dtype=c["kv_dtype"],
-                            permute_pages=c["permute_pages"], seed=rank_seed(c["seed"], rank),
-                            device=dev, name=args.config, q_len=args.q_len)
-    d = w.to(dev)
+    w = build_workload(args.config, rank, dev, args.bs, args.q_len)
+    dec = Decoder(mla, w, dev)
     torch.cuda.empty_cache()
-    plan = mla.mla_decode_plan(w.kv_indptr, w.kv_last_page_len, page_size=w.page_size,
-                               q_dtype=w.q_dtype, kv_dtype=w.kv_dtype, q_len=w.q_len)
-    info = plan.info()
-    ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=dev)
-    out = torch.empty(w.bs * w.q_len, 16, 512, dtype=torch.bfloat16, device=dev)
-    lse = torch.empty(w.bs * w.q_len, 16, dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    kw = dict(workspace=ws, q_scale=d.q_scale, kv_scale=d.kv_scale, kv_e8m0=d.kv_e8m0,
-              kv_indices=d.kv_indices, lse=lse)
-    alg_bytes = w.algorithmic_bytes()
-    kv_bytes = w.total_tokens() * w.kv_bytes_per_token()
-    flush = kv_bytes < 2 * L2_BYTES
-    scratch = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if flush else None
-
-    def step():
-        mla.mla_decode_run(plan, d.q, d.kv, out, **kw)
-
-    for _ in range(max(3, args.warmup)):
-        if flush:
-            scratch.fill_(1)
-        step()
-    torch.cuda.synchronize()
-    mla.mla_decode_check(plan, ws)
-
+    info, alg_bytes = dec.info, dec.alg_bytes
+    meta = dict(config_meta(args.config, w),
+                l2="flushed between steps (2x L2 write)" if dec.flush else
+                f"inputs larger than L2 ({dec.kv_bytes/1e9:.2f} GB KV)",
+                algorithmic_bytes=alg_bytes, num_ctas=info.num_ctas,
+                num_partials=info.num_partials)
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(K)]
-    ev_s1 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-             for _ in range(K)]
-    for a, b in ev_s1:   # torch creates the CUDA event on first record
-        a.record(stream)
-        b.record(stream)
-    with clock_sampler(local) as clk:
-        if dist is not None:
-            dist.barrier()
-        torch.cuda.synchronize()
-        t_start = time.perf_counter()
-        for i in range(K):
-            if flush:
-                scratch.fill_(1)
-            ev[i][0].record(stream)
-            step()
-            ev[i][1].record(stream)
-        torch.cuda.synchronize()
-        t_end = time.perf_counter()
-        clk.mark(t_start, t_end)
-        t_wall = t_end - t_start
-        if dist is not None:
-            dist.barrier()
-        # second pass: the stage-1 kernel alone, between events the library
-        # records around its launch (kept out of the headline loop because an
-        # event between the two kernels would serialise their launches)
-        for i in range(K):
-            if flush:
-                scratch.fill_(1)
-            plan.set_stage1_events(*ev_s1[i])
-            step()
-        torch.cuda.synchronize()
-    plan.set_stage1_events(None, None)
-    mla.mla_decode_check(plan, ws)
-    step_ms = sum(a.elapsed_time(b) for a, b in ev) / K
-    s1_ms = sum(a.elapsed_time(b) for a, b in ev_s1) / K
-    # the job's time is the slowest rank's; its work is every rank's batch
-    (step_ms, s1_ms), (total_bytes,) = reduce_over_ranks(dist, [step_ms, s1_ms], [alg_bytes],
-                                                         device=dev)
-    clocks = clk.summary()
+    step_ms, s1_ms, clocks, t_wall = dec.measure(K, args.warmup, dist, local)
+    (total_bytes,) = reduce_over_ranks(dist, [], [alg_bytes], device=dev)[1]
 
     # end to end through the public API: pinned host inputs -> device, decode,
     # output + lse -> pinned host, every step.  Inputs are double-buffered on
     # the device: step i+1's copy (on its own stream) overlaps step i's decode.
     e2e = None
     if not args.no_e2e:
+        d, plan, out, lse, ws = dec.d, dec.plan, dec.out, dec.lse, dec.ws
+        stream = torch.cuda.current_stream(dev)
         host = {k: (None if v is None else v.cpu().pin_memory())
                 for k, v in (("q", d.q), ("kv", d.kv), ("q_scale", d.q_scale),
                              ("kv_scale", d.kv_scale), ("kv_e8m0", d.kv_e8m0),
@@ -478,30 +532,50 @@ def main():
         e2e = {"value": aggregate_gbs(total_bytes, e2e_ms), "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                "steps": E, "overlap": "double-buffered inputs: a step's copy overlaps the previous decode"}
-        del dev_in, host
+        del dev_in, host, d, plan, out, lse, ws
+
+    # every other configuration of the suite, measured the same way in the
+    # same run (the headline configuration's entry is the measurement above)
+    per_config = None
+    if args.per_config and not args.bs and args.q_len == 1:
+        per_config = {args.config: config_entry(dec, step_ms, s1_ms, clocks, total_bytes, peak)}
+        w_cpu = w.to("cpu") if rank == 0 and not args.no_cpu_baseline else None
+        del dec, w
+        torch.cuda.empty_cache()
+        for name in synth.CONFIGS:
+            if name == args.config:
+                continue
+            other = Decoder(mla, build_workload(name, rank, dev), dev)
+            o_ms, o_s1, o_clk, _ = other.measure(min(K, args.per_config_steps), args.warmup,
+                                                 dist, local)
+            (o_total,) = reduce_over_ranks(dist, [], [other.alg_bytes], device=dev)[1]
+            per_config[name] = config_entry(other, o_ms, o_s1, o_clk, o_total, peak)
+            del other
+            torch.cuda.empty_cache()
+        per_config = {name: per_config[name] for name in synth.CONFIGS}
+    else:
+        w_cpu = w.to("cpu") if rank == 0 and not args.no_cpu_baseline else None
 
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
         return
 
-    peak, peak_kind = load_peaks()
     achieved = alg_bytes / (s1_ms * 1e-3) / 1e9
     # the committed DRAM counts are for the configuration as named
     traffic = stage1_traffic(args.config) if not args.bs and args.q_len == 1 else None
     gbs = aggregate_gbs(total_bytes, step_ms)
+    cfg = synth.CONFIGS[args.config]
     line = {
         "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": max(3, args.warmup), "ms_per_step": step_ms, "us_per_call": step_ms * 1e3,
         "pct_of_8TBps": 100.0 * (alg_bytes / (step_ms * 1e-3) / 1e9) / NOMINAL_HBM_GBS,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": w.kv_dtype if w.q_dtype == w.kv_dtype else f"{w.q_dtype}q/{w.kv_dtype}kv",
-        "data": "synthetic: seeded N(0,1) q and KV, per-tensor e4m3 quantisation (amax/448)",
-        "config": dict(config_meta(args.config, w),
-                       l2="flushed between steps (2x L2 write)" if flush else
-                       f"inputs larger than L2 ({kv_bytes/1e9:.2f} GB KV)",
-                       algorithmic_bytes=alg_bytes, num_ctas=info.num_ctas,
-                       num_partials=info.num_partials),
+        "dtype": cfg["kv_dtype"] if cfg["q_dtype"] == cfg["kv_dtype"]
+        else f"{cfg['q_dtype']}q/{cfg['kv_dtype']}kv",
+        "data": "synthetic: seeded N(0,1) q and KV, per-tensor e4m3 quantisation (amax/448), "
+                "MXFP4 per the OCP MX rule",
+        "config": meta,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind, "traffic": traffic,
                      "kernel": "mla_stage1_kernel", "stage1_us": s1_ms * 1e3},
@@ -511,9 +585,11 @@ def main():
     }
     if e2e is not None:
         line["e2e"] = e2e
-    if not args.no_cpu_baseline:
+    if per_config is not None:
+        line["per_config"] = per_config
+    if w_cpu is not None:
         try:
-            v, cores, sample = cpu_baseline(w.to("cpu"))
+            v, cores, sample = cpu_baseline(w_cpu)
             line["cpu_baseline"] = {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle",
                                     "sample": sample}
         except Exception as e:  # the oracle is optional for the GPU number itself

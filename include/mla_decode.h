@@ -25,6 +25,9 @@
  *   - Pointers named *_host are host memory; every other data pointer is
  *     device memory owned by the caller.  The plan object is owned by the
  *     library and released with mla_plan_destroy.
+ *   - A plan is not thread-safe: mla_decode_run updates caches inside it
+ *     (tensor maps, which workspace holds its table), so one plan must not
+ *     be used by two host threads at the same time.  Different plans may.
  */
 #ifndef MLA_DECODE_H_
 #define MLA_DECODE_H_
@@ -42,7 +45,8 @@ typedef enum {
   MLA_OK = 0,
   MLA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer, bad indptr */
   MLA_ERR_UNSUPPORTED = 2,   /* valid but not implemented combination (dtype / page size) */
-  MLA_ERR_WORKSPACE = 3,     /* workspace smaller than mla_plan_workspace_size() */
+  MLA_ERR_WORKSPACE = 3,     /* workspace smaller than mla_plan_workspace_size(), or (from
+                                mla_decode_check) holding another plan's table */
   MLA_ERR_CUDA = 4,          /* a CUDA runtime / driver call failed */
   MLA_ERR_DEVICE_TIMEOUT = 5 /* a device-side pipeline wait gave up (see mla_decode_check) */
 } mla_status;
@@ -169,18 +173,27 @@ void mla_plan_destroy(mla_plan* plan);
  *              p*page_size + r.  16-byte aligned.
  *   kv_scale   device fp32 [1]; required for e4m3 KV, ignored otherwise.
  *   kv_e8m0, kv_e8m0_row_stride
- *              MXFP4 only: e8m0 scale rows (>= 18 bytes each, row stride in
- *              bytes); NULL / ignored for other KV types.
+ *              MXFP4 only: e8m0 scale rows, 18 bytes used per row (the
+ *              pages' [total_kv, 18] layout), row stride in bytes: even and
+ *              >= 18, base 2-byte aligned (MLA_ERR_INVALID_ARG below 18,
+ *              MLA_ERR_UNSUPPORTED if odd).  NULL / ignored for other KV types.
  *   kv_pool_rows  number of rows in the KV pool (bounds every access).
  *   kv_indices device int32 page table, indexed from kv_indptr; NULL = the
- *              identity table (request b's pages are kv_indptr[b]..).
- *              Every entry must be a page inside the pool.
+ *              identity table (request b's pages are kv_indptr[b]..; they
+ *              must all lie inside the pool, else MLA_ERR_INVALID_ARG).
+ *              Every entry must be a page inside the pool: an entry outside
+ *              it is read as page 0 and reported by mla_decode_check.
  *   workspace, workspace_bytes
  *              device scratch of at least mla_plan_workspace_size() bytes,
  *              256-byte aligned.  The work table is copied into it on the
  *              first run with a given workspace pointer (one host-to-device
  *              copy on `stream`); afterwards runs only launch kernels.  A
- *              workspace belongs to one plan.
+ *              workspace belongs to one plan.  If the memory at that address
+ *              was freed and reused for another plan's workspace (a caching
+ *              allocator hands out the same address again), the kernels find
+ *              the other plan's stamp in it, write nothing, and the next
+ *              mla_decode_check returns MLA_ERR_WORKSPACE; the plan then
+ *              uploads its table again on its next run.
  *   out        [batch,16,512] bf16, 16-byte aligned.
  *   lse        [batch,16] fp32 natural-log LSE of the scaled scores, or NULL.
  *              Empty requests give out = 0 and lse = -inf.
@@ -195,8 +208,19 @@ mla_status mla_decode_run(mla_plan* plan, const void* q, const float* q_scale, c
 
 /*
  * Synchronises `stream`, reads the workspace's device error word and clears
- * it.  Returns MLA_OK, MLA_ERR_DEVICE_TIMEOUT if a kernel's bounded
- * pipeline wait gave up since the last check, or MLA_ERR_CUDA.
+ * it.  Returns
+ *   MLA_OK                  nothing went wrong since the last check;
+ *   MLA_ERR_DEVICE_TIMEOUT  a kernel's bounded pipeline wait gave up;
+ *   MLA_ERR_INVALID_ARG     a page-table entry pointed outside the pool (that
+ *                           entry was read as page 0, so the outputs of its
+ *                           request are wrong; nothing outside the pool was
+ *                           touched);
+ *   MLA_ERR_WORKSPACE       the workspace held another plan's table, so the
+ *                           run wrote no output (see mla_decode_run);
+ *   MLA_ERR_CUDA            a CUDA call failed.
+ * workspace NULL checks the library's own array used by
+ * mla_decode_run_noalloc on the current device instead (errors of a
+ * no-allocation call are readable until the next such call on the device).
  */
 mla_status mla_decode_check(const mla_plan* plan, void* workspace, mla_stream_t stream);
 
@@ -230,6 +254,9 @@ mla_status mla_selftest_bounded_wait(const mla_plan* plan, void* workspace, size
  *   - Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
  *   - Every call copies its plan's work table into the array (one
  *     host-to-device copy on `stream`), which also clears the error word.
+ *   - Device-side errors of a call (a bounded wait that gave up, a page
+ *     outside the pool) are read with mla_decode_check(plan, NULL, stream)
+ *     before the next call on the device clears them.
  *   - All calls share the one array: calls that overlap on the GPU (other
  *     streams, other threads) race and corrupt each other; order them.
  * Errors: as mla_decode_run, plus MLA_ERR_WORKSPACE for an oversized plan

@@ -224,8 +224,12 @@ def mla_selftest_bounded_wait(plan: Plan, workspace, limit_us: int = 10000, stre
         int(limit_us), _stream_ptr(stream)))
 
 
-def mla_decode_check(plan: Plan, workspace, stream=None) -> None:
-    """Synchronise and raise MlaError if a device-side wait gave up."""
+def mla_decode_check(plan: Plan, workspace=None, stream=None) -> None:
+    """Synchronise, read and clear the workspace's device error word, and
+    raise MlaError if it was set: status 5 (a device-side wait gave up), 1 (a
+    page-table entry outside the pool), 3 (the workspace held another plan's
+    table; nothing was written).  workspace=None checks the library's own
+    array that mla_decode_run_noalloc uses."""
     _check("mla_decode_check", _lib.mla_decode_check(plan.handle, _ptr(workspace),
                                                      _stream_ptr(stream)))
 

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
+#include <chrono>
 #include <cstdint>
 #include <cstring>
 #include <new>
@@ -172,10 +174,21 @@ void assign_slots(mla_plan* P, const std::vector<int32_t>& len) {
   P->num_partials = next;
 }
 
+// A process-wide unique stamp per plan.  The first value mixes the clock in,
+// so that plans of two runs of a program do not share stamps either.
+uint64_t next_stamp() {
+  static std::atomic<uint64_t> counter{
+      (static_cast<uint64_t>(
+           std::chrono::steady_clock::now().time_since_epoch().count()) * 0x9E3779B97F4A7C15ull) |
+      1ull};
+  return counter.fetch_add(0x9E3779B97F4A7C15ull * 2ull);
+}
+
 void layout_workspace(mla_plan* P) {
   size_t off = 0;
   P->off_err = off;
-  off = align256(off + 16);
+  static_assert(sizeof(mla::WsHeader) == 16, "workspace header");
+  off = align256(off + sizeof(mla::WsHeader));
   P->off_indptr = off;                                       // CtaHead per CTA
   off = align256(off + sizeof(CtaHead) * (P->cta_indptr.size() - 1));
   P->off_items = off;
@@ -188,10 +201,15 @@ void layout_workspace(mla_plan* P) {
   off = align256(off + sizeof(float) * static_cast<size_t>(P->num_partials) * P->rows);
   P->ws_bytes = std::max<size_t>(off, 256);
   P->table.assign(P->off_part_o, 0);
+  P->stamp = next_stamp();
+  mla::WsHeader hdr{};
+  hdr.stamp = P->stamp;
+  std::memcpy(P->table.data() + P->off_err, &hdr, sizeof(hdr));
   for (size_t c = 0; c + 1 < P->cta_indptr.size(); ++c) {
     CtaHead h{};
     h.it0 = P->cta_indptr[c];
     h.it1 = P->cta_indptr[c + 1];
+    h.stamp = P->stamp;
     if (h.it0 < h.it1) h.first = P->items[h.it0];
     std::memcpy(P->table.data() + P->off_indptr + c * sizeof(CtaHead), &h, sizeof(h));
   }
@@ -239,26 +257,19 @@ bool make_kv_map(CUtensorMap* map, const void* kv, int kv_dtype, int64_t rows, i
 
 // MXFP4 pool: packed rows of 288 bytes as a 3-D tensor {32 B, row, chunk}
 // (chunk = the 64 values of two scale blocks); a box of box_rows rows lands
-// chunk-major as [chunk][row][32 B] (no swizzle).  Scale rows (stride a
-// multiple of 16, >= 32 bytes): 32-byte boxes of sc_rows rows, [row][32 B].
-bool make_mx_maps(CUtensorMap* kvmap, CUtensorMap* scmap, const void* kv, const uint8_t* e8m0,
-                  int64_t e8m0_stride, int64_t rows, int box_rows, int sc_rows) {
+// chunk-major as [chunk][row][32 B] (no swizzle).  The e8m0 scale rows are
+// not copied by TMA: the dequantising threads read them from global memory,
+// so that any row stride (the pages' rows are 18 bytes) is accepted.
+bool make_mx_map(CUtensorMap* kvmap, const void* kv, int64_t rows, int box_rows) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return false;
   const cuuint64_t dims[3] = {32, static_cast<cuuint64_t>(rows), 9};
   const cuuint64_t strides[2] = {288, 32};
   const cuuint32_t box[3] = {32, static_cast<cuuint32_t>(box_rows), 9};
   const cuuint32_t estr[3] = {1, 1, 1};
-  if (enc(kvmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(kv), dims, strides, box, estr,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return false;
-  const cuuint64_t sdims[2] = {32, static_cast<cuuint64_t>(rows)};
-  const cuuint64_t sstr[1] = {static_cast<cuuint64_t>(e8m0_stride)};
-  const cuuint32_t sbox[2] = {32, static_cast<cuuint32_t>(sc_rows)};
-  return enc(scmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(e8m0), sdims, sstr,
-             sbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return enc(kvmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(kv), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -296,6 +307,7 @@ mla_status mla_decode_plan_q(const int32_t* kv_indptr_host, const int32_t* kv_la
   std::vector<int32_t> len(nv), page_base(nv), npages(nv), vis0(nv, 0);
   std::vector<int64_t> tiles(nv);
   int64_t total_tok = 0, total_tiles = 0;
+  int64_t identity_rows = 0;      // pool rows the identity table reaches
   for (int32_t b = 0; b < batch_size; ++b) {
     const int64_t np = static_cast<int64_t>(kv_indptr_host[b + 1]) - kv_indptr_host[b];
     if (np < 0) return MLA_ERR_INVALID_ARG;
@@ -306,6 +318,8 @@ mla_status mla_decode_plan_q(const int32_t* kv_indptr_host, const int32_t* kv_la
       n -= page_size - last;
     }
     if (n > INT32_MAX - mla::kTile) return MLA_ERR_INVALID_ARG;
+    if (n > 0)
+      identity_rows = std::max(identity_rows, static_cast<int64_t>(kv_indptr_host[b]) * page_size + n);
     for (int32_t t = 0; t < qv; ++t) {
       const int32_t r = b * qv + t;
       const int64_t first_seen = n - q_len + 1 + (pairs ? 2 * t : t);
@@ -336,6 +350,7 @@ mla_status mla_decode_plan_q(const int32_t* kv_indptr_host, const int32_t* kv_la
   P->kv_dtype = kv_dtype;
   P->qmode = pairs ? mla::kQFp8KvFp8x2 : qmode;
   P->total_tokens = total_tok;
+  P->identity_rows = identity_rows;
   P->total_tiles = total_tiles;
   P->cta_indptr.assign(1, 0);
   if (num_splits == 0) {
@@ -427,10 +442,14 @@ mla_status mla_decode_run(mla_plan* plan, const void* q, const float* q_scale, c
   if (plan->q_dtype == MLA_DTYPE_FP8_E4M3 && q_scale == nullptr) return MLA_ERR_INVALID_ARG;
   if (plan->kv_dtype == MLA_DTYPE_FP8_E4M3 && kv_scale == nullptr) return MLA_ERR_INVALID_ARG;
   if (plan->kv_dtype == MLA_DTYPE_MXFP4) {
-    if (kv_e8m0 == nullptr || !aligned(kv_e8m0, 16)) return MLA_ERR_INVALID_ARG;
-    if (kv_e8m0_row_stride < 32 || kv_e8m0_row_stride % 16 != 0) return MLA_ERR_UNSUPPORTED;
+    if (kv_e8m0 == nullptr || kv_e8m0_row_stride < 18) return MLA_ERR_INVALID_ARG;
+    // scale rows are read two bytes at a time
+    if (kv_e8m0_row_stride % 2 != 0 || !aligned(kv_e8m0, 2)) return MLA_ERR_UNSUPPORTED;
   }
   if (workspace_bytes < plan->ws_bytes) return MLA_ERR_WORKSPACE;
+  // without a page table, request b's rows follow from kv_indptr: all of them
+  // must lie inside the pool
+  if (kv_indices == nullptr && plan->identity_rows > kv_pool_rows) return MLA_ERR_INVALID_ARG;
   // Identity table: one TMA box of 128 rows per tile.  Page table with a
   // page size that is a multiple of 8: one box per 8-row group (a group never
   // straddles a page).  Other page sizes (bf16 / fp8 KV): every row is
@@ -451,20 +470,11 @@ mla_status mla_decode_run(mla_plan* plan, const void* q, const float* q_scale, c
   // bytes per row of the tile the UMMAs read (MXFP4 is dequantised to e4m3)
   const uint32_t row_bytes = mla::kQkDim * (plan->kv_dtype == MLA_DTYPE_BF16 ? 2 : 1);
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-  // MXFP4 with the identity table: a tile's 128 scale rows are contiguous, one box
-  const bool sc_one_box = plan->kv_dtype == MLA_DTYPE_MXFP4 && kv_indices == nullptr;
-  const int sc_rows = sc_one_box ? mla::kTile : box_rows;
-  if (plan->tmap_ptr != kv || plan->tmap_rows != kv_pool_rows || plan->tmap_box_rows != box_rows ||
-      plan->tmap_sc_ptr != kv_e8m0 || plan->tmap_sc_stride != kv_e8m0_row_stride ||
-      plan->tmap_sc_rows != sc_rows) {
+  if (plan->tmap_ptr != kv || plan->tmap_rows != kv_pool_rows || plan->tmap_box_rows != box_rows) {
     const bool ok = plan->kv_dtype == MLA_DTYPE_MXFP4
-                        ? make_mx_maps(&plan->tmap, &plan->tmap_sc, kv, kv_e8m0, kv_e8m0_row_stride,
-                                       kv_pool_rows, box_rows, sc_rows)
+                        ? make_mx_map(&plan->tmap, kv, kv_pool_rows, box_rows)
                         : make_kv_map(&plan->tmap, kv, plan->kv_dtype, kv_pool_rows, box_rows);
     if (!ok) return MLA_ERR_CUDA;
-    plan->tmap_sc_ptr = kv_e8m0;
-    plan->tmap_sc_stride = kv_e8m0_row_stride;
-    plan->tmap_sc_rows = sc_rows;
     plan->tmap_ptr = kv;
     plan->tmap_rows = kv_pool_rows;
     plan->tmap_box_rows = box_rows;
@@ -482,7 +492,6 @@ mla_status mla_decode_run(mla_plan* plan, const void* q, const float* q_scale, c
   if (plan->num_ctas > 0) {
     mla::Stage1Params p{};
     p.tmap_kv = plan->tmap;
-    p.tmap_sc = plan->tmap_sc;
     p.q = q;
     p.q_scale = q_scale;
     p.kv_scale = kv_scale;
@@ -494,6 +503,7 @@ mla_status mla_decode_run(mla_plan* plan, const void* q, const float* q_scale, c
     p.out = static_cast<uint16_t*>(out);
     p.lse = lse;
     p.err = err;
+    p.stamp = plan->stamp;
     p.page_size = plan->page_size;
     p.box_rows = box_rows;
     p.gather = gather;
@@ -501,7 +511,8 @@ mla_status mla_decode_run(mla_plan* plan, const void* q, const float* q_scale, c
     p.chunk_stride = static_cast<uint32_t>(box_rows) * 64u;    // [group][chunk][rows][64 B]
     p.group_stride = box_rows == 8 ? row_bytes * 8u : 512u;
     p.pool_rows = kv_pool_rows;
-    p.sc_one_box = sc_one_box ? 1 : 0;
+    p.kv_e8m0 = kv_e8m0;
+    p.sc_stride = kv_e8m0_row_stride;
     if (plan->ev_before != nullptr && cudaEventRecord(plan->ev_before, stream) != cudaSuccess)
       return MLA_ERR_CUDA;
     if (mla::launch_stage1(plan->qmode, p, plan->num_ctas, stream) != cudaSuccess)
@@ -512,6 +523,8 @@ mla_status mla_decode_run(mla_plan* plan, const void* q, const float* q_scale, c
   if (!plan->jobs.empty()) {
     mla::Stage2Params s{};
     s.jobs = reinterpret_cast<const MergeJob*>(ws + plan->off_jobs);
+    s.err = err;
+    s.stamp = plan->stamp;
     s.part_o = part_o;
     s.part_lse = part_lse;
     s.out = static_cast<uint16_t*>(out);
@@ -525,7 +538,12 @@ mla_status mla_decode_run(mla_plan* plan, const void* q, const float* q_scale, c
 }
 
 mla_status mla_decode_check(const mla_plan* plan, void* workspace, mla_stream_t stream_) {
-  if (plan == nullptr || workspace == nullptr) return MLA_ERR_INVALID_ARG;
+  if (plan == nullptr) return MLA_ERR_INVALID_ARG;
+  if (workspace == nullptr) {
+    // the array mla_decode_run_noalloc uses on the current device
+    const mla_status st = mla::static_workspace(&workspace);
+    if (st != MLA_OK) return st;
+  }
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   int32_t word = 0;
   int32_t* dev = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + plan->off_err);
@@ -534,7 +552,13 @@ mla_status mla_decode_check(const mla_plan* plan, void* workspace, mla_stream_t 
     return MLA_ERR_CUDA;
   if (word == 0) return MLA_OK;
   if (cudaMemset(dev, 0, sizeof(word)) != cudaSuccess) return MLA_ERR_CUDA;
-  return (word & ~mla::kErrBadPage) ? MLA_ERR_DEVICE_TIMEOUT : MLA_ERR_INVALID_ARG;
+  if (word & mla::kErrStale) {
+    // the workspace held another plan's table: upload this plan's again on
+    // its next run with this workspace
+    if (plan->uploaded_ws == workspace) plan->uploaded_ws = nullptr;
+    return MLA_ERR_WORKSPACE;
+  }
+  return (word & mla::kErrTimeout) ? MLA_ERR_DEVICE_TIMEOUT : MLA_ERR_INVALID_ARG;
 }
 
 mla_status mla_plan_set_stage1_events(mla_plan* plan, void* before, void* after) {

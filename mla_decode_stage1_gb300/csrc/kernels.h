@@ -22,10 +22,22 @@ constexpr float kTau = 4.0f;
 constexpr float kPLoScale = 16.0f;    // the low part of p is stored x2^4
 // (p <= 2^(kPOff+kTau) = 256, so |p - e4m3(p)| * 16 <= 256 <= 448)
 
-// Device error word bits (one per pipeline role that gave up a wait).
+// Device error word bits: one per pipeline role that gave up a wait, a page
+// outside the pool, and a workspace that holds another plan's table.
 enum : int32_t {
   kErrProducer = 1, kErrMma = 2, kErrSoftmax = 4, kErrQPrep = 8, kErrDrain = 16,
-  kErrBadPage = 32, kErrDequant = 64
+  kErrBadPage = 32, kErrDequant = 64, kErrStale = 128
+};
+constexpr int32_t kErrTimeout = kErrProducer | kErrMma | kErrSoftmax | kErrQPrep | kErrDrain |
+                                kErrDequant;
+
+// Workspace header (the first 16 bytes of every plan's workspace): the
+// device error word, then the stamp of the plan whose table was uploaded
+// last.  Every CTA head carries the stamp too.
+struct WsHeader {
+  int32_t err;
+  int32_t pad;
+  uint64_t stamp;
 };
 
 // One work item: a contiguous token range of one request.
@@ -46,7 +58,7 @@ static_assert(sizeof(WorkItem) == 32, "work item is two int4");
 // load gives a CTA everything its first tile needs.
 struct CtaHead {
   int32_t it0, it1;   // items [it0, it1) of the work-item array
-  int32_t pad0, pad1;
+  uint64_t stamp;     // the plan's stamp
   WorkItem first;     // items[it0] (unused when it0 == it1)
 };
 static_assert(sizeof(CtaHead) == 48, "CTA head is three int4");
@@ -70,9 +82,7 @@ enum QMode : int {
 
 struct Stage1Params {
   CUtensorMap tmap_kv;          // KV pool as [chunk 64 B][row][64 B], 64-byte swizzle;
-                                // MXFP4: packed rows as [half 144 B][row][144 B]
-  CUtensorMap tmap_sc;          // MXFP4 only: e8m0 scale rows, 32-byte boxes of box_rows rows
-                                // (128 rows with sc_one_box)
+                                // MXFP4: packed rows as [chunk 32 B][row][32 B]
   const void* q;                // [bs,16,576]
   const float* q_scale;         // device [1] (fp8 q) or null
   const float* kv_scale;        // device [1] (fp8 kv) or null
@@ -83,7 +93,8 @@ struct Stage1Params {
   float* part_lse;              // [num_partials,16] log2 domain
   uint16_t* out;                // [bs,16,512] bf16 bits
   float* lse;                   // [bs,16] natural log, nullable
-  int32_t* err;                 // device error word
+  int32_t* err;                 // device error word (the workspace header)
+  uint64_t stamp;               // the plan's stamp; the workspace must carry the same
   int32_t page_size;
   int32_t box_rows;             // rows per TMA box: 128 (identity table) or 8 (page table)
   int32_t gather;               // 1: page size not a multiple of 8 (bf16 / fp8 KV); rows are
@@ -92,11 +103,14 @@ struct Stage1Params {
   uint32_t chunk_stride;        // smem bytes between 64-byte column chunks of a tile
   uint32_t group_stride;        // smem bytes between 8-row groups of a tile
   int64_t pool_rows;
-  int32_t sc_one_box;           // MXFP4, identity table: a tile's 128 scale rows in one box
+  const uint8_t* kv_e8m0;       // MXFP4 only: e8m0 scale rows (18 bytes used per row)
+  int64_t sc_stride;            // bytes between scale rows (even, >= 18)
 };
 
 struct Stage2Params {
   const MergeJob* jobs;
+  int32_t* err;                 // device error word (the workspace header)
+  uint64_t stamp;               // the plan's stamp
   int32_t rows;                 // output rows per request: 16 heads x query tokens
   int32_t wide;                 // 1: some request has many partials (one CTA per row)
   const float* part_o;

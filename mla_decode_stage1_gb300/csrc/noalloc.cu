@@ -19,12 +19,13 @@
 #include "mla_decode.h"
 #include "plan.h"
 
+namespace mla {
 namespace {
 
-// Maximum workspace a plan may need to use this entry point: 16 MiB covers
-// the work table and split partials of balanced plans for batches of a few
-// hundred requests (bs=256 x 8192 tokens needs about 9.5 MB).
-constexpr size_t kStaticWorkspaceBytes = size_t(16) << 20;
+// kStaticWorkspaceBytes (16 MiB), the largest workspace a plan may need to
+// use this entry point, covers the work table and split partials of balanced
+// plans for batches of a few hundred requests (bs=256 x 8192 tokens needs
+// about 9.5 MB).
 
 // The workspace.  In host code `g_static_workspace` names a host-side stand-in,
 // not the device array: only the address from cudaGetSymbolAddress below may
@@ -34,6 +35,8 @@ static __device__ __align__(256) unsigned char g_static_workspace[kStaticWorkspa
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
 void* g_device_ptr[kMaxDevices] = {};
+
+}  // namespace
 
 // Device address of the array on the current device; looked up once per
 // device (with that device current) and cached.
@@ -51,7 +54,7 @@ mla_status static_workspace(void** out) {
   return MLA_OK;
 }
 
-}  // namespace
+}  // namespace mla
 
 extern "C" mla_status mla_decode_run_noalloc(mla_plan* plan, const void* q, const float* q_scale,
                                              const void* kv, const float* kv_scale,
@@ -59,14 +62,14 @@ extern "C" mla_status mla_decode_run_noalloc(mla_plan* plan, const void* q, cons
                                              int64_t kv_pool_rows, const int32_t* kv_indices,
                                              void* out, float* lse, mla_stream_t stream) {
   if (plan == nullptr) return MLA_ERR_INVALID_ARG;
-  if (plan->ws_bytes > kStaticWorkspaceBytes) return MLA_ERR_WORKSPACE;
+  if (plan->ws_bytes > mla::kStaticWorkspaceBytes) return MLA_ERR_WORKSPACE;
   void* ws = nullptr;
-  const mla_status st = static_workspace(&ws);
+  const mla_status st = mla::static_workspace(&ws);
   if (st != MLA_OK) return st;
   // Every call shares the array and it keeps what the last call left there:
   // copy this plan's work table in again (that also zeroes the error word),
   // whatever plan used the array before.
   plan->uploaded_ws = nullptr;
   return mla_decode_run(plan, q, q_scale, kv, kv_scale, kv_e8m0, kv_e8m0_row_stride, kv_pool_rows,
-                        kv_indices, ws, kStaticWorkspaceBytes, out, lse, stream);
+                        kv_indices, ws, mla::kStaticWorkspaceBytes, out, lse, stream);
 }

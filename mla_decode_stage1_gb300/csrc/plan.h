@@ -9,6 +9,7 @@
 #include <vector>
 
 #include "kernels.h"
+#include "mla_decode.h"
 
 struct mla_plan {
   int32_t bs = 0, page_size = 0, num_splits = 0;   // bs: rows of q (requests x q_len)
@@ -19,6 +20,7 @@ struct mla_plan {
   int32_t num_ctas = 0, num_partials = 0;
   int32_t max_parts = 0;   // most partials of one request (stage 2 goes wide above 4)
   int64_t total_tokens = 0, total_tiles = 0;
+  int64_t identity_rows = 0;   // pool rows the requests reach without a page table
   std::vector<int32_t> cta_indptr;
   std::vector<mla::WorkItem> items;
   std::vector<mla::MergeJob> jobs;
@@ -26,15 +28,20 @@ struct mla_plan {
   size_t off_err = 0, off_indptr = 0, off_items = 0, off_jobs = 0, off_part_o = 0,
          off_part_lse = 0, ws_bytes = 0;
   std::vector<uint8_t> table;  // image of [0, off_part_o) uploaded once per workspace
-  // per-run caches
-  void* uploaded_ws = nullptr;
+  uint64_t stamp = 0;          // unique per plan; written into the table header and CTA heads
+  // per-run caches (the upload cache is reset by mla_decode_check when a
+  // kernel found another plan's table in the workspace)
+  mutable void* uploaded_ws = nullptr;
   CUtensorMap tmap;
   const void* tmap_ptr = nullptr;
   int64_t tmap_rows = -1;
   int32_t tmap_box_rows = -1;
-  CUtensorMap tmap_sc;
-  const void* tmap_sc_ptr = nullptr;
-  int64_t tmap_sc_stride = -1;
-  int32_t tmap_sc_rows = -1;
   cudaEvent_t ev_before = nullptr, ev_after = nullptr;
 };
+
+namespace mla {
+// Device address of the library's own workspace array on the current device
+// (noalloc.cu), looked up once per device.
+mla_status static_workspace(void** out);
+constexpr size_t kStaticWorkspaceBytes = size_t(16) << 20;
+}  // namespace mla

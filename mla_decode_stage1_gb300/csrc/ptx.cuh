@@ -90,6 +90,12 @@ __device__ __forceinline__ int32_t ld_nc_early(const int32_t* ptr) {
   return v;
 }
 
+__device__ __forceinline__ uint16_t ld_nc_u16_early(const uint16_t* ptr) {
+  uint16_t v;
+  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(ptr));
+  return v;
+}
+
 // ------------------------------------------------------------ cp.async rows
 // 16-byte asynchronous copy global -> shared (cached in L1, so that the other
 // 16-byte pieces of the same line hit there).

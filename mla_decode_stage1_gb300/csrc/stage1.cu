@@ -78,7 +78,6 @@ struct Layout {
   static constexpr int kQBytes = kQAtoms * kQAtomBytes;
   static constexpr int kPRow = 2 * kRows;                           // P bytes per token
   static constexpr int kPBytes = kTile * kPRow;
-  static constexpr int kScBytes = kMx ? kTile * 32 : 0;             // e8m0 rows per tile slot
   static constexpr int kRawRowBytes = kQkDim / 2;                   // packed MXFP4 row
   static constexpr bool kQ8 = (QM == kQFp8KvFp8 || QM == kQFp8KvBf16 || QM == kQFp8KvFp8x2);
   static constexpr int kQSrcBytes = kRows * kQkDim * (kQ8 ? 1 : 2);  // one request's q
@@ -86,15 +85,16 @@ struct Layout {
   // TMEM: S^T at 0 (2 buffers x 2 K-halves x 32 columns), O^T from 128
   static constexpr uint32_t kTmemCols = 128 + 4 * kOCols <= 256 ? 256 : 512;
   static constexpr int kMiscBytes = 2560;
+  static constexpr int kScRowBytes = kMx ? kTile * 24 : 0;         // e8m0 row of each dequant thread
   static constexpr int kMaxSmem = 232448;
   static constexpr int kNumTiles =
-      (kMaxSmem - 1024 - 2 * kQBytes - 2 * kPBytes - kMiscBytes - kQSrcBytes) /
-      (kTileBytes + kScBytes);
+      (kMaxSmem - 1024 - 2 * kQBytes - 2 * kPBytes - kMiscBytes - kScRowBytes - kQSrcBytes) /
+      kTileBytes;
   static constexpr int kQOff = kNumTiles * kTileBytes;
   static constexpr int kPOff = kQOff + 2 * kQBytes;
-  static constexpr int kScOff = kPOff + 2 * kPBytes;
-  static constexpr int kMiscOff = kScOff + kNumTiles * kScBytes;
-  static constexpr int kQStageOff = kMiscOff + kMiscBytes;           // raw q of the next item
+  static constexpr int kMiscOff = kPOff + 2 * kPBytes;
+  static constexpr int kScRowOff = kMiscOff + kMiscBytes;
+  static constexpr int kQStageOff = kScRowOff + kScRowBytes;         // raw q of the next item
   static constexpr int kSmemBytes = kQStageOff + kQSrcBytes + 1024;
   static_assert(kNumTiles >= 1 && kNumTiles <= 4, "tile ring");
   static_assert(kSmemBytes <= kMaxSmem, "shared memory over budget");
@@ -118,6 +118,7 @@ struct Misc {
   uint64_t deq_a[4];                 // its dims 0-319 dequantised (first QK^T K-half)
   uint64_t upper_free[4];            // PV no longer reads the slot's upper box halves
   int32_t abort_dq;                  // set by a dequant thread whose bounded wait gave up
+  int32_t stale;                     // the workspace holds another plan's table
   float uexp[2][128];                // per-token power of two u_t = r_t - 127 of a slot
   uint2 e2m1_tab[16];                // e4m3 tables for 2^k, k = index - 14 (k <= -14: all 0)
 };
@@ -294,7 +295,7 @@ __device__ void run_producer(const Stage1Params& p, Misc* ms, uint32_t ring, int
     ahead.advance();
     const uint32_t s = t % L::kNumTiles, ph = (t / L::kNumTiles) & 1u;
     const uint32_t full = smem_u32(&ms->full[s]);
-    const uint32_t raw_bytes = p.box_rows * L::kRawRowBytes, sc_bytes = p.box_rows * 32u;
+    const uint32_t raw_bytes = p.box_rows * L::kRawRowBytes;
     // Before waiting for the slot to be free: resolve the rows and arm the
     // slot's next full phase with the bytes to come.  That arrive must fall
     // in the next phase, so the slot's previous tile must have landed first
@@ -308,28 +309,18 @@ __device__ void run_producer(const Stage1Params& p, Misc* ms, uint32_t ring, int
       if (!ok) break;
     }
     if (lane == 0)
-      mbar_arrive_expect_tx(full, L::kMx && p.sc_one_box
-                                      ? static_cast<uint32_t>(f.nbox) * raw_bytes + kTile * 32u
-                                      : static_cast<uint32_t>(f.nbox) *
-                                            (L::kMx ? raw_bytes + sc_bytes : box_bytes));
+      mbar_arrive_expect_tx(full, static_cast<uint32_t>(f.nbox) * (L::kMx ? raw_bytes : box_bytes));
     // (MXFP4: the packed rows land in the upper box halves, free once PV has
     // read O blocks 2-3; the dequantisation waits for the whole slot)
     ok = __all_sync(0xffffffffu, mbar_wait(L::kMx ? smem_u32(&ms->upper_free[s]) : smem_u32(&ms->empty[s]),
                                            ph ^ 1u, p.err, kErrProducer));
     if (!ok) break;
     if constexpr (L::kMx) {
-      // packed rows of box i into the upper half of box i's e4m3 region,
-      // scale rows beside the slot: one box per 8 rows, or (identity table)
-      // all 128 in one box, which takes 15 copy operations off every tile
-      if (lane < f.nbox) {
+      // packed rows of box i into the upper half of box i's e4m3 region
+      // (the e8m0 scale rows are read by the dequantising threads)
+      if (lane < f.nbox)
         tma_load_3d(ring + s * L::kTileBytes + lane * box_bytes + raw_bytes, &p.tmap_kv, full, 0,
                     row, 0, pol);
-        if (!p.sc_one_box)
-          tma_load_2d(ring + L::kScOff + s * L::kScBytes + lane * sc_bytes, &p.tmap_sc, full, 0,
-                      row, pol);
-      }
-      if (p.sc_one_box && lane == 0)
-        tma_load_2d(ring + L::kScOff + s * L::kScBytes, &p.tmap_sc, full, 0, row, pol);
     } else {
       if (lane < f.nbox)
         tma_load_3d(ring + s * L::kTileBytes + lane * box_bytes, &p.tmap_kv, full, 0, row, 0, pol);
@@ -504,6 +495,47 @@ __device__ __forceinline__ uint2 e2m1x8_to_e4m3(uint32_t w, uint32_t lo, uint32_
   const uint32_t w4 = w << 4;
   const uint32_t s0 = prmt(w4, w, 0xD9C8u), s1 = prmt(w4, w, 0xFBEAu);
   return make_uint2(m0 | (s0 & 0x80808080u), m1 | (s1 & 0x80808080u));
+}
+
+// ------------------------------------------------------- MXFP4 scale rows
+// The dequantising thread of token `tq` reads that token's 18 e8m0 bytes
+// from global memory itself (no TMA box: the pages' scale rows are 18 bytes,
+// which no tensor map can stride over).  The row is found as the producer
+// finds it: through the page table, a page outside the pool replaced by page
+// 0.  The loads of a tile are issued one tile ahead and its page-table entry
+// two tiles ahead, so neither waits on the path.
+
+// Raw page-table entry of token tq of the cursor's tile (0 for the identity
+// table or a token past the tile's end).
+__device__ __forceinline__ int32_t scale_page(const Stage1Params& p, const TileCursor& c, int tq) {
+  if (c.done() || tq >= c.nvalid() || p.kv_indices == nullptr) return 0;
+  return ld_nc_early(p.kv_indices + c.w.page_base + (c.t0() + tq) / p.page_size);
+}
+
+// Issues the nine 2-byte loads of the token's scale row (zeros past the
+// tile's end); `page` is scale_page() of the same tile and token.
+__device__ __forceinline__ void scale_load(const Stage1Params& p, const TileCursor& c, int tq,
+                                           int32_t page, uint16_t (&h)[9]) {
+  if (c.done() || tq >= c.nvalid()) {
+#pragma unroll
+    for (int i = 0; i < 9; ++i) h[i] = 0;
+    return;
+  }
+  const int pos = c.t0() + tq;
+  int64_t row;
+  if (p.kv_indices == nullptr) {
+    row = static_cast<int64_t>(c.w.page_base) * p.page_size + pos;
+    if (row >= p.pool_rows) row = 0;   // (the host rejects such plans; never reached)
+  } else {
+    if (page < 0 || static_cast<int64_t>(page + 1) * p.page_size > p.pool_rows) {
+      atomicOr(p.err, kErrBadPage);
+      page = 0;
+    }
+    row = static_cast<int64_t>(page) * p.page_size + pos % p.page_size;
+  }
+  const uint16_t* src = reinterpret_cast<const uint16_t*>(p.kv_e8m0 + row * p.sc_stride);
+#pragma unroll
+  for (int i = 0; i < 9; ++i) h[i] = ld_nc_u16_early(src + i);
 }
 
 // ----------------------------------------------------- q staging helpers
@@ -684,10 +716,35 @@ __device__ void run_dequant(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
   // this thread's row: box t/8, row t%8 (8-row boxes)
   const uint32_t box_off = (t >> 3) * 4608u, r8 = t & 7u;
   const uint32_t swz = (r8 >> 1) & 3u;                 // 64-byte swizzle of this row
-  TileCursor c;
+  // this thread's copy of its token's scale row (nine 2-byte block pairs)
+  uint16_t* sc = reinterpret_cast<uint16_t*>(ring_gen + L::kScRowOff + t * 24);
+  TileCursor c, a1, a2;                                // this tile, the next, the one after
   c.init(p.items, it0, it1, first);
+  a1 = c;
+  a1.advance();
+  a2 = a1;
+  a2.advance();
+  uint16_t h[9];
+  scale_load(p, c, t, scale_page(p, c, t), h);
+  int32_t page1 = scale_page(p, a1, t);
   while (!c.done()) {
     const uint32_t tt = c.t, s = tt % L::kNumTiles;
+    // this tile's scale bytes into shared memory, then the next tile's loads
+    int r = 0;
+    {
+      uint32_t ew[5];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) ew[i] = h[2 * i] | (static_cast<uint32_t>(h[2 * i + 1]) << 16);
+      ew[4] = h[8];
+      *reinterpret_cast<uint2*>(sc) = make_uint2(ew[0], ew[1]);
+      *reinterpret_cast<uint2*>(sc + 4) = make_uint2(ew[2], ew[3]);
+      *reinterpret_cast<uint32_t*>(sc + 8) = ew[4];
+#pragma unroll
+      for (int b = 0; b < 18; ++b)
+        r = max(r, static_cast<int>((ew[b >> 2] >> ((b & 3) * 8)) & 0xFFu));
+    }
+    scale_load(p, a1, t, page1, h);
+    page1 = scale_page(p, a2, t);
     if (!mbar_wait(smem_u32(&ms->full[s]), (tt / L::kNumTiles) & 1u, p.err, kErrDequant)) *abort = 1;
     // e4m3 rows are written over the whole slot: PV of its previous tile
     // must have finished (the packed rows only needed the upper halves)
@@ -697,30 +754,20 @@ __device__ void run_dequant(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
     if (*abort) return;
     uint8_t* box = ring_gen + s * L::kTileBytes + box_off;
     const uint8_t* raw = box + 2304u + r8 * 32u;
-    const uint8_t* sc = ring_gen + L::kScOff + s * L::kScBytes + t * 32;
-    int r = 0;
-    {
-      const uint4 e0 = reinterpret_cast<const uint4*>(sc)[0];
-      const uint32_t e1 = reinterpret_cast<const uint32_t*>(sc)[4];
-      const uint32_t ew[5] = {e0.x, e0.y, e0.z, e0.w, e1};
-#pragma unroll
-      for (int b = 0; b < 18; ++b)
-        r = max(r, static_cast<int>((ew[b >> 2] >> ((b & 3) * 8)) & 0xFFu));
-    }
     ms->uexp[s][t] = static_cast<float>(r - 127);
     uint8_t* row = box + r8 * 64u;
     // packed chunk ch+1 and its two scale bytes are read while chunk ch is
     // converted (reading early is always safe; only writes must wait)
     uint4 na = reinterpret_cast<const uint4*>(raw)[0];
     uint4 nb = reinterpret_cast<const uint4*>(raw)[1];
-    uint32_t neb = reinterpret_cast<const uint16_t*>(sc)[0];
+    uint32_t neb = sc[0];
     auto chunk = [&](int ch, bool sync) {
       const uint4 a = na, b = nb;
       const uint32_t eb = neb;                          // e8m0 of blocks 2ch, 2ch+1
       if (ch < 8) {
         na = reinterpret_cast<const uint4*>(raw + (ch + 1) * 256)[0];
         nb = reinterpret_cast<const uint4*>(raw + (ch + 1) * 256)[1];
-        neb = reinterpret_cast<const uint16_t*>(sc)[ch + 1];
+        neb = sc[ch + 1];
       }
       if (sync) __syncwarp();                           // the box read the packed chunks
       const uint2 t0 = ms->e2m1_tab[max(static_cast<int>(eb & 0xFFu) - r, -14) + 14];
@@ -756,6 +803,8 @@ __device__ void run_dequant(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
     const bool first = c.j == 0;
     const int it = c.it, k = c.k;
     c.advance();
+    a1 = a2;
+    a2.advance();
     if (first && it + 1 < it1 && !qprep_group<QM>(p, ms, qgen, stage, it + 1, k + 1, it1, t)) return;
   }
 }
@@ -1157,6 +1206,12 @@ __global__ void __launch_bounds__(Layout<QM>::kThreads, 1) mla_stage1_kernel(con
   const WorkItem first = head.first;
 
   if (threadIdx.x == 0) {
+    // The workspace must hold this plan's table: its stamp in the header and
+    // in this CTA's head.  Otherwise (another plan's table was uploaded at
+    // this address since) nothing is read from the table and nothing is
+    // written; mla_decode_check reports it.
+    const uint64_t hs = reinterpret_cast<const WsHeader*>(p.err)->stamp;
+    ms->stale = (hs != p.stamp || head.stamp != p.stamp) ? 1 : 0;
     for (int i = 0; i < L::kNumTiles; ++i) {
       mbar_init(smem_u32(&ms->full[i]), p.gather ? 32 : 1);   // gather: one per producer lane
       mbar_init(smem_u32(&ms->empty[i]), L::kPvIssuers);
@@ -1191,7 +1246,9 @@ __global__ void __launch_bounds__(Layout<QM>::kThreads, 1) mla_stage1_kernel(con
   tc_fence_after();
   const uint32_t tmem = ms->tmem_base;
 
-  if (warp == 0) {
+  if (ms->stale) {
+    if (threadIdx.x == 0) atomicOr(p.err, kErrStale);
+  } else if (warp == 0) {
     run_producer<QM>(p, ms, ring, it0, it1, first, lane);
   } else if (warp == 1 || warp == 3) {
     run_qk<QM>(p, ms, ring, ring + L::kQOff, tmem, it0, it1, first, warp == 3 ? 1 : 0, lane);

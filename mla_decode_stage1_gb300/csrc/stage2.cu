@@ -21,13 +21,27 @@
 
 namespace mla {
 
+// Whether the workspace holds this plan's table.  Lane 0 reads the header
+// stamp and the warp takes its answer, so that the whole warp leaves or stays.
+__device__ __forceinline__ bool table_is_ours(const Stage2Params& p, int lane) {
+  uint64_t hs = 0;
+  if (lane == 0) hs = reinterpret_cast<const WsHeader*>(p.err)->stamp;
+  hs = __shfl_sync(0xffffffffu, hs, 0);
+  if (hs == p.stamp) return true;
+  if (lane == 0) atomicOr(p.err, kErrStale);
+  return false;
+}
+
 __global__ void __launch_bounds__(256) mla_stage2_kernel(const Stage2Params p) {
   const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   const int job = gw / p.rows, h = gw % p.rows;   // h: output row of the request
   if (job >= p.num_jobs) return;
-  // The job table is plan data (not written by stage 1): read it first.
+  // The job table is plan data (not written by stage 1): read it first,
+  // together with the stamp of the table the workspace holds.  A table of
+  // another plan is not used: nothing is written (mla_decode_check reports it).
   const MergeJob J = p.jobs[job];
+  if (!table_is_ours(p, lane)) return;
   uint16_t* out = p.out + (static_cast<int64_t>(J.b) * p.rows + h) * kVDim;
   // Launched as a programmatic dependent of stage 1: wait here until stage 1
   // has completed and its partials are visible.
@@ -117,11 +131,18 @@ constexpr int kWideBatch = 16;                // partials per warp per round tri
 __global__ void __launch_bounds__(256) mla_stage2_wide_kernel(const Stage2Params p) {
   __shared__ float red_m[8], red_w[8];
   __shared__ float4 red_acc[8][32];
+  __shared__ int ours;
   const int quarter = blockIdx.x % kWideSplit, rowid = blockIdx.x / kWideSplit;
   const int job = rowid / p.rows, h = rowid % p.rows;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (job >= p.num_jobs) return;
   const MergeJob J = p.jobs[job];
+  if (warp == 0) {
+    const bool ok = table_is_ours(p, lane);
+    if (lane == 0) ours = ok ? 1 : 0;
+  }
+  __syncthreads();
+  if (!ours) return;                      // the whole CTA leaves together
   const int col = quarter * 32 + lane;        // this lane's float4 column (dims 4 col ..)
   uint16_t* out = p.out + (static_cast<int64_t>(J.b) * p.rows + h) * kVDim;
   asm volatile("griddepcontrol.wait;" ::: "memory");

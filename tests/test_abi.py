@@ -99,6 +99,22 @@ def test_run_rejects_bad_arguments_without_launching(mla):
     # ... and a pool that is not whole pages is invalid
     assert lib.mla_decode_run(pl4.handle, a256, None, a256, None, a256, 32, 18, a256, a256,
                               1 << 14, a256, None, None) == 1
+    # without a page table the requests' rows must lie inside the pool
+    assert lib.mla_decode_run(pl.handle, a256, None, a256, a256, None, 0, 15, None, a256,
+                              1 << 12, a256, None, None) == 1
+    # MXFP4 scale rows: 18 bytes (the pages' rows) and more are accepted; a
+    # narrower row is invalid, an odd stride unsupported (rows are read two
+    # bytes at a time), a missing scale pointer invalid
+    plm = plan(mla, [0, 16], ps=1, qd="bf16", kd="mxfp4")
+    assert lib.mla_decode_run(plm.handle, a256, None, a256, None, a256, 16, 16, None, a256,
+                              1 << 14, a256, None, None) == 1
+    assert lib.mla_decode_run(plm.handle, a256, None, a256, None, a256, 19, 16, None, a256,
+                              1 << 14, a256, None, None) == 2
+    assert lib.mla_decode_run(plm.handle, a256, None, a256, None,
+                              ctypes.c_void_p(a256.value + 1), 18, 16, None, a256,
+                              1 << 14, a256, None, None) == 2
+    assert lib.mla_decode_run(plm.handle, a256, None, a256, None, None, 18, 16, None, a256,
+                              1 << 14, a256, None, None) == 1
 
 
 def test_unsupported_combinations(mla):

@@ -91,15 +91,21 @@ def test_reference_arm_prints_its_json_line():
     import json
     import subprocess
     import sys
-    import __graft_entry__
-    __graft_entry__._builder().build()          # the package loads its library on import
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
-                        "--config", "bs4_kv1024_bf16", "--steps", "1", "--warmup", "0"],
-                       capture_output=True, text=True, timeout=300, cwd=root)
+    # run the arm as bench.py's __main__, then list what the process mapped:
+    # the oracle's library, never the CUDA decode library
+    code = ("import runpy, sys; sys.argv = ['bench.py', '--impl', 'reference', '--config', "
+            "'bs4_kv1024_bf16', '--steps', '1', '--warmup', '0']; "
+            "runpy.run_path('bench.py', run_name='__main__'); "
+            "maps = open('/proc/self/maps').read(); "
+            "print('MAPS', 'libmla_decode' in maps, 'libmla_oracle' in maps, "
+            "'mla_decode_stage1_gb300' in sys.modules)")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300,
+                       cwd=root)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [l for l in r.stdout.splitlines() if l.strip()]
-    d = json.loads(lines[-1])
+    assert lines[-1] == "MAPS False True False", lines[-1]
+    d = json.loads(lines[-2])
     for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
                 "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
                 "cpu_baseline", "e2e"):

@@ -74,6 +74,7 @@ def test_e2m1_matches_page_lut():
     vals = np.array([float(r[1]) for r in rows])
     ours = oracle.decode("e2m1", codes)
     assert np.array_equal(ours, vals)
+    # the sign of the zero at code 8 follows the format (see the file's header)
     assert np.array_equal(np.signbit(ours), np.signbit(vals))
 
 

@@ -27,7 +27,7 @@ def _mla():
 
 def run_gpu(w, num_splits=0, num_sms=0):
     mla = _mla()
-    from mla_decode_stage1_gb300 import synth  # noqa: F401
+    import workloads as synth  # noqa: F401
     plan = mla.mla_decode_plan(w.kv_indptr, w.kv_last_page_len, page_size=w.page_size,
                                q_dtype=w.q_dtype, kv_dtype=w.kv_dtype, num_splits=num_splits,
                                num_sms=num_sms, q_len=w.q_len)
@@ -61,7 +61,7 @@ def compare(o, lse, o_ref, l_ref, kv_dtype, lengths):
 
 
 def check(w, num_splits=0, num_sms=0, select=None):
-    from mla_decode_stage1_gb300 import synth
+    import workloads as synth
     o, lse, plan = run_gpu(w, num_splits=num_splits, num_sms=num_sms)
     sel = list(range(w.bs)) if select is None else list(select)
     o_ref, l_ref = oracle.mla_decode(**synth.oracle_args(w, select=sel))
@@ -79,7 +79,7 @@ COMBOS = [("bf16", "bf16"), ("bf16", "fp8"), ("fp8", "fp8"), ("fp8", "bf16")]
 
 @pytest.mark.parametrize("q_dtype,kv_dtype", COMBOS)
 def test_ragged_contiguous(q_dtype, kv_dtype):
-    from mla_decode_stage1_gb300 import synth
+    import workloads as synth
     lengths = [1, 127, 128, 129, 300, 0, 1000]
     w = synth.make_workload(bs=len(lengths), lengths=lengths, page_size=1, q_dtype=q_dtype,
                             kv_dtype=kv_dtype, seed=21)
@@ -91,7 +91,7 @@ def test_ragged_contiguous(q_dtype, kv_dtype):
 def test_paged_permuted_partial_pages(q_dtype, kv_dtype, page_size):
     # page sizes that are multiples of 8 use one TMA box per 8-row group,
     # the others gather every row through its own page-table entry
-    from mla_decode_stage1_gb300 import synth
+    import workloads as synth
     lengths = [5, 700, 1, 0, 2049, 383]
     w = synth.make_workload(bs=len(lengths), lengths=lengths, page_size=page_size,
                             q_dtype=q_dtype, kv_dtype=kv_dtype, permute_pages=True, seed=22,
@@ -101,7 +101,7 @@ def test_paged_permuted_partial_pages(q_dtype, kv_dtype, page_size):
 
 @pytest.mark.parametrize("num_splits", [1, 2, 3, 7])
 def test_forced_splits(num_splits):
-    from mla_decode_stage1_gb300 import synth
+    import workloads as synth
     lengths = [1, 130, 900, 4096, 0]
     w = synth.make_workload(bs=len(lengths), lengths=lengths, page_size=8, q_dtype="bf16",
                             kv_dtype="fp8", permute_pages=True, seed=23)
@@ -112,7 +112,7 @@ def test_forced_splits(num_splits):
 def test_few_ctas_many_items(num_sms):
     # few CTAs: each walks many items and tiles (ring wrap, q double buffer,
     # item boundaries inside the pipeline)
-    from mla_decode_stage1_gb300 import synth
+    import workloads as synth
     lengths = [300, 1, 1024, 129, 77, 2000, 0, 640]
     for qd, kd in (("bf16", "fp8"), ("fp8", "fp8"), ("bf16", "bf16")):
         w = synth.make_workload(bs=len(lengths), lengths=lengths, page_size=16, q_dtype=qd,
@@ -120,31 +120,44 @@ def test_few_ctas_many_items(num_sms):
         check(w, num_sms=num_sms)
 
 
-@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8", "mxfp4"])
 def test_peaked_softmax_and_rescale(kv_dtype):
-    # q scaled up: a few tokens dominate, outputs are O(1) and the running max
-    # keeps growing across tiles (forces the O rescale path).
-    from mla_decode_stage1_gb300 import synth
+    # q scaled up: a few tokens dominate, outputs are O(1), and KV rows scaled
+    # by a growing factor (before they are encoded) make later tokens score
+    # higher, so the running max keeps growing across tiles (the O rescale
+    # path) in every format
+    import workloads as synth
     lengths = [1500, 640, 3000]
     w = synth.make_workload(bs=3, lengths=lengths, page_size=1, q_dtype="bf16", kv_dtype=kv_dtype,
-                            seed=25, q_std=6.0)
-    # make later tokens score higher: scale KV rows by a growing factor
-    kv = w.kv
-    if kv_dtype == "bf16":
-        ramp = torch.linspace(0.5, 1.5, kv.shape[0]).unsqueeze(1)
-        w.kv = (kv.float() * ramp).to(torch.bfloat16)
+                            seed=25, q_std=6.0, kv_ramp=(0.5, 1.5))
     check(w, num_sms=2)
 
 
+def test_bf16_q_wide_range_within_a_request_fp8_kv():
+    # bf16 q meeting fp8 KV is split into two e4m3 terms with one scale per
+    # request: one head 2^8 larger than the others and the rope dims 2^-6
+    # smaller put most elements far below the request's largest |q|
+    import workloads as synth
+    lengths = [700, 129, 2000, 1]
+    w = synth.make_workload(bs=4, lengths=lengths, page_size=8, q_dtype="bf16", kv_dtype="fp8",
+                            permute_pages=True, seed=59)
+    q = w.q.float()
+    q[:, 3, :] *= 2.0 ** 8
+    q[:, :, 512:] *= 2.0 ** -6
+    w.q = q.to(torch.bfloat16)
+    check(w)
+    check(w, num_splits=3)
+
+
 def test_single_request_single_token():
-    from mla_decode_stage1_gb300 import synth
+    import workloads as synth
     for qd, kd in COMBOS:
         w = synth.make_workload(bs=1, lengths=[1], page_size=1, q_dtype=qd, kv_dtype=kd, seed=26)
         check(w)
 
 
 def test_all_empty_batch():
-    from mla_decode_stage1_gb300 import synth
+    import workloads as synth
     w = synth.make_workload(bs=2, lengths=[0, 0], page_size=1, q_dtype="bf16", kv_dtype="fp8",
                             seed=27)
     o, lse, _ = run_gpu(w)
@@ -153,7 +166,7 @@ def test_all_empty_batch():
 
 @pytest.mark.parametrize("name", ["bs4_kv1024_bf16", "bs32_kv1024_fp8kv"])
 def test_small_benchmark_configs_full(name):
-    from mla_decode_stage1_gb300 import synth
+    import workloads as synth
     check(synth.make_config(name))
 
 
@@ -161,7 +174,7 @@ def test_small_benchmark_configs_full(name):
 def test_large_benchmark_configs_sampled(name):
     # the full configuration on the GPU, in the launch configuration the
     # benchmark times; the oracle checks a seeded sample of requests
-    from mla_decode_stage1_gb300 import synth
+    import workloads as synth
     w = synth.make_config(name, device="cuda")
     rng = np.random.default_rng(7)
     sel = sorted(rng.choice(w.bs, size=6, replace=False).tolist() + [0, w.bs - 1])
@@ -170,7 +183,7 @@ def test_large_benchmark_configs_sampled(name):
 
 @pytest.mark.parametrize("page_size,permute", [(1, False), (16, True)])
 def test_mxfp4_ragged(page_size, permute):
-    from mla_decode_stage1_gb300 import synth
+    import workloads as synth
     lengths = [1, 127, 128, 129, 700, 0, 2049]
     w = synth.make_workload(bs=len(lengths), lengths=lengths, page_size=page_size, q_dtype="bf16",
                             kv_dtype="mxfp4", permute_pages=permute, seed=41)
@@ -178,7 +191,7 @@ def test_mxfp4_ragged(page_size, permute):
 
 
 def test_mxfp4_wide_scale_rows_and_few_ctas():
-    from mla_decode_stage1_gb300 import synth
+    import workloads as synth
     lengths = [300, 1024, 5, 2000]
     w = synth.make_workload(bs=4, lengths=lengths, page_size=1, q_dtype="bf16", kv_dtype="mxfp4",
                             seed=42, scale_stride=48)
@@ -188,7 +201,7 @@ def test_mxfp4_wide_scale_rows_and_few_ctas():
 
 def test_mxfp4_spread_block_exponents():
     # scale exponents spread over 8 binades inside a token: still exact
-    from mla_decode_stage1_gb300 import synth
+    import workloads as synth
     w = synth.make_workload(bs=2, lengths=[500, 77], page_size=1, q_dtype="bf16",
                             kv_dtype="mxfp4", seed=43)
     g = torch.Generator().manual_seed(5)
@@ -200,7 +213,7 @@ def test_mxfp4_very_spread_block_exponents():
     # exponents spread over 30 binades inside a token: blocks more than 8
     # binades below the row's largest are rounded to e4m3 subnormals or to 0
     # (they are then below 2^-8 of that block, far inside the tolerance)
-    from mla_decode_stage1_gb300 import synth
+    import workloads as synth
     w = synth.make_workload(bs=3, lengths=[300, 129, 1000], page_size=8, permute_pages=True,
                             q_dtype="bf16", kv_dtype="mxfp4", seed=45)
     g = torch.Generator().manual_seed(6)
@@ -208,22 +221,22 @@ def test_mxfp4_very_spread_block_exponents():
     check(w)
 
 
-def test_mxfp4_unsupported_scale_stride():
-    mla = _mla()
-    from mla_decode_stage1_gb300 import synth
-    w = synth.make_workload(bs=1, lengths=[64], page_size=1, q_dtype="bf16", kv_dtype="mxfp4",
-                            seed=44, scale_stride=18)
-    plan = mla.mla_decode_plan(w.kv_indptr, None, page_size=1, q_dtype="bf16", kv_dtype="mxfp4")
-    d = w.to("cuda")
-    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
-    out = torch.empty(1, 16, 512, dtype=torch.bfloat16, device="cuda")
-    with pytest.raises(mla.MlaError) as e:
-        mla.mla_decode_run(plan, d.q, d.kv, out, workspace=ws, kv_e8m0=d.kv_e8m0)
-    assert e.value.status == 2
+@pytest.mark.parametrize("scale_stride", [18, 32, 48])
+@pytest.mark.parametrize("page_size,permute", [(1, False), (8, True), (24, True)])
+def test_mxfp4_scale_row_strides(scale_stride, page_size, permute):
+    # the pages' 18-byte e8m0 rows and wider strides; contiguous and paged
+    # pools, a ragged last tile and an empty request
+    import workloads as synth
+    lengths = [300, 0, 129, 1000, 64]
+    w = synth.make_workload(bs=len(lengths), lengths=lengths, page_size=page_size,
+                            q_dtype="bf16", kv_dtype="mxfp4", permute_pages=permute,
+                            seed=44, scale_stride=scale_stride, extra_pool_pages=2)
+    assert w.kv_e8m0.shape[1] == scale_stride
+    check(w)
 
 
 def test_mxfp4_benchmark_config_sampled():
-    from mla_decode_stage1_gb300 import synth
+    import workloads as synth
     w = synth.make_config("bs256_varkv_mxfp4", device="cuda")
     rng = np.random.default_rng(8)
     sel = sorted(rng.choice(w.bs, size=6, replace=False).tolist() + [0, w.bs - 1])
@@ -234,7 +247,7 @@ def test_split_merge_repeated_launches_same_workspace():
     # the plan's table is uploaded on the first launch into a workspace only;
     # later launches reuse it and must give identical results
     mla = _mla()
-    from mla_decode_stage1_gb300 import synth
+    import workloads as synth
     lengths = [900, 0, 4096, 130, 2500]
     w = synth.make_workload(bs=len(lengths), lengths=lengths, page_size=8, q_dtype="bf16",
                             kv_dtype="fp8", permute_pages=True, seed=46)
@@ -269,7 +282,7 @@ def test_soak_interleaved_plans_are_deterministic(q_dtype, kv_dtype, q_len):
     # wait may give up, every repeat must be bitwise identical to the plan's
     # first result, and the first results must match the oracle.
     mla = _mla()
-    from mla_decode_stage1_gb300 import synth
+    import workloads as synth
     ps = 1 if kv_dtype == "mxfp4" else 8
     rng = np.random.default_rng(70 + len(q_dtype) + len(kv_dtype) + q_len)
     wa = synth.make_workload(bs=24, lengths=[int(x) for x in rng.integers(0, 3000, 24)], page_size=ps,
@@ -319,7 +332,7 @@ def test_soak_interleaved_plans_are_deterministic(q_dtype, kv_dtype, q_len):
 def test_one_long_request_over_every_sm(kv_dtype):
     # one request cut into as many items as there are CTAs: stage 2 merges
     # well over a hundred partials per head
-    from mla_decode_stage1_gb300 import synth
+    import workloads as synth
     n = 40000
     w = synth.make_workload(bs=2, lengths=[n, 0], page_size=1, q_dtype="bf16",
                             kv_dtype=kv_dtype, seed=47)
@@ -333,7 +346,7 @@ def test_one_long_request_over_every_sm(kv_dtype):
 @pytest.mark.parametrize("q_len", [2, 4])
 def test_qlen_causal_decode(q_dtype, kv_dtype, q_len):
     # requests shorter than q_len leave their first query tokens empty
-    from mla_decode_stage1_gb300 import synth
+    import workloads as synth
     lengths = [1, 3, 130, 0, 1000, 2049]
     page = 8 if kv_dtype == "mxfp4" else 4
     w = synth.make_workload(bs=len(lengths), lengths=lengths, page_size=page, q_dtype=q_dtype,
@@ -346,7 +359,7 @@ def test_qlen_causal_decode(q_dtype, kv_dtype, q_len):
 def test_qlen_splits_and_few_ctas(num_splits, num_sms, q_len):
     # fp8 q + fp8 KV with an even number of query tokens runs them in pairs
     # (32 q rows per tile); three tokens run as causal prefixes
-    from mla_decode_stage1_gb300 import synth
+    import workloads as synth
     lengths = [700, 5, 4096, 129, 1, 2, 128]
     w = synth.make_workload(bs=len(lengths), lengths=lengths, page_size=16, q_dtype="fp8",
                             kv_dtype="fp8", permute_pages=True, seed=49, q_len=q_len)
@@ -356,7 +369,7 @@ def test_qlen_splits_and_few_ctas(num_splits, num_sms, q_len):
 def test_qlen2_fp8_token_zero_without_kv_in_an_item():
     # items that hold only a request's last token leave query token 0 with no
     # token to attend to in that item (partial lse = -inf, weight 0)
-    from mla_decode_stage1_gb300 import synth
+    import workloads as synth
     lengths = [129, 257, 1, 2049]
     w = synth.make_workload(bs=4, lengths=lengths, page_size=1, q_dtype="fp8", kv_dtype="fp8",
                             seed=51, q_len=2)
@@ -367,7 +380,7 @@ def test_qlen2_fp8_token_zero_without_kv_in_an_item():
 def test_qlen2_fp8_peaked_scores():
     # large scores: the running max moves across tiles and the lazy rescale
     # runs on 16-row groups
-    from mla_decode_stage1_gb300 import synth
+    import workloads as synth
     w = synth.make_workload(bs=3, lengths=[1500, 640, 3000], page_size=8, q_dtype="fp8",
                             kv_dtype="fp8", permute_pages=True, seed=52, q_len=2, q_std=6.0)
     check(w, num_sms=2)
@@ -378,7 +391,7 @@ def test_qlen_large_batch_sampled(q_dtype):
     # bs=64 x 8192 tokens, two query tokens, in the balanced launch the
     # planner picks (one CTA group per query token)
     _mla()
-    from mla_decode_stage1_gb300 import synth
+    import workloads as synth
     w = synth.make_workload(bs=64, lengths=[8192] * 64, page_size=8, q_dtype=q_dtype,
                             kv_dtype="fp8", permute_pages=True, seed=50, q_len=2, device="cuda")
     rng = np.random.default_rng(9)
@@ -412,7 +425,7 @@ def test_random_sweep(seed):
     # formats, lengths (empty, partial tiles), page sizes (row gather and
     # 8-row boxes), page permutation, several query tokens, fixed splits and
     # few-CTA plans drawn from one seed; every output against the oracle
-    from mla_decode_stage1_gb300 import synth
+    import workloads as synth
     kw, num_splits, num_sms = _random_case(seed)
     w = synth.make_workload(seed=60 + seed, **kw)
     check(w, num_splits=num_splits, num_sms=num_sms)
@@ -426,7 +439,7 @@ def test_bounded_wait_times_out_and_context_survives():
     # workspace then decode correctly
     mla = _mla()
     import time
-    from mla_decode_stage1_gb300 import synth
+    import workloads as synth
     w = synth.make_workload(bs=3, lengths=[300, 0, 1000], page_size=8, q_dtype="bf16",
                             kv_dtype="fp8", permute_pages=True, seed=53)
     plan = mla.mla_decode_plan(w.kv_indptr, w.kv_last_page_len, page_size=8, q_dtype="bf16",
@@ -450,12 +463,93 @@ def test_bounded_wait_times_out_and_context_survives():
             o_ref, l_ref, "fp8", w.lengths)
 
 
+def test_workspace_reused_by_another_plan_is_detected():
+    # plan A uploads its table into a workspace; the same memory then serves
+    # as plan B's workspace behind A's back (a caching allocator hands the
+    # address out again).  A's next run finds B's stamp: it writes nothing
+    # and mla_decode_check reports MLA_ERR_WORKSPACE.  A's run after that
+    # uploads its table again and is correct.
+    mla = _mla()
+    import workloads as synth
+    wa = synth.make_workload(bs=4, lengths=[700, 1, 3000, 129], page_size=8, q_dtype="fp8",
+                             kv_dtype="fp8", permute_pages=True, seed=56)
+    wb = synth.make_workload(bs=3, lengths=[50, 5000, 0], page_size=8, q_dtype="fp8",
+                             kv_dtype="fp8", permute_pages=True, seed=57)
+    pa = mla.mla_decode_plan(wa.kv_indptr, wa.kv_last_page_len, page_size=8, q_dtype="fp8",
+                             kv_dtype="fp8")
+    pb = mla.mla_decode_plan(wb.kv_indptr, wb.kv_last_page_len, page_size=8, q_dtype="fp8",
+                             kv_dtype="fp8", num_splits=3)
+    assert pa.info().num_merge_jobs > 0 and pb.info().num_merge_jobs > 0
+    da, db = wa.to("cuda"), wb.to("cuda")
+    ws = torch.empty(max(pa.workspace_bytes, pb.workspace_bytes), dtype=torch.uint8, device="cuda")
+
+    def run(plan, w, d):
+        out = torch.full((w.bs, 16, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+        lse = torch.full((w.bs, 16), float("nan"), dtype=torch.float32, device="cuda")
+        mla.mla_decode_run(plan, d.q, d.kv, out, workspace=ws, q_scale=d.q_scale,
+                           kv_scale=d.kv_scale, kv_indices=d.kv_indices, lse=lse)
+        return out, lse
+
+    out0, lse0 = run(pa, wa, da)
+    mla.mla_decode_check(pa, ws)
+    run(pb, wb, db)                                   # B's table replaces A's
+    mla.mla_decode_check(pb, ws)
+    out1, lse1 = run(pa, wa, da)                      # A believes its table is there
+    with pytest.raises(mla.MlaError) as e:
+        mla.mla_decode_check(pa, ws)
+    assert e.value.status == 3                        # MLA_ERR_WORKSPACE
+    assert torch.isnan(out1.float()).all() and torch.isnan(lse1).all()   # nothing written
+    out2, lse2 = run(pa, wa, da)                      # uploads A's table again
+    mla.mla_decode_check(pa, ws)
+    assert torch.equal(out2, out0) and torch.equal(lse2, lse0)
+    o_ref, l_ref = oracle.mla_decode(**synth.oracle_args(wa))
+    compare(out2.float().cpu().numpy().astype(np.float64), lse2.cpu().numpy().astype(np.float64),
+            o_ref, l_ref, "fp8", wa.lengths)
+
+
+@pytest.mark.parametrize("kv_dtype,page_size", [("fp8", 8), ("bf16", 4), ("mxfp4", 8),
+                                                ("fp8", 3)])
+def test_page_outside_the_pool_is_reported(kv_dtype, page_size):
+    # one page-table entry of request 1 points past the pool (and one of
+    # request 3 is negative): the kernels read page 0 in their place, touch
+    # nothing outside the pool, and mla_decode_check reports
+    # MLA_ERR_INVALID_ARG once; the other requests are unaffected
+    mla = _mla()
+    import workloads as synth
+    lengths = [300, 200, 129, 77]
+    w = synth.make_workload(bs=4, lengths=lengths, page_size=page_size, q_dtype="bf16",
+                            kv_dtype=kv_dtype, permute_pages=True, seed=58)
+    pool_pages = w.pool_rows // page_size
+    ind = w.kv_indices.clone()
+    ind[int(w.kv_indptr[1]) + 1] = pool_pages + 7
+    ind[int(w.kv_indptr[3])] = -1
+    w.kv_indices = ind
+    plan = mla.mla_decode_plan(w.kv_indptr, w.kv_last_page_len, page_size=page_size,
+                               q_dtype="bf16", kv_dtype=kv_dtype)
+    d = w.to("cuda")
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
+    out = torch.full((w.bs, 16, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((w.bs, 16), float("nan"), dtype=torch.float32, device="cuda")
+    mla.mla_decode_run(plan, d.q, d.kv, out, workspace=ws, kv_scale=d.kv_scale,
+                       kv_e8m0=d.kv_e8m0, kv_indices=d.kv_indices, lse=lse)
+    with pytest.raises(mla.MlaError) as e:
+        mla.mla_decode_check(plan, ws)
+    assert e.value.status == 1                        # MLA_ERR_INVALID_ARG
+    mla.mla_decode_check(plan, ws)                    # reported once, then cleared
+    o = out.float().cpu().numpy().astype(np.float64)
+    l = lse.cpu().numpy().astype(np.float64)
+    assert np.isfinite(o).all()
+    good = [0, 2]
+    o_ref, l_ref = oracle.mla_decode(**synth.oracle_args(w, select=good))
+    compare(o[good], l[good], o_ref, l_ref, kv_dtype, [lengths[b] for b in good])
+
+
 def test_decode_call_captures_in_a_cuda_graph():
     # after one run has uploaded the plan's table into the workspace, a call
     # only launches kernels on the stream: it can be captured in a CUDA graph
     # and replayed (stage 2 keeps its programmatic dependency on stage 1)
     mla = _mla()
-    from mla_decode_stage1_gb300 import synth
+    import workloads as synth
     w = synth.make_workload(bs=5, lengths=[700, 1, 0, 3000, 129], page_size=8, q_dtype="fp8",
                             kv_dtype="fp8", permute_pages=True, seed=54)
     plan = mla.mla_decode_plan(w.kv_indptr, w.kv_last_page_len, page_size=8, q_dtype="fp8",
@@ -489,7 +583,7 @@ def test_decode_call_captures_in_a_cuda_graph():
 def test_many_partials_per_request_wide_merge(q_len):
     # more than 4 partials per request: stage 2 merges with one CTA of eight
     # warps per output row; empty requests and short ones in the same batch
-    from mla_decode_stage1_gb300 import synth
+    import workloads as synth
     lengths = [5000, 0, 1, 130, 3000]
     w = synth.make_workload(bs=len(lengths), lengths=lengths, page_size=8, q_dtype="fp8",
                             kv_dtype="fp8", permute_pages=True, seed=55, q_len=q_len)

@@ -4,7 +4,9 @@ This module only *makes inputs*: Gaussian q and latent KV, the storage
 encodings the KV cache arrives in (bf16, fp8-e4m3 with a per-tensor scale,
 MXFP4), page tables and request lengths.  It holds none of the decode
 arithmetic, and both the CUDA path and the fp64 oracle take their inputs
-from here.
+from here.  It lives outside the library package on purpose, so that the
+oracle-side processes (the CPU baseline, the reference arm of bench.py) never
+load the CUDA library.
 
 Input recipe (the leaderboard's own generator is not on the pages; these
 follow the facts the pages state):
@@ -89,7 +91,7 @@ def quant_fp8_per_tensor(x: torch.Tensor):
     return q.view(torch.uint8), scale.to(torch.float32)
 
 
-MX_SCALE_STRIDE = 32   # e8m0 bytes per row: 18 used, padded to a 16-byte multiple
+MX_SCALE_STRIDE = 18   # e8m0 bytes per row, as the pages store them
 
 
 def quant_mxfp4_rows(x: torch.Tensor, scale_stride: int = MX_SCALE_STRIDE):
@@ -116,12 +118,16 @@ def quant_mxfp4_rows(x: torch.Tensor, scale_stride: int = MX_SCALE_STRIDE):
 def make_workload(*, bs: int, lengths, page_size: int = 1, q_dtype: str = "bf16",
                   kv_dtype: str = "bf16", permute_pages: bool = False, seed: int = 0,
                   device="cpu", scale_stride: int = MX_SCALE_STRIDE, name: str = "custom",
-                  q_std: float = 1.0, extra_pool_pages: int = 0, q_len: int = 1) -> Workload:
+                  q_std: float = 1.0, extra_pool_pages: int = 0, q_len: int = 1,
+                  kv_ramp=None) -> Workload:
     """Build a seeded workload.  `lengths` is a list of token counts (0 allowed).
     q_len query tokens per request give q rows [bs*q_len, 16, 576].
     Pages hold `page_size` tokens; the last page of a request may be partial
     (kv_last_page_len).  permute_pages scatters every request's pages through
-    a seeded permutation of the whole pool."""
+    a seeded permutation of the whole pool.  kv_ramp=(lo, hi) scales pool row
+    r of the Gaussian source by lo + (hi - lo) r / (rows - 1) before it is
+    encoded, so that later rows score ever higher (a running maximum that
+    keeps moving)."""
     lengths = [int(x) for x in lengths]
     assert len(lengths) == bs and page_size >= 1
     g = torch.Generator(device=device)
@@ -136,6 +142,8 @@ def make_workload(*, bs: int, lengths, page_size: int = 1, q_dtype: str = "bf16"
 
     q32 = torch.randn(bs * q_len, HEADS, QK_DIM, generator=g, device=device) * q_std
     kv32 = torch.randn(rows, QK_DIM, generator=g, device=device)
+    if kv_ramp is not None:
+        kv32 *= torch.linspace(float(kv_ramp[0]), float(kv_ramp[1]), rows, device=device).unsqueeze(1)
     if permute_pages:
         perm = torch.randperm(total_pages, generator=g, device=device).to(torch.int32)
         indices = perm[: sum(npages)].cpu()
