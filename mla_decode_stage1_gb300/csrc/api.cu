@@ -255,23 +255,6 @@ bool make_kv_map(CUtensorMap* map, const void* kv, int kv_dtype, int64_t rows, i
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// MXFP4 pool: packed rows of 288 bytes as a 3-D tensor {32 B, row, chunk}
-// (chunk = the 64 values of two scale blocks); a box of box_rows rows lands
-// chunk-major as [chunk][row][32 B] (no swizzle).  The e8m0 scale rows are
-// not copied by TMA: the dequantising threads read them from global memory,
-// so that any row stride (the pages' rows are 18 bytes) is accepted.
-bool make_mx_map(CUtensorMap* kvmap, const void* kv, int64_t rows, int box_rows) {
-  EncodeTiledFn enc = encode_fn();
-  if (enc == nullptr) return false;
-  const cuuint64_t dims[3] = {32, static_cast<cuuint64_t>(rows), 9};
-  const cuuint64_t strides[2] = {288, 32};
-  const cuuint32_t box[3] = {32, static_cast<cuuint32_t>(box_rows), 9};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return enc(kvmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(kv), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 }  // namespace
@@ -454,27 +437,25 @@ mla_status mla_decode_run(mla_plan* plan, const void* q, const float* q_scale, c
   // page size that is a multiple of 8: one box per 8-row group (a group never
   // straddles a page).  Other page sizes (bf16 / fp8 KV): every row is
   // gathered on its own (cp.async), laid out as for the identity table.
+  // MXFP4 rows are copied with plain bulk copies (no tensor map) and
+  // dequantised into the 8-row-group layout, for any page size.
+  const bool mx = plan->kv_dtype == MLA_DTYPE_MXFP4;
   int box_rows = mla::kTile;
   int gather = 0;
   if (kv_indices != nullptr) {
     if (kv_pool_rows % plan->page_size != 0) return MLA_ERR_INVALID_ARG;
-    if (plan->page_size % 8 == 0)
+    if (plan->page_size % 8 == 0 || mx)
       box_rows = 8;
-    else if (plan->kv_dtype == MLA_DTYPE_MXFP4)
-      return MLA_ERR_UNSUPPORTED;
     else
       gather = 1;
   }
-  // MXFP4 rows are dequantised in place box by box: always 8-row boxes
-  if (plan->kv_dtype == MLA_DTYPE_MXFP4) box_rows = 8;
+  if (mx) box_rows = 8;
   // bytes per row of the tile the UMMAs read (MXFP4 is dequantised to e4m3)
   const uint32_t row_bytes = mla::kQkDim * (plan->kv_dtype == MLA_DTYPE_BF16 ? 2 : 1);
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-  if (plan->tmap_ptr != kv || plan->tmap_rows != kv_pool_rows || plan->tmap_box_rows != box_rows) {
-    const bool ok = plan->kv_dtype == MLA_DTYPE_MXFP4
-                        ? make_mx_map(&plan->tmap, kv, kv_pool_rows, box_rows)
-                        : make_kv_map(&plan->tmap, kv, plan->kv_dtype, kv_pool_rows, box_rows);
-    if (!ok) return MLA_ERR_CUDA;
+  if (!mx && (plan->tmap_ptr != kv || plan->tmap_rows != kv_pool_rows ||
+              plan->tmap_box_rows != box_rows)) {
+    if (!make_kv_map(&plan->tmap, kv, plan->kv_dtype, kv_pool_rows, box_rows)) return MLA_ERR_CUDA;
     plan->tmap_ptr = kv;
     plan->tmap_rows = kv_pool_rows;
     plan->tmap_box_rows = box_rows;

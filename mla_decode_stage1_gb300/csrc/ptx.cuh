@@ -90,9 +90,9 @@ __device__ __forceinline__ int32_t ld_nc_early(const int32_t* ptr) {
   return v;
 }
 
-__device__ __forceinline__ uint16_t ld_nc_u16_early(const uint16_t* ptr) {
+__device__ __forceinline__ uint32_t ld_nc_u8_early(const uint8_t* ptr) {
   uint16_t v;
-  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(ptr));
+  asm volatile("ld.global.nc.u8 %0, [%1];" : "=h"(v) : "l"(ptr));
   return v;
 }
 
@@ -151,6 +151,16 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
+// The same with an L2 cache policy.
+__device__ __forceinline__ void bulk_load_hint(uint32_t dst, const void* src, uint32_t bytes,
+                                               uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
 // 3-D tiled bulk tensor load (coordinates innermost first).
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int32_t x, int32_t y, int32_t z, uint64_t policy) {
@@ -167,6 +177,20 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
 }
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ----------------------------------------------------- register reallocation
+// Per-warpgroup register limits (all four warps of a warpgroup execute it).
+// Raising a limit draws on the registers the CTA was launched with
+// (threads x registers per thread at launch): the sum of the warpgroups'
+// limits must stay within that pool, or the raising warps wait forever.
+template <uint32_t N>
+__device__ __forceinline__ void regs_raise() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N) : "memory");
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_lower() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N) : "memory");
 }
 
 // ------------------------------------------------------------------- tcgen05

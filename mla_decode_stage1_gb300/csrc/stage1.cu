@@ -21,13 +21,16 @@
 //  * a tcgen05.mma costs the issuing thread about the same time whatever
 //    its N, so QK^T and PV are issued by separate warps that run side by
 //    side: warps 1 and 3 each issue half of the QK^T K-steps into their own
-//    S accumulator; warps 2 and 13 issue PV for O blocks 0-1 and 2-3 (MXFP4:
-//    warp 2 alone).  Warp 0 is the TMA producer; warps 4-11 do the softmax
-//    and the epilogue in two groups of 8 heads (two-token mode: one group
-//    per query token, 16 heads each; one thread per token / per
+//    S accumulator; warps 2 and 13 (MXFP4: 2 and 0) issue PV for O blocks
+//    0-1 and 2-3.  Warp 0 is the TMA producer (bf16 / fp8); warps 4-11 do
+//    the softmax and the epilogue in two groups of 8 heads (two-token mode:
+//    one group per query token, 16 heads each; one thread per token / per
 //    output dim, TMEM lane = thread) and convert the first item's q; warp
-//    12 converts the q of later items (MXFP4: warps 12-15 dequantise the
-//    packed rows in place and prepare every item's q);
+//    12 converts the q of later items;
+//  * MXFP4: warps 12-19 copy the packed rows into four landing units (plain
+//    bulk copies, any page size), dequantise them into the e4m3 tile slot
+//    and prepare every item's q; the warpgroups then run with their own
+//    register limits (setmaxnreg);
 //  * every mbarrier wait is bounded (see mbar_wait) and reports into the
 //    device error word instead of hanging.
 //
@@ -60,13 +63,22 @@ struct Layout {
   static constexpr int kRows = kHeads * kQL;                        // q rows, token-major
   static constexpr bool kHiLo = (QM == kQBf16KvFp8 || kMx);         // q as two e4m3 terms
   static constexpr int kNq = kRows * (kHiLo ? 2 : 1);               // UMMA N of QK^T
-  // Warps: producer, 2 QK^T issuers, PV issuer(s), two head groups of four
-  // softmax warps (kH q rows each), then either a q warp (14 warps) or, for
-  // MXFP4, 4 dequant warps that also prepare q (16 warps, register cap 128).
+  // Warps: producer (MXFP4: a PV issuer), 2 QK^T issuers, PV issuers, two
+  // head groups of four softmax warps (kH q rows each), then either a q warp
+  // (14 warps) or, for MXFP4, 8 dequant warps that also prepare q and copy
+  // the packed rows (20 warps).
   static constexpr int kHeadGroups = 2;
   static constexpr int kH = kRows / kHeadGroups;                    // q rows per softmax thread
-  static constexpr int kThreads = kMx ? 512 : 448;
-  static constexpr int kPvIssuers = kMx ? 1 : 2;
+  static constexpr int kThreads = kMx ? 640 : 448;
+  // MXFP4 register plan per warpgroup (setmaxnreg after the launch): the
+  // producer and UMMA issuers need few, the softmax warps many
+  static constexpr int kRegsLaunch = 96;
+  static constexpr int kRegsIssue = 56, kRegsSoftmax = 104, kRegsDequant = 104;
+  static constexpr int kRegsPlanned = 128 * kRegsIssue + 256 * kRegsSoftmax + 256 * kRegsDequant;
+  static_assert(!kMx || (kThreads == 640 && kRegsPlanned <= kThreads * kRegsLaunch &&
+                         kRegsIssue <= kRegsLaunch),
+                "the warpgroups' register limits exceed the launch's pool");
+  static constexpr int kPvIssuers = 2;
   static constexpr int kElem = kKv8 ? 1 : 2;
   static constexpr int kRowBytes = kQkDim * kElem;                  // 576 | 1152
   static constexpr int kChunks = kRowBytes / 64;                    // 64-byte column chunks
@@ -81,25 +93,35 @@ struct Layout {
   static constexpr int kRawRowBytes = kQkDim / 2;                   // packed MXFP4 row
   static constexpr bool kQ8 = (QM == kQFp8KvFp8 || QM == kQFp8KvBf16 || QM == kQFp8KvFp8x2);
   static constexpr int kQSrcBytes = kRows * kQkDim * (kQ8 ? 1 : 2);  // one request's q
+  // q staging buffer (raw q of the next item); MXFP4 converts q from global
+  // memory, and keeps one q buffer, so that its landing ring fits
+  static constexpr int kQStageBytes = kMx ? 0 : kQSrcBytes;
+  static constexpr int kQBufs = kMx ? 1 : 2;
   static constexpr uint32_t kOCols = kRows * (kKv8 ? 2 : 1);       // TMEM columns per O block
   // TMEM: S^T at 0 (2 buffers x 2 K-halves x 32 columns), O^T from 128
   static constexpr uint32_t kTmemCols = 128 + 4 * kOCols <= 256 ? 256 : 512;
   static constexpr int kMiscBytes = 2560;
-  static constexpr int kScRowBytes = kMx ? kTile * 24 : 0;         // e8m0 row of each dequant thread
+  // MXFP4: packed rows land in kUnits landing units, unit q holding rows
+  // 32q .. 32q+31 of every tile (row-major, 288 bytes a row)
+  static constexpr int kUnitRows = 32;
+  static constexpr int kUnitBytes = kUnitRows * kRawRowBytes;      // 9216
+  static constexpr int kUnits = kMx ? 4 : 0;
   static constexpr int kMaxSmem = 232448;
   static constexpr int kNumTiles =
-      (kMaxSmem - 1024 - 2 * kQBytes - 2 * kPBytes - kMiscBytes - kScRowBytes - kQSrcBytes) /
-      kTileBytes;
+      kMx ? 2
+          : (kMaxSmem - 1024 - kQBufs * kQBytes - 2 * kPBytes - kMiscBytes - kQStageBytes) /
+                kTileBytes;
   static constexpr int kQOff = kNumTiles * kTileBytes;
-  static constexpr int kPOff = kQOff + 2 * kQBytes;
+  static constexpr int kPOff = kQOff + kQBufs * kQBytes;
   static constexpr int kMiscOff = kPOff + 2 * kPBytes;
-  static constexpr int kScRowOff = kMiscOff + kMiscBytes;
-  static constexpr int kQStageOff = kScRowOff + kScRowBytes;         // raw q of the next item
-  static constexpr int kSmemBytes = kQStageOff + kQSrcBytes + 1024;
+  static constexpr int kUnitOff = kMiscOff + kMiscBytes;
+  static constexpr int kQStageOff = kUnitOff + kUnits * kUnitBytes;  // raw q of the next item
+  static constexpr int kSmemBytes = kQStageOff + kQStageBytes + 1024;
   static_assert(kNumTiles >= 1 && kNumTiles <= 4, "tile ring");
   static_assert(kSmemBytes <= kMaxSmem, "shared memory over budget");
   static_assert(kTileBytes % 1024 == 0 && kQBytes % 1024 == 0, "operand alignment");
   static_assert(kNq <= 32, "S^T columns per K-half");
+  static_assert(kUnitOff % 16 == 0 && kUnitBytes % 16 == 0, "bulk copy alignment");
 };
 
 // Misc region: barriers, reduction scratch, q scales, TMEM address.
@@ -114,12 +136,12 @@ struct Misc {
   uint64_t q_stage_free;             // the softmax warps converted the first item's q
   float qred[8];                     // per-warp |q| maxima (q prepared by a warp group)
   // MXFP4 only
-  uint64_t deq[4];                   // tile slot dequantised (128 dequant threads)
-  uint64_t deq_a[4];                 // its dims 0-319 dequantised (first QK^T K-half)
-  uint64_t upper_free[4];            // PV no longer reads the slot's upper box halves
-  int32_t abort_dq;                  // set by a dequant thread whose bounded wait gave up
+  uint64_t unit_full[4];             // landing unit filled (the two warps of its rows)
+  uint64_t deq_a[4];                 // tile slot chunks 0-4 (dims 0-319) dequantised: the
+                                     // first QK^T K-half (dims 0-287) may start
+  uint64_t deq_b[4];                 // chunks 5-8 dequantised (the slot is complete)
   int32_t stale;                     // the workspace holds another plan's table
-  float uexp[2][128];                // per-token power of two u_t = r_t - 127 of a slot
+  int16_t uexp[2][128];              // per-token power of two u_t = r_t - 127 of a slot
   uint2 e2m1_tab[16];                // e4m3 tables for 2^k, k = index - 14 (k <= -14: all 0)
 };
 static_assert(sizeof(Misc) <= 2560, "misc region");
@@ -237,7 +259,7 @@ __device__ void run_producer(const Stage1Params& p, Misc* ms, uint32_t ring, int
   bool ok = true;
   uint32_t t = 0;
   while (!cur.done() && ok) {
-    if (!L::kMx && p.gather) {
+    if (p.gather) {
       // Page size not a multiple of 8: lane l copies rows l, l+32, l+64,
       // l+96 of the tile, each through its own page-table entry, in 16-byte
       // pieces into the identity-table layout ([chunk][128 rows][64 B], the
@@ -295,7 +317,6 @@ __device__ void run_producer(const Stage1Params& p, Misc* ms, uint32_t ring, int
     ahead.advance();
     const uint32_t s = t % L::kNumTiles, ph = (t / L::kNumTiles) & 1u;
     const uint32_t full = smem_u32(&ms->full[s]);
-    const uint32_t raw_bytes = p.box_rows * L::kRawRowBytes;
     // Before waiting for the slot to be free: resolve the rows and arm the
     // slot's next full phase with the bytes to come.  That arrive must fall
     // in the next phase, so the slot's previous tile must have landed first
@@ -308,23 +329,11 @@ __device__ void run_producer(const Stage1Params& p, Misc* ms, uint32_t ring, int
       ok = __all_sync(0xffffffffu, mbar_wait(full, ph ^ 1u, p.err, kErrProducer));
       if (!ok) break;
     }
-    if (lane == 0)
-      mbar_arrive_expect_tx(full, static_cast<uint32_t>(f.nbox) * (L::kMx ? raw_bytes : box_bytes));
-    // (MXFP4: the packed rows land in the upper box halves, free once PV has
-    // read O blocks 2-3; the dequantisation waits for the whole slot)
-    ok = __all_sync(0xffffffffu, mbar_wait(L::kMx ? smem_u32(&ms->upper_free[s]) : smem_u32(&ms->empty[s]),
-                                           ph ^ 1u, p.err, kErrProducer));
+    if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(f.nbox) * box_bytes);
+    ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ms->empty[s]), ph ^ 1u, p.err, kErrProducer));
     if (!ok) break;
-    if constexpr (L::kMx) {
-      // packed rows of box i into the upper half of box i's e4m3 region
-      // (the e8m0 scale rows are read by the dequantising threads)
-      if (lane < f.nbox)
-        tma_load_3d(ring + s * L::kTileBytes + lane * box_bytes + raw_bytes, &p.tmap_kv, full, 0,
-                    row, 0, pol);
-    } else {
-      if (lane < f.nbox)
-        tma_load_3d(ring + s * L::kTileBytes + lane * box_bytes, &p.tmap_kv, full, 0, row, 0, pol);
-    }
+    if (lane < f.nbox)
+      tma_load_3d(ring + s * L::kTileBytes + lane * box_bytes, &p.tmap_kv, full, 0, row, 0, pol);
     cur.advance();
     ++t;
   }
@@ -358,8 +367,9 @@ __device__ void run_qk(const Stage1Params& p, Misc* ms, uint32_t ring, uint32_t 
   while (!qc.done()) {
     const uint32_t t = qc.t, sb = t & 1u, s = t % L::kNumTiles;
     // the whole warp waits (converged); lane 0 issues
+    const int qb = qc.k % L::kQBufs;
     if (q_ready != qc.k) {
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ms->q_full[qc.k & 1]), (qc.k >> 1) & 1,
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ms->q_full[qb]), (qc.k / L::kQBufs) & 1,
                                              p.err, kErrMma)))
         break;
       q_ready = qc.k;
@@ -367,16 +377,16 @@ __device__ void run_qk(const Stage1Params& p, Misc* ms, uint32_t ring, uint32_t 
     if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ms->s_empty[sb]), ((t >> 1) & 1u) ^ 1u,
                                            p.err, kErrMma)))
       break;
-    // the tile is ready once it landed (MXFP4: once the dims of this K-half
-    // were dequantised)
+    // the tile is ready once it landed (MXFP4: once the chunks holding this
+    // K-half were dequantised: 0-4 for dims 0-287, all for dims 288-575)
     const uint32_t ready = !L::kMx ? smem_u32(&ms->full[s])
-                           : half == 0 ? smem_u32(&ms->deq_a[s]) : smem_u32(&ms->deq[s]);
+                           : half == 0 ? smem_u32(&ms->deq_a[s]) : smem_u32(&ms->deq_b[s]);
     if (!__all_sync(0xffffffffu, mbar_wait(ready, (t / L::kNumTiles) & 1u, p.err, kErrMma)))
       break;
     tc_fence_after();
     if (p.gather) fence_proxy_async_smem();   // rows copied by cp.async (generic proxy)
     const uint32_t tile = ring + s * L::kTileBytes;
-    const uint32_t qaddr = qbase + (qc.k & 1) * L::kQBytes;
+    const uint32_t qaddr = qbase + qb * L::kQBytes;
     const uint32_t d = tmem + kColS + 64 * sb + 32 * half;
     const int k0 = half * (L::kKSteps / 2), k1 = k0 + L::kKSteps / 2;
     if (lane == 0) {
@@ -393,7 +403,7 @@ __device__ void run_qk(const Stage1Params& p, Misc* ms, uint32_t ring, uint32_t 
         umma_f16(d, a, b, idesc, kk != k0);
     }
     tc_commit(smem_u32(&ms->s_full[sb]));
-    if (qc.j == qc.ntile - 1) tc_commit(smem_u32(&ms->q_empty[qc.k & 1]));
+    if (qc.j == qc.ntile - 1) tc_commit(smem_u32(&ms->q_empty[qb]));
     }
     __syncwarp();
     qc.advance();
@@ -426,11 +436,7 @@ __device__ void run_pv(const Stage1Params& p, Misc* ms, uint32_t ring, uint32_t 
     const bool first = pc.j == 0;
     if (lane == 0) {
     for (int i = 0; i < kBlocks; ++i) {
-      // MXFP4 (one issuer): O blocks 2-3 first.  Their V chunks 4-7 and the
-      // rope chunk 8 are the upper half of every 8-row box, where the next
-      // packed rows land, so the producer may refill the slot as soon as
-      // they are read; blocks 0-1 follow.
-      const int c = L::kMx ? (i + 2) & 3 : kBlocks * half + i;
+      const int c = kBlocks * half + i;
       const uint32_t d = tmem + kColO + L::kOCols * c;
       // B = P^T, MN-major: one kPRow-byte row per token (fp8: the q rows of
       // p_hi then of p_lo; bf16: the q rows), 8-token groups of 8 rows, with
@@ -455,7 +461,6 @@ __device__ void run_pv(const Stage1Params& p, Misc* ms, uint32_t ring, uint32_t 
           umma_f16(d, a, b, idesc, (first && kk == 0) ? 0u : 1u);
         }
       }
-      if (L::kMx && i == 1) tc_commit(smem_u32(&ms->upper_free[s]));
     }
     tc_commit(smem_u32(&ms->pv_done[pb]));
     tc_commit(smem_u32(&ms->empty[s]));      // QK^T of this tile completed before P existed
@@ -484,6 +489,17 @@ __device__ __forceinline__ void e2m1_e4m3_table(int k, uint32_t& lo, uint32_t& h
   hi = c | (d << 16);
 }
 
+// The same table computed instead of loaded, for k in [-5, 0]: there every
+// product m 2^k of a nonzero magnitude is a normal e4m3 number, whose code
+// is that of m (0x30, 0x38, 0x3C, 0x40, 0x44, 0x48, 0x4C for .5 .. 6) with
+// k added to the exponent field (bits 3-6), so each nonzero byte moves by
+// 8k.  Below k = -5 the smallest magnitudes turn subnormal: the shared
+// table built by e2m1_e4m3_table() serves those blocks.
+__device__ __forceinline__ void e2m1_e4m3_table_normal(int k, uint32_t& lo, uint32_t& hi) {
+  lo = 0x3C383000u + static_cast<uint32_t>(k) * 0x08080800u;
+  hi = 0x4C484440u + static_cast<uint32_t>(k) * 0x08080808u;
+}
+
 // Eight packed e2m1 codes (nibble n = element n) -> eight e4m3 bytes: the
 // magnitude through the table (byte permute with the sign bits cleared), the
 // sign from bit 3 of each nibble.  That bit is the msb of byte n/2 of w << 4
@@ -498,33 +514,62 @@ __device__ __forceinline__ uint2 e2m1x8_to_e4m3(uint32_t w, uint32_t lo, uint32_
 }
 
 // ------------------------------------------------------- MXFP4 scale rows
-// The dequantising thread of token `tq` reads that token's 18 e8m0 bytes
-// from global memory itself (no TMA box: the pages' scale rows are 18 bytes,
+// The dequantising threads of token `tq` read that token's 18 e8m0 bytes
+// from global memory themselves (no TMA box: the pages' scale rows are 18 bytes,
 // which no tensor map can stride over).  The row is found as the producer
 // finds it: through the page table, a page outside the pool replaced by page
 // 0.  The loads of a tile are issued one tile ahead and its page-table entry
 // two tiles ahead, so neither waits on the path.
 
-// Raw page-table entry of token tq of the cursor's tile (0 for the identity
+// A light cursor over the same tiles as TileCursor, for looking ahead: only
+// what locating a token's pool row needs (ntile == 0 once past the end).
+struct TileAhead {
+  int it, j, ntile, tok_begin, tok_end, page_base;
+  __device__ __forceinline__ void from(const TileCursor& c) {
+    it = c.it;
+    j = c.j;
+    ntile = c.ntile;
+    tok_begin = c.w.tok_begin;
+    tok_end = c.w.tok_end;
+    page_base = c.w.page_base;
+  }
+  __device__ __forceinline__ void advance(const WorkItem* items, int it1) {
+    if (ntile == 0 || ++j < ntile) return;
+    j = 0;
+    ntile = 0;
+    if (++it < it1) {
+      const WorkItem& w = items[it];
+      tok_begin = w.tok_begin;
+      tok_end = w.tok_end;
+      page_base = w.page_base;
+      ntile = (tok_end - tok_begin + kTile - 1) / kTile;
+    }
+  }
+  __device__ __forceinline__ int t0() const { return tok_begin + j * kTile; }
+  __device__ __forceinline__ int nvalid() const { return min(kTile, tok_end - t0()); }
+};
+
+// Raw page-table entry of token tq of a look-ahead tile (0 for the identity
 // table or a token past the tile's end).
-__device__ __forceinline__ int32_t scale_page(const Stage1Params& p, const TileCursor& c, int tq) {
-  if (c.done() || tq >= c.nvalid() || p.kv_indices == nullptr) return 0;
-  return ld_nc_early(p.kv_indices + c.w.page_base + (c.t0() + tq) / p.page_size);
+__device__ __forceinline__ int32_t scale_page(const Stage1Params& p, const TileAhead& c, int tq) {
+  if (c.ntile == 0 || tq >= c.nvalid() || p.kv_indices == nullptr) return 0;
+  return ld_nc_early(p.kv_indices + c.page_base + (c.t0() + tq) / p.page_size);
 }
 
-// Issues the nine 2-byte loads of the token's scale row (zeros past the
-// tile's end); `page` is scale_page() of the same tile and token.
-__device__ __forceinline__ void scale_load(const Stage1Params& p, const TileCursor& c, int tq,
-                                           int32_t page, uint16_t (&h)[9]) {
-  if (c.done() || tq >= c.nvalid()) {
+// Issues the nine 1-byte loads of bytes hb, hb + 2, .. hb + 16 of the
+// token's scale row (the blocks of one dequant half; zeros past the tile's
+// end); `page` is scale_page() of the same tile and token.
+__device__ __forceinline__ void scale_load(const Stage1Params& p, const TileAhead& c, int tq,
+                                           int hb, int32_t page, uint32_t (&e)[9]) {
+  if (c.ntile == 0 || tq >= c.nvalid()) {
 #pragma unroll
-    for (int i = 0; i < 9; ++i) h[i] = 0;
+    for (int i = 0; i < 9; ++i) e[i] = 0;
     return;
   }
   const int pos = c.t0() + tq;
   int64_t row;
   if (p.kv_indices == nullptr) {
-    row = static_cast<int64_t>(c.w.page_base) * p.page_size + pos;
+    row = static_cast<int64_t>(c.page_base) * p.page_size + pos;
     if (row >= p.pool_rows) row = 0;   // (the host rejects such plans; never reached)
   } else {
     if (page < 0 || static_cast<int64_t>(page + 1) * p.page_size > p.pool_rows) {
@@ -533,9 +578,9 @@ __device__ __forceinline__ void scale_load(const Stage1Params& p, const TileCurs
     }
     row = static_cast<int64_t>(page) * p.page_size + pos % p.page_size;
   }
-  const uint16_t* src = reinterpret_cast<const uint16_t*>(p.kv_e8m0 + row * p.sc_stride);
+  const uint8_t* src = p.kv_e8m0 + row * p.sc_stride + hb;
 #pragma unroll
-  for (int i = 0; i < 9; ++i) h[i] = ld_nc_u16_early(src + i);
+  for (int i = 0; i < 9; ++i) e[i] = ld_nc_u8_early(src + 2 * i);
 }
 
 // ----------------------------------------------------- q staging helpers
@@ -653,159 +698,290 @@ __device__ __forceinline__ void q_convert(const Stage1Params& p, Misc* ms, const
   }
 }
 
-// MXFP4 variant: the four dequant warps (128 threads, named barrier 3)
-// prepare q of item `it` (ordinal k) into q buffer k & 1, then start the copy
-// of the next item's q.  Returns false once the group gave up.
+// MXFP4: the eight dequant warps (256 threads, named barrier 3) prepare q of
+// every item straight from global memory into the single q buffer.  All the
+// request's bf16 values are held in registers while |q|max over the request
+// is reduced, then split into two e4m3 terms (q_split_store).
 template <int QM>
-__device__ bool qprep_group(const Stage1Params& p, Misc* ms, uint8_t* qgen, uint8_t* stage, int it,
-                            int k, int it1, int t) {
+__device__ __forceinline__ void q_convert_mx(const Stage1Params& p, Misc* ms, int b, uint8_t* dst,
+                                             int i, float& c_hi, float& c_lo) {
   using L = Layout<QM>;
-  volatile int32_t* abort = &ms->abort_dq;
-  const uint32_t qb = k & 1;
-  if (!mbar_wait(smem_u32(&ms->q_empty[qb]), ((k >> 1) & 1) ^ 1, p.err, kErrQPrep)) *abort = 1;
-  if (!mbar_wait(smem_u32(&ms->q_stage), k & 1, p.err, kErrQPrep)) *abort = 1;
-  named_bar_sync(3, 128);
-  if (*abort) return false;
+  constexpr float kSmScale = 1.0f / 24.0f;                       // 1/sqrt(576)
+  constexpr int kN = 256, kV = kHeads * kQkDim / 8;              // 1152 vectors of 8 bf16
+  constexpr int kPer = (kV + kN - 1) / kN;
+  const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.q) +
+                                                    static_cast<int64_t>(b) * kHeads * kQkDim * 2);
+  // two passes over the request's q (the second from L1/L2): |q|max, then the
+  // split, so that no vector stays live across the reduction
+  float amax = 0.f;
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int v = i + kN * u;
+    if (v >= kV) break;
+    const uint4 x = __ldg(src + v);
+    const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&x);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(h2[e]);
+      amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if ((i & 31) == 0) ms->qred[i >> 5] = amax;
+  named_bar_sync(3, kN);
+  amax = 0.f;
+#pragma unroll
+  for (int w = 0; w < kN / 32; ++w) amax = fmaxf(amax, ms->qred[w]);
+  amax = fmaxf(amax, 1e-30f);
+  const float s_hi = amax / 448.0f, inv_hi = 448.0f / amax;
+#pragma unroll 1
+  for (int u = 0; u < kPer; ++u) {
+    const int v = i + kN * u;
+    if (v < kV) q_split_store(__ldg(src + v), v, s_hi, inv_hi, dst, L::kQAtomBytes);
+  }
+  c_hi = s_hi * kSmScale * kLog2e;
+  c_lo = c_hi * (1.0f / 16.0f);
+}
+
+// q of item k (request b) into the q buffer, once QK^T of item k-1 and its
+// softmax released the buffer.  `failed` carries this thread's failed waits;
+// the group's barrier ORs them, so that all 256 threads leave together
+// (returns false) or carry on together.
+template <int QM>
+__device__ bool qprep_mx(const Stage1Params& p, Misc* ms, uint8_t* qgen, int b, int k, int d,
+                         bool& failed) {
+  if (k > 0 && !failed && !mbar_wait(smem_u32(&ms->q_empty[0]), (k - 1) & 1, p.err, kErrQPrep))
+    failed = true;
+  if (named_bar_any(3, 256, failed)) return false;
   float c_hi, c_lo;
-  q_convert<QM>(p, ms, stage, qgen + qb * L::kQBytes, t, 128, 3, c_hi, c_lo);
+  q_convert_mx<QM>(p, ms, b, qgen, d, c_hi, c_lo);
   fence_proxy_async_smem();
-  named_bar_sync(3, 128);                           // staging buffer and qred free again
-  if (t == 0) {
-    if (it + 1 < it1) q_fetch<QM>(p, ms, stage, p.items[it + 1].b);
-    ms->qscale[qb][0] = c_hi;
-    ms->qscale[qb][1] = c_lo;
-    mbar_arrive(smem_u32(&ms->q_full[qb]));
+  named_bar_sync(3, 256);                           // every thread wrote its part; qred free
+  if (d == 0) {
+    ms->qscale[0][0] = c_hi;
+    ms->qscale[0][1] = c_lo;
+    mbar_arrive(smem_u32(&ms->q_full[0]));
   }
   return true;
 }
 
-// Four warps turn the packed MXFP4 rows of a tile slot into the e4m3 tile the
-// UMMAs read (thread t = token t).  With r_t the largest e8m0 exponent of the
-// token, block b becomes e2m1 * 2^(E_b - r_t): exact in e4m3 while
-// E_b - r_t >= -8.  The remaining factor 2^(r_t - 127) of the token is left
-// to the softmax (u_t = r_t - 127 in shared memory).
-//
-// In place, without holding a row in registers: 8-row box i of the slot owns
-// bytes [i*4608, (i+1)*4608) of e4m3 rows ([chunk c][8 rows][64 B], chunk c =
-// dims 64c..64c+63) and its packed rows land chunk-major in the upper half,
-// [chunk c][8 rows][32 B] at 2304 + 256c.  Packed chunk c therefore lies in
-// e4m3 chunk floor(4.5 + c/2) >= c, so writing e4m3 chunk c only overwrites
-// packed chunks the box's 8 threads (one quarter of a warp) have already
-// read: a warp barrier between the reads and the writes of each chunk is
-// enough.
-//
-// The same threads prepare q: item 0's before the first tile, item k+1's
-// right after the first tile of item k (its q buffer is free by then: QK^T
-// of item k-1 has been issued on tiles this group already dequantised).
-template <int QM>
-__device__ void run_dequant(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, uint8_t* qgen,
-                            uint8_t* stage, int it0, int it1, const WorkItem& first, int t) {
-  using L = Layout<QM>;
-  static_assert(L::kRowBytes * 8 == 4608 && L::kRawRowBytes * 8 == 2304, "box layout");
-  volatile int32_t* abort = &ms->abort_dq;
-  if (it0 >= it1) return;
-  if (t == 0) q_fetch<QM>(p, ms, stage, first.b);
-  if (t < 15) {
-    uint32_t lo, hi;
-    e2m1_e4m3_table(t - 14, lo, hi);
-    ms->e2m1_tab[t] = make_uint2(lo, hi);
+// Chunks [j0, j1) of one dequant thread: block 2j + h of its token (packed
+// in x[j], e8m0 byte in eb[j]) into e4m3 chunk j of its row at dst,
+// pieces pc0 / pc1; zeros for a row past the tile's end.  Returns whether
+// anything was written (the caller then fences the writes for the UMMAs).
+template <int kN>
+__device__ __forceinline__ bool half_of_tile(bool ok, bool live, bool fast, const uint4 (&x)[kN],
+                                             const uint32_t (&eb)[kN], int r, const uint2* tab,
+                                             uint8_t* dst, uint32_t pc0, uint32_t pc1, int j0,
+                                             int j1) {
+  if (!ok) return false;
+#pragma unroll
+  for (int j = 0; j < kN; ++j) {
+    if (j < j0 || j >= j1) continue;
+    uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
+    if (live) {
+      const int k = static_cast<int>(eb[j]) - r;
+      uint32_t lo, hi;
+      if (fast) {
+        e2m1_e4m3_table_normal(k, lo, hi);
+      } else {
+        const uint2 tb = tab[max(k, -14) + 14];
+        lo = tb.x;
+        hi = tb.y;
+      }
+      const uint2 e0 = e2m1x8_to_e4m3(x[j].x, lo, hi), e1 = e2m1x8_to_e4m3(x[j].y, lo, hi);
+      const uint2 e2 = e2m1x8_to_e4m3(x[j].z, lo, hi), e3 = e2m1x8_to_e4m3(x[j].w, lo, hi);
+      o0 = make_uint4(e0.x, e0.y, e1.x, e1.y);
+      o1 = make_uint4(e2.x, e2.y, e3.x, e3.y);
+    }
+    *reinterpret_cast<uint4*>(dst + j * 512 + pc0) = o0;
+    *reinterpret_cast<uint4*>(dst + j * 512 + pc1) = o1;
   }
-  // (qprep_group and every tile begin with a group barrier, so the tables
-  // are visible before their first use)
-  if (!qprep_group<QM>(p, ms, qgen, stage, it0, 0, it1, t)) return;
-  // this thread's row: box t/8, row t%8 (8-row boxes)
-  const uint32_t box_off = (t >> 3) * 4608u, r8 = t & 7u;
-  const uint32_t swz = (r8 >> 1) & 3u;                 // 64-byte swizzle of this row
-  // this thread's copy of its token's scale row (nine 2-byte block pairs)
-  uint16_t* sc = reinterpret_cast<uint16_t*>(ring_gen + L::kScRowOff + t * 24);
-  TileCursor c, a1, a2;                                // this tile, the next, the one after
+  return true;
+}
+
+// The packed rows of one warp for a tile: rows 16 wi .. 16 wi + 15 of the
+// tile (wi = the warp's index among the dequant warps) into unit wi / 2 at
+// row (wi & 1) * 16, with plain bulk copies, one per run of rows contiguous
+// in the pool (one for the identity table, one per page otherwise), issued by
+// the lane of the run's first row.  Lane l holds row 4 (l >> 3) + (l & 3) of
+// the sixteen when (l >> 2) & 1 == 0 ("row lanes"); `page` is the row's raw
+// page-table entry (checked here: a page outside the pool reads page 0 and is
+// reported).  The lanes' arrive on the unit's barrier counts the bytes.
+__device__ __forceinline__ void copy_rows(const Stage1Params& p, const TileAhead& c, int wi,
+                                          int lane, int32_t page, uint32_t unit, uint32_t bar,
+                                          uint64_t pol) {
+  constexpr uint32_t kRow = kQkDim / 2;                    // packed bytes per row
+  const int nvalid = c.ntile ? c.nvalid() : 0;
+  if (p.kv_indices == nullptr) {                            // identity table: one copy, lane 0
+    if (lane == 0) {
+      const int nrows = max(0, min(16, nvalid - 16 * wi));
+      mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nrows) * kRow);
+      if (nrows > 0)
+        bulk_load_hint(unit + (wi & 1) * 16 * kRow,
+                       p.kv + (static_cast<int64_t>(c.page_base) * p.page_size + c.t0() + 16 * wi) * kRow,
+                       static_cast<uint32_t>(nrows) * kRow, bar, pol);
+    }
+    return;
+  }
+  const int r16 = 4 * (lane >> 3) + (lane & 3);             // this lane's row among the sixteen
+  const int row = 16 * wi + r16;
+  const bool row_lane = ((lane >> 2) & 1) == 0;
+  const int nrows = max(0, min(16, nvalid - 16 * wi));      // rows of this warp in the tile
+  bool head = false;
+  int64_t grow = 0;
+  if (row_lane && r16 < nrows) {
+    const int pos = c.t0() + row;
+    if (page < 0 || static_cast<int64_t>(page + 1) * p.page_size > p.pool_rows) {
+      atomicOr(p.err, kErrBadPage);
+      page = 0;
+    }
+    grow = static_cast<int64_t>(page) * p.page_size + pos % p.page_size;
+    head = r16 == 0 || pos % p.page_size == 0;
+  }
+  const uint32_t heads = __ballot_sync(0xffffffffu, head);
+  if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nrows) * kRow);
+  __syncwarp();                                              // the bytes are expected first
+  if (head) {
+    // the run ends at the next head's row (row lanes are in row order)
+    const uint32_t later = heads & ~((2u << lane) - 1u);
+    const int end = later ? 4 * ((__ffs(later) - 1) >> 3) + ((__ffs(later) - 1) & 3) : nrows;
+    bulk_load_hint(unit + ((wi & 1) * 16 + r16) * kRow, p.kv + grow * kRow,
+                   static_cast<uint32_t>(end - r16) * kRow, bar, pol);
+  }
+}
+
+// Eight warps turn the packed MXFP4 rows of a tile into the e4m3 tile slot
+// the UMMAs read, and copy the packed rows in.  Dequant warp wi owns rows
+// 16 wi .. 16 wi + 15 of every tile: lane l works on row
+// 16 wi + 4 (l >> 3) + (l & 3) and, with h = (l >> 2) & 1, on every other
+// scale block of it (the even blocks 0, 2, .. 16 for h = 0, the odd ones for
+// h = 1).  Block 2j + h is the h-th 32-byte half of e4m3 chunk j, so a
+// thread's nine blocks go to the same two swizzled 16-byte pieces of chunks
+// 0-8: every address is a fixed offset from the thread's row.  In each group
+// of eight lanes (four rows, both halves) the 16-byte reads of the landing
+// unit and the swizzled e4m3 writes hit eight different bank groups.
+//
+// Landing: unit q holds rows 32q .. 32q+31 of every tile, filled by the two
+// warps of those rows.  A warp loads its nine blocks per thread into
+// registers and, in the same warp, issues the copies of the same rows of the
+// next tile into the unit, so the copy flies while this tile is converted.
+// Chunks 0-4 (dims 0-319, which hold the first QK^T K-half) are published
+// before chunks 5-8.
+//
+// With r_t the token's largest e8m0 exponent, block b becomes
+// e2m1 * 2^(E_b - r_t): exact in e4m3 while E_b - r_t >= -8.  The remaining
+// factor 2^(r_t - 127) of the token is left to the softmax (u_t in shared
+// memory).  The e4m3 magnitudes of a block are computed for
+// E_b - r_t >= -5 (every block of the token within five binades of its
+// largest, the common case) and looked up otherwise.  Rows past the tile's
+// end are written as zeros, so that 0 * V stays 0 in PV.
+//
+// The same threads prepare q: item 0's before the first tile, item k's
+// right after dequantising item k's first tile (QK^T of item k waits for it).
+template <int QM>
+__device__ void run_dequant_mx(const Stage1Params& p, Misc* ms, uint8_t* ring_gen,
+                               uint8_t* units_gen, uint8_t* qgen, int it0, int it1,
+                               const WorkItem& first, int d) {
+  using L = Layout<QM>;
+  static_assert(L::kRowBytes * 8 == 4608 && L::kRawRowBytes == 288, "row layout");
+  if (it0 >= it1) return;
+  const int lane = d & 31, wi = d >> 5;
+  const int row = 16 * wi + 4 * (lane >> 3) + (lane & 3), h = (lane >> 2) & 1, wq = wi >> 1;
+  const uint64_t pol = l2_policy_evict_first();
+  const uint32_t unit = smem_u32(units_gen) + wq * L::kUnitBytes;
+  const uint32_t ubar = smem_u32(&ms->unit_full[wq]);
+  bool failed = false;                                 // a bounded wait of this thread gave up
+  TileCursor c;                                        // this tile
+  TileAhead a0, a1, a2;                                // it, the next, the one after
   c.init(p.items, it0, it1, first);
-  a1 = c;
-  a1.advance();
+  a0.from(c);
+  a1 = a0;
+  a1.advance(p.items, it1);
   a2 = a1;
-  a2.advance();
-  uint16_t h[9];
-  scale_load(p, c, t, scale_page(p, c, t), h);
-  int32_t page1 = scale_page(p, a1, t);
+  a2.advance(p.items, it1);
+  // the first tile's rows: page entries, packed-row copies, scale bytes
+  {
+    const int32_t pg0 = scale_page(p, a0, row);
+    copy_rows(p, a0, wi, lane, pg0, unit, ubar, pol);
+  }
+  uint32_t ec[9], en[9];                               // scale bytes: this tile, the next
+  scale_load(p, a0, row, h, scale_page(p, a0, row), ec);
+  int32_t pg1 = scale_page(p, a1, row);                // raw page entry of this row, next tile
+  if (d < 15) {
+    uint32_t lo, hi;
+    e2m1_e4m3_table(d - 14, lo, hi);
+    ms->e2m1_tab[d] = make_uint2(lo, hi);
+  }
+  // (qprep_mx and every tile begin with a group barrier, so the tables are
+  // visible before their first use)
+  if (!qprep_mx<QM>(p, ms, qgen, first.b, 0, d, failed)) return;
+  // this row in the e4m3 tile: 8-row group at 4608, 64-byte chunk j at
+  // 512 j, row at 64; this thread's two 16-byte pieces under the 64-byte
+  // swizzle
+  const uint32_t row_off = (row >> 3) * 4608u + (row & 7) * 64u;
+  const uint32_t swz = ((row & 7) >> 1) & 3u;
+  const uint32_t pc0 = ((2u * h) ^ swz) << 4, pc1 = ((2u * h + 1u) ^ swz) << 4;
+  // No group barrier per tile: once a bounded wait of a thread gave up
+  // (`failed`), that thread skips every later wait and all work, so it runs
+  // through its remaining tiles at once; the group decides to leave together
+  // at the barrier of the next q preparation (or the loop ends).
   while (!c.done()) {
     const uint32_t tt = c.t, s = tt % L::kNumTiles;
-    // this tile's scale bytes into shared memory, then the next tile's loads
-    int r = 0;
-    {
-      uint32_t ew[5];
+    const int nvalid = c.nvalid();
+    // this tile's scale bytes: r = max over all 18 (this thread's nine and
+    // those of lane ^ 4, the other half of the token), and the smallest of
+    // this thread's nine
+    int r = 0, emin = 255;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) ew[i] = h[2 * i] | (static_cast<uint32_t>(h[2 * i + 1]) << 16);
-      ew[4] = h[8];
-      *reinterpret_cast<uint2*>(sc) = make_uint2(ew[0], ew[1]);
-      *reinterpret_cast<uint2*>(sc + 4) = make_uint2(ew[2], ew[3]);
-      *reinterpret_cast<uint32_t*>(sc + 8) = ew[4];
+    for (int j = 0; j < 9; ++j) {
+      r = max(r, static_cast<int>(ec[j]));
+      emin = min(emin, static_cast<int>(ec[j]));
+    }
+    r = max(r, __shfl_xor_sync(0xffffffffu, r, 4));
+    scale_load(p, a1, row, h, pg1, en);
+    const bool live = row < nvalid;
+    const bool fast = emin - r >= -5;                  // all nine blocks on the computed path
+    bool ok = !failed && mbar_wait(ubar, tt & 1u, p.err, kErrDequant);
+    // this thread's nine packed blocks into registers, then the next tile's
+    // copy of the same rows into the unit (after this warp's reads)
+    uint4 x[9];
+    if (ok && live) {
+      const uint4* src = reinterpret_cast<const uint4*>(units_gen + wq * L::kUnitBytes +
+                                                        (row & 31) * L::kRawRowBytes) + h;
 #pragma unroll
-      for (int b = 0; b < 18; ++b)
-        r = max(r, static_cast<int>((ew[b >> 2] >> ((b & 3) * 8)) & 0xFFu));
+      for (int j = 0; j < 9; ++j) x[j] = src[2 * j];
     }
-    scale_load(p, a1, t, page1, h);
-    page1 = scale_page(p, a2, t);
-    if (!mbar_wait(smem_u32(&ms->full[s]), (tt / L::kNumTiles) & 1u, p.err, kErrDequant)) *abort = 1;
-    // e4m3 rows are written over the whole slot: PV of its previous tile
-    // must have finished (the packed rows only needed the upper halves)
-    if (!mbar_wait(smem_u32(&ms->empty[s]), ((tt / L::kNumTiles) & 1u) ^ 1u, p.err, kErrDequant))
-      *abort = 1;
-    named_bar_sync(3, 128);
-    if (*abort) return;
-    uint8_t* box = ring_gen + s * L::kTileBytes + box_off;
-    const uint8_t* raw = box + 2304u + r8 * 32u;
-    ms->uexp[s][t] = static_cast<float>(r - 127);
-    uint8_t* row = box + r8 * 64u;
-    // packed chunk ch+1 and its two scale bytes are read while chunk ch is
-    // converted (reading early is always safe; only writes must wait)
-    uint4 na = reinterpret_cast<const uint4*>(raw)[0];
-    uint4 nb = reinterpret_cast<const uint4*>(raw)[1];
-    uint32_t neb = sc[0];
-    auto chunk = [&](int ch, bool sync) {
-      const uint4 a = na, b = nb;
-      const uint32_t eb = neb;                          // e8m0 of blocks 2ch, 2ch+1
-      if (ch < 8) {
-        na = reinterpret_cast<const uint4*>(raw + (ch + 1) * 256)[0];
-        nb = reinterpret_cast<const uint4*>(raw + (ch + 1) * 256)[1];
-        neb = sc[ch + 1];
-      }
-      if (sync) __syncwarp();                           // the box read the packed chunks
-      const uint2 t0 = ms->e2m1_tab[max(static_cast<int>(eb & 0xFFu) - r, -14) + 14];
-      const uint2 t1 = ms->e2m1_tab[max(static_cast<int>(eb >> 8) - r, -14) + 14];
-      const uint32_t lo0 = t0.x, hi0 = t0.y, lo1 = t1.x, hi1 = t1.y;
-      const uint2 o0 = e2m1x8_to_e4m3(a.x, lo0, hi0), o1 = e2m1x8_to_e4m3(a.y, lo0, hi0);
-      const uint2 o2 = e2m1x8_to_e4m3(a.z, lo0, hi0), o3 = e2m1x8_to_e4m3(a.w, lo0, hi0);
-      const uint2 o4 = e2m1x8_to_e4m3(b.x, lo1, hi1), o5 = e2m1x8_to_e4m3(b.y, lo1, hi1);
-      const uint2 o6 = e2m1x8_to_e4m3(b.z, lo1, hi1), o7 = e2m1x8_to_e4m3(b.w, lo1, hi1);
-      uint8_t* dst = row + ch * 512;
-      *reinterpret_cast<uint4*>(dst + ((0u ^ swz) << 4)) = make_uint4(o0.x, o0.y, o1.x, o1.y);
-      *reinterpret_cast<uint4*>(dst + ((1u ^ swz) << 4)) = make_uint4(o2.x, o2.y, o3.x, o3.y);
-      *reinterpret_cast<uint4*>(dst + ((2u ^ swz) << 4)) = make_uint4(o4.x, o4.y, o5.x, o5.y);
-      *reinterpret_cast<uint4*>(dst + ((3u ^ swz) << 4)) = make_uint4(o6.x, o6.y, o7.x, o7.y);
-    };
-    // e4m3 chunks 0-3 lie below every packed chunk: no barrier.  From chunk
-    // 4 on, e4m3 chunk ch overwrites packed chunks 2ch-9 and 2ch-8, which
-    // the box's threads read (one chunk ahead) in earlier iterations: a warp
-    // barrier before each write orders those reads first.
-#pragma unroll 1
-    for (int ch = 0; ch < 4; ++ch) chunk(ch, false);
-#pragma unroll 1
-    for (int ch = 4; ch < 9; ++ch) {
-      chunk(ch, true);
-      if (ch == 4) {
-        // dims 0-319 done: the first QK^T K-half (dims 0-287) may start
-        fence_proxy_async_smem();
-        mbar_arrive(smem_u32(&ms->deq_a[s]));
-      }
+    fence_proxy_async_smem();                          // the reads before the async-proxy writes
+    __syncwarp();
+    if (__all_sync(0xffffffffu, ok)) copy_rows(p, a1, wi, lane, pg1, unit, ubar, pol);
+    pg1 = scale_page(p, a2, row);
+    // the slot is overwritten whole: PV of its previous tile must be done
+    ok = ok && mbar_wait(smem_u32(&ms->empty[s]), ((tt / L::kNumTiles) & 1u) ^ 1u, p.err,
+                         kErrDequant);
+    if (!ok) failed = true;
+    uint8_t* dst = ring_gen + s * L::kTileBytes + row_off;
+    // the token's factor for the softmax (read once S of the tile exists)
+    if (h == 0 && ok) ms->uexp[s][row] = static_cast<int16_t>(live ? r - 127 : 0);
+    if (half_of_tile(ok, live, fast, x, ec, r, ms->e2m1_tab, dst, pc0, pc1, 0, 5)) {
+      fence_proxy_async_smem();
     }
-    fence_proxy_async_smem();
-    mbar_arrive(smem_u32(&ms->deq[s]));
-    const bool first = c.j == 0;
-    const int it = c.it, k = c.k;
+    __syncwarp();
+    if (ok && lane == 0) mbar_arrive(smem_u32(&ms->deq_a[s]));   // chunks 0-4
+    if (half_of_tile(ok, live, fast, x, ec, r, ms->e2m1_tab, dst, pc0, pc1, 5, 9)) {
+      fence_proxy_async_smem();
+    }
+    __syncwarp();
+    if (ok && lane == 0) mbar_arrive(smem_u32(&ms->deq_b[s]));   // chunks 5-8
+#pragma unroll
+    for (int j = 0; j < 9; ++j) ec[j] = en[j];
+    const bool item_start = c.j == 0;
+    const int k = c.k, b = c.w.b;
     c.advance();
     a1 = a2;
-    a2.advance();
-    if (first && it + 1 < it1 && !qprep_group<QM>(p, ms, qgen, stage, it + 1, k + 1, it1, t)) return;
+    a2.advance(p.items, it1);
+    if (item_start && k > 0 && !qprep_mx<QM>(p, ms, qgen, b, k, d, failed)) return;
   }
 }
 
@@ -933,8 +1109,8 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
   float m[kH], l[kH];
   for (int it = it0; it < it1; ++it, ++k) {
     const WorkItem w = it == it0 ? first : p.items[it];
-    const uint32_t qb = k & 1;
-    wait_or_flag(smem_u32(&ms->q_full[qb]), (k >> 1) & 1, p.err, kErrSoftmax, abort);
+    const uint32_t qb = k % L::kQBufs;
+    wait_or_flag(smem_u32(&ms->q_full[qb]), (k / L::kQBufs) & 1, p.err, kErrSoftmax, abort);
     const float c_hi = ms->qscale[qb][0], c_lo = ms->qscale[qb][1];
     named_bar_sync(bar, 128);
     if (*abort) return;
@@ -977,7 +1153,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
       // P use s + u (the factor of its V row), l uses s: P' = p 2^u.
       float gl = 1.0f;                                   // 2^-u, turns P' back into p
       if constexpr (L::kMx) {
-        const int u = static_cast<int>(ms->uexp[g % L::kNumTiles][tq]);
+        const int u = ms->uexp[g % L::kNumTiles][tq];
         const float f = u >= -126 ? __int_as_float((u + 127) << 23) : 0.0f;
         gl = (valid && u <= 126) ? __int_as_float((127 - u) << 23) : 0.0f;
 #pragma unroll
@@ -1088,12 +1264,12 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
         static_assert(L::kPRow == 32, "bf16 P rows: one query token");
         *reinterpret_cast<uint4*>(prow + ((16u * hg) ^ flip)) = make_uint4(bw[0], bw[1], bw[2], bw[3]);
       }
-      if (nvalid < kTile) {
+      if (!L::kMx && nvalid < kTile) {
         // Tail tile: rows past the range may hold anything (stale tiles,
         // unused page slots); zero their V bytes so that 0 * V stays 0.
+        // (The MXFP4 dequantisation writes those rows as zeros itself.)
         const uint32_t s2 = g % L::kNumTiles;
-        wait_or_flag(L::kMx ? smem_u32(&ms->deq[s2]) : smem_u32(&ms->full[s2]),
-                     (g / L::kNumTiles) & 1u, p.err, kErrSoftmax, abort);
+        wait_or_flag(smem_u32(&ms->full[s2]), (g / L::kNumTiles) & 1u, p.err, kErrSoftmax, abort);
         if (!valid) {
           uint8_t* row = ring_gen + s2 * L::kTileBytes + (tq >> 3) * gs + (tq & 7) * 64;
           constexpr int kZc = L::kVChunks / kHG;       // chunks zeroed by each group
@@ -1202,8 +1378,16 @@ __global__ void __launch_bounds__(Layout<QM>::kThreads, 1) mla_stage1_kernel(con
   Misc* ms = reinterpret_cast<Misc*>(smem + L::kMiscOff);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const CtaHead& head = p.heads[blockIdx.x];
-  const int it0 = head.it0, it1 = head.it1;
-  const WorkItem first = head.first;
+  // bf16 / fp8: the CTA's item range and first item are loaded at once, so
+  // that the loads overlap the set-up below (MXFP4 reads them after its
+  // register limits are set, see below)
+  int it0 = 0, it1 = 0;
+  WorkItem first{};
+  if constexpr (!L::kMx) {
+    it0 = head.it0;
+    it1 = head.it1;
+    first = head.first;
+  }
 
   if (threadIdx.x == 0) {
     // The workspace must hold this plan's table: its stamp in the header and
@@ -1225,18 +1409,20 @@ __global__ void __launch_bounds__(Layout<QM>::kThreads, 1) mla_stage1_kernel(con
       mbar_init(smem_u32(&ms->q_empty[i]), 2 + L::kHeadGroups);  // QK^T issuers + softmax groups
     }
     for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&ms->drain[i]), 1);
-    for (int i = 0; i < L::kNumTiles; ++i) {
-      mbar_init(smem_u32(&ms->deq[i]), 128);
-      mbar_init(smem_u32(&ms->deq_a[i]), 128);
-      mbar_init(smem_u32(&ms->upper_free[i]), 1);
+    if constexpr (L::kMx) {
+      for (int i = 0; i < L::kNumTiles; ++i) {
+        mbar_init(smem_u32(&ms->deq_a[i]), 8);       // one arrival per dequant warp
+        mbar_init(smem_u32(&ms->deq_b[i]), 8);
+      }
+      for (int i = 0; i < L::kUnits; ++i)
+        mbar_init(smem_u32(&ms->unit_full[i]), 2);   // the two dequant warps of its rows
     }
     mbar_init(smem_u32(&ms->q_stage), 1);
     mbar_init(smem_u32(&ms->q_stage_free), 1);
-    ms->abort_dq = 0;
     ms->abort_sm = 0;
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) prefetch_tensormap(&p.tmap_kv);
+  if (!L::kMx && warp == 0 && lane == 0) prefetch_tensormap(&p.tmap_kv);
   if (warp == 1) {
     tmem_alloc(smem_u32(&ms->tmem_base), L::kTmemCols);
     tmem_relinquish();
@@ -1246,22 +1432,54 @@ __global__ void __launch_bounds__(Layout<QM>::kThreads, 1) mla_stage1_kernel(con
   tc_fence_after();
   const uint32_t tmem = ms->tmem_base;
 
+  // MXFP4: the CTA's item range and first item are read by every role after
+  // its warpgroup set its register limit, so that nothing is live across it.
+  auto head_items = [&](int& i0, int& i1, WorkItem& f) {
+    i0 = head.it0;
+    i1 = head.it1;
+    f = head.first;
+  };
   if (ms->stale) {
     if (threadIdx.x == 0) atomicOr(p.err, kErrStale);
-  } else if (warp == 0) {
-    run_producer<QM>(p, ms, ring, it0, it1, first, lane);
-  } else if (warp == 1 || warp == 3) {
-    run_qk<QM>(p, ms, ring, ring + L::kQOff, tmem, it0, it1, first, warp == 3 ? 1 : 0, lane);
-  } else if (warp == 2 || (!L::kMx && warp == 13)) {
-    run_pv<QM>(p, ms, ring, ring + L::kPOff, tmem, it0, it1, first, warp == 13 ? 1 : 0, lane);
-  } else if (warp < 4 + 4 * L::kHeadGroups) {
-    run_softmax<QM>(p, ms, smem, smem + L::kPOff, smem + L::kQOff, smem + L::kQStageOff, tmem, it0,
-                    it1, first, threadIdx.x - 128);
   } else if constexpr (L::kMx) {
-    run_dequant<QM>(p, ms, smem, smem + L::kQOff, smem + L::kQStageOff, it0, it1, first,
-                    threadIdx.x - 384);
+    // One branch per warpgroup, each opening with its register limit (every
+    // warp of the group executes the same setmaxnreg), so that the limit
+    // governs the role code it dominates: 0 = UMMA issuers, 1-2 = softmax,
+    // 3-4 = dequantisation (with the landing copies).
+    const int wg = warp >> 2;
+    if (wg == 0) {
+      regs_lower<L::kRegsIssue>();
+      head_items(it0, it1, first);
+      if (warp == 0 || warp == 2)
+        run_pv<QM>(p, ms, ring, ring + L::kPOff, tmem, it0, it1, first, warp == 0 ? 1 : 0, lane);
+      else
+        run_qk<QM>(p, ms, ring, ring + L::kQOff, tmem, it0, it1, first, warp == 3 ? 1 : 0, lane);
+    } else if (wg <= 2) {
+      if constexpr (L::kRegsSoftmax < L::kRegsLaunch) regs_lower<L::kRegsSoftmax>();
+      if constexpr (L::kRegsSoftmax > L::kRegsLaunch) regs_raise<L::kRegsSoftmax>();
+      head_items(it0, it1, first);
+      run_softmax<QM>(p, ms, smem, smem + L::kPOff, smem + L::kQOff, smem + L::kQStageOff, tmem,
+                      it0, it1, first, threadIdx.x - 128);
+    } else {
+      if constexpr (L::kRegsDequant < L::kRegsLaunch) regs_lower<L::kRegsDequant>();
+      if constexpr (L::kRegsDequant > L::kRegsLaunch) regs_raise<L::kRegsDequant>();
+      head_items(it0, it1, first);
+      run_dequant_mx<QM>(p, ms, smem, smem + L::kUnitOff, smem + L::kQOff, it0, it1, first,
+                         threadIdx.x - 384);
+    }
   } else {
-    run_qprep<QM>(p, ms, smem + L::kQOff, smem + L::kQStageOff, it0, it1, first, lane);
+    if (warp == 0) {
+      run_producer<QM>(p, ms, ring, it0, it1, first, lane);
+    } else if (warp == 1 || warp == 3) {
+      run_qk<QM>(p, ms, ring, ring + L::kQOff, tmem, it0, it1, first, warp == 3 ? 1 : 0, lane);
+    } else if (warp == 2 || warp == 13) {
+      run_pv<QM>(p, ms, ring, ring + L::kPOff, tmem, it0, it1, first, warp == 13 ? 1 : 0, lane);
+    } else if (warp < 4 + 4 * L::kHeadGroups) {
+      run_softmax<QM>(p, ms, smem, smem + L::kPOff, smem + L::kQOff, smem + L::kQStageOff, tmem,
+                      it0, it1, first, threadIdx.x - 128);
+    } else {
+      run_qprep<QM>(p, ms, smem + L::kQOff, smem + L::kQStageOff, it0, it1, first, lane);
+    }
   }
 
   tc_fence_before();
@@ -1286,7 +1504,15 @@ int stage1_smem_bytes(int qmode) {
 
 template <int QM>
 static cudaError_t launch_t(const Stage1Params& p, int num_ctas, cudaStream_t stream) {
-  const int smem = Layout<QM>::kSmemBytes;
+  using L = Layout<QM>;
+  const int smem = L::kSmemBytes;
+  if constexpr (L::kMx) {
+    // the warpgroups' register limits must fit the pool the launch provides
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, mla_stage1_kernel<QM>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs * L::kThreads < L::kRegsPlanned) return cudaErrorInvalidConfiguration;
+  }
   cudaError_t e = cudaFuncSetAttribute(mla_stage1_kernel<QM>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;

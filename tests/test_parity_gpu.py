@@ -181,7 +181,7 @@ def test_large_benchmark_configs_sampled(name):
     check(w, select=sel)
 
 
-@pytest.mark.parametrize("page_size,permute", [(1, False), (16, True)])
+@pytest.mark.parametrize("page_size,permute", [(1, False), (16, True), (7, True)])
 def test_mxfp4_ragged(page_size, permute):
     import workloads as synth
     lengths = [1, 127, 128, 129, 700, 0, 2049]
@@ -222,7 +222,7 @@ def test_mxfp4_very_spread_block_exponents():
 
 
 @pytest.mark.parametrize("scale_stride", [18, 32, 48])
-@pytest.mark.parametrize("page_size,permute", [(1, False), (8, True), (24, True)])
+@pytest.mark.parametrize("page_size,permute", [(1, False), (3, True), (8, True), (24, True)])
 def test_mxfp4_scale_row_strides(scale_stride, page_size, permute):
     # the pages' 18-byte e8m0 rows and wider strides; contiguous and paged
     # pools, a ragged last tile and an empty request
@@ -348,7 +348,7 @@ def test_qlen_causal_decode(q_dtype, kv_dtype, q_len):
     # requests shorter than q_len leave their first query tokens empty
     import workloads as synth
     lengths = [1, 3, 130, 0, 1000, 2049]
-    page = 8 if kv_dtype == "mxfp4" else 4
+    page = 4
     w = synth.make_workload(bs=len(lengths), lengths=lengths, page_size=page, q_dtype=q_dtype,
                             kv_dtype=kv_dtype, permute_pages=True, seed=48, q_len=q_len)
     check(w)
@@ -407,10 +407,7 @@ def _random_case(seed):
                          ("bf16", "mxfp4")][rng.integers(5)]
     bs = int(rng.integers(1, 9))
     lengths = [int(x) for x in rng.choice([0, 1, 2, 127, 128, 129, 255, 300, 1000, 2500], size=bs)]
-    if kv_dtype == "mxfp4":
-        page_size = int(rng.choice([1, 8, 16, 64]))
-    else:
-        page_size = int(rng.choice([1, 2, 3, 8, 16, 40, 64]))
+    page_size = int(rng.choice([1, 2, 3, 8, 16, 40, 64]))
     permute = page_size > 1 and bool(rng.integers(2))
     q_len = int(rng.choice([1, 1, 2, 3]))
     mode = int(rng.integers(3))
@@ -508,7 +505,7 @@ def test_workspace_reused_by_another_plan_is_detected():
 
 
 @pytest.mark.parametrize("kv_dtype,page_size", [("fp8", 8), ("bf16", 4), ("mxfp4", 8),
-                                                ("fp8", 3)])
+                                                ("fp8", 3), ("mxfp4", 5)])
 def test_page_outside_the_pool_is_reported(kv_dtype, page_size):
     # one page-table entry of request 1 points past the pool (and one of
     # request 3 is negative): the kernels read page 0 in their place, touch
