@@ -57,6 +57,12 @@ def parse():
     ap.add_argument("--no-per-config", dest="per_config", action="store_false")
     ap.add_argument("--per-config-steps", type=int, default=50,
                     help="timed steps of each other configuration")
+    ap.add_argument("--unit-tokens", type=int, default=0,
+                    help="plan option: tokens between cut points (32, 64, 128; 0 = 128)")
+    ap.add_argument("--item-cost", type=int, default=0,
+                    help="plan option: cost of an extra request in a CTA (0 = 1)")
+    ap.add_argument("--autotune", dest="autotune", action="store_true", default=False,
+                    help="choose each configuration's plan with mla_decode_autotune (untimed)")
     return ap.parse_args()
 
 
@@ -352,15 +358,29 @@ class Decoder:
     """One configuration made ready to decode: its plan, workspace, outputs
     and (for inputs smaller than twice the L2) the buffer that flushes L2."""
 
-    def __init__(self, mla, w, dev):
+    def __init__(self, mla, w, dev, unit_tokens=0, item_cost=0, autotune=False):
         import torch
         self.mla, self.w, self.d = mla, w, w.to(dev)
-        self.plan = mla.mla_decode_plan(w.kv_indptr, w.kv_last_page_len, page_size=w.page_size,
-                                        q_dtype=w.q_dtype, kv_dtype=w.kv_dtype, q_len=w.q_len)
-        self.info = self.plan.info()
-        self.ws = torch.empty(max(self.plan.workspace_bytes, 256), dtype=torch.uint8, device=dev)
         self.out = torch.empty(w.bs * w.q_len, 16, 512, dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty(w.bs * w.q_len, 16, dtype=torch.float32, device=dev)
+        self.tuned = None
+        if autotune:
+            d = self.d
+            kw = dict(page_size=w.page_size, q_dtype=w.q_dtype, kv_dtype=w.kv_dtype,
+                      q_scale=d.q_scale, kv_scale=d.kv_scale, kv_e8m0=d.kv_e8m0,
+                      kv_indices=d.kv_indices, lse=self.lse, q_len=w.q_len)
+            need = mla.mla_decode_autotune(w.kv_indptr, w.kv_last_page_len, d.q, d.kv, self.out, **kw)
+            self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+            self.plan, self.tuned = mla.mla_decode_autotune(w.kv_indptr, w.kv_last_page_len, d.q,
+                                                            d.kv, self.out, workspace=self.ws,
+                                                            reps=5, **kw)
+        else:
+            self.plan = mla.mla_decode_plan(w.kv_indptr, w.kv_last_page_len, page_size=w.page_size,
+                                            q_dtype=w.q_dtype, kv_dtype=w.kv_dtype, q_len=w.q_len,
+                                            unit_tokens=unit_tokens, item_cost=item_cost)
+            self.ws = torch.empty(max(self.plan.workspace_bytes, 256), dtype=torch.uint8,
+                                  device=dev)
+        self.info = self.plan.info()
         self.alg_bytes = w.algorithmic_bytes()
         self.kv_bytes = w.total_tokens() * w.kv_bytes_per_token()
         self.flush = self.kv_bytes < 2 * L2_BYTES
@@ -436,9 +456,18 @@ def config_entry(dec, step_ms, s1_ms, clocks, total_bytes, peak):
             "pct_of_8TBps": 100.0 * (dec.alg_bytes / (step_ms * 1e-3) / 1e9) / NOMINAL_HBM_GBS,
             "stage1_us": s1_ms * 1e3, "stage1_GBps": s1, "stage1_frac": s1 / peak,
             "algorithmic_bytes": dec.alg_bytes, "num_ctas": dec.info.num_ctas,
-            "num_partials": dec.info.num_partials,
+            "num_partials": dec.info.num_partials, "plan": plan_meta(dec),
             "l2": "flushed between steps (2x L2 write)" if dec.flush else "inputs larger than L2",
             "clocks": clocks}
+
+
+def plan_meta(dec):
+    """The plan options in use (and, after autotune, every candidate's time)."""
+    m = {"unit_tokens": dec.info.unit_tokens, "item_cost": dec.info.item_cost,
+         "num_ctas": dec.info.num_ctas}
+    if dec.tuned is not None:
+        m["autotune"] = [dict(o, median_ms=ms) for o, ms in dec.tuned]
+    return m
 
 
 def main():
@@ -463,14 +492,14 @@ def main():
 
     # every rank owns one batch of the configured shape (weak scaling)
     w = build_workload(args.config, rank, dev, args.bs, args.q_len)
-    dec = Decoder(mla, w, dev)
+    dec = Decoder(mla, w, dev, args.unit_tokens, args.item_cost, args.autotune)
     torch.cuda.empty_cache()
     info, alg_bytes = dec.info, dec.alg_bytes
     meta = dict(config_meta(args.config, w),
                 l2="flushed between steps (2x L2 write)" if dec.flush else
                 f"inputs larger than L2 ({dec.kv_bytes/1e9:.2f} GB KV)",
                 algorithmic_bytes=alg_bytes, num_ctas=info.num_ctas,
-                num_partials=info.num_partials)
+                num_partials=info.num_partials, plan=plan_meta(dec))
     K = args.steps
     step_ms, s1_ms, clocks, t_wall = dec.measure(K, args.warmup, dist, local)
     (total_bytes,) = reduce_over_ranks(dist, [], [alg_bytes], device=dev)[1]
@@ -545,7 +574,8 @@ def main():
         for name in synth.CONFIGS:
             if name == args.config:
                 continue
-            other = Decoder(mla, build_workload(name, rank, dev), dev)
+            other = Decoder(mla, build_workload(name, rank, dev), dev, args.unit_tokens,
+                            args.item_cost, args.autotune)
             o_ms, o_s1, o_clk, _ = other.measure(min(K, args.per_config_steps), args.warmup,
                                                  dist, local)
             (o_total,) = reduce_over_ranks(dist, [], [other.alg_bytes], device=dev)[1]

@@ -72,6 +72,8 @@ typedef struct {
   int64_t total_tiles;       /* 128-token tiles over all requests */
   size_t workspace_bytes;
   int32_t q_len;             /* query tokens per request */
+  int32_t unit_tokens;       /* tokens between possible cut points (mla_plan_options) */
+  int32_t item_cost;         /* cost of an extra request in a CTA (balanced plan) */
 } mla_plan_info;
 
 /*
@@ -142,6 +144,100 @@ mla_status mla_decode_plan_q(const int32_t* kv_indptr_host, const int32_t* kv_la
                              int32_t batch_size, int32_t q_len, int32_t page_size,
                              mla_dtype q_dtype, mla_dtype kv_dtype, int32_t num_splits,
                              int32_t num_sms, mla_plan** plan_out);
+
+/*
+ * Plan options (mla_decode_plan_ex, mla_decode_autotune).  All zero gives
+ * the plan of mla_decode_plan with num_splits = 0 on every SM.
+ *   num_splits   0: balanced plan; S > 0: every request cut into S ranges.
+ *   num_sms      CTAs of a balanced plan; 0 = the SM count of the device.
+ *   item_cost    balanced plan: what an extra request in a CTA costs, in
+ *                half tiles (an epilogue before the next request's first
+ *                tile); 0 = 1.  Larger values give fewer requests per CTA.
+ *   unit_tokens  tokens between the planner's possible cut points: 128 (a
+ *                whole tile; 0 means 128), 64 or 32.  Finer cuts spread small
+ *                batches over more CTAs (each then loads only its rows).
+ */
+typedef struct {
+  int32_t num_splits;
+  int32_t num_sms;
+  int32_t item_cost;
+  int32_t unit_tokens;
+} mla_plan_options;
+
+/*
+ * mla_decode_plan_ex -- mla_decode_plan_q with plan options (NULL = all
+ * zero).  Errors: as mla_decode_plan_q; MLA_ERR_INVALID_ARG for an item cost
+ * outside [0, 64] or a unit other than 0, 32, 64, 128.
+ */
+mla_status mla_decode_plan_ex(const int32_t* kv_indptr_host, const int32_t* kv_last_page_len_host,
+                              int32_t batch_size, int32_t q_len, int32_t page_size,
+                              mla_dtype q_dtype, mla_dtype kv_dtype,
+                              const mla_plan_options* options, mla_plan** plan_out);
+
+/* One timed candidate of mla_decode_autotune: its options and the median
+ * time of its timed calls in milliseconds (< 0: not timed, its workspace did
+ * not fit). */
+typedef struct {
+  mla_plan_options options;
+  float ms;
+} mla_tune_result;
+
+#define MLA_TUNE_IGNORE_CACHE 1   /* mla_decode_autotune flag: time even a shape seen before */
+
+/*
+ * mla_decode_autotune -- choose the plan of one batch shape by timing
+ * candidate plans on the caller's inputs (the runtime autotune of the
+ * earlier version of submission 600081: _time_fn / _aiter_best /
+ * _best_for_shape).  The candidates are the default balanced plan, item
+ * costs 2 and 4, cut units of 64 and 32 tokens, the split count of the
+ * pages' split tables for this (batch, length) if it has one, and one split
+ * per request.  Every candidate runs once (uploading its table), then `reps`
+ * calls (1 .. 1000) are timed one by one with CUDA events on `stream`; the
+ * candidate with the smallest median time wins (mla_autotune_select), and
+ * the winner is remembered for the shape (batch, query tokens, page size,
+ * formats, total and largest request length, page table or not, device) for
+ * the rest of the process: a later call for the same shape returns that
+ * plan without timing unless flags has MLA_TUNE_IGNORE_CACHE.
+ *
+ * Arguments: the shape as for mla_decode_plan_q, the inputs and outputs as
+ * for mla_decode_run (out and lse are overwritten by the timed calls).
+ * workspace NULL: nothing runs; *workspace_needed receives the workspace the
+ * largest candidate needs (the two-call pattern).  Otherwise candidates
+ * whose workspace exceeds workspace_bytes are skipped.  results (up to
+ * max_results, may be NULL with max_results 0) receive each candidate's
+ * options and median time, *num_results their count (0 when the cached
+ * choice was used).  *plan_out receives the chosen plan (library-owned,
+ * release it with mla_plan_destroy).
+ *
+ * This call synchronises `stream` (it reads the timings and the device error
+ * word) and is meant for a first call per shape, not for the timed path.
+ * Errors: MLA_ERR_INVALID_ARG (arguments; a page outside the pool),
+ * MLA_ERR_WORKSPACE (no candidate fits the workspace), MLA_ERR_CUDA,
+ * MLA_ERR_DEVICE_TIMEOUT, and the errors of mla_decode_plan_ex and
+ * mla_decode_run.
+ */
+mla_status mla_decode_autotune(const int32_t* kv_indptr_host,
+                               const int32_t* kv_last_page_len_host, int32_t batch_size,
+                               int32_t q_len, int32_t page_size, mla_dtype q_dtype,
+                               mla_dtype kv_dtype, const void* q, const float* q_scale,
+                               const void* kv, const float* kv_scale, const uint8_t* kv_e8m0,
+                               int64_t kv_e8m0_row_stride, int64_t kv_pool_rows,
+                               const int32_t* kv_indices, void* workspace,
+                               size_t workspace_bytes, void* out, float* lse, int32_t reps,
+                               int32_t flags, mla_stream_t stream, mla_tune_result* results,
+                               int32_t max_results, int32_t* num_results,
+                               size_t* workspace_needed, mla_plan** plan_out);
+
+/*
+ * The selection rule of mla_decode_autotune, on the host: ms holds
+ * num_candidates x reps times (candidate-major); a candidate with a negative
+ * or NaN time was not run and is skipped.  *best receives the candidate with
+ * the smallest median (for an even reps, the mean of the middle two), the
+ * first one on ties.  Errors: MLA_ERR_INVALID_ARG on bad arguments or when
+ * no candidate was run.
+ */
+mla_status mla_autotune_select(const float* ms, int32_t num_candidates, int32_t reps,
+                               int32_t* best);
 
 /* Bytes of device workspace mla_decode_run needs for this plan (work table,
  * split partials, error word).  Errors: MLA_ERR_INVALID_ARG on NULL. */

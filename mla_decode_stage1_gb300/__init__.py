@@ -19,9 +19,11 @@ HEADS, QK_DIM, V_DIM, TILE = 16, 576, 512, 128
 DTYPES = {"bf16": 0, "fp8": 1, "mxfp4": 2}
 STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED", 3: "MLA_ERR_WORKSPACE",
           4: "MLA_ERR_CUDA", 5: "MLA_ERR_DEVICE_TIMEOUT"}
-EXPORTS = ("mla_decode_plan", "mla_decode_plan_q", "mla_plan_workspace_size", "mla_plan_get_info", "mla_plan_get_work",
-           "mla_plan_destroy", "mla_decode_run", "mla_decode_check", "mla_status_string",
-           "mla_plan_set_stage1_events", "mla_decode_run_noalloc", "mla_selftest_bounded_wait")
+EXPORTS = ("mla_decode_plan", "mla_decode_plan_q", "mla_decode_plan_ex", "mla_plan_workspace_size",
+           "mla_plan_get_info", "mla_plan_get_work", "mla_plan_destroy", "mla_decode_run",
+           "mla_decode_check", "mla_status_string", "mla_plan_set_stage1_events",
+           "mla_decode_run_noalloc", "mla_selftest_bounded_wait", "mla_decode_autotune",
+           "mla_autotune_select")
 
 
 class MlaError(RuntimeError):
@@ -35,7 +37,20 @@ class PlanInfo(ctypes.Structure):
                 ("num_ctas", ctypes.c_int32), ("num_items", ctypes.c_int32),
                 ("num_partials", ctypes.c_int32), ("num_merge_jobs", ctypes.c_int32),
                 ("total_tokens", ctypes.c_int64), ("total_tiles", ctypes.c_int64),
-                ("workspace_bytes", ctypes.c_size_t), ("q_len", ctypes.c_int32)]
+                ("workspace_bytes", ctypes.c_size_t), ("q_len", ctypes.c_int32),
+                ("unit_tokens", ctypes.c_int32), ("item_cost", ctypes.c_int32)]
+
+
+class PlanOptions(ctypes.Structure):
+    _fields_ = [("num_splits", ctypes.c_int32), ("num_sms", ctypes.c_int32),
+                ("item_cost", ctypes.c_int32), ("unit_tokens", ctypes.c_int32)]
+
+
+class TuneResult(ctypes.Structure):
+    _fields_ = [("options", PlanOptions), ("ms", ctypes.c_float)]
+
+
+TUNE_IGNORE_CACHE = 1
 
 
 def _load():
@@ -48,6 +63,13 @@ def _load():
                                     ctypes.POINTER(P)]
     lib.mla_decode_plan_q.argtypes = [P, P, i32, i32, i32, ctypes.c_int, ctypes.c_int, i32, i32,
                                       ctypes.POINTER(P)]
+    lib.mla_decode_plan_ex.argtypes = [P, P, i32, i32, i32, ctypes.c_int, ctypes.c_int, P,
+                                       ctypes.POINTER(P)]
+    lib.mla_decode_autotune.argtypes = [P, P, i32, i32, i32, ctypes.c_int, ctypes.c_int,
+                                        P, P, P, P, P, i64, i64, P, P, sz, P, P, i32, i32, P,
+                                        P, i32, ctypes.POINTER(i32), ctypes.POINTER(sz),
+                                        ctypes.POINTER(P)]
+    lib.mla_autotune_select.argtypes = [P, i32, i32, ctypes.POINTER(i32)]
     lib.mla_plan_workspace_size.argtypes = [P, ctypes.POINTER(sz)]
     lib.mla_plan_get_info.argtypes = [P, ctypes.POINTER(PlanInfo)]
     lib.mla_plan_get_work.argtypes = [P, P, P]
@@ -63,7 +85,8 @@ def _load():
     for name in ("mla_decode_plan", "mla_plan_workspace_size", "mla_plan_get_info",
                  "mla_plan_get_work", "mla_decode_run", "mla_decode_check",
                  "mla_plan_set_stage1_events", "mla_decode_run_noalloc", "mla_decode_plan_q",
-                 "mla_selftest_bounded_wait"):
+                 "mla_selftest_bounded_wait", "mla_decode_plan_ex", "mla_decode_autotune",
+                 "mla_autotune_select"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
 
@@ -137,16 +160,23 @@ class Plan:
 
 def mla_decode_plan(kv_indptr, kv_last_page_len=None, *, page_size: int, q_dtype: str,
                     kv_dtype: str, num_splits: int = 0, num_sms: int = 0,
-                    batch_size: int | None = None, q_len: int = 1) -> Plan:
+                    batch_size: int | None = None, q_len: int = 1, item_cost: int = 0,
+                    unit_tokens: int = 0) -> Plan:
     """Plan a batch from the HOST kv_indptr (in pages) and optional last-page
     lengths.  num_sms=0 queries the current CUDA device.  q_len > 1 plans
     q_len query tokens per request (mla_decode_plan_q): q, out and lse then
-    hold [bs, q_len, 16, ...] rows."""
+    hold [bs, q_len, 16, ...] rows.  item_cost / unit_tokens other than 0
+    select the plan options of mla_decode_plan_ex."""
     ind, ind_p = _i32_array(kv_indptr)
     last, last_p = _i32_array(kv_last_page_len)
     bs = len(ind) - 1 if batch_size is None else int(batch_size)
     h = ctypes.c_void_p()
-    if int(q_len) == 1:
+    if item_cost or unit_tokens:
+        opts = PlanOptions(int(num_splits), int(num_sms), int(item_cost), int(unit_tokens))
+        _check("mla_decode_plan_ex", _lib.mla_decode_plan_ex(
+            ind_p, last_p, bs, int(q_len), int(page_size), DTYPES[q_dtype], DTYPES[kv_dtype],
+            ctypes.byref(opts), ctypes.byref(h)))
+    elif int(q_len) == 1:
         _check("mla_decode_plan", _lib.mla_decode_plan(ind_p, last_p, bs, int(page_size),
                                                        DTYPES[q_dtype], DTYPES[kv_dtype],
                                                        int(num_splits), int(num_sms),
@@ -213,6 +243,52 @@ def mla_decode_run_noalloc(plan: Plan, q, kv, out, *, q_scale=None, kv_scale=Non
                                          _ptr(kv_indices), _ptr(out), _ptr(lse),
                                          _stream_ptr(stream))
     _check("mla_decode_run_noalloc", status)
+
+
+def mla_decode_autotune(kv_indptr, kv_last_page_len, q, kv, out, *, page_size: int,
+                        q_dtype: str, kv_dtype: str, workspace=None, q_scale=None,
+                        kv_scale=None, kv_e8m0=None, kv_indices=None, lse=None,
+                        kv_pool_rows: int | None = None, q_len: int = 1, reps: int = 5,
+                        ignore_cache: bool = False, stream=None):
+    """Time the candidate plans of this batch shape on these inputs and return
+    (chosen Plan, [(options dict, median ms), ...]).  With workspace=None only
+    the workspace the largest candidate needs is returned, as an int."""
+    ind, ind_p = _i32_array(kv_indptr)
+    last, last_p = _i32_array(kv_last_page_len)
+    bs = len(ind) - 1
+    results = (TuneResult * 16)()
+    nres = ctypes.c_int32()
+    need = ctypes.c_size_t()
+    h = ctypes.c_void_p()
+    rows = int(kv.shape[0]) if kv_pool_rows is None else int(kv_pool_rows)
+    stride = 0 if kv_e8m0 is None else int(kv_e8m0.stride(0))
+    ws_ptr = None if workspace is None else workspace.data_ptr()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("mla_decode_autotune", _lib.mla_decode_autotune(
+        ind_p, last_p, bs, int(q_len), int(page_size), DTYPES[q_dtype], DTYPES[kv_dtype],
+        _ptr(q), _ptr(q_scale), _ptr(kv), _ptr(kv_scale), _ptr(kv_e8m0), stride, rows,
+        _ptr(kv_indices), ws_ptr, ws_bytes, _ptr(out), _ptr(lse), int(reps),
+        TUNE_IGNORE_CACHE if ignore_cache else 0, _stream_ptr(stream), results, 16,
+        ctypes.byref(nres), ctypes.byref(need), ctypes.byref(h)))
+    if workspace is None:
+        return need.value
+    plan = Plan(h, q_dtype, kv_dtype, int(page_size))
+    plan.q_len = int(q_len)
+    table = [({"num_splits": r.options.num_splits, "num_sms": r.options.num_sms,
+               "item_cost": r.options.item_cost, "unit_tokens": r.options.unit_tokens}, r.ms)
+             for r in results[: nres.value]]
+    return plan, table
+
+
+def mla_autotune_select(ms) -> int:
+    """The autotuner's choice among candidates: ms is [candidates][reps] of
+    times (negative = not run); returns the index of the smallest median."""
+    import numpy as np
+    a = np.ascontiguousarray(ms, dtype=np.float32)
+    best = ctypes.c_int32()
+    _check("mla_autotune_select", _lib.mla_autotune_select(
+        a.ctypes.data_as(ctypes.c_void_p), int(a.shape[0]), int(a.shape[1]), ctypes.byref(best)))
+    return best.value
 
 
 def mla_selftest_bounded_wait(plan: Plan, workspace, limit_us: int = 10000, stream=None) -> None:

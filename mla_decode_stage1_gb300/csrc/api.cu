@@ -37,16 +37,16 @@ int qmode_of(int q_dtype, int kv_dtype) {
 }
 
 // Items of the balanced plan over the requests listed in `order`: their
-// tiles, in that order, cut into at most G contiguous ranges, one per CTA,
-// appended to the plan.  A range costs 2 per tile plus 1 for every item past
-// its first: an item boundary inside a CTA (an epilogue before the next
-// item's first tile) costs about half a tile period.  The smallest maximum
-// cost that G greedy ranges reach is found by bisection.
-constexpr int64_t kItemCost = 1;   // an extra item in a CTA, in half tiles
-
+// units (`unit` tokens each, a whole 128-token tile by default), in that
+// order, cut into at most G contiguous ranges, one per CTA, appended to the
+// plan.  A range costs 2 per unit plus kItemCost for every item past its
+// first: an item boundary inside a CTA (an epilogue before the next item's
+// first tile) costs about half a tile period by default.  The smallest
+// maximum cost that G greedy ranges reach is found by bisection.
 void plan_balanced(mla_plan* P, const std::vector<int32_t>& order, const std::vector<int64_t>& tiles,
                    const std::vector<int32_t>& len, const std::vector<int32_t>& page_base,
-                   const std::vector<int32_t>& npages, int32_t G) {
+                   const std::vector<int32_t>& npages, int32_t G, int64_t kItemCost,
+                   int32_t unit) {
   int64_t T = 0;
   for (const int32_t r : order) T += tiles[r];
   if (G > T) G = static_cast<int32_t>(T);
@@ -118,8 +118,8 @@ void plan_balanced(mla_plan* P, const std::vector<int32_t>& order, const std::ve
     }
     WorkItem w{};
     w.b = b;
-    w.tok_begin = static_cast<int32_t>(t0 * mla::kTile);
-    w.tok_end = static_cast<int32_t>(std::min<int64_t>((t0 + take) * mla::kTile, len[b]));
+    w.tok_begin = static_cast<int32_t>(t0 * unit);
+    w.tok_end = static_cast<int32_t>(std::min<int64_t>((t0 + take) * unit, len[b]));
     w.slot = 0;
     w.page_base = page_base[b];
     w.npages = npages[b];
@@ -130,10 +130,10 @@ void plan_balanced(mla_plan* P, const std::vector<int32_t>& order, const std::ve
 }
 
 // Items of the fixed-split plan: request b cut into S ranges of
-// ceil(tiles_b / S) tiles; one CTA per non-empty range.
+// ceil(units_b / S) units; one CTA per non-empty range.
 void plan_fixed(mla_plan* P, const std::vector<int64_t>& tiles, const std::vector<int32_t>& len,
                 const std::vector<int32_t>& page_base, const std::vector<int32_t>& npages,
-                int32_t S) {
+                int32_t S, int32_t unit) {
   P->cta_indptr.assign(1, 0);
   for (int32_t b = 0; b < P->bs; ++b) {
     const int64_t per = (tiles[b] + S - 1) / S;
@@ -142,8 +142,8 @@ void plan_fixed(mla_plan* P, const std::vector<int64_t>& tiles, const std::vecto
       if (t1 <= t0) continue;
       WorkItem w{};
       w.b = b;
-      w.tok_begin = static_cast<int32_t>(t0 * mla::kTile);
-      w.tok_end = static_cast<int32_t>(std::min<int64_t>(t1 * mla::kTile, len[b]));
+      w.tok_begin = static_cast<int32_t>(t0 * unit);
+      w.tok_end = static_cast<int32_t>(std::min<int64_t>(t1 * unit, len[b]));
       w.page_base = page_base[b];
       w.npages = npages[b];
       P->items.push_back(w);
@@ -261,12 +261,19 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 extern "C" {
 
-mla_status mla_decode_plan_q(const int32_t* kv_indptr_host, const int32_t* kv_last_page_len_host,
-                             int32_t batch_size, int32_t q_len, int32_t page_size,
-                             mla_dtype q_dtype, mla_dtype kv_dtype, int32_t num_splits,
-                             int32_t num_sms, mla_plan** plan_out) {
+mla_status mla_decode_plan_ex(const int32_t* kv_indptr_host, const int32_t* kv_last_page_len_host,
+                              int32_t batch_size, int32_t q_len, int32_t page_size,
+                              mla_dtype q_dtype, mla_dtype kv_dtype,
+                              const mla_plan_options* options, mla_plan** plan_out) {
   if (plan_out == nullptr) return MLA_ERR_INVALID_ARG;
   *plan_out = nullptr;
+  const mla_plan_options o = options != nullptr ? *options : mla_plan_options{0, 0, 0, 0};
+  int32_t num_splits = o.num_splits, num_sms = o.num_sms;
+  const int64_t item_cost = o.item_cost == 0 ? 1 : o.item_cost;
+  const int32_t unit = o.unit_tokens == 0 ? mla::kTile : o.unit_tokens;
+  if (o.item_cost < 0 || o.item_cost > 64 ||
+      (unit != 32 && unit != 64 && unit != mla::kTile))
+    return MLA_ERR_INVALID_ARG;
   if (kv_indptr_host == nullptr || batch_size < 1 || page_size < 1 || num_splits < 0 ||
       num_sms < 0 || q_len < 1 || q_len > MLA_MAX_Q_LEN ||
       static_cast<int64_t>(batch_size) * q_len > INT32_MAX / mla::kHeads)
@@ -288,8 +295,8 @@ mla_status mla_decode_plan_q(const int32_t* kv_indptr_host, const int32_t* kv_la
   const int32_t qv = pairs ? q_len / 2 : q_len;    // virtual requests per request
   const int32_t nv = batch_size * qv;
   std::vector<int32_t> len(nv), page_base(nv), npages(nv), vis0(nv, 0);
-  std::vector<int64_t> tiles(nv);
-  int64_t total_tok = 0, total_tiles = 0;
+  std::vector<int64_t> tiles(nv);                  // cut units of each virtual request
+  int64_t total_tok = 0, total_tiles = 0, total_units = 0;
   int64_t identity_rows = 0;      // pool rows the identity table reaches
   for (int32_t b = 0; b < batch_size; ++b) {
     const int64_t np = static_cast<int64_t>(kv_indptr_host[b + 1]) - kv_indptr_host[b];
@@ -310,9 +317,10 @@ mla_status mla_decode_plan_q(const int32_t* kv_indptr_host, const int32_t* kv_la
       vis0[r] = static_cast<int32_t>(std::max<int64_t>(0, first_seen));
       page_base[r] = kv_indptr_host[b];
       npages[r] = static_cast<int32_t>(np);
-      tiles[r] = (len[r] + mla::kTile - 1) / mla::kTile;
+      tiles[r] = (len[r] + unit - 1) / unit;
       total_tok += len[r];
-      total_tiles += tiles[r];
+      total_tiles += (len[r] + mla::kTile - 1) / mla::kTile;
+      total_units += tiles[r];
     }
   }
   if (num_sms == 0) {
@@ -335,16 +343,19 @@ mla_status mla_decode_plan_q(const int32_t* kv_indptr_host, const int32_t* kv_la
   P->total_tokens = total_tok;
   P->identity_rows = identity_rows;
   P->total_tiles = total_tiles;
+  P->unit_tokens = unit;
+  P->item_cost = static_cast<int32_t>(item_cost);
+  P->num_sms = num_sms;
   P->cta_indptr.assign(1, 0);
   if (num_splits == 0) {
-    const int32_t G = static_cast<int32_t>(std::min<int64_t>(num_sms, total_tiles));
+    const int32_t G = static_cast<int32_t>(std::min<int64_t>(num_sms, total_units));
     std::vector<int32_t> order;
     if (qv == 1 || G < qv) {
       // query-token-major order: the q_len passes over a request's KV stay
       // close in time when the CTAs are too few to group them
       for (int32_t t = 0; t < qv; ++t)
         for (int32_t b = 0; b < batch_size; ++b) order.push_back(b * qv + t);
-      plan_balanced(P, order, tiles, len, page_base, npages, G);
+      plan_balanced(P, order, tiles, len, page_base, npages, G, item_cost, unit);
     } else {
       // one group of CTAs per query token (or pair), each balanced over
       // every request: CTA i of each group reads the same KV at about the
@@ -354,17 +365,26 @@ mla_status mla_decode_plan_q(const int32_t* kv_indptr_host, const int32_t* kv_la
         for (int32_t b = 0; b < batch_size; ++b) order.push_back(b * qv + t);
         const int32_t Gt = static_cast<int32_t>((static_cast<int64_t>(G) * (t + 1)) / qv -
                                                 (static_cast<int64_t>(G) * t) / qv);
-        plan_balanced(P, order, tiles, len, page_base, npages, Gt);
+        plan_balanced(P, order, tiles, len, page_base, npages, Gt, item_cost, unit);
       }
     }
   } else {
-    plan_fixed(P, tiles, len, page_base, npages, num_splits);
+    plan_fixed(P, tiles, len, page_base, npages, num_splits, unit);
   }
   for (WorkItem& w : P->items) w.vis0 = vis0[w.b];
   assign_slots(P, len);
   layout_workspace(P);
   *plan_out = P;
   return MLA_OK;
+}
+
+mla_status mla_decode_plan_q(const int32_t* kv_indptr_host, const int32_t* kv_last_page_len_host,
+                             int32_t batch_size, int32_t q_len, int32_t page_size,
+                             mla_dtype q_dtype, mla_dtype kv_dtype, int32_t num_splits,
+                             int32_t num_sms, mla_plan** plan_out) {
+  const mla_plan_options o{num_splits, num_sms, 0, 0};
+  return mla_decode_plan_ex(kv_indptr_host, kv_last_page_len_host, batch_size, q_len, page_size,
+                            q_dtype, kv_dtype, &o, plan_out);
 }
 
 mla_status mla_decode_plan(const int32_t* kv_indptr_host, const int32_t* kv_last_page_len_host,
@@ -393,6 +413,8 @@ mla_status mla_plan_get_info(const mla_plan* plan, mla_plan_info* info) {
   info->total_tokens = plan->total_tokens;
   info->total_tiles = plan->total_tiles;
   info->workspace_bytes = plan->ws_bytes;
+  info->unit_tokens = plan->unit_tokens;
+  info->item_cost = plan->item_cost;
   return MLA_OK;
 }
 
@@ -449,7 +471,9 @@ mla_status mla_decode_run(mla_plan* plan, const void* q, const float* q_scale, c
     else
       gather = 1;
   }
-  if (mx) box_rows = 8;
+  // MXFP4, and plans cut below whole tiles (a CTA's rows are then fewer
+  // than 128): 8-row groups
+  if (mx || plan->unit_tokens < mla::kTile) box_rows = 8;
   // bytes per row of the tile the UMMAs read (MXFP4 is dequantised to e4m3)
   const uint32_t row_bytes = mla::kQkDim * (plan->kv_dtype == MLA_DTYPE_BF16 ? 2 : 1);
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);

@@ -19,6 +19,9 @@ struct mla_plan {
   int q_dtype = 0, kv_dtype = 0, qmode = 0;
   int32_t num_ctas = 0, num_partials = 0;
   int32_t max_parts = 0;   // most partials of one request (stage 2 goes wide above 4)
+  int32_t unit_tokens = mla::kTile;   // tokens between the planner's possible cut points
+  int32_t item_cost = 1;              // cost of an extra item in a CTA (balanced plan)
+  int32_t num_sms = 0;                // CTAs the balanced plan was cut for
   int64_t total_tokens = 0, total_tiles = 0;
   int64_t identity_rows = 0;   // pool rows the requests reach without a page table
   std::vector<int32_t> cta_indptr;

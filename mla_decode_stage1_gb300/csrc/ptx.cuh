@@ -90,6 +90,11 @@ __device__ __forceinline__ int32_t ld_nc_early(const int32_t* ptr) {
   return v;
 }
 
+__device__ __forceinline__ uint64_t ld_nc_early_u64(const uint64_t* ptr) {
+  uint64_t v;
+  asm volatile("ld.global.nc.b64 %0, [%1];" : "=l"(v) : "l"(ptr));
+  return v;
+}
 __device__ __forceinline__ uint32_t ld_nc_u8_early(const uint8_t* ptr) {
   uint16_t v;
   asm volatile("ld.global.nc.u8 %0, [%1];" : "=h"(v) : "l"(ptr));

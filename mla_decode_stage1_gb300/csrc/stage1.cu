@@ -1393,9 +1393,10 @@ __global__ void __launch_bounds__(Layout<QM>::kThreads, 1) mla_stage1_kernel(con
     // The workspace must hold this plan's table: its stamp in the header and
     // in this CTA's head.  Otherwise (another plan's table was uploaded at
     // this address since) nothing is read from the table and nothing is
-    // written; mla_decode_check reports it.
-    const uint64_t hs = reinterpret_cast<const WsHeader*>(p.err)->stamp;
-    ms->stale = (hs != p.stamp || head.stamp != p.stamp) ? 1 : 0;
+    // written; mla_decode_check reports it.  The two stamps are loaded first
+    // and compared after the barrier set-up, which hides their latency.
+    const uint64_t hs = ld_nc_early_u64(&reinterpret_cast<const WsHeader*>(p.err)->stamp);
+    const uint64_t cs = ld_nc_early_u64(&head.stamp);
     for (int i = 0; i < L::kNumTiles; ++i) {
       mbar_init(smem_u32(&ms->full[i]), p.gather ? 32 : 1);   // gather: one per producer lane
       mbar_init(smem_u32(&ms->empty[i]), L::kPvIssuers);
@@ -1421,6 +1422,7 @@ __global__ void __launch_bounds__(Layout<QM>::kThreads, 1) mla_stage1_kernel(con
     mbar_init(smem_u32(&ms->q_stage_free), 1);
     ms->abort_sm = 0;
     fence_mbar_init();
+    ms->stale = (hs != p.stamp || cs != p.stamp) ? 1 : 0;
   }
   if (!L::kMx && warp == 0 && lane == 0) prefetch_tensormap(&p.tmap_kv);
   if (warp == 1) {

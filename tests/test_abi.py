@@ -128,13 +128,13 @@ def lengths_of(indptr, last, ps):
     return n
 
 
-def check_partition(pl, lengths):
+def check_partition(pl, lengths, unit=128):
     ind, items = pl.work()
     info = pl.info()
     assert ind[0] == 0 and ind[-1] == info.num_items and np.all(np.diff(ind) >= 1)
     covered = {b: [] for b in range(len(lengths))}
     for b, t0, t1, slot in items:
-        assert 0 <= t0 < t1 <= lengths[b] and t0 % 128 == 0
+        assert 0 <= t0 < t1 <= lengths[b] and t0 % unit == 0
         covered[b].append((t0, t1, slot))
     nslots = set()
     for b, rngs in covered.items():
@@ -378,3 +378,90 @@ def test_randomized_plans_partition_every_query_token(mla, seed):
     assert pl.workspace_bytes >= info.num_partials * rows * (512 + 1) * 4
     if S == 0 and q_len == 1 and info.num_ctas > 0:
         assert max(plan_costs(ind, items)) <= uniform_split_max_cost(vlens, sms)
+
+
+# ------------------------------------------------- plan options and autotune
+
+def plan_ex(mla, indptr, ps=1, qd="bf16", kd="fp8", S=0, sms=152, item_cost=0, unit=0):
+    return mla.mla_decode_plan(np.asarray(indptr, np.int32), None, page_size=ps, q_dtype=qd,
+                               kv_dtype=kd, num_splits=S, num_sms=sms, item_cost=item_cost,
+                               unit_tokens=unit)
+
+
+@pytest.mark.parametrize("unit", [32, 64, 128])
+@pytest.mark.parametrize("bs,kv", [(4, 1024), (32, 1024), (5, 777), (64, 8192)])
+def test_plan_cut_units(mla, unit, bs, kv):
+    # finer cut points: every item starts on a unit boundary, the partition
+    # still covers every token once, and a small batch spreads over more CTAs
+    indptr = np.arange(bs + 1) * kv
+    pl = plan_ex(mla, indptr, unit=unit)
+    check_partition(pl, [kv] * bs, unit=unit)
+    info = pl.info()
+    assert info.unit_tokens == unit
+    units = bs * -(-kv // unit)
+    if units <= 152:
+        assert info.num_ctas == units          # one unit per CTA
+    else:
+        assert 1 <= info.num_ctas <= 152
+    assert info.total_tiles == bs * -(-kv // 128)
+
+
+def test_plan_item_cost_bounds(mla):
+    # under its own item cost, the balanced plan's most expensive CTA is
+    # never dearer than that of the plain equal split of the tiles (the bound
+    # the planner's bisection starts from)
+    rng = np.random.default_rng(3)
+    lens = rng.integers(1, 3000, 300)
+    indptr = np.concatenate([[0], np.cumsum(lens)])
+    tiles = [(n + 127) // 128 for n in lens]
+    owner = [b for b, t in enumerate(tiles) for _ in range(t)]
+    T, G = len(owner), 152
+    for cost in (1, 2, 4, 16):
+        pl = plan_ex(mla, indptr, item_cost=cost)
+        ind, items = check_partition(pl, lens)
+        assert pl.info().item_cost == cost
+        worst = max(2 * sum((t1 - t0 + 127) // 128 for _, t0, t1, _ in items[ind[c]:ind[c + 1]])
+                    + cost * (ind[c + 1] - ind[c] - 1) for c in range(len(ind) - 1))
+        equal = max(2 * len(seg) + cost * (len(set(seg)) - 1)
+                    for seg in (owner[T * i // G: T * (i + 1) // G] for i in range(G)) if seg)
+        assert worst <= equal
+
+
+def test_plan_options_validated(mla):
+    indptr = np.array([0, 100], np.int32)
+    for kw in (dict(unit=48), dict(unit=256), dict(item_cost=-1), dict(item_cost=65)):
+        with pytest.raises(mla.MlaError) as e:
+            plan_ex(mla, indptr, **kw)
+        assert e.value.status == 1
+    # all zero is the default plan
+    a, b = plan_ex(mla, indptr).work(), plan(mla, indptr, sms=152).work()
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_autotune_selects_the_smallest_median(mla):
+    sel = mla.mla_autotune_select
+    assert sel([[3.0, 1.0, 2.0], [2.5, 2.4, 2.6], [9.0, 0.1, 9.0]]) == 0   # medians 2, 2.5, 9
+    assert sel([[3.0, 3.1, 2.9], [2.5, 2.4, 2.6], [0.1, 9.0, 9.0]]) == 1   # medians 3, 2.5, 9
+    assert sel([[5.0, 5.0, 5.0], [-1.0, 0.1, 0.1], [4.0, 6.0, 4.5]]) == 2  # a run with -1 is skipped
+    assert sel([[2.0, 2.0], [2.0, 2.0], [1.0, 3.0]]) == 0                  # ties: the first
+    assert sel([[1.0, 4.0], [2.0, 2.2]]) == 1                              # even reps: mean of the middle two
+    assert sel([[float("nan"), 1.0], [7.0, 7.0]]) == 1                     # NaN: not run
+    with pytest.raises(mla.MlaError):
+        sel([[-1.0], [-2.0]])
+
+
+def test_autotune_workspace_query_without_a_gpu(mla):
+    # workspace NULL: the plans are built and the largest workspace reported;
+    # nothing is launched (so this runs on a host without a GPU)
+    lib = mla._lib
+    indptr = np.arange(5, dtype=np.int32) * 1024
+    need = ctypes.c_size_t()
+    nres = ctypes.c_int32()
+    st = lib.mla_decode_autotune(indptr.ctypes.data_as(ctypes.c_void_p), None, 4, 1, 1, 0, 1,
+                                 None, None, None, None, None, 0, 4096, None, None, 0, None, None,
+                                 3, 0, None, None, 0, ctypes.byref(nres), ctypes.byref(need),
+                                 None)
+    # (num_sms 0 needs the device: without a GPU the query reports MLA_ERR_CUDA)
+    assert st in (0, 4)
+    if st == 0:
+        assert need.value > 0 and nres.value == 0

@@ -25,12 +25,12 @@ def _mla():
     return mla
 
 
-def run_gpu(w, num_splits=0, num_sms=0):
+def run_gpu(w, num_splits=0, num_sms=0, **plan_kw):
     mla = _mla()
     import workloads as synth  # noqa: F401
     plan = mla.mla_decode_plan(w.kv_indptr, w.kv_last_page_len, page_size=w.page_size,
                                q_dtype=w.q_dtype, kv_dtype=w.kv_dtype, num_splits=num_splits,
-                               num_sms=num_sms, q_len=w.q_len)
+                               num_sms=num_sms, q_len=w.q_len, **plan_kw)
     d = w.to("cuda")
     ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
     rows = w.bs * w.q_len
@@ -60,9 +60,9 @@ def compare(o, lse, o_ref, l_ref, kv_dtype, lengths):
             f"request {b}: lse max err {np.abs(lse[b]-l_ref[b]).max()}"
 
 
-def check(w, num_splits=0, num_sms=0, select=None):
+def check(w, num_splits=0, num_sms=0, select=None, **plan_kw):
     import workloads as synth
-    o, lse, plan = run_gpu(w, num_splits=num_splits, num_sms=num_sms)
+    o, lse, plan = run_gpu(w, num_splits=num_splits, num_sms=num_sms, **plan_kw)
     sel = list(range(w.bs)) if select is None else list(select)
     o_ref, l_ref = oracle.mla_decode(**synth.oracle_args(w, select=sel))
     # rows b*q_len + t; query token t of a request with n tokens sees the
@@ -586,3 +586,72 @@ def test_many_partials_per_request_wide_merge(q_len):
                             kv_dtype="fp8", permute_pages=True, seed=55, q_len=q_len)
     plan = check(w, num_splits=20)
     assert plan.info().num_partials > 20
+
+
+# ------------------------------------------------- plan options, autotune
+
+@pytest.mark.parametrize("unit", [32, 64])
+@pytest.mark.parametrize("q_dtype,kv_dtype,page_size", [
+    ("bf16", "bf16", 1), ("bf16", "fp8", 8), ("fp8", "fp8", 1), ("bf16", "fp8", 3),
+    ("bf16", "mxfp4", 1), ("bf16", "mxfp4", 3), ("fp8", "fp8", 16)])
+def test_sub_tile_cut_units(unit, q_dtype, kv_dtype, page_size):
+    # items that start inside a tile (cut every 32 or 64 tokens): a CTA loads
+    # only its rows; ragged and empty requests, page tables and MXFP4
+    import workloads as synth
+    lengths = [1024, 1024, 300, 0, 77, 129]
+    w = synth.make_workload(bs=len(lengths), lengths=lengths, page_size=page_size,
+                            q_dtype=q_dtype, kv_dtype=kv_dtype, permute_pages=page_size > 1,
+                            seed=80)
+    plan = check(w, unit_tokens=unit)
+    assert plan.info().unit_tokens == unit
+    check(w, unit_tokens=unit, item_cost=4, num_sms=7)
+
+
+@pytest.mark.parametrize("q_len", [1, 2])
+def test_sub_tile_cut_units_several_query_tokens(q_len):
+    import workloads as synth
+    lengths = [700, 5, 1030, 64]
+    w = synth.make_workload(bs=len(lengths), lengths=lengths, page_size=8, q_dtype="fp8",
+                            kv_dtype="fp8", permute_pages=True, seed=81, q_len=q_len)
+    check(w, unit_tokens=32)
+
+
+@pytest.mark.parametrize("q_dtype,kv_dtype,page_size", [("bf16", "bf16", 1), ("bf16", "mxfp4", 1),
+                                                        ("fp8", "fp8", 8)])
+def test_autotune_choice_matches_the_oracle(q_dtype, kv_dtype, page_size):
+    # every candidate is timed on these inputs; the chosen plan is the one
+    # with the smallest median, and its result matches the oracle; the same
+    # shape again is served from the cache without timing
+    mla = _mla()
+    import workloads as synth
+    lengths = [1024, 1024, 1024, 1024]
+    w = synth.make_workload(bs=4, lengths=lengths, page_size=page_size, q_dtype=q_dtype,
+                            kv_dtype=kv_dtype, permute_pages=page_size > 1, seed=82)
+    d = w.to("cuda")
+    out = torch.empty(4, 16, 512, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(4, 16, dtype=torch.float32, device="cuda")
+    kw = dict(page_size=page_size, q_dtype=q_dtype, kv_dtype=kv_dtype, q_scale=d.q_scale,
+              kv_scale=d.kv_scale, kv_e8m0=d.kv_e8m0, kv_indices=d.kv_indices, lse=lse)
+    need = mla.mla_decode_autotune(w.kv_indptr, w.kv_last_page_len, d.q, d.kv, out, **kw)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    plan, table = mla.mla_decode_autotune(w.kv_indptr, w.kv_last_page_len, d.q, d.kv, out,
+                                          workspace=ws, reps=3, ignore_cache=True, **kw)
+    assert len(table) >= 6 and all(ms > 0 for _, ms in table)
+    info = plan.info()
+    best = min(table, key=lambda r: r[1])
+    chosen = [r for r in table if r[1] == best[1]][0][0]
+    assert info.unit_tokens == (chosen["unit_tokens"] or 128)
+    assert info.item_cost == (chosen["item_cost"] or 1)
+    res = torch.full((4, 16, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    res_lse = torch.full((4, 16), float("nan"), dtype=torch.float32, device="cuda")
+    mla.mla_decode_run(plan, d.q, d.kv, res, workspace=ws, q_scale=d.q_scale, kv_scale=d.kv_scale,
+                       kv_e8m0=d.kv_e8m0, kv_indices=d.kv_indices, lse=res_lse)
+    mla.mla_decode_check(plan, ws)
+    o_ref, l_ref = oracle.mla_decode(**synth.oracle_args(w))
+    compare(res.float().cpu().numpy().astype(np.float64), res_lse.cpu().numpy().astype(np.float64),
+            o_ref, l_ref, kv_dtype, lengths)
+    plan2, table2 = mla.mla_decode_autotune(w.kv_indptr, w.kv_last_page_len, d.q, d.kv, out,
+                                            workspace=ws, reps=3, **kw)
+    assert table2 == []
+    assert plan2.info().unit_tokens == info.unit_tokens and plan2.info().item_cost == info.item_cost
+    assert plan2.info().num_ctas == info.num_ctas
