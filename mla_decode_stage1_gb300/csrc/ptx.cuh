@@ -95,6 +95,14 @@ __device__ __forceinline__ uint64_t ld_nc_early_u64(const uint64_t* ptr) {
   asm volatile("ld.global.nc.b64 %0, [%1];" : "=l"(v) : "l"(ptr));
   return v;
 }
+// 16 bytes, issued where it is written, not kept in L1 (read once).
+__device__ __forceinline__ uint4 ld_nc_na_v4(const void* ptr) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(ptr));
+  return v;
+}
 __device__ __forceinline__ uint32_t ld_nc_u8_early(const uint8_t* ptr) {
   uint16_t v;
   asm volatile("ld.global.nc.u8 %0, [%1];" : "=h"(v) : "l"(ptr));
@@ -156,15 +164,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
-// The same with an L2 cache policy.
-__device__ __forceinline__ void bulk_load_hint(uint32_t dst, const void* src, uint32_t bytes,
-                                               uint32_t bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar), "l"(policy)
-      : "memory");
-}
 
 // 3-D tiled bulk tensor load (coordinates innermost first).
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,

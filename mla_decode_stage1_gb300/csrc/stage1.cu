@@ -27,8 +27,8 @@
 //    one group per query token, 16 heads each; one thread per token / per
 //    output dim, TMEM lane = thread) and convert the first item's q; warp
 //    12 converts the q of later items;
-//  * MXFP4: warps 12-19 copy the packed rows into four landing units (plain
-//    bulk copies, any page size), dequantise them into the e4m3 tile slot
+//  * MXFP4: warps 12-19 load the packed rows from global memory straight
+//    into registers (any page size), dequantise them into the e4m3 tile slot
 //    and prepare every item's q; the warpgroups then run with their own
 //    register limits (setmaxnreg);
 //  * every mbarrier wait is bounded (see mbar_wait) and reports into the
@@ -65,8 +65,8 @@ struct Layout {
   static constexpr int kNq = kRows * (kHiLo ? 2 : 1);               // UMMA N of QK^T
   // Warps: producer (MXFP4: a PV issuer), 2 QK^T issuers, PV issuers, two
   // head groups of four softmax warps (kH q rows each), then either a q warp
-  // (14 warps) or, for MXFP4, 8 dequant warps that also prepare q and copy
-  // the packed rows (20 warps).
+  // (14 warps) or, for MXFP4, 8 dequant warps that also load the packed
+  // rows and prepare q (20 warps).
   static constexpr int kHeadGroups = 2;
   static constexpr int kH = kRows / kHeadGroups;                    // q rows per softmax thread
   static constexpr int kThreads = kMx ? 640 : 448;
@@ -94,18 +94,13 @@ struct Layout {
   static constexpr bool kQ8 = (QM == kQFp8KvFp8 || QM == kQFp8KvBf16 || QM == kQFp8KvFp8x2);
   static constexpr int kQSrcBytes = kRows * kQkDim * (kQ8 ? 1 : 2);  // one request's q
   // q staging buffer (raw q of the next item); MXFP4 converts q from global
-  // memory, and keeps one q buffer, so that its landing ring fits
+  // memory into its one q buffer
   static constexpr int kQStageBytes = kMx ? 0 : kQSrcBytes;
   static constexpr int kQBufs = kMx ? 1 : 2;
   static constexpr uint32_t kOCols = kRows * (kKv8 ? 2 : 1);       // TMEM columns per O block
   // TMEM: S^T at 0 (2 buffers x 2 K-halves x 32 columns), O^T from 128
   static constexpr uint32_t kTmemCols = 128 + 4 * kOCols <= 256 ? 256 : 512;
   static constexpr int kMiscBytes = 2560;
-  // MXFP4: packed rows land in kUnits landing units, unit q holding rows
-  // 32q .. 32q+31 of every tile (row-major, 288 bytes a row)
-  static constexpr int kUnitRows = 32;
-  static constexpr int kUnitBytes = kUnitRows * kRawRowBytes;      // 9216
-  static constexpr int kUnits = kMx ? 4 : 0;
   static constexpr int kMaxSmem = 232448;
   static constexpr int kNumTiles =
       kMx ? 2
@@ -114,14 +109,12 @@ struct Layout {
   static constexpr int kQOff = kNumTiles * kTileBytes;
   static constexpr int kPOff = kQOff + kQBufs * kQBytes;
   static constexpr int kMiscOff = kPOff + 2 * kPBytes;
-  static constexpr int kUnitOff = kMiscOff + kMiscBytes;
-  static constexpr int kQStageOff = kUnitOff + kUnits * kUnitBytes;  // raw q of the next item
+  static constexpr int kQStageOff = kMiscOff + kMiscBytes;        // raw q of the next item
   static constexpr int kSmemBytes = kQStageOff + kQStageBytes + 1024;
   static_assert(kNumTiles >= 1 && kNumTiles <= 4, "tile ring");
   static_assert(kSmemBytes <= kMaxSmem, "shared memory over budget");
   static_assert(kTileBytes % 1024 == 0 && kQBytes % 1024 == 0, "operand alignment");
   static_assert(kNq <= 32, "S^T columns per K-half");
-  static_assert(kUnitOff % 16 == 0 && kUnitBytes % 16 == 0, "bulk copy alignment");
 };
 
 // Misc region: barriers, reduction scratch, q scales, TMEM address.
@@ -136,7 +129,6 @@ struct Misc {
   uint64_t q_stage_free;             // the softmax warps converted the first item's q
   float qred[8];                     // per-warp |q| maxima (q prepared by a warp group)
   // MXFP4 only
-  uint64_t unit_full[4];             // landing unit filled (the two warps of its rows)
   uint64_t deq_a[4];                 // tile slot chunks 0-4 (dims 0-319) dequantised: the
                                      // first QK^T K-half (dims 0-287) may start
   uint64_t deq_b[4];                 // chunks 5-8 dequantised (the slot is complete)
@@ -556,27 +548,32 @@ __device__ __forceinline__ int32_t scale_page(const Stage1Params& p, const TileA
   return ld_nc_early(p.kv_indices + c.page_base + (c.t0() + tq) / p.page_size);
 }
 
-// Issues the nine 1-byte loads of bytes hb, hb + 2, .. hb + 16 of the
-// token's scale row (the blocks of one dequant half; zeros past the tile's
-// end); `page` is scale_page() of the same tile and token.
-__device__ __forceinline__ void scale_load(const Stage1Params& p, const TileAhead& c, int tq,
-                                           int hb, int32_t page, uint32_t (&e)[9]) {
-  if (c.ntile == 0 || tq >= c.nvalid()) {
+// Pool row of token tq of a look-ahead tile, or -1 past the tile's end.
+// `page` is scale_page() of the same tile and token: a page outside the pool
+// reads page 0 and is reported.
+__device__ __forceinline__ int64_t pool_row(const Stage1Params& p, const TileAhead& c, int tq,
+                                            int32_t page) {
+  if (c.ntile == 0 || tq >= c.nvalid()) return -1;
+  const int pos = c.t0() + tq;
+  if (p.kv_indices == nullptr) {
+    const int64_t row = static_cast<int64_t>(c.page_base) * p.page_size + pos;
+    return row < p.pool_rows ? row : 0;   // (the host rejects such plans; never reached)
+  }
+  if (page < 0 || static_cast<int64_t>(page + 1) * p.page_size > p.pool_rows) {
+    atomicOr(p.err, kErrBadPage);
+    page = 0;
+  }
+  return static_cast<int64_t>(page) * p.page_size + pos % p.page_size;
+}
+
+// Issues the nine 1-byte loads of bytes hb, hb + 2, .. hb + 16 of scale row
+// `row` (the blocks of one dequant half; zeros for row -1).
+__device__ __forceinline__ void scale_load(const Stage1Params& p, int64_t row, int hb,
+                                           uint32_t (&e)[9]) {
+  if (row < 0) {
 #pragma unroll
     for (int i = 0; i < 9; ++i) e[i] = 0;
     return;
-  }
-  const int pos = c.t0() + tq;
-  int64_t row;
-  if (p.kv_indices == nullptr) {
-    row = static_cast<int64_t>(c.page_base) * p.page_size + pos;
-    if (row >= p.pool_rows) row = 0;   // (the host rejects such plans; never reached)
-  } else {
-    if (page < 0 || static_cast<int64_t>(page + 1) * p.page_size > p.pool_rows) {
-      atomicOr(p.err, kErrBadPage);
-      page = 0;
-    }
-    row = static_cast<int64_t>(page) * p.page_size + pos % p.page_size;
   }
   const uint8_t* src = p.kv_e8m0 + row * p.sc_stride + hb;
 #pragma unroll
@@ -768,13 +765,16 @@ __device__ bool qprep_mx(const Stage1Params& p, Misc* ms, uint8_t* qgen, int b, 
 
 // Chunks [j0, j1) of one dequant thread: block 2j + h of its token (packed
 // in x[j], e8m0 byte in eb[j]) into e4m3 chunk j of its row at dst,
-// pieces pc0 / pc1; zeros for a row past the tile's end.  Returns whether
-// anything was written (the caller then fences the writes for the UMMAs).
+// pieces pc0 / pc1; zeros for a row past the tile's end.  As soon as block j
+// is converted, x[j] is reloaded with the same block of the next tile's row
+// (from `next`, unless null), so each load has one tile period to arrive.
+// Returns whether anything was written (the caller then fences the writes
+// for the UMMAs).
 template <int kN>
-__device__ __forceinline__ bool half_of_tile(bool ok, bool live, bool fast, const uint4 (&x)[kN],
+__device__ __forceinline__ bool half_of_tile(bool ok, bool live, bool fast, uint4 (&x)[kN],
                                              const uint32_t (&eb)[kN], int r, const uint2* tab,
                                              uint8_t* dst, uint32_t pc0, uint32_t pc1, int j0,
-                                             int j1) {
+                                             int j1, const uint8_t* next) {
   if (!ok) return false;
 #pragma unroll
   for (int j = 0; j < kN; ++j) {
@@ -795,80 +795,29 @@ __device__ __forceinline__ bool half_of_tile(bool ok, bool live, bool fast, cons
       o0 = make_uint4(e0.x, e0.y, e1.x, e1.y);
       o1 = make_uint4(e2.x, e2.y, e3.x, e3.y);
     }
+    if (next != nullptr) x[j] = ld_nc_na_v4(next + 32 * j);
     *reinterpret_cast<uint4*>(dst + j * 512 + pc0) = o0;
     *reinterpret_cast<uint4*>(dst + j * 512 + pc1) = o1;
   }
   return true;
 }
 
-// The packed rows of one warp for a tile: rows 16 wi .. 16 wi + 15 of the
-// tile (wi = the warp's index among the dequant warps) into unit wi / 2 at
-// row (wi & 1) * 16, with plain bulk copies, one per run of rows contiguous
-// in the pool (one for the identity table, one per page otherwise), issued by
-// the lane of the run's first row.  Lane l holds row 4 (l >> 3) + (l & 3) of
-// the sixteen when (l >> 2) & 1 == 0 ("row lanes"); `page` is the row's raw
-// page-table entry (checked here: a page outside the pool reads page 0 and is
-// reported).  The lanes' arrive on the unit's barrier counts the bytes.
-__device__ __forceinline__ void copy_rows(const Stage1Params& p, const TileAhead& c, int wi,
-                                          int lane, int32_t page, uint32_t unit, uint32_t bar,
-                                          uint64_t pol) {
-  constexpr uint32_t kRow = kQkDim / 2;                    // packed bytes per row
-  const int nvalid = c.ntile ? c.nvalid() : 0;
-  if (p.kv_indices == nullptr) {                            // identity table: one copy, lane 0
-    if (lane == 0) {
-      const int nrows = max(0, min(16, nvalid - 16 * wi));
-      mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nrows) * kRow);
-      if (nrows > 0)
-        bulk_load_hint(unit + (wi & 1) * 16 * kRow,
-                       p.kv + (static_cast<int64_t>(c.page_base) * p.page_size + c.t0() + 16 * wi) * kRow,
-                       static_cast<uint32_t>(nrows) * kRow, bar, pol);
-    }
-    return;
-  }
-  const int r16 = 4 * (lane >> 3) + (lane & 3);             // this lane's row among the sixteen
-  const int row = 16 * wi + r16;
-  const bool row_lane = ((lane >> 2) & 1) == 0;
-  const int nrows = max(0, min(16, nvalid - 16 * wi));      // rows of this warp in the tile
-  bool head = false;
-  int64_t grow = 0;
-  if (row_lane && r16 < nrows) {
-    const int pos = c.t0() + row;
-    if (page < 0 || static_cast<int64_t>(page + 1) * p.page_size > p.pool_rows) {
-      atomicOr(p.err, kErrBadPage);
-      page = 0;
-    }
-    grow = static_cast<int64_t>(page) * p.page_size + pos % p.page_size;
-    head = r16 == 0 || pos % p.page_size == 0;
-  }
-  const uint32_t heads = __ballot_sync(0xffffffffu, head);
-  if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nrows) * kRow);
-  __syncwarp();                                              // the bytes are expected first
-  if (head) {
-    // the run ends at the next head's row (row lanes are in row order)
-    const uint32_t later = heads & ~((2u << lane) - 1u);
-    const int end = later ? 4 * ((__ffs(later) - 1) >> 3) + ((__ffs(later) - 1) & 3) : nrows;
-    bulk_load_hint(unit + ((wi & 1) * 16 + r16) * kRow, p.kv + grow * kRow,
-                   static_cast<uint32_t>(end - r16) * kRow, bar, pol);
-  }
-}
-
 // Eight warps turn the packed MXFP4 rows of a tile into the e4m3 tile slot
-// the UMMAs read, and copy the packed rows in.  Dequant warp wi owns rows
-// 16 wi .. 16 wi + 15 of every tile: lane l works on row
-// 16 wi + 4 (l >> 3) + (l & 3) and, with h = (l >> 2) & 1, on every other
-// scale block of it (the even blocks 0, 2, .. 16 for h = 0, the odd ones for
-// h = 1).  Block 2j + h is the h-th 32-byte half of e4m3 chunk j, so a
-// thread's nine blocks go to the same two swizzled 16-byte pieces of chunks
-// 0-8: every address is a fixed offset from the thread's row.  In each group
-// of eight lanes (four rows, both halves) the 16-byte reads of the landing
-// unit and the swizzled e4m3 writes hit eight different bank groups.
+// the UMMAs read.  Dequant warp wi owns rows 16 wi .. 16 wi + 15 of every
+// tile: lane l works on row 16 wi + 4 (l >> 3) + (l & 3) and, with
+// h = (l >> 2) & 1, on every other scale block of it (the even blocks 0, 2,
+// .. 16 for h = 0, the odd ones for h = 1).  Block 2j + h is the h-th
+// 32-byte half of e4m3 chunk j, so a thread's nine blocks go to the same two
+// swizzled 16-byte pieces of chunks 0-8: every address is a fixed offset
+// from the thread's row, and in each group of eight lanes (four rows, both
+// halves) the swizzled e4m3 writes hit eight different bank groups.
 //
-// Landing: unit q holds rows 32q .. 32q+31 of every tile, filled by the two
-// warps of those rows.  A warp loads its nine blocks per thread into
-// registers and, in the same warp, issues the copies of the same rows of the
-// next tile into the unit, so the copy flies while this tile is converted.
-// Chunks 0-4 (dims 0-319, which hold the first QK^T K-half) are published
-// before chunks 5-8.
+// The packed blocks go from global memory straight into registers: block j
+// of the next tile is loaded as soon as block j of this tile is converted,
+// so every load has a tile period to arrive and nothing lands in shared
+// memory first.  (An L2 prefetch of the rows two tiles ahead made the
+// kernel slower.)  Chunks 0-4 (dims 0-319, which hold the first QK^T
+// K-half) are published before chunks 5-8.
 //
 // With r_t the token's largest e8m0 exponent, block b becomes
 // e2m1 * 2^(E_b - r_t): exact in e4m3 while E_b - r_t >= -8.  The remaining
@@ -881,17 +830,13 @@ __device__ __forceinline__ void copy_rows(const Stage1Params& p, const TileAhead
 // The same threads prepare q: item 0's before the first tile, item k's
 // right after dequantising item k's first tile (QK^T of item k waits for it).
 template <int QM>
-__device__ void run_dequant_mx(const Stage1Params& p, Misc* ms, uint8_t* ring_gen,
-                               uint8_t* units_gen, uint8_t* qgen, int it0, int it1,
-                               const WorkItem& first, int d) {
+__device__ void run_dequant_mx(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, uint8_t* qgen,
+                               int it0, int it1, const WorkItem& first, int d) {
   using L = Layout<QM>;
   static_assert(L::kRowBytes * 8 == 4608 && L::kRawRowBytes == 288, "row layout");
   if (it0 >= it1) return;
   const int lane = d & 31, wi = d >> 5;
-  const int row = 16 * wi + 4 * (lane >> 3) + (lane & 3), h = (lane >> 2) & 1, wq = wi >> 1;
-  const uint64_t pol = l2_policy_evict_first();
-  const uint32_t unit = smem_u32(units_gen) + wq * L::kUnitBytes;
-  const uint32_t ubar = smem_u32(&ms->unit_full[wq]);
+  const int row = 16 * wi + 4 * (lane >> 3) + (lane & 3), h = (lane >> 2) & 1;
   bool failed = false;                                 // a bounded wait of this thread gave up
   TileCursor c;                                        // this tile
   TileAhead a0, a1, a2;                                // it, the next, the one after
@@ -901,13 +846,18 @@ __device__ void run_dequant_mx(const Stage1Params& p, Misc* ms, uint8_t* ring_ge
   a1.advance(p.items, it1);
   a2 = a1;
   a2.advance(p.items, it1);
-  // the first tile's rows: page entries, packed-row copies, scale bytes
-  {
-    const int32_t pg0 = scale_page(p, a0, row);
-    copy_rows(p, a0, wi, lane, pg0, unit, ubar, pol);
-  }
+  // the first tile's packed blocks and scale bytes
+  uint4 x[9];
   uint32_t ec[9], en[9];                               // scale bytes: this tile, the next
-  scale_load(p, a0, row, h, scale_page(p, a0, row), ec);
+  {
+    const int64_t r0 = pool_row(p, a0, row, scale_page(p, a0, row));
+    if (r0 >= 0) {
+      const uint8_t* src = p.kv + r0 * L::kRawRowBytes + 16 * h;
+#pragma unroll
+      for (int j = 0; j < 9; ++j) x[j] = ld_nc_na_v4(src + 32 * j);
+    }
+    scale_load(p, r0, h, ec);
+  }
   int32_t pg1 = scale_page(p, a1, row);                // raw page entry of this row, next tile
   if (d < 15) {
     uint32_t lo, hi;
@@ -940,36 +890,27 @@ __device__ void run_dequant_mx(const Stage1Params& p, Misc* ms, uint8_t* ring_ge
       emin = min(emin, static_cast<int>(ec[j]));
     }
     r = max(r, __shfl_xor_sync(0xffffffffu, r, 4));
-    scale_load(p, a1, row, h, pg1, en);
+    // the next tile's row: its scale bytes now, its packed blocks while this
+    // tile's are converted
+    const int64_t rn = pool_row(p, a1, row, pg1);
+    scale_load(p, rn, h, en);
+    const uint8_t* next = rn >= 0 ? p.kv + rn * L::kRawRowBytes + 16 * h : nullptr;
+    pg1 = scale_page(p, a2, row);
     const bool live = row < nvalid;
     const bool fast = emin - r >= -5;                  // all nine blocks on the computed path
-    bool ok = !failed && mbar_wait(ubar, tt & 1u, p.err, kErrDequant);
-    // this thread's nine packed blocks into registers, then the next tile's
-    // copy of the same rows into the unit (after this warp's reads)
-    uint4 x[9];
-    if (ok && live) {
-      const uint4* src = reinterpret_cast<const uint4*>(units_gen + wq * L::kUnitBytes +
-                                                        (row & 31) * L::kRawRowBytes) + h;
-#pragma unroll
-      for (int j = 0; j < 9; ++j) x[j] = src[2 * j];
-    }
-    fence_proxy_async_smem();                          // the reads before the async-proxy writes
-    __syncwarp();
-    if (__all_sync(0xffffffffu, ok)) copy_rows(p, a1, wi, lane, pg1, unit, ubar, pol);
-    pg1 = scale_page(p, a2, row);
     // the slot is overwritten whole: PV of its previous tile must be done
-    ok = ok && mbar_wait(smem_u32(&ms->empty[s]), ((tt / L::kNumTiles) & 1u) ^ 1u, p.err,
-                         kErrDequant);
+    const bool ok = !failed && mbar_wait(smem_u32(&ms->empty[s]),
+                                         ((tt / L::kNumTiles) & 1u) ^ 1u, p.err, kErrDequant);
     if (!ok) failed = true;
     uint8_t* dst = ring_gen + s * L::kTileBytes + row_off;
     // the token's factor for the softmax (read once S of the tile exists)
     if (h == 0 && ok) ms->uexp[s][row] = static_cast<int16_t>(live ? r - 127 : 0);
-    if (half_of_tile(ok, live, fast, x, ec, r, ms->e2m1_tab, dst, pc0, pc1, 0, 5)) {
+    if (half_of_tile(ok, live, fast, x, ec, r, ms->e2m1_tab, dst, pc0, pc1, 0, 5, next)) {
       fence_proxy_async_smem();
     }
     __syncwarp();
     if (ok && lane == 0) mbar_arrive(smem_u32(&ms->deq_a[s]));   // chunks 0-4
-    if (half_of_tile(ok, live, fast, x, ec, r, ms->e2m1_tab, dst, pc0, pc1, 5, 9)) {
+    if (half_of_tile(ok, live, fast, x, ec, r, ms->e2m1_tab, dst, pc0, pc1, 5, 9, next)) {
       fence_proxy_async_smem();
     }
     __syncwarp();
@@ -1415,8 +1356,6 @@ __global__ void __launch_bounds__(Layout<QM>::kThreads, 1) mla_stage1_kernel(con
         mbar_init(smem_u32(&ms->deq_a[i]), 8);       // one arrival per dequant warp
         mbar_init(smem_u32(&ms->deq_b[i]), 8);
       }
-      for (int i = 0; i < L::kUnits; ++i)
-        mbar_init(smem_u32(&ms->unit_full[i]), 2);   // the two dequant warps of its rows
     }
     mbar_init(smem_u32(&ms->q_stage), 1);
     mbar_init(smem_u32(&ms->q_stage_free), 1);
@@ -1447,7 +1386,7 @@ __global__ void __launch_bounds__(Layout<QM>::kThreads, 1) mla_stage1_kernel(con
     // One branch per warpgroup, each opening with its register limit (every
     // warp of the group executes the same setmaxnreg), so that the limit
     // governs the role code it dominates: 0 = UMMA issuers, 1-2 = softmax,
-    // 3-4 = dequantisation (with the landing copies).
+    // 3-4 = dequantisation (with the loads of the packed rows).
     const int wg = warp >> 2;
     if (wg == 0) {
       regs_lower<L::kRegsIssue>();
@@ -1466,7 +1405,7 @@ __global__ void __launch_bounds__(Layout<QM>::kThreads, 1) mla_stage1_kernel(con
       if constexpr (L::kRegsDequant < L::kRegsLaunch) regs_lower<L::kRegsDequant>();
       if constexpr (L::kRegsDequant > L::kRegsLaunch) regs_raise<L::kRegsDequant>();
       head_items(it0, it1, first);
-      run_dequant_mx<QM>(p, ms, smem, smem + L::kUnitOff, smem + L::kQOff, it0, it1, first,
+      run_dequant_mx<QM>(p, ms, smem, smem + L::kQOff, it0, it1, first,
                          threadIdx.x - 384);
     }
   } else {
