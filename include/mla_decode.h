@@ -345,8 +345,7 @@ mla_status mla_selftest_bounded_wait(const mla_plan* plan, void* workspace, size
  *   - Plans needing more than 16 MiB (mla_plan_workspace_size) are rejected
  *     with MLA_ERR_WORKSPACE before anything is enqueued.
  *   - The first call on a device looks the array's address up
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     (cudaGetSymbolAddress) with that device current.
  *   - Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
  *   - Every call copies its plan's work table into the array (one
  *     host-to-device copy on `stream`), which also clears the error word.
