@@ -93,8 +93,8 @@ typedef struct {
  *   page_size             tokens per page, >= 1.  With a page table, a
  *                         multiple of 8 lets one TMA box copy 8 rows of a
  *                         page; other sizes (bf16 / fp8 KV) copy every row
- *                         on its own.  MXFP4 rows are copied in runs of
- *                         rows contiguous in the pool, for any page size.
+ *                         on its own.  MXFP4 rows are loaded row by row
+ *                         by the dequantising threads, for any page size.
  *   q_dtype               MLA_DTYPE_BF16 or MLA_DTYPE_FP8_E4M3.
  *   kv_dtype              MLA_DTYPE_BF16, MLA_DTYPE_FP8_E4M3 or MLA_DTYPE_MXFP4.
  *   num_splits            0: the planner balances 128-token tiles over the

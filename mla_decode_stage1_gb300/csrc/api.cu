@@ -459,8 +459,8 @@ mla_status mla_decode_run(mla_plan* plan, const void* q, const float* q_scale, c
   // page size that is a multiple of 8: one box per 8-row group (a group never
   // straddles a page).  Other page sizes (bf16 / fp8 KV): every row is
   // gathered on its own (cp.async), laid out as for the identity table.
-  // MXFP4 rows are copied with plain bulk copies (no tensor map) and
-  // dequantised into the 8-row-group layout, for any page size.
+  // MXFP4 rows are loaded by the dequantising threads themselves (no tensor
+  // map) and written in the 8-row-group layout, for any page size.
   const bool mx = plan->kv_dtype == MLA_DTYPE_MXFP4;
   int box_rows = mla::kTile;
   int gather = 0;

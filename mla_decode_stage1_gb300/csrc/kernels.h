@@ -82,7 +82,7 @@ enum QMode : int {
 
 struct Stage1Params {
   CUtensorMap tmap_kv;          // KV pool as [chunk 64 B][row][64 B], 64-byte swizzle
-                                // (bf16 / fp8; MXFP4 rows are read with plain bulk copies)
+                                // (bf16 / fp8; MXFP4 rows are read with plain loads)
   const void* q;                // [bs,16,576]
   const float* q_scale;         // device [1] (fp8 q) or null
   const float* kv_scale;        // device [1] (fp8 kv) or null
@@ -99,7 +99,7 @@ struct Stage1Params {
   int32_t box_rows;             // rows per TMA box: 128 (identity table) or 8 (page table)
   int32_t gather;               // 1: page size not a multiple of 8 (bf16 / fp8 KV); rows are
                                 // gathered one by one with cp.async instead of TMA boxes
-  const uint8_t* kv;            // KV pool base (row gather, MXFP4 bulk copies)
+  const uint8_t* kv;            // KV pool base (row gather, MXFP4 row loads)
   uint32_t chunk_stride;        // smem bytes between 64-byte column chunks of a tile
   uint32_t group_stride;        // smem bytes between 8-row groups of a tile
   int64_t pool_rows;
