@@ -74,6 +74,9 @@ typedef struct {
   int32_t q_len;             /* query tokens per request */
   int32_t unit_tokens;       /* tokens between possible cut points (mla_plan_options) */
   int32_t item_cost;         /* cost of an extra request in a CTA (balanced plan) */
+  int32_t cluster_size;      /* 8: split requests are merged inside stage 1, in
+                                thread-block clusters of that many CTAs (mla_plan_options
+                                merge); 0: by stage 2 */
 } mla_plan_info;
 
 /*
@@ -156,12 +159,20 @@ mla_status mla_decode_plan_q(const int32_t* kv_indptr_host, const int32_t* kv_la
  *   unit_tokens  tokens between the planner's possible cut points: 128 (a
  *                whole tile; 0 means 128), 64 or 32.  Finer cuts spread small
  *                batches over more CTAs (each then loads only its rows).
+ *   merge        0: when every CTA holds one item and every request is split
+ *                over 8 consecutive CTAs (a small batch of equal lengths, one
+ *                query token, bf16 or fp8 KV), each request's CTAs run as one
+ *                thread-block cluster and merge its partials through
+ *                distributed shared memory: no partials in the workspace, no
+ *                stage-2 launch.  If the device cannot hold such a cluster,
+ *                run falls back to stage 2.  1: always merge with stage 2.
  */
 typedef struct {
   int32_t num_splits;
   int32_t num_sms;
   int32_t item_cost;
   int32_t unit_tokens;
+  int32_t merge;
 } mla_plan_options;
 
 /*
@@ -188,7 +199,8 @@ typedef struct {
  * mla_decode_autotune -- choose the plan of one batch shape by timing
  * candidate plans on the caller's inputs (the runtime autotune of the
  * earlier version of submission 600081: _time_fn / _aiter_best /
- * _best_for_shape).  The candidates are the default balanced plan, item
+ * _best_for_shape).  The candidates are the default balanced plan (and,
+ * when it merges inside clusters, the same plan merged by stage 2), item
  * costs 2 and 4, cut units of 64 and 32 tokens, the split count of the
  * pages' split tables for this (batch, length) if it has one, and one split
  * per request.  Every candidate runs once (uploading its table), then `reps`

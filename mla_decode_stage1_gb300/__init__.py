@@ -38,12 +38,14 @@ class PlanInfo(ctypes.Structure):
                 ("num_partials", ctypes.c_int32), ("num_merge_jobs", ctypes.c_int32),
                 ("total_tokens", ctypes.c_int64), ("total_tiles", ctypes.c_int64),
                 ("workspace_bytes", ctypes.c_size_t), ("q_len", ctypes.c_int32),
-                ("unit_tokens", ctypes.c_int32), ("item_cost", ctypes.c_int32)]
+                ("unit_tokens", ctypes.c_int32), ("item_cost", ctypes.c_int32),
+                ("cluster_size", ctypes.c_int32)]
 
 
 class PlanOptions(ctypes.Structure):
     _fields_ = [("num_splits", ctypes.c_int32), ("num_sms", ctypes.c_int32),
-                ("item_cost", ctypes.c_int32), ("unit_tokens", ctypes.c_int32)]
+                ("item_cost", ctypes.c_int32), ("unit_tokens", ctypes.c_int32),
+                ("merge", ctypes.c_int32)]
 
 
 class TuneResult(ctypes.Structure):
@@ -161,18 +163,20 @@ class Plan:
 def mla_decode_plan(kv_indptr, kv_last_page_len=None, *, page_size: int, q_dtype: str,
                     kv_dtype: str, num_splits: int = 0, num_sms: int = 0,
                     batch_size: int | None = None, q_len: int = 1, item_cost: int = 0,
-                    unit_tokens: int = 0) -> Plan:
+                    unit_tokens: int = 0, merge: int = 0) -> Plan:
     """Plan a batch from the HOST kv_indptr (in pages) and optional last-page
     lengths.  num_sms=0 queries the current CUDA device.  q_len > 1 plans
     q_len query tokens per request (mla_decode_plan_q): q, out and lse then
-    hold [bs, q_len, 16, ...] rows.  item_cost / unit_tokens other than 0
-    select the plan options of mla_decode_plan_ex."""
+    hold [bs, q_len, 16, ...] rows.  item_cost / unit_tokens / merge other
+    than 0 select the plan options of mla_decode_plan_ex (merge=1: always
+    merge split requests with stage 2, never inside a cluster)."""
     ind, ind_p = _i32_array(kv_indptr)
     last, last_p = _i32_array(kv_last_page_len)
     bs = len(ind) - 1 if batch_size is None else int(batch_size)
     h = ctypes.c_void_p()
-    if item_cost or unit_tokens:
-        opts = PlanOptions(int(num_splits), int(num_sms), int(item_cost), int(unit_tokens))
+    if item_cost or unit_tokens or merge:
+        opts = PlanOptions(int(num_splits), int(num_sms), int(item_cost), int(unit_tokens),
+                           int(merge))
         _check("mla_decode_plan_ex", _lib.mla_decode_plan_ex(
             ind_p, last_p, bs, int(q_len), int(page_size), DTYPES[q_dtype], DTYPES[kv_dtype],
             ctypes.byref(opts), ctypes.byref(h)))
@@ -275,7 +279,8 @@ def mla_decode_autotune(kv_indptr, kv_last_page_len, q, kv, out, *, page_size: i
     plan = Plan(h, q_dtype, kv_dtype, int(page_size))
     plan.q_len = int(q_len)
     table = [({"num_splits": r.options.num_splits, "num_sms": r.options.num_sms,
-               "item_cost": r.options.item_cost, "unit_tokens": r.options.unit_tokens}, r.ms)
+               "item_cost": r.options.item_cost, "unit_tokens": r.options.unit_tokens,
+               "merge": r.options.merge}, r.ms)
              for r in results[: nres.value]]
     return plan, table
 

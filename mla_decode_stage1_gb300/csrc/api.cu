@@ -261,17 +261,43 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 extern "C" {
 
+// Split requests can be merged inside stage 1 when the CTAs of every
+// request form one thread-block cluster: every CTA holds one item, request
+// b's items are CTAs 8k .. 8k + 7 of one cluster k, and every request is
+// split so (stage 2 also zero-fills empty requests, so a batch with one
+// keeps it).  One query token per request, bf16 or fp8 KV.  Only eight-way
+// splits use it: with 2 or 4 partials per request the narrow stage-2 merge
+// (one round trip) was faster than the cluster launch and its barriers
+// (0.2-0.6 us per call on GB300), with 8 the cluster merge saved 0.7-2.2 us.
+constexpr int32_t kClusterMerge = 8;
+static int32_t cluster_size_of(const mla_plan* P) {
+  if (P->q_len != 1 || P->qmode == mla::kQBf16KvMx || P->qmode == mla::kQFp8KvFp8x2 ||
+      P->num_ctas < 2 || static_cast<int32_t>(P->items.size()) != P->num_ctas || P->jobs.empty())
+    return 0;
+  for (int32_t c = 0; c < P->num_ctas; ++c)
+    if (P->cta_indptr[c + 1] - P->cta_indptr[c] != 1) return 0;
+  const int32_t cs = P->jobs[0].count;
+  if (cs != kClusterMerge ||
+      static_cast<int64_t>(P->jobs.size()) * cs != P->num_ctas)
+    return 0;
+  for (const MergeJob& j : P->jobs)
+    if (j.count != cs) return 0;
+  for (int32_t c = 0; c < P->num_ctas; ++c)
+    if (P->items[c].b != P->items[(c / cs) * cs].b || P->items[c].slot < 0) return 0;
+  return cs;
+}
+
 mla_status mla_decode_plan_ex(const int32_t* kv_indptr_host, const int32_t* kv_last_page_len_host,
                               int32_t batch_size, int32_t q_len, int32_t page_size,
                               mla_dtype q_dtype, mla_dtype kv_dtype,
                               const mla_plan_options* options, mla_plan** plan_out) {
   if (plan_out == nullptr) return MLA_ERR_INVALID_ARG;
   *plan_out = nullptr;
-  const mla_plan_options o = options != nullptr ? *options : mla_plan_options{0, 0, 0, 0};
+  const mla_plan_options o = options != nullptr ? *options : mla_plan_options{0, 0, 0, 0, 0};
   int32_t num_splits = o.num_splits, num_sms = o.num_sms;
   const int64_t item_cost = o.item_cost == 0 ? 1 : o.item_cost;
   const int32_t unit = o.unit_tokens == 0 ? mla::kTile : o.unit_tokens;
-  if (o.item_cost < 0 || o.item_cost > 64 ||
+  if (o.item_cost < 0 || o.item_cost > 64 || o.merge < 0 || o.merge > 1 ||
       (unit != 32 && unit != 64 && unit != mla::kTile))
     return MLA_ERR_INVALID_ARG;
   if (kv_indptr_host == nullptr || batch_size < 1 || page_size < 1 || num_splits < 0 ||
@@ -374,6 +400,7 @@ mla_status mla_decode_plan_ex(const int32_t* kv_indptr_host, const int32_t* kv_l
   for (WorkItem& w : P->items) w.vis0 = vis0[w.b];
   assign_slots(P, len);
   layout_workspace(P);
+  P->cluster = o.merge == 0 ? cluster_size_of(P) : 0;
   *plan_out = P;
   return MLA_OK;
 }
@@ -382,7 +409,7 @@ mla_status mla_decode_plan_q(const int32_t* kv_indptr_host, const int32_t* kv_la
                              int32_t batch_size, int32_t q_len, int32_t page_size,
                              mla_dtype q_dtype, mla_dtype kv_dtype, int32_t num_splits,
                              int32_t num_sms, mla_plan** plan_out) {
-  const mla_plan_options o{num_splits, num_sms, 0, 0};
+  const mla_plan_options o{num_splits, num_sms, 0, 0, 0};
   return mla_decode_plan_ex(kv_indptr_host, kv_last_page_len_host, batch_size, q_len, page_size,
                             q_dtype, kv_dtype, &o, plan_out);
 }
@@ -413,6 +440,7 @@ mla_status mla_plan_get_info(const mla_plan* plan, mla_plan_info* info) {
   info->total_tokens = plan->total_tokens;
   info->total_tiles = plan->total_tiles;
   info->workspace_bytes = plan->ws_bytes;
+  info->cluster_size = plan->cluster;
   info->unit_tokens = plan->unit_tokens;
   info->item_cost = plan->item_cost;
   return MLA_OK;
@@ -494,6 +522,18 @@ mla_status mla_decode_run(mla_plan* plan, const void* q, const float* q_scale, c
   float* part_o = reinterpret_cast<float*>(ws + plan->off_part_o);
   float* part_lse = reinterpret_cast<float*>(ws + plan->off_part_lse);
   int32_t* err = reinterpret_cast<int32_t*>(ws + plan->off_err);
+  // cluster merge when the plan allows it and this device can hold such a
+  // cluster (checked once per plan and device); otherwise stage 2 merges
+  bool cluster = false;
+  if (plan->cluster > 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
+    if (plan->cluster_dev != dev) {
+      plan->cluster_fits = mla::stage1_cluster_fits(plan->qmode, plan->cluster);
+      plan->cluster_dev = dev;
+    }
+    cluster = plan->cluster_fits;
+  }
   if (plan->num_ctas > 0) {
     mla::Stage1Params p{};
     p.tmap_kv = plan->tmap;
@@ -518,6 +558,7 @@ mla_status mla_decode_run(mla_plan* plan, const void* q, const float* q_scale, c
     p.pool_rows = kv_pool_rows;
     p.kv_e8m0 = kv_e8m0;
     p.sc_stride = kv_e8m0_row_stride;
+    p.cluster = cluster ? plan->cluster : 0;
     if (plan->ev_before != nullptr && cudaEventRecord(plan->ev_before, stream) != cudaSuccess)
       return MLA_ERR_CUDA;
     if (mla::launch_stage1(plan->qmode, p, plan->num_ctas, stream) != cudaSuccess)
@@ -525,7 +566,7 @@ mla_status mla_decode_run(mla_plan* plan, const void* q, const float* q_scale, c
     if (plan->ev_after != nullptr && cudaEventRecord(plan->ev_after, stream) != cudaSuccess)
       return MLA_ERR_CUDA;
   }
-  if (!plan->jobs.empty()) {
+  if (!plan->jobs.empty() && !cluster) {
     mla::Stage2Params s{};
     s.jobs = reinterpret_cast<const MergeJob*>(ws + plan->off_jobs);
     s.err = err;

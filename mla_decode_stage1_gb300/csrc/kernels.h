@@ -99,6 +99,9 @@ struct Stage1Params {
   int32_t box_rows;             // rows per TMA box: 128 (identity table) or 8 (page table)
   int32_t gather;               // 1: page size not a multiple of 8 (bf16 / fp8 KV); rows are
                                 // gathered one by one with cp.async instead of TMA boxes
+  int32_t cluster;              // 0: split items write partials for stage 2; cs (a divisor of
+                                // 512, at most 8): the grid is in clusters of cs CTAs, one
+                                // request each, whose partials are merged inside the cluster
   const uint8_t* kv;            // KV pool base (row gather, MXFP4 row loads)
   uint32_t chunk_stride;        // smem bytes between 64-byte column chunks of a tile
   uint32_t group_stride;        // smem bytes between 8-row groups of a tile
@@ -124,5 +127,8 @@ struct Stage2Params {
 cudaError_t launch_stage1(int qmode, const Stage1Params& p, int num_ctas, cudaStream_t stream);
 cudaError_t launch_stage2(const Stage2Params& p, cudaStream_t stream);
 int stage1_smem_bytes(int qmode);
+// Whether stage 1 of `qmode` can run in clusters of `cs` CTAs on the current
+// device (at least one such cluster fits).
+bool stage1_cluster_fits(int qmode, int cs);
 
 }  // namespace mla

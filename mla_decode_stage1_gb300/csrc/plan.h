@@ -22,6 +22,7 @@ struct mla_plan {
   int32_t unit_tokens = mla::kTile;   // tokens between the planner's possible cut points
   int32_t item_cost = 1;              // cost of an extra item in a CTA (balanced plan)
   int32_t num_sms = 0;                // CTAs the balanced plan was cut for
+  int32_t cluster = 0;                // CTAs per cluster merging a request inside stage 1 (0: stage 2)
   int64_t total_tokens = 0, total_tiles = 0;
   int64_t identity_rows = 0;   // pool rows the requests reach without a page table
   std::vector<int32_t> cta_indptr;
@@ -40,6 +41,8 @@ struct mla_plan {
   int64_t tmap_rows = -1;
   int32_t tmap_box_rows = -1;
   cudaEvent_t ev_before = nullptr, ev_after = nullptr;
+  mutable int cluster_dev = -1;       // device whose cluster fit was checked (cluster_fits)
+  mutable bool cluster_fits = false;
 };
 
 namespace mla {

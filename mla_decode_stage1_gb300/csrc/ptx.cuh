@@ -143,6 +143,47 @@ __device__ __forceinline__ bool named_bar_any(uint32_t id, uint32_t nthreads, bo
   return r != 0;
 }
 
+// ------------------------------------------------------------------ clusters
+// Rank of this CTA in its thread-block cluster.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster arrives, then waits for all the
+// others: shared-memory writes before it are visible to the whole cluster
+// after it.  Each thread of the cluster must execute it the same number of
+// times.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// The same without release / acquire ordering: only that every thread of the
+// cluster got here (for instance, that all reads of this CTA's shared memory
+// by the others have returned, their values being used before).
+__device__ __forceinline__ void cluster_sync_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed;\n\tbarrier.cluster.wait;" ::: "memory");
+}
+// The address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t dsmem_addr(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+// (No memory clobber: these loads are ordered against the writes they read
+// by the cluster barrier between them, which has one.)
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ float4 ld_dsmem_v4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr));
+  return v;
+}
+
 // ----------------------------------------------------------------------- TMA
 // 2-D tiled bulk tensor load into shared memory, completion counted in bytes
 // on `bar`.  x is the element index along the contiguous dimension, y the row.

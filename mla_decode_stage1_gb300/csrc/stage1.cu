@@ -1242,13 +1242,22 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
       for (int h = 0; h < kH; ++h) inv[h] = lt[h] > 0.0f ? inv[h] : 0.0f;
     }
     const int slot = w.slot;
+    // cluster merge: the CTA's partial stays in its own shared memory (its
+    // tile ring, idle once the item's last PV is done) as [row][512] fp32
+    // plus the rows' log2 LSE; the cluster's CTAs read it after a barrier.
+    // (Another CTA's ring may still be in use: nothing is written there.)
+    const bool to_cluster = p.cluster > 0 && slot >= 0;
+    float* xo = reinterpret_cast<float*>(ring_gen);
     // rows of this group's q rows in the partial slot or in out (request b's
     // rows are b * kRows .. : [query token][head])
     const int64_t row0 = (slot >= 0 ? static_cast<int64_t>(slot) : static_cast<int64_t>(w.b)) *
                              L::kRows + h0;
     auto store_block = [&](int c, float (&o)[kH]) {
       const int d = c * 128 + tq;
-      if (slot >= 0) {
+      if (to_cluster) {
+#pragma unroll
+        for (int h = 0; h < kH; ++h) xo[(h0 + h) * kVDim + d] = o[h];
+      } else if (slot >= 0) {
         float* po = p.part_o + row0 * kVDim + d;
 #pragma unroll
         for (int h = 0; h < kH; ++h) po[h * kVDim] = o[h];
@@ -1300,11 +1309,72 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
         if (h == tq) { mh = m[h]; lh = lt[h]; }
       float lse2 = mh + __log2f(lh) - kPOff;
       if constexpr (L::kQL > 1) lse2 = lh > 0.0f ? lse2 : -INFINITY;
-      if (slot >= 0)
+      if (to_cluster)
+        xo[L::kRows * kVDim + h0 + tq] = lse2;
+      else if (slot >= 0)
         p.part_lse[row0 + tq] = lse2;
       else if (p.lse != nullptr)
         p.lse[row0 + tq] = lse2 * kLn2;
     }
+  }
+}
+
+// ------------------------------------------------------------ cluster merge
+// The CTAs of a cluster hold the cs partials of one request (request b) in
+// their shared memory: [16 rows][512] fp32 and the rows' log2 LSE after it
+// (the epilogue above).  CTA `rank` merges dims [rank 512/cs, (rank+1) 512/cs)
+// of every row, reading all cs partials through distributed shared memory:
+// M = max_s lse_s, w_s = 2^(lse_s - M), o = sum_s w_s o_s / sum_s w_s, as the
+// stage-2 merge does (the merge of the split-KV kernels of submission 668813,
+// _mla_mxfp4_stage2_log2).  Rank 0 writes the rows' natural-log LSE.
+template <int QM>
+__device__ void cluster_merge(const Stage1Params& p, const uint8_t* smem, int b) {
+  using L = Layout<QM>;
+  static_assert(L::kRows == kHeads, "cluster merge: one query token per request");
+  const int cs = p.cluster;
+  const uint32_t rank = cluster_ctarank();
+  const int span = kVDim / cs, vec = span / 4;                 // dims / float4s of this CTA
+  const uint32_t xo = smem_u32(smem), xl = xo + kHeads * kVDim * 4;
+  for (int v = threadIdx.x; v < kHeads * vec; v += L::kThreads) {
+    const int h = v / vec, d = static_cast<int>(rank) * span + 4 * (v % vec);
+    // every load of the cs partials is issued before the first use
+    float ls[8];
+    float4 o[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j < cs) {
+        ls[j] = ld_dsmem_f32(dsmem_addr(xl + 4u * h, j));
+        o[j] = ld_dsmem_v4(dsmem_addr(xo + 4u * (h * kVDim + d), j));
+      } else {
+        ls[j] = -INFINITY;
+        o[j] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      }
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) M = fmaxf(M, ls[j]);
+    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    float W = 0.0f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float w = ex2(ls[j] - M);          // 0 for an empty or absent partial
+        W += w;
+        acc.x += w > 0.0f ? w * o[j].x : 0.0f;
+        acc.y += w > 0.0f ? w * o[j].y : 0.0f;
+        acc.z += w > 0.0f ? w * o[j].z : 0.0f;
+        acc.w += w > 0.0f ? w * o[j].w : 0.0f;
+      }
+    }
+    const float inv = W > 0.0f ? 1.0f / W : 0.0f;
+    const __nv_bfloat162 x = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+    const __nv_bfloat162 y = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+    uint2 o2;
+    o2.x = *reinterpret_cast<const uint32_t*>(&x);
+    o2.y = *reinterpret_cast<const uint32_t*>(&y);
+    *reinterpret_cast<uint2*>(p.out + (static_cast<int64_t>(b) * kHeads + h) * kVDim + d) = o2;
+    if (d == 0 && p.lse != nullptr)
+      p.lse[static_cast<int64_t>(b) * kHeads + h] = W > 0.0f ? (M + __log2f(W)) * kLn2 : -INFINITY;
   }
 }
 
@@ -1425,6 +1495,20 @@ __global__ void __launch_bounds__(Layout<QM>::kThreads, 1) mla_stage1_kernel(con
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (!L::kMx && L::kRows == kHeads) {
+    // cluster merge: every thread of every CTA of the cluster reaches both
+    // barriers (each role's loop ends, its waits being bounded).  The first
+    // publishes the partials; the second keeps each CTA's partial alive until
+    // the others have read it (their loads have returned: the merge used the
+    // values), and needs no release ordering of the merge's global stores
+    if (p.cluster > 0) {
+      cluster_sync();
+      // (the CTA head is read again here, so that nothing stays live
+      // across the roles for the merge)
+      if (!ms->stale && head.it0 < head.it1) cluster_merge<QM>(p, smem, head.first.b);
+      cluster_sync_relaxed();
+    }
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, L::kTmemCols);
@@ -1457,8 +1541,60 @@ static cudaError_t launch_t(const Stage1Params& p, int num_ctas, cudaStream_t st
   cudaError_t e = cudaFuncSetAttribute(mla_stage1_kernel<QM>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
+  if (p.cluster > 0) {
+    if (L::kMx || L::kRows != kHeads || num_ctas % p.cluster != 0) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_ctas);
+    cfg.blockDim = dim3(L::kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(p.cluster);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, mla_stage1_kernel<QM>, p);
+  }
   mla_stage1_kernel<QM><<<num_ctas, Layout<QM>::kThreads, smem, stream>>>(p);
   return cudaGetLastError();
+}
+
+template <int QM>
+static bool cluster_fits_t(int cs) {
+  using L = Layout<QM>;
+  if (L::kMx || L::kRows != kHeads) return false;
+  if (cudaFuncSetAttribute(mla_stage1_kernel<QM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           L::kSmemBytes) != cudaSuccess)
+    return false;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cs);
+  cfg.blockDim = dim3(L::kThreads);
+  cfg.dynamicSmemBytes = L::kSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, mla_stage1_kernel<QM>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return n > 0;
+}
+
+bool stage1_cluster_fits(int qmode, int cs) {
+  switch (qmode) {
+    case kQBf16KvBf16: return cluster_fits_t<kQBf16KvBf16>(cs);
+    case kQFp8KvFp8: return cluster_fits_t<kQFp8KvFp8>(cs);
+    case kQBf16KvFp8: return cluster_fits_t<kQBf16KvFp8>(cs);
+    case kQFp8KvBf16: return cluster_fits_t<kQFp8KvBf16>(cs);
+  }
+  return false;
 }
 
 cudaError_t launch_stage1(int qmode, const Stage1Params& p, int num_ctas, cudaStream_t stream) {

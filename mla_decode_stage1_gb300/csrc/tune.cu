@@ -44,10 +44,10 @@ int32_t table_splits(int32_t bs, int64_t kv_len, bool mxfp4) {
 // heavier item costs, finer cut points, and fixed splits.
 std::vector<mla_plan_options> candidates(int32_t bs, int64_t max_len, bool mxfp4) {
   std::vector<mla_plan_options> c = {
-      {0, 0, 1, 128}, {0, 0, 2, 128}, {0, 0, 4, 128}, {0, 0, 1, 64}, {0, 0, 1, 32}};
+      {0, 0, 1, 128, 0}, {0, 0, 2, 128, 0}, {0, 0, 4, 128, 0}, {0, 0, 1, 64, 0}, {0, 0, 1, 32, 0}};
   const int32_t s = table_splits(bs, max_len, mxfp4);
-  if (s > 0) c.push_back({s, 0, 0, 0});
-  c.push_back({1, 0, 0, 0});
+  if (s > 0) c.push_back({s, 0, 0, 0, 0});
+  c.push_back({1, 0, 0, 0, 0});
   return c;
 }
 
@@ -112,8 +112,9 @@ mla_status mla_decode_autotune(const int32_t* kv_indptr_host,
     max_len = std::max(max_len, n);
   }
   const bool mx = kv_dtype == MLA_DTYPE_MXFP4;
-  const std::vector<mla_plan_options> cand = candidates(batch_size, max_len, mx);
-  // plans and the workspace the largest needs
+  std::vector<mla_plan_options> cand = candidates(batch_size, max_len, mx);
+  // plans and the workspace the largest needs; when the default plan merges
+  // inside clusters, its stage-2 form is a candidate too
   std::vector<mla_plan*> plans(cand.size(), nullptr);
   size_t need = 0;
   for (size_t i = 0; i < cand.size(); ++i) {
@@ -125,6 +126,12 @@ mla_status mla_decode_autotune(const int32_t* kv_indptr_host,
       return st;
     }
     need = std::max(need, plans[i]->ws_bytes);
+    if (i == 0 && plans[0]->cluster > 0) {
+      mla_plan_options o = cand[0];
+      o.merge = 1;
+      cand.insert(cand.begin() + 1, o);
+      plans.insert(plans.begin() + 1, nullptr);
+    }
   }
   if (workspace_needed != nullptr) *workspace_needed = need;
   auto release = [&](int32_t keep) {
@@ -153,7 +160,8 @@ mla_status mla_decode_autotune(const int32_t* kv_indptr_host,
       for (size_t i = 0; i < cand.size(); ++i) {
         const mla_plan_options& o = cand[i];
         if (o.num_splits == it->second.num_splits && o.num_sms == it->second.num_sms &&
-            o.item_cost == it->second.item_cost && o.unit_tokens == it->second.unit_tokens) {
+            o.item_cost == it->second.item_cost && o.unit_tokens == it->second.unit_tokens &&
+            o.merge == it->second.merge) {
           release(static_cast<int32_t>(i));
           *plan_out = plans[i];
           return MLA_OK;

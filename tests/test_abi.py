@@ -465,3 +465,71 @@ def test_autotune_workspace_query_without_a_gpu(mla):
     assert st in (0, 4)
     if st == 0:
         assert need.value > 0 and nres.value == 0
+
+
+def expected_cluster(cta_indptr, items, bs):
+    """The rule, restated: every CTA holds one item and every request is split
+    over 8 consecutive CTAs (one cluster per request)."""
+    if len(cta_indptr) < 3 or not np.all(np.diff(cta_indptr) == 1):
+        return 0
+    b = items[:, 0]
+    per_req = np.bincount(b, minlength=bs)
+    cs = int(per_req[0])
+    if cs != 8 or np.any(per_req != cs) or np.any(items[:, 3] < 0):
+        return 0
+    for k in range(len(b) // cs):
+        if len(set(b[k * cs:(k + 1) * cs].tolist())) != 1:
+            return 0
+    return cs
+
+
+@pytest.mark.parametrize("bs,kv,sms,qd,kd,want", [
+    (4, 1024, 152, "bf16", "bf16", 8),     # 32 one-tile CTAs, 8 per request
+    (32, 1024, 152, "bf16", "fp8", 0),     # 4 CTAs of 2 tiles per request: stage 2 is faster
+    (8, 512, 152, "fp8", "fp8", 0),        # 4 one-tile CTAs per request
+    (16, 1024, 152, "fp8", "fp8", 8),      # 128 one-tile CTAs, 8 per request
+    (64, 8192, 152, "bf16", "fp8", 0),     # CTAs straddle requests: stage 2
+    (1, 2048, 8, "bf16", "fp8", 8),        # 8 CTAs of 2 tiles
+    (3, 1000, 152, "bf16", "fp8", 8),      # 24 CTAs, the last tile of each request ragged
+    (5, 300, 152, "bf16", "fp8", 0),       # 3 tiles per request: no cluster size fits
+])
+def test_cluster_merge_plans(mla, bs, kv, sms, qd, kd, want):
+    indptr = np.arange(bs + 1, dtype=np.int32) * kv
+    pl = plan(mla, indptr, qd=qd, kd=kd, sms=sms)
+    info = pl.info()
+    cta_indptr, items = pl.work()
+    assert expected_cluster(cta_indptr, items, bs) == want
+    assert info.cluster_size == want
+    # the stage-2 form of the same plan on request (merge=1)
+    pl2 = mla.mla_decode_plan(indptr, None, page_size=1, q_dtype=qd, kv_dtype=kd, num_sms=sms,
+                              merge=1)
+    assert pl2.info().cluster_size == 0
+    assert np.array_equal(pl2.work()[1], items)
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_cluster_merge_rule_on_random_batches(mla, seed):
+    rng = np.random.default_rng(seed)
+    bs = int(rng.integers(1, 20))
+    equal = rng.random() < 0.6
+    lens = np.full(bs, int(rng.integers(1, 2048))) if equal else rng.integers(0, 2048, bs)
+    indptr = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    sms = int(rng.choice([4, 16, 64, 152]))
+    pl = plan(mla, indptr, sms=sms)
+    cta_indptr, items = pl.work()
+    assert pl.info().cluster_size == expected_cluster(cta_indptr, items, bs)
+
+
+def test_no_cluster_merge_for_mxfp4_or_several_tokens(mla):
+    eq = np.arange(5, dtype=np.int32) * 1024
+    assert plan(mla, eq, sms=152).info().cluster_size == 8
+    assert plan(mla, eq, kd="mxfp4", sms=152).info().cluster_size == 0
+    pq = mla.mla_decode_plan(eq, None, page_size=1, q_dtype="fp8", kv_dtype="fp8", num_sms=152,
+                             q_len=2)
+    assert pq.info().cluster_size == 0
+    pq = mla.mla_decode_plan(eq, None, page_size=1, q_dtype="bf16", kv_dtype="fp8", num_sms=152,
+                             q_len=3)
+    assert pq.info().cluster_size == 0
+    # an empty request keeps stage 2 (it zero-fills that request)
+    with_empty = np.array([0, 1024, 1024, 2048, 3072, 4096], np.int32)
+    assert plan(mla, with_empty, sms=152).info().cluster_size == 0

@@ -243,6 +243,53 @@ def test_mxfp4_benchmark_config_sampled():
     check(w, select=sel)
 
 
+@pytest.mark.parametrize("q_dtype,kv_dtype", COMBOS)
+@pytest.mark.parametrize("bs,length,page_size,permute,cs", [
+    (4, 1024, 1, False, 8),     # C1's shape: 8 one-tile CTAs per request
+    (16, 1024, 8, True, 8),     # paged, permuted: 128 CTAs in 16 clusters
+    (3, 1000, 16, True, 8),     # ragged last tile in every request, partial last pages
+    (1, 1024, 7, True, 8),      # page size 7: gathered rows (bf16 / fp8 KV)
+])
+def test_cluster_merge_against_stage2_and_oracle(q_dtype, kv_dtype, bs, length, page_size,
+                                                 permute, cs):
+    # split requests merged inside stage 1 through a thread-block cluster
+    # (distributed shared memory) against the oracle, and against the same
+    # plan merged by stage 2
+    import workloads as synth
+    w = synth.make_workload(bs=bs, lengths=[length] * bs, page_size=page_size, q_dtype=q_dtype,
+                            kv_dtype=kv_dtype, permute_pages=permute, seed=61)
+    plan = check(w, num_sms=152)
+    assert plan.info().cluster_size == cs
+    o1, l1, _ = run_gpu(w, num_sms=152)
+    o2, l2, plan2 = run_gpu(w, num_sms=152, merge=1)
+    assert plan2.info().cluster_size == 0
+    assert np.allclose(o1, o2, atol=1e-2, rtol=1e-2) and np.allclose(l1, l2, atol=1e-4, rtol=1e-5)
+
+
+def test_cluster_merge_repeated_and_bitwise_stable():
+    # the cluster path keeps no state between calls: repeated calls give the
+    # same bytes
+    mla = _mla()
+    import workloads as synth
+    w = synth.make_workload(bs=4, lengths=[1024] * 4, page_size=1, q_dtype="bf16",
+                            kv_dtype="fp8", seed=62)
+    plan = mla.mla_decode_plan(w.kv_indptr, None, page_size=1, q_dtype="bf16", kv_dtype="fp8")
+    if plan.info().cluster_size == 0:
+        pytest.skip("this device's SM count gives no cluster plan for the shape")
+    d = w.to("cuda")
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(5):
+        out = torch.full((4, 16, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+        lse = torch.full((4, 16), float("nan"), dtype=torch.float32, device="cuda")
+        mla.mla_decode_run(plan, d.q, d.kv, out, workspace=ws, q_scale=d.q_scale,
+                           kv_scale=d.kv_scale, lse=lse)
+        outs.append((out, lse))
+    mla.mla_decode_check(plan, ws)
+    for out, lse in outs[1:]:
+        assert torch.equal(out, outs[0][0]) and torch.equal(lse, outs[0][1])
+
+
 def test_split_merge_repeated_launches_same_workspace():
     # the plan's table is uploaded on the first launch into a workspace only;
     # later launches reuse it and must give identical results
@@ -458,6 +505,45 @@ def test_bounded_wait_times_out_and_context_survives():
     o_ref, l_ref = oracle.mla_decode(**synth.oracle_args(w))
     compare(out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64),
             o_ref, l_ref, "fp8", w.lengths)
+
+
+def test_workspace_reused_by_another_plan_is_detected_in_cluster_mode():
+    # as below, with plan A merging inside clusters: the CTAs that find B's
+    # stamp still meet at the cluster barriers, write nothing, and the error
+    # is reported
+    mla = _mla()
+    import workloads as synth
+    wa = synth.make_workload(bs=4, lengths=[1024] * 4, page_size=1, q_dtype="fp8",
+                             kv_dtype="fp8", seed=63)
+    wb = synth.make_workload(bs=3, lengths=[50, 5000, 0], page_size=8, q_dtype="fp8",
+                             kv_dtype="fp8", permute_pages=True, seed=57)
+    pa = mla.mla_decode_plan(wa.kv_indptr, None, page_size=1, q_dtype="fp8", kv_dtype="fp8",
+                             num_sms=152)
+    pb = mla.mla_decode_plan(wb.kv_indptr, wb.kv_last_page_len, page_size=8, q_dtype="fp8",
+                             kv_dtype="fp8", num_splits=3)
+    assert pa.info().cluster_size == 8
+    da, db = wa.to("cuda"), wb.to("cuda")
+    ws = torch.empty(max(pa.workspace_bytes, pb.workspace_bytes), dtype=torch.uint8, device="cuda")
+
+    def run(plan, w, d):
+        out = torch.full((w.bs, 16, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+        lse = torch.full((w.bs, 16), float("nan"), dtype=torch.float32, device="cuda")
+        mla.mla_decode_run(plan, d.q, d.kv, out, workspace=ws, q_scale=d.q_scale,
+                           kv_scale=d.kv_scale, kv_indices=d.kv_indices, lse=lse)
+        return out, lse
+
+    out0, lse0 = run(pa, wa, da)
+    mla.mla_decode_check(pa, ws)
+    run(pb, wb, db)
+    mla.mla_decode_check(pb, ws)
+    out1, lse1 = run(pa, wa, da)
+    with pytest.raises(mla.MlaError) as e:
+        mla.mla_decode_check(pa, ws)
+    assert e.value.status == 3
+    assert torch.isnan(out1.float()).all() and torch.isnan(lse1).all()
+    out2, lse2 = run(pa, wa, da)
+    mla.mla_decode_check(pa, ws)
+    assert torch.equal(out2, out0) and torch.equal(lse2, lse0)
 
 
 def test_workspace_reused_by_another_plan_is_detected():
