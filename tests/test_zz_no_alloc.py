@@ -130,3 +130,20 @@ def test_noalloc_rejects_plans_over_the_limit():
     with pytest.raises(mla.MlaError) as e:
         mla.mla_decode_run_noalloc(plan, q, kv, out, q_scale=s, kv_scale=s)
     assert e.value.status == 3
+
+
+def test_noalloc_cluster_merge_plan_matches_regular_entry_point():
+    # a plan whose split requests merge inside thread-block clusters (no
+    # stage 2, no partials in the array) through the no-allocation entry
+    mla, workloads = _setup()
+    w = workloads.make_workload(bs=4, lengths=[1024] * 4, page_size=1, q_dtype="bf16",
+                                kv_dtype="bf16", seed=35)
+    plan = mla.mla_decode_plan(w.kv_indptr, None, page_size=1, q_dtype="bf16", kv_dtype="bf16",
+                               num_sms=152)
+    assert plan.info().cluster_size == 8
+    d = w.to("cuda")
+    ref, ref_lse = _regular(mla, plan, w, d)
+    for _ in range(2):
+        out, lse = _noalloc(mla, plan, w, d)
+        mla.mla_decode_check(plan, None)
+        assert torch.equal(out, ref) and torch.equal(lse, ref_lse)
