@@ -464,7 +464,8 @@ def config_entry(dec, step_ms, s1_ms, clocks, total_bytes, peak):
 def plan_meta(dec):
     """The plan options in use (and, after autotune, every candidate's time)."""
     m = {"unit_tokens": dec.info.unit_tokens, "item_cost": dec.info.item_cost,
-         "num_ctas": dec.info.num_ctas}
+         "num_ctas": dec.info.num_ctas,
+         "merge": "cluster of %d" % dec.info.cluster_size if dec.info.cluster_size else "stage 2"}
     if dec.tuned is not None:
         m["autotune"] = [dict(o, median_ms=ms) for o, ms in dec.tuned]
     return m
@@ -609,7 +610,8 @@ def main():
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind, "traffic": traffic,
                      "kernel": "mla_stage1_kernel", "stage1_us": s1_ms * 1e3},
-        "gpu_launches": K * (1 + (1 if info.num_merge_jobs > 0 else 0)),
+        # stage 1, plus stage 2 unless the plan merges inside clusters
+        "gpu_launches": K * (1 + (1 if info.num_merge_jobs > 0 and info.cluster_size == 0 else 0)),
         "clocks": clocks,
         "wall_s_timed": t_wall,
     }
