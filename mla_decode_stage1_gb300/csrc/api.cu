@@ -272,6 +272,7 @@ extern "C" {
 constexpr int32_t kClusterMerge = 8;
 static int32_t cluster_size_of(const mla_plan* P) {
   if (P->q_len != 1 || P->qmode == mla::kQBf16KvMx || P->qmode == mla::kQFp8KvFp8x2 ||
+      P->qmode == mla::kQBf16KvFp8x2 ||
       P->num_ctas < 2 || static_cast<int32_t>(P->items.size()) != P->num_ctas || P->jobs.empty())
     return 0;
   for (int32_t c = 0; c < P->num_ctas; ++c)
@@ -310,14 +311,14 @@ mla_status mla_decode_plan_ex(const int32_t* kv_indptr_host, const int32_t* kv_l
   const int qmode = qmode_of(q_dtype, kv_dtype);
   if (qmode < 0) return MLA_ERR_UNSUPPORTED;
   if (kv_indptr_host[0] < 0) return MLA_ERR_INVALID_ARG;
-  // With fp8 q and KV and an even q_len, query tokens run in pairs: pair p
-  // of request b is "virtual request" r = b * q_len / 2 + p, whose 32 q rows
-  // (tokens 2p, 2p+1) share every tile (kQFp8KvFp8x2); its first token sees
+  // With fp8 KV (fp8 or bf16 q) and an even q_len, query tokens run in pairs:
+  // pair p of request b is "virtual request" r = b * q_len / 2 + p, whose 32
+  // q rows (tokens 2p, 2p+1) share every tile (kQFp8KvFp8x2, kQBf16KvFp8x2); its first token sees
   // vis0 = n - q_len + 1 + 2p tokens, its second one more.  Otherwise query
   // token t of request b is virtual request r = b * q_len + t (its q, out
   // and lse row): it attends to the request's first n - q_len + 1 + t
   // tokens.  Either way through the request's own pages.
-  const bool pairs = q_len % 2 == 0 && qmode == mla::kQFp8KvFp8;
+  const bool pairs = q_len % 2 == 0 && (qmode == mla::kQFp8KvFp8 || qmode == mla::kQBf16KvFp8);
   const int32_t qv = pairs ? q_len / 2 : q_len;    // virtual requests per request
   const int32_t nv = batch_size * qv;
   std::vector<int32_t> len(nv), page_base(nv), npages(nv), vis0(nv, 0);
@@ -365,7 +366,7 @@ mla_status mla_decode_plan_ex(const int32_t* kv_indptr_host, const int32_t* kv_l
   P->num_splits = num_splits;
   P->q_dtype = q_dtype;
   P->kv_dtype = kv_dtype;
-  P->qmode = pairs ? mla::kQFp8KvFp8x2 : qmode;
+  P->qmode = !pairs ? qmode : qmode == mla::kQFp8KvFp8 ? mla::kQFp8KvFp8x2 : mla::kQBf16KvFp8x2;
   P->total_tokens = total_tok;
   P->identity_rows = identity_rows;
   P->total_tiles = total_tiles;

@@ -76,8 +76,10 @@ enum QMode : int {
   kQFp8KvBf16 = 3,    // kind::f16, q decoded to bf16 (exact), B = 16 rows
   kQBf16KvMx = 4,     // MXFP4 KV dequantised in shared memory to e4m3 with a per-token
                       // power of two; then as kQBf16KvFp8
-  kQFp8KvFp8x2 = 5    // two query tokens per request, fp8 q and KV: kind::f8f6f4,
+  kQFp8KvFp8x2 = 5,   // two query tokens per request, fp8 q and KV: kind::f8f6f4,
                       // B = 32 q rows (token-major), causal over the last two positions
+  kQBf16KvFp8x2 = 6   // two query tokens per request, bf16 q and fp8 KV: B = [q_hi; q_lo]
+                      // of the 32 q rows (64 rows), as kQBf16KvFp8 for one token
 };
 
 struct Stage1Params {

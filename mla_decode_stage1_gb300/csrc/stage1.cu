@@ -57,11 +57,13 @@ namespace mla {
 template <int QM>
 struct Layout {
   static constexpr bool kMx = (QM == kQBf16KvMx);                  // MXFP4 KV, dequantised
-  static constexpr bool kKv8 =
-      (QM == kQFp8KvFp8 || QM == kQBf16KvFp8 || kMx || QM == kQFp8KvFp8x2);
-  static constexpr int kQL = (QM == kQFp8KvFp8x2) ? 2 : 1;         // query tokens per request
+  static constexpr bool kKv8 = (QM == kQFp8KvFp8 || QM == kQBf16KvFp8 || kMx ||
+                                QM == kQFp8KvFp8x2 || QM == kQBf16KvFp8x2);
+  static constexpr int kQL =                                         // query tokens per request
+      (QM == kQFp8KvFp8x2 || QM == kQBf16KvFp8x2) ? 2 : 1;
   static constexpr int kRows = kHeads * kQL;                        // q rows, token-major
-  static constexpr bool kHiLo = (QM == kQBf16KvFp8 || kMx);         // q as two e4m3 terms
+  static constexpr bool kHiLo =                                      // q as two e4m3 terms
+      (QM == kQBf16KvFp8 || kMx || QM == kQBf16KvFp8x2);
   static constexpr int kNq = kRows * (kHiLo ? 2 : 1);               // UMMA N of QK^T
   // Warps: producer (MXFP4: a PV issuer), 2 QK^T issuers, PV issuers, two
   // head groups of four softmax warps (kH q rows each), then either a q warp
@@ -93,13 +95,18 @@ struct Layout {
   static constexpr int kRawRowBytes = kQkDim / 2;                   // packed MXFP4 row
   static constexpr bool kQ8 = (QM == kQFp8KvFp8 || QM == kQFp8KvBf16 || QM == kQFp8KvFp8x2);
   static constexpr int kQSrcBytes = kRows * kQkDim * (kQ8 ? 1 : 2);  // one request's q
-  // q staging buffer (raw q of the next item); MXFP4 converts q from global
-  // memory into its one q buffer
-  static constexpr int kQStageBytes = kMx ? 0 : kQSrcBytes;
-  static constexpr int kQBufs = kMx ? 1 : 2;
+  // q staging buffer (raw q of the next item); MXFP4 and bf16 q in pairs
+  // convert q from global memory into their one q buffer (so that two KV
+  // tiles fit)
+  static constexpr bool kQGlobal = kMx || QM == kQBf16KvFp8x2;
+  static constexpr int kQStageBytes = kQGlobal ? 0 : kQSrcBytes;
+  static constexpr int kQBufs = kQGlobal ? 1 : 2;
   static constexpr uint32_t kOCols = kRows * (kKv8 ? 2 : 1);       // TMEM columns per O block
-  // TMEM: S^T at 0 (2 buffers x 2 K-halves x 32 columns), O^T from 128
-  static constexpr uint32_t kTmemCols = 128 + 4 * kOCols <= 256 ? 256 : 512;
+  // TMEM: S^T at 0 (2 buffers x 2 K-halves x kSC columns), then O^T: four
+  // 128-dim blocks of kOCols columns (fp8 KV: the q rows of p_hi, then of p_lo)
+  static constexpr uint32_t kSC = kNq > 32 ? kNq : 32;              // columns per S K-half
+  static constexpr uint32_t kColO = 4 * kSC;
+  static constexpr uint32_t kTmemCols = kColO + 4 * kOCols <= 256 ? 256 : 512;
   static constexpr int kMiscBytes = 2560;
   static constexpr int kMaxSmem = 232448;
   static constexpr int kNumTiles =
@@ -114,7 +121,7 @@ struct Layout {
   static_assert(kNumTiles >= 1 && kNumTiles <= 4, "tile ring");
   static_assert(kSmemBytes <= kMaxSmem, "shared memory over budget");
   static_assert(kTileBytes % 1024 == 0 && kQBytes % 1024 == 0, "operand alignment");
-  static_assert(kNq <= 32, "S^T columns per K-half");
+  static_assert(kNq <= 64 && kTmemCols >= kColO + 4 * kOCols, "TMEM columns");
 };
 
 // Misc region: barriers, reduction scratch, q scales, TMEM address.
@@ -139,10 +146,10 @@ struct Misc {
 static_assert(sizeof(Misc) <= 2560, "misc region");
 static_assert(offsetof(Misc, red) % 16 == 0, "reduction scratch is read as float4");
 
-// TMEM columns: S^T as 2 buffers x 2 K-halves x 32 columns [0,128) (the two
-// QK^T issuers each accumulate half of the 576 dims), then O^T: four 128-dim
-// blocks of kOCols columns (fp8 KV: the q rows of p_hi, then of p_lo).
-constexpr uint32_t kColS = 0, kColO = 128;
+// TMEM columns: S^T from 0 as 2 buffers x 2 K-halves (the two QK^T issuers
+// each accumulate half of the 576 dims) x Layout::kSC columns, then O^T from
+// Layout::kColO.
+constexpr uint32_t kColS = 0;
 
 // Byte offset of (row, byte x) inside a 128-byte-wide K-major operand with
 // the 128-byte swizzle (8-row / 1024-byte atoms, 16-byte chunks XOR row%8).
@@ -379,7 +386,7 @@ __device__ void run_qk(const Stage1Params& p, Misc* ms, uint32_t ring, uint32_t 
     if (p.gather) fence_proxy_async_smem();   // rows copied by cp.async (generic proxy)
     const uint32_t tile = ring + s * L::kTileBytes;
     const uint32_t qaddr = qbase + qb * L::kQBytes;
-    const uint32_t d = tmem + kColS + 64 * sb + 32 * half;
+    const uint32_t d = tmem + kColS + 2 * L::kSC * sb + L::kSC * half;
     const int k0 = half * (L::kKSteps / 2), k1 = k0 + L::kKSteps / 2;
     if (lane == 0) {
     // descriptors built once per tile; a K step only moves the start address
@@ -429,7 +436,7 @@ __device__ void run_pv(const Stage1Params& p, Misc* ms, uint32_t ring, uint32_t 
     if (lane == 0) {
     for (int i = 0; i < kBlocks; ++i) {
       const int c = kBlocks * half + i;
-      const uint32_t d = tmem + kColO + L::kOCols * c;
+      const uint32_t d = tmem + L::kColO + L::kOCols * c;
       // B = P^T, MN-major: one kPRow-byte row per token (fp8: the q rows of
       // p_hi then of p_lo; bf16: the q rows), 8-token groups of 8 rows, with
       // the swizzle of the row width (32 or 64 bytes).
@@ -591,11 +598,11 @@ __device__ __forceinline__ void q_fetch(const Stage1Params& p, Misc* ms, uint8_t
             L::kQSrcBytes, bar);
 }
 
-// Eight bf16 q values (vector `vid` of the [16 heads][576] q) -> their e4m3
+// Eight bf16 q values (vector `vid` of the [rows][576] q) -> their e4m3
 // q_hi = rn(q / s_hi) and q_lo = rn(16 (q - q_hi s_hi) / s_hi) bytes, stored
-// as rows h and 16 + h of the K-major, 128-byte-swizzled q operand.
+// as rows h and rows + h of the K-major, 128-byte-swizzled q operand.
 __device__ __forceinline__ void q_split_store(const uint4 v, int vid, float s_hi, float inv_hi,
-                                              uint8_t* dst, int atom_bytes) {
+                                              uint8_t* dst, int atom_bytes, int rows) {
   const int h = vid / 72, d0 = (vid % 72) * 8;
   const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v);
   uint32_t hw[2], lw[2];
@@ -617,7 +624,7 @@ __device__ __forceinline__ void q_split_store(const uint4 v, int vid, float s_hi
   const int atom = d0 >> 7, x = d0 & 127;
   uint8_t* base = dst + atom * atom_bytes;
   *reinterpret_cast<uint2*>(base + sw128(h, x)) = make_uint2(hw[0], hw[1]);
-  *reinterpret_cast<uint2*>(base + sw128(16 + h, x)) = make_uint2(lw[0], lw[1]);
+  *reinterpret_cast<uint2*>(base + sw128(rows + h, x)) = make_uint2(lw[0], lw[1]);
 }
 
 // Writes q of one request from the staging buffer into q buffer `dst` (the
@@ -633,7 +640,7 @@ __device__ __forceinline__ void q_convert(const Stage1Params& p, Misc* ms, const
   using L = Layout<QM>;
   constexpr float kSmScale = 1.0f / 24.0f;          // 1/sqrt(576)
   c_lo = 0.f;
-  if constexpr (QM == kQBf16KvFp8 || QM == kQBf16KvMx) {
+  if constexpr (QM == kQBf16KvFp8 || QM == kQBf16KvMx || QM == kQBf16KvFp8x2) {
     constexpr int kV = L::kQSrcBytes / 16;           // 16-byte vectors of 8 bf16
     const uint4* src = reinterpret_cast<const uint4*>(stage);
     float amax = 0.f;
@@ -656,7 +663,8 @@ __device__ __forceinline__ void q_convert(const Stage1Params& p, Misc* ms, const
     }
     amax = fmaxf(amax, 1e-30f);
     const float s_hi = amax / 448.0f, inv_hi = 448.0f / amax;
-    for (int v = i; v < kV; v += n) q_split_store(src[v], v, s_hi, inv_hi, dst, L::kQAtomBytes);
+    for (int v = i; v < kV; v += n)
+      q_split_store(src[v], v, s_hi, inv_hi, dst, L::kQAtomBytes, L::kRows);
     const float kvs = (QM == kQBf16KvMx) ? 1.0f : __ldg(p.kv_scale);
     c_hi = s_hi * kvs * kSmScale * kLog2e;
     c_lo = c_hi * (1.0f / 16.0f);
@@ -735,7 +743,7 @@ __device__ __forceinline__ void q_convert_mx(const Stage1Params& p, Misc* ms, in
 #pragma unroll 1
   for (int u = 0; u < kPer; ++u) {
     const int v = i + kN * u;
-    if (v < kV) q_split_store(__ldg(src + v), v, s_hi, inv_hi, dst, L::kQAtomBytes);
+    if (v < kV) q_split_store(__ldg(src + v), v, s_hi, inv_hi, dst, L::kQAtomBytes, L::kRows);
   }
   c_hi = s_hi * kSmScale * kLog2e;
   c_lo = c_hi * (1.0f / 16.0f);
@@ -946,6 +954,9 @@ __device__ void run_qprep(const Stage1Params& p, Misc* ms, uint8_t* qgen, uint8_
   using L = Layout<QM>;
   const uint32_t stage_bar = smem_u32(&ms->q_stage);
   if (it0 >= it1) return;
+  // bf16 q in pairs: the softmax warps convert every item's q from global
+  // memory into the one q buffer (run_softmax); nothing to do here
+  if constexpr (L::kQGlobal) return;
   if (lane == 0) q_fetch<QM>(p, ms, stage, first.b);
   if (it0 + 1 >= it1) return;
   // the softmax warps are done with the first item's staged q
@@ -1030,12 +1041,18 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
     if (it0 < it1) {
       // The first item's q gates the first QK^T: all softmax threads convert
       // it (into q buffer 0) while they would otherwise wait for S.
+      // (bf16 q in pairs: straight from global memory, no staging buffer)
       constexpr int kN = 128 * kHG;
-      wait_or_flag(smem_u32(&ms->q_stage), 0, p.err, kErrSoftmax, abort);
+      const uint8_t* src = stage;
+      if constexpr (L::kQGlobal) {
+        src = static_cast<const uint8_t*>(p.q) + static_cast<int64_t>(first.b) * L::kQSrcBytes;
+      } else {
+        wait_or_flag(smem_u32(&ms->q_stage), 0, p.err, kErrSoftmax, abort);
+      }
       named_bar_sync(6, kN);
       if (*abort) return;
       float c_hi, c_lo;
-      q_convert<QM>(p, ms, stage, qgen, tid, kN, 6, c_hi, c_lo);
+      q_convert<QM>(p, ms, src, qgen, tid, kN, 6, c_hi, c_lo);
       fence_proxy_async_smem();
       named_bar_sync(6, kN);
       if (tid == 0) {
@@ -1063,16 +1080,16 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
       tc_fence_after();
       float s[kH];
       {
-        // S^T columns of buffer sb: two K-halves of 32 columns; q split in two
+        // S^T columns of buffer sb: two K-halves of kSC columns; q split in two
         // terms puts the rows of q_hi first, then those of q_lo
-        const uint32_t sc = tl + kColS + 64 * sb + h0;
+        const uint32_t sc = tl + kColS + 2 * L::kSC * sb + h0;
         float a0[kH], a1[kH];
         tmem_ld(sc, a0);
-        tmem_ld(sc + 32, a1);
+        tmem_ld(sc + L::kSC, a1);
         if constexpr (L::kHiLo) {
           float b0[kH], b1[kH];
           tmem_ld(sc + L::kRows, b0);
-          tmem_ld(sc + 32 + L::kRows, b1);
+          tmem_ld(sc + L::kSC + L::kRows, b1);
           tmem_wait_ld();
 #pragma unroll
           for (int h = 0; h < kH; ++h) s[h] = (a0[h] + a1[h]) * c_hi + (b0[h] + b1[h]) * c_lo;
@@ -1139,7 +1156,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
         const int nparts = L::kKv8 ? 2 : 1;
         for (int part = 0; part < nparts; ++part) {
           for (int c = 0; c < 4; ++c) {
-            const uint32_t col = kColO + L::kOCols * c + L::kRows * part + h0;
+            const uint32_t col = L::kColO + L::kOCols * c + L::kRows * part + h0;
             float o[kH];
             tmem_ld(tl + col, o);
             tmem_wait_ld();
@@ -1224,6 +1241,29 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
       tc_fence_before();
       mbar_arrive(smem_u32(&ms->p_full[sb]));
     }
+    if constexpr (L::kQGlobal && !L::kMx) {
+      // bf16 q in pairs (one q buffer): QK^T of this item's last tile is
+      // done, so its q buffer is free; convert the next item's q into it
+      // before the epilogue, with all softmax threads
+      if (it + 1 < it1) {
+        constexpr int kN = 128 * kHG;
+        wait_or_flag(smem_u32(&ms->q_empty[0]), static_cast<uint32_t>(k) & 1u, p.err,
+                     kErrSoftmax, abort);
+        const uint8_t* src =
+            static_cast<const uint8_t*>(p.q) + static_cast<int64_t>(p.items[it + 1].b) * L::kQSrcBytes;
+        named_bar_sync(6, kN);
+        if (*abort) return;
+        float c_hi2, c_lo2;
+        q_convert<QM>(p, ms, src, qgen, tid, kN, 6, c_hi2, c_lo2);
+        fence_proxy_async_smem();
+        named_bar_sync(6, kN);
+        if (tid == 0) {
+          ms->qscale[0][0] = c_hi2;
+          ms->qscale[0][1] = c_lo2;
+          mbar_arrive(smem_u32(&ms->q_full[0]));
+        }
+      }
+    }
     // ------------------------------------------------------------ epilogue
     const uint32_t gl = g - 1;
     wait_or_flag(smem_u32(&ms->pv_done[gl & 1u]), (gl >> 1) & 1u, p.err, kErrSoftmax, abort);
@@ -1276,8 +1316,8 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
       float oh[4][kH], ol[4][kH];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        tmem_ld(tl + kColO + L::kOCols * c + h0, oh[c]);
-        if constexpr (L::kKv8) tmem_ld(tl + kColO + L::kOCols * c + L::kRows + h0, ol[c]);
+        tmem_ld(tl + L::kColO + L::kOCols * c + h0, oh[c]);
+        if constexpr (L::kKv8) tmem_ld(tl + L::kColO + L::kOCols * c + L::kRows + h0, ol[c]);
       }
       tmem_wait_ld();
 #pragma unroll
@@ -1292,8 +1332,8 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint8_t* ring_gen, 
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         float oh[kH], ol[kH];
-        tmem_ld(tl + kColO + L::kOCols * c + h0, oh);
-        if constexpr (L::kKv8) tmem_ld(tl + kColO + L::kOCols * c + L::kRows + h0, ol);
+        tmem_ld(tl + L::kColO + L::kOCols * c + h0, oh);
+        if constexpr (L::kKv8) tmem_ld(tl + L::kColO + L::kOCols * c + L::kRows + h0, ol);
         tmem_wait_ld();
 #pragma unroll
         for (int h = 0; h < kH; ++h)
@@ -1523,6 +1563,7 @@ int stage1_smem_bytes(int qmode) {
     case kQFp8KvBf16: return Layout<kQFp8KvBf16>::kSmemBytes;
     case kQBf16KvMx: return Layout<kQBf16KvMx>::kSmemBytes;
     case kQFp8KvFp8x2: return Layout<kQFp8KvFp8x2>::kSmemBytes;
+    case kQBf16KvFp8x2: return Layout<kQBf16KvFp8x2>::kSmemBytes;
   }
   return -1;
 }
@@ -1605,6 +1646,7 @@ cudaError_t launch_stage1(int qmode, const Stage1Params& p, int num_ctas, cudaSt
     case kQFp8KvBf16: return launch_t<kQFp8KvBf16>(p, num_ctas, stream);
     case kQBf16KvMx: return launch_t<kQBf16KvMx>(p, num_ctas, stream);
     case kQFp8KvFp8x2: return launch_t<kQFp8KvFp8x2>(p, num_ctas, stream);
+    case kQBf16KvFp8x2: return launch_t<kQBf16KvFp8x2>(p, num_ctas, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -256,8 +256,9 @@ def test_all_empty_batch_has_no_ctas_and_only_fill_jobs(mla):
 # ------------------------------------------------- several query tokens
 
 def plan_q(mla, indptr, q_len, last=None, ps=1, S=0, sms=148):
+    # bf16 q and KV: every query token is planned on its own (fp8 KV pairs them)
     return mla.mla_decode_plan(np.asarray(indptr, np.int32), last, page_size=ps, q_dtype="bf16",
-                               kv_dtype="fp8", num_splits=S, num_sms=sms, q_len=q_len)
+                               kv_dtype="bf16", num_splits=S, num_sms=sms, q_len=q_len)
 
 
 def virtual_lengths(lengths, q_len):
@@ -302,13 +303,15 @@ def test_qlen_plan_rejects_bad_q_len(mla):
         assert e.value.status == 1
 
 
+@pytest.mark.parametrize("qd", ["fp8", "bf16"])
 @pytest.mark.parametrize("S,sms", [(0, 152), (0, 7), (3, 152)])
-def test_qlen2_fp8_plans_whole_requests(mla, S, sms):
-    # two query tokens with fp8 q and KV share every tile: the plan covers
-    # each request's tokens once, and a partial holds 32 rows (2 x 16 heads)
+def test_qlen2_fp8_plans_whole_requests(mla, S, sms, qd):
+    # two query tokens with fp8 KV (fp8 or bf16 q) share every tile: the plan
+    # covers each request's tokens once, and a partial holds 32 rows (2 x 16
+    # heads)
     lens = [0, 1, 2, 300, 1000, 4096, 129]
     indptr = np.concatenate([[0], np.cumsum(lens)])
-    pl = mla.mla_decode_plan(np.asarray(indptr, np.int32), None, page_size=1, q_dtype="fp8",
+    pl = mla.mla_decode_plan(np.asarray(indptr, np.int32), None, page_size=1, q_dtype=qd,
                              kv_dtype="fp8", num_splits=S, num_sms=sms, q_len=2)
     info = pl.info()
     assert info.batch_size == len(lens) and info.q_len == 2
@@ -316,12 +319,13 @@ def test_qlen2_fp8_plans_whole_requests(mla, S, sms):
     assert pl.workspace_bytes >= info.num_partials * 32 * (512 + 1) * 4
 
 
-def test_even_qlen_fp8_plans_pairs_of_query_tokens(mla):
-    # q_len = 4 with fp8 q and KV: pair p of request b is planned request
-    # 2b + p, covering the tokens its second query token sees
+@pytest.mark.parametrize("qd", ["fp8", "bf16"])
+def test_even_qlen_fp8_plans_pairs_of_query_tokens(mla, qd):
+    # q_len = 4 with fp8 KV: pair p of request b is planned request 2b + p,
+    # covering the tokens its second query token sees
     lens = [0, 1, 3, 4, 300, 1000]
     indptr = np.concatenate([[0], np.cumsum(lens)])
-    pl = mla.mla_decode_plan(np.asarray(indptr, np.int32), None, page_size=1, q_dtype="fp8",
+    pl = mla.mla_decode_plan(np.asarray(indptr, np.int32), None, page_size=1, q_dtype=qd,
                              kv_dtype="fp8", num_sms=20, q_len=4)
     pair_lens = [max(0, n - 4 + 2 + 2 * p) for n in lens for p in range(2)]
     check_partition(pl, pair_lens)
@@ -366,7 +370,7 @@ def test_randomized_plans_partition_every_query_token(mla, seed):
                              num_sms=sms, q_len=q_len)
     info = pl.info()
     assert info.batch_size == len(lens) and info.q_len == q_len
-    pairs = q_len % 2 == 0 and (qd, kd) == ("fp8", "fp8")
+    pairs = q_len % 2 == 0 and kd == "fp8"
     if pairs:
         vlens = [max(0, int(x) - q_len + 2 + 2 * p) for x in n for p in range(q_len // 2)]
     else:
