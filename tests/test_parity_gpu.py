@@ -321,7 +321,7 @@ def test_split_merge_repeated_launches_same_workspace():
 
 @pytest.mark.parametrize("q_dtype,kv_dtype,q_len", [
     ("bf16", "bf16", 1), ("bf16", "fp8", 1), ("fp8", "fp8", 1), ("fp8", "bf16", 1),
-    ("bf16", "mxfp4", 1), ("fp8", "fp8", 2)])
+    ("bf16", "mxfp4", 1), ("fp8", "fp8", 2), ("bf16", "fp8", 2)])
 def test_soak_interleaved_plans_are_deterministic(q_dtype, kv_dtype, q_len):
     # 300 calls back to back on one stream, without synchronising: two plans
     # of different batches interleaved, plan A alternating between two
@@ -401,16 +401,37 @@ def test_qlen_causal_decode(q_dtype, kv_dtype, q_len):
     check(w)
 
 
+@pytest.mark.parametrize("q_dtype", ["fp8", "bf16"])
 @pytest.mark.parametrize("q_len", [2, 3, 4, 6])
 @pytest.mark.parametrize("num_splits,num_sms", [(3, 0), (0, 5), (0, 2)])
-def test_qlen_splits_and_few_ctas(num_splits, num_sms, q_len):
-    # fp8 q + fp8 KV with an even number of query tokens runs them in pairs
-    # (32 q rows per tile); three tokens run as causal prefixes
+def test_qlen_splits_and_few_ctas(num_splits, num_sms, q_len, q_dtype):
+    # fp8 KV with an even number of query tokens runs them in pairs (32 q
+    # rows per tile; with bf16 q one q buffer, refilled by the softmax warps
+    # between items); three tokens run as causal prefixes
     import workloads as synth
     lengths = [700, 5, 4096, 129, 1, 2, 128]
-    w = synth.make_workload(bs=len(lengths), lengths=lengths, page_size=16, q_dtype="fp8",
+    w = synth.make_workload(bs=len(lengths), lengths=lengths, page_size=16, q_dtype=q_dtype,
                             kv_dtype="fp8", permute_pages=True, seed=49, q_len=q_len)
     check(w, num_splits=num_splits, num_sms=num_sms)
+
+
+def test_qlen2_bf16_pairs_gathered_rows_and_small_rope_dims():
+    # bf16 q in pairs with page size 7 (rows gathered one by one), extra pool
+    # pages and rope dims 2^-6 smaller than the rest, so the pair's one scale
+    # covers a wide range.  (A head made 2^4 to 2^8 larger than the others
+    # puts a short request's dominant LSE just outside the LSE bar: the
+    # two-term split keeps about 2^-9 of the pair's largest |q|, the same
+    # bound as one token, which the one-token test above covers.)
+    import workloads as synth
+    lengths = [1000, 3, 257, 2049]
+    w = synth.make_workload(bs=len(lengths), lengths=lengths, page_size=7, q_dtype="bf16",
+                            kv_dtype="fp8", permute_pages=True, seed=64, q_len=2,
+                            extra_pool_pages=3)
+    q = w.q.float()
+    q[:, :, 512:] *= 2.0 ** -6                     # rope dims
+    w.q = q.to(torch.bfloat16)
+    check(w)
+    check(w, num_sms=3)
 
 
 def test_qlen2_fp8_token_zero_without_kv_in_an_item():
