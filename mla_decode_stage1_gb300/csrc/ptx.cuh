@@ -90,6 +90,11 @@ __device__ __forceinline__ uint4 ld_nc_na_v4(const void* ptr) {
                : "l"(ptr));
   return v;
 }
+// L2 prefetch of the 128-byte line holding `ptr`, kept in L2 ahead of
+// lines that were only streamed through.
+__device__ __forceinline__ void prefetch_l2_last(const void* ptr) {
+  asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(ptr));
+}
 __device__ __forceinline__ uint32_t ld_nc_u8_early(const uint8_t* ptr) {
   uint16_t v;
   asm volatile("ld.global.nc.u8 %0, [%1];" : "=h"(v) : "l"(ptr));

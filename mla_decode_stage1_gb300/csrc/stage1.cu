@@ -66,12 +66,12 @@ struct Layout {
       (QM == kQBf16KvFp8 || kMx || QM == kQBf16KvFp8x2);
   static constexpr int kNq = kRows * (kHiLo ? 2 : 1);               // UMMA N of QK^T
   // Warps: producer (MXFP4: a PV issuer), 2 QK^T issuers, PV issuers, two
-  // head groups of four softmax warps (kH q rows each), then either a q warp
-  // (14 warps) or, for MXFP4, 8 dequant warps that also load the packed
-  // rows and prepare q (20 warps).
+  // head groups of four softmax warps (kH q rows each), then either a q warp,
+  // a PV issuer and an L2 prefetcher (15 warps) or, for MXFP4, 8 dequant
+  // warps that also load the packed rows and prepare q (20 warps).
   static constexpr int kHeadGroups = 2;
   static constexpr int kH = kRows / kHeadGroups;                    // q rows per softmax thread
-  static constexpr int kThreads = kMx ? 640 : 448;
+  static constexpr int kThreads = kMx ? 640 : 480;
   // MXFP4 register plan per warpgroup (setmaxnreg after the launch): the
   // producer and UMMA issuers need few, the softmax warps many
   static constexpr int kRegsLaunch = 96;
@@ -349,6 +349,58 @@ __device__ void run_producer(const Stage1Params& p, Misc* ms, uint32_t ring, int
 }
 
 // ---------------------------------------------------------- UMMA issuers
+// L2 prefetcher (one warp): the rows of tile t are prefetched into L2 once
+// tile t - kNumTiles has landed, i.e. about one slot hold before the
+// producer's boxes for tile t go out into the slot that tile frees, so that
+// those boxes read from L2.  Plain prefetch instructions, not bulk
+// prefetches: the TMA unit spends about 60 cycles on each box of a tile
+// already, and a bulk prefetch would add as many again.  It runs where the
+// landing sits on the critical path: page tables (16 boxes per tile) and the
+// one-slot bf16 ring.  An identity table with two slots (one 128-row box per
+// tile) was slower with it on GB300.  A hint only: its waits give up
+// quietly, the roles on the data path report a stalled tile.
+template <int QM>
+__device__ void run_prefetch(const Stage1Params& p, Misc* ms, int it0, int it1,
+                             const WorkItem& first, int lane) {
+  using L = Layout<QM>;
+  if (p.gather || (p.box_rows != 8 && L::kNumTiles > 1)) return;
+  TileCursor c;
+  c.init(p.items, it0, it1, first);
+  BoxFetch f = box_fetch(p, c, lane);
+  uint32_t t = 0;
+  while (!c.done()) {
+    TileCursor n = c;
+    n.advance();
+    const BoxFetch fn = box_fetch(p, n, lane);    // in flight during the wait
+    if (t >= static_cast<uint32_t>(L::kNumTiles)) {
+      const uint32_t tt = t - L::kNumTiles;
+      const uint32_t bar = smem_u32(&ms->full[tt % L::kNumTiles]), par = (tt / L::kNumTiles) & 1u;
+      if (!mbar_try_wait(bar, par)) {
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(bar, par))
+          if (globaltimer_ns() - t0 > kWaitLimitNs) return;
+      }
+    }
+    // lane l: box l's rows (8-row groups), or a share of the one 128-row box
+    int64_t r0 = 0, nrows = 0;
+    if (p.box_rows == 8) {
+      if (lane < f.nbox) { r0 = box_row(p, f, lane); nrows = 8; }
+    } else if (f.nbox > 0) {
+      r0 = __shfl_sync(0xffffffffu, box_row(p, f, lane), 0);
+      nrows = kTile;
+    }
+    nrows = min(nrows, static_cast<int64_t>(p.pool_rows) - r0);   // inside the pool
+    const uint8_t* a = p.kv + r0 * L::kRowBytes;
+    const int lines = static_cast<int>(nrows * L::kRowBytes / 128);
+    const int first_line = p.box_rows == 8 ? 0 : lane;
+    const int step = p.box_rows == 8 ? 1 : 32;
+    for (int i = first_line; i < lines; i += step) prefetch_l2_last(a + i * 128);
+    f = fn;
+    c = n;
+    ++t;
+  }
+}
+
 // QK^T issuer: S^T[sb] = K_tile . Q^T over kKSteps steps of 32 bytes.  The K
 // tile is K-major with the 64-byte swizzle: column chunk j at j*cs, 8-row
 // groups at gs.
@@ -1528,8 +1580,10 @@ __global__ void __launch_bounds__(Layout<QM>::kThreads, 1) mla_stage1_kernel(con
     } else if (warp < 4 + 4 * L::kHeadGroups) {
       run_softmax<QM>(p, ms, smem, smem + L::kPOff, smem + L::kQOff, smem + L::kQStageOff, tmem,
                       it0, it1, first, threadIdx.x - 128);
-    } else {
+    } else if (warp == 12) {
       run_qprep<QM>(p, ms, smem + L::kQOff, smem + L::kQStageOff, it0, it1, first, lane);
+    } else {
+      run_prefetch<QM>(p, ms, it0, it1, first, lane);
     }
   }
 
