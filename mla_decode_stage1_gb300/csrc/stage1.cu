@@ -372,7 +372,15 @@ __device__ void run_prefetch(const Stage1Params& p, Misc* ms, int it0, int it1,
     TileCursor n = c;
     n.advance();
     const BoxFetch fn = box_fetch(p, n, lane);    // in flight during the wait
-    if (t >= static_cast<uint32_t>(L::kNumTiles)) {
+    // (the first kNumTiles tiles go out at once: a prefetch would only
+    // compete with their boxes)
+    if (t < static_cast<uint32_t>(L::kNumTiles)) {
+      f = fn;
+      c = n;
+      ++t;
+      continue;
+    }
+    {
       const uint32_t tt = t - L::kNumTiles;
       const uint32_t bar = smem_u32(&ms->full[tt % L::kNumTiles]), par = (tt / L::kNumTiles) & 1u;
       if (!mbar_try_wait(bar, par)) {
