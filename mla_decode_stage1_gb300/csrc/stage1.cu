@@ -26,7 +26,9 @@
 //    the softmax and the epilogue in two groups of 8 heads (two-token mode:
 //    one group per query token, 16 heads each; one thread per token / per
 //    output dim, TMEM lane = thread) and convert the first item's q; warp
-//    12 converts the q of later items;
+//    12 converts the q of later items; warp 14 prefetches each tile's rows
+//    into L2 a slot hold ahead (page tables, and the one-slot bf16 ring),
+//    so that the producer's boxes read from L2;
 //  * MXFP4: warps 12-19 load the packed rows from global memory straight
 //    into registers (any page size), dequantise them into the e4m3 tile slot
 //    and prepare every item's q; the warpgroups then run with their own
@@ -140,6 +142,7 @@ struct Misc {
                                      // first QK^T K-half (dims 0-287) may start
   uint64_t deq_b[4];                 // chunks 5-8 dequantised (the slot is complete)
   int32_t stale;                     // the workspace holds another plan's table
+  uint32_t landed;                   // tiles the first QK^T issuer has seen land (bf16 / fp8)
   int16_t uexp[2][128];              // per-token power of two u_t = r_t - 127 of a slot
   uint2 e2m1_tab[16];                // e4m3 tables for 2^k, k = index - 14 (k <= -14: all 0)
 };
@@ -356,14 +359,16 @@ __device__ void run_producer(const Stage1Params& p, Misc* ms, uint32_t ring, int
 // prefetches: the TMA unit spends about 60 cycles on each box of a tile
 // already, and a bulk prefetch would add as many again.  It runs where the
 // landing sits on the critical path: page tables (16 boxes per tile) and the
-// one-slot bf16 ring.  An identity table with two slots (one 128-row box per
-// tile) was slower with it on GB300.  A hint only: its waits give up
-// quietly, the roles on the data path report a stalled tile.
+// one-slot bf16 ring.  Two cases were slower with it on GB300 and skip it:
+// an identity table with two slots (one 128-row box per tile), and bf16 q in
+// pairs (whose softmax warps read the next item's q from global memory).  A
+// hint only: its waits give up quietly, the roles on the data path report a
+// stalled tile.
 template <int QM>
 __device__ void run_prefetch(const Stage1Params& p, Misc* ms, int it0, int it1,
                              const WorkItem& first, int lane) {
   using L = Layout<QM>;
-  if (p.gather || (p.box_rows != 8 && L::kNumTiles > 1)) return;
+  if (QM == kQBf16KvFp8x2 || p.gather || (p.box_rows != 8 && L::kNumTiles > 1)) return;
   TileCursor c;
   c.init(p.items, it0, it1, first);
   BoxFetch f = box_fetch(p, c, lane);
@@ -381,12 +386,18 @@ __device__ void run_prefetch(const Stage1Params& p, Misc* ms, int it0, int it1,
       continue;
     }
     {
-      const uint32_t tt = t - L::kNumTiles;
-      const uint32_t bar = smem_u32(&ms->full[tt % L::kNumTiles]), par = (tt / L::kNumTiles) & 1u;
-      if (!mbar_try_wait(bar, par)) {
+      // Tile t - kNumTiles has landed once the first QK^T issuer has seen it
+      // land.  A count, not the slot's mbarrier: this warp may fall two
+      // phases behind a slot, and a parity wait would then wait for a phase
+      // that never comes.
+      const volatile uint32_t* landed = &ms->landed;
+      const uint32_t need = t - L::kNumTiles + 1;
+      if (*landed < need) {
         const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(bar, par))
+        while (*landed < need) {
           if (globaltimer_ns() - t0 > kWaitLimitNs) return;
+          __nanosleep(128);
+        }
       }
     }
     // lane l: box l's rows (8-row groups), or a share of the one 128-row box
@@ -442,6 +453,7 @@ __device__ void run_qk(const Stage1Params& p, Misc* ms, uint32_t ring, uint32_t 
                            : half == 0 ? smem_u32(&ms->deq_a[s]) : smem_u32(&ms->deq_b[s]);
     if (!__all_sync(0xffffffffu, mbar_wait(ready, (t / L::kNumTiles) & 1u, p.err, kErrMma)))
       break;
+    if (half == 0 && lane == 0) *reinterpret_cast<volatile uint32_t*>(&ms->landed) = t + 1;
     tc_fence_after();
     if (p.gather) fence_proxy_async_smem();   // rows copied by cp.async (generic proxy)
     const uint32_t tile = ring + s * L::kTileBytes;
@@ -1530,6 +1542,7 @@ __global__ void __launch_bounds__(Layout<QM>::kThreads, 1) mla_stage1_kernel(con
     mbar_init(smem_u32(&ms->q_stage), 1);
     mbar_init(smem_u32(&ms->q_stage_free), 1);
     ms->abort_sm = 0;
+    ms->landed = 0;
     fence_mbar_init();
     ms->stale = (hs != p.stamp || cs != p.stamp) ? 1 : 0;
   }

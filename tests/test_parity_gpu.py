@@ -496,6 +496,51 @@ def test_random_sweep(seed):
     check(w, num_splits=num_splits, num_sms=num_sms)
 
 
+# Every wait in the kernels is bounded (200 ms), and the waits of hint-only
+# roles give up without flagging an error.  A wait that can miss its phase
+# would then show only as a call that takes the bound: these cases (several
+# tiles and items per CTA, every role layout) must finish far below it.
+STALL_CASES = [
+    # (q dtype, KV dtype, page size, q_len, CTAs (0 = the device's SMs), batch, length range)
+    ("fp8", "fp8", 8, 1, 16, 12, (1000, 6000)),
+    ("bf16", "fp8", 8, 3, 0, 64, (8192, 8193)),     # bs=64 x 8192, three query tokens
+    ("bf16", "fp8", 8, 3, 16, 10, (500, 5000)),
+    ("fp8", "fp8", 8, 2, 16, 10, (500, 5000)),
+    ("bf16", "fp8", 16, 4, 24, 8, (500, 5000)),
+    ("bf16", "bf16", 1, 1, 16, 8, (1000, 6000)),    # one-slot ring, identity table
+    ("bf16", "bf16", 8, 3, 16, 8, (500, 5000)),
+    ("fp8", "bf16", 8, 1, 0, 16, (1000, 6000)),
+    ("bf16", "mxfp4", 1, 1, 16, 8, (1000, 6000)),
+]
+
+
+@pytest.mark.parametrize("q_dtype,kv_dtype,page_size,q_len,num_sms,bs,span", STALL_CASES)
+def test_calls_finish_far_below_the_wait_bound(q_dtype, kv_dtype, page_size, q_len, num_sms,
+                                                bs, span):
+    mla = _mla()
+    import workloads as synth
+    rng = np.random.default_rng(91)
+    lengths = rng.integers(span[0], span[1], size=bs).tolist()
+    w = synth.make_workload(bs=bs, lengths=lengths, page_size=page_size, q_dtype=q_dtype,
+                            kv_dtype=kv_dtype, permute_pages=page_size > 1, seed=92,
+                            q_len=q_len, device="cuda")
+    plan = mla.mla_decode_plan(w.kv_indptr, w.kv_last_page_len, page_size=w.page_size,
+                               q_dtype=q_dtype, kv_dtype=kv_dtype, num_sms=num_sms, q_len=q_len)
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
+    out = torch.empty((bs * q_len, 16, 512), dtype=torch.bfloat16, device="cuda")
+    times = []
+    for _ in range(3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        mla.mla_decode_run(plan, w.q, w.kv, out, workspace=ws, q_scale=w.q_scale,
+                           kv_scale=w.kv_scale, kv_e8m0=w.kv_e8m0, kv_indices=w.kv_indices)
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    mla.mla_decode_check(plan, ws)
+    assert max(times) < 20.0, f"a call took {max(times):.1f} ms (the wait bound is 200 ms)"
+
+
 # ------------------------------------------------- failure detection
 
 def test_bounded_wait_times_out_and_context_survives():
