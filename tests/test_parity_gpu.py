@@ -511,6 +511,10 @@ STALL_CASES = [
     ("bf16", "bf16", 8, 3, 16, 8, (500, 5000)),
     ("fp8", "bf16", 8, 1, 0, 16, (1000, 6000)),
     ("bf16", "mxfp4", 1, 1, 16, 8, (1000, 6000)),
+    ("bf16", "mxfp4", 8, 3, 16, 8, (500, 5000)),
+    ("fp8", "fp8", 12, 1, 16, 8, (1000, 6000)),     # rows gathered one by one
+    ("fp8", "bf16", 7, 2, 16, 8, (500, 5000)),
+    ("bf16", "bf16", 1, 1, 0, 4, (1024, 1025)),     # eight-way splits merged in clusters
 ]
 
 
