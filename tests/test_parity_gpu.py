@@ -501,7 +501,8 @@ def test_random_sweep(seed):
 # would then show only as a call that takes the bound: these cases (several
 # tiles and items per CTA, every role layout) must finish far below it.
 STALL_CASES = [
-    # (q dtype, KV dtype, page size, q_len, CTAs (0 = the device's SMs), batch, length range)
+    # (q dtype, KV dtype, page size, q_len, CTAs (0 = the device's SMs), batch, length range
+    #  [, cut unit in tokens])
     ("fp8", "fp8", 8, 1, 16, 12, (1000, 6000)),
     ("bf16", "fp8", 8, 3, 0, 64, (8192, 8193)),     # bs=64 x 8192, three query tokens
     ("bf16", "fp8", 8, 3, 16, 10, (500, 5000)),
@@ -515,12 +516,15 @@ STALL_CASES = [
     ("fp8", "fp8", 12, 1, 16, 8, (1000, 6000)),     # rows gathered one by one
     ("fp8", "bf16", 7, 2, 16, 8, (500, 5000)),
     ("bf16", "bf16", 1, 1, 0, 4, (1024, 1025)),     # eight-way splits merged in clusters
+    ("fp8", "fp8", 1, 1, 16, 8, (1000, 6000), 32),  # 32-token cut units (8-row boxes)
+    ("bf16", "bf16", 8, 2, 16, 8, (500, 5000), 64),
 ]
 
 
-@pytest.mark.parametrize("q_dtype,kv_dtype,page_size,q_len,num_sms,bs,span", STALL_CASES)
+@pytest.mark.parametrize("q_dtype,kv_dtype,page_size,q_len,num_sms,bs,span,unit",
+                         [c if len(c) == 8 else c + (0,) for c in STALL_CASES])
 def test_calls_finish_far_below_the_wait_bound(q_dtype, kv_dtype, page_size, q_len, num_sms,
-                                                bs, span):
+                                                bs, span, unit):
     mla = _mla()
     import workloads as synth
     rng = np.random.default_rng(91)
@@ -529,7 +533,8 @@ def test_calls_finish_far_below_the_wait_bound(q_dtype, kv_dtype, page_size, q_l
                             kv_dtype=kv_dtype, permute_pages=page_size > 1, seed=92,
                             q_len=q_len, device="cuda")
     plan = mla.mla_decode_plan(w.kv_indptr, w.kv_last_page_len, page_size=w.page_size,
-                               q_dtype=q_dtype, kv_dtype=kv_dtype, num_sms=num_sms, q_len=q_len)
+                               q_dtype=q_dtype, kv_dtype=kv_dtype, num_sms=num_sms, q_len=q_len,
+                               unit_tokens=unit)
     ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
     out = torch.empty((bs * q_len, 16, 512), dtype=torch.bfloat16, device="cuda")
     times = []
