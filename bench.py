@@ -550,19 +550,27 @@ def main():
         e2e_step(0)                              # both input buffers once, untimed
         e2e_step(1)
         torch.cuda.synchronize()
-        if dist is not None:
-            dist.barrier()
-        e0.record(stream)
-        copy_stream.wait_stream(stream)          # every timed copy starts after e0
-        for i in range(2, E + 2):
-            e2e_step(i)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = e0.elapsed_time(e1) / E
+        # Three timed batches of E steps; the median batch is reported.  The
+        # host link is shared with the rest of the machine, and one batch in
+        # a few can read at half speed while another job copies.
+        batches = []
+        for rep in range(3):
+            if dist is not None:
+                dist.barrier()
+            e0.record(stream)
+            copy_stream.wait_stream(stream)      # every timed copy starts after e0
+            for i in range(2 + rep * E, 2 + (rep + 1) * E):
+                e2e_step(i)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            batches.append(e0.elapsed_time(e1) / E)
+        e2e_ms = sorted(batches)[1]
         (e2e_ms,), _ = reduce_over_ranks(dist, [e2e_ms], [], device=dev)
         e2e = {"value": aggregate_gbs(total_bytes, e2e_ms), "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-               "steps": E, "overlap": "double-buffered inputs: a step's copy overlaps the previous decode"}
+               "steps": E, "batches": 3, "batch_ms_per_step": [round(b, 4) for b in batches],
+               "summary": "median of the three batches",
+               "overlap": "double-buffered inputs: a step's copy overlaps the previous decode"}
         del dev_in, host, d, plan, out, lse, ws
 
     # every other configuration of the suite, measured the same way in the

@@ -336,9 +336,9 @@ mla_status mla_decode_check(const mla_plan* plan, void* workspace, mla_stream_t 
  * mla_selftest_bounded_wait -- exercises the timeout path of the pipeline
  * waits on the GPU.  It launches one warp that waits, with the same bounded
  * wait every decode pipeline stage uses, on an mbarrier that nothing arrives
- * on, for limit_us microseconds (1 .. 1000000).  The wait gives up and sets
- * the producer bit of the workspace's device error word, and the kernel
- * returns.  The next mla_decode_check then returns MLA_ERR_DEVICE_TIMEOUT and
+ * on, for limit_us microseconds (1 .. 1000000).  The workspace's device error
+ * word is cleared first; the wait gives up and sets its producer bit, and the
+ * kernel returns.  The next mla_decode_check then returns MLA_ERR_DEVICE_TIMEOUT and
  * clears the word; the CUDA context stays usable.  Enqueued on `stream`.
  * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_WORKSPACE, MLA_ERR_CUDA.
  */

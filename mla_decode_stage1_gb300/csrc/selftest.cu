@@ -33,7 +33,10 @@ extern "C" mla_status mla_selftest_bounded_wait(const mla_plan* plan, void* work
     return MLA_ERR_INVALID_ARG;
   if (workspace_bytes < plan->ws_bytes) return MLA_ERR_WORKSPACE;
   int32_t* err = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + plan->off_err);
-  mla::bounded_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-      err, static_cast<uint64_t>(limit_us) * 1000u);
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // The word starts clear, whatever the workspace held before: the check
+  // that follows must see this wait's bit alone.
+  if (cudaMemsetAsync(err, 0, sizeof(int32_t), st) != cudaSuccess) return MLA_ERR_CUDA;
+  mla::bounded_wait_kernel<<<1, 32, 0, st>>>(err, static_cast<uint64_t>(limit_us) * 1000u);
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
